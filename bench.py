@@ -1,0 +1,428 @@
+"""Benchmark of the NVFP4 MoE decode hot path on GB300.
+
+One step = one MoE decode pass over a batch of 256 tokens with 128 experts
+and top-8 routing: route, quantise the BF16 activations on the fly into
+route order, gate_up grouped GEMM (K=6144, N=4096), quantise the
+route-ordered intermediate, down grouped GEMM (K=2048, N=6144) with the
+weighted scatter-combine back to token order.  The metric is the grouped
+GEMM throughput at ~16 tokens per expert, in TFLOPS, with HBM GB/s and the
+roofline fraction alongside.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs its own replica (independent batches, no
+data-path collective): weak scaling.  Weights are NVFP4, resident in HBM
+(2.72 GB per step, far larger than L2, so every step streams them from
+HBM).  `--impl reference` times the CPU oracle on a bounded sample of the
+same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from moe_grouped_gemm_nvfp4_gb300 import inputs, moe  # noqa: E402
+from moe_grouped_gemm_nvfp4_gb300 import nvfp4 as F  # noqa: E402
+
+METRIC = "NVFP4 grouped-GEMM TFLOPS & HBM GB/s (frac. of roofline) at 16-64 tok/expert"
+UNIT = "TFLOPS"
+E, TOPK, T = 128, 8, 256
+K1, N1 = 6144, 4096        # gate_up
+K2, N2 = 2048, 6144        # down
+FALLBACK_HBM_GBS = 6800.0
+
+
+def workload_config():
+    return {
+        "workload": f"moe_decode_layer E{E} top{TOPK} T{T}: gate_up K{K1} N{N1} + down K{K2} N{N2}",
+        "tokens_per_expert_mean": T * TOPK / E,
+        "global_batch": T,
+        "weights": "NVFP4 E2M1 + E4M3/16 + FP32 per expert, ~N(0,0.02) before quantisation",
+        "activations": "BF16 ~N(0,1), quantised on the fly each step",
+        "l2": "inputs larger than L2 (2.72 GB of expert weights streamed per step)",
+        "parallelism": "replicas",
+    }
+
+
+def flops_per_step():
+    R = T * TOPK
+    return 2.0 * R * N1 * K1 + 2.0 * R * N2 * K2
+
+
+def gemm_bytes(K, N, n_active, R, out_rows):
+    """Algorithmic bytes of one grouped-GEMM launch: NVFP4 weights of the
+    active experts (0.5 + 1/16 B per element), the quantised activations
+    read once (same rate), BF16 output written once."""
+    w = n_active * N * K * (0.5 + 1.0 / 16)
+    a = R * K * (0.5 + 1.0 / 16)
+    o = out_rows * N * 2.0
+    return w + a + o
+
+
+def step_bytes(n_active):
+    """Algorithmic HBM bytes of a step: weights of the active experts, BF16
+    activations in (x, h) and BF16 outputs (gate_up, down) once each."""
+    R = T * TOPK
+    w = n_active * (N1 * K1 + N2 * K2) * (0.5 + 1.0 / 16)
+    io = 2.0 * (T * K1 + R * K2 + R * N1 + T * N2)
+    return w + io
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d.get("hbm_gbs", FALLBACK_HBM_GBS)), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "common.cuh", "kernels.h"):
+        with open(os.path.join(ROOT, "moe_grouped_gemm_nvfp4_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per gate_up launch from the committed ncu summary, or None
+    when the kernel source changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return d.get("dram_bytes_per_gate_up_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.5)
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 8]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        # samples taken while the GPU was loaded (clock within 60% of max or the
+        # middle of the sequence when the timed region was shorter than a sample)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def build_problem(device, seed_base=2):
+    """Resident NVFP4 weights and one batch of per-step inputs (seeded)."""
+    t0 = time.time()
+    w1 = torch.empty((E, N1, K1), dtype=torch.bfloat16, device=device)
+    w2 = torch.empty((E, N2, K2), dtype=torch.bfloat16, device=device)
+    for e in range(E):
+        w1[e] = inputs.device_normal_bf16((N1, K1), 0.02, seed_base * 100003 + e, device)
+        w2[e] = inputs.device_normal_bf16((N2, K2), 0.02, (seed_base + 1) * 100003 + e, device)
+    W1 = moe.quantize_experts(w1)
+    W2 = moe.quantize_experts(w2)
+    g = inputs.rng(seed_base)
+    x = inputs.normal_bf16(g, (T, K1))
+    ids = inputs.uniform_topk(g, T, E, TOPK)
+    h = inputs.normal_bf16(inputs.rng(seed_base + 1), (T * TOPK, K2))
+    wts = inputs.dirichlet_weights(inputs.rng(seed_base + 1), T, TOPK)
+    torch.cuda.synchronize()
+    setup_s = time.time() - t0
+    host = dict(x=x, ids=torch.from_numpy(ids), h=h, wts=torch.from_numpy(wts))
+    return W1, W2, w1, w2, host, setup_s
+
+
+def run_ours(args, rank, world, local_rank):
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    W1, W2, w1, w2, host, setup_s = build_problem(device)
+    ids_np = host["ids"].numpy()
+    n_active = int(np.count_nonzero(np.bincount(ids_np.reshape(-1), minlength=E)))
+    del w1, w2
+    torch.cuda.empty_cache()
+    layer = moe.DecodeLayer(W1, W2, T, TOPK, device)
+    dev_in = {k: v.to(device) for k, v in host.items()}
+    stream = torch.cuda.current_stream()
+
+    def step(timing=None):
+        return layer.step(dev_in["x"], dev_in["ids"], dev_in["h"], dev_in["wts"], timing=timing)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    F.nvfp4_device_status(reset=True)
+    # soak ~0.5 s so the clocks under load are representative, then time K steps
+    soak_end = time.time() + 0.5
+    while time.time() < soak_end:
+        step()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(2)]
+          for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    start.record()
+    for i in range(args.steps):
+        step(timing=ev[i])
+    end.record()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    status = F.nvfp4_device_status(reset=True)
+    if status != F.NVFP4_OK:
+        raise RuntimeError(f"device status {F.nvfp4_status_string(status)} during the timed run")
+    ms_total = start.elapsed_time(end)
+    gu_ms = statistics.mean(e[0][0].elapsed_time(e[0][1]) for e in ev)
+    dn_ms = statistics.mean(e[1][0].elapsed_time(e[1][1]) for e in ev)
+
+    # end to end through the public API with host buffers: H2D of the step's
+    # inputs from pinned memory, the step, D2H of both outputs
+    pinned = {k: v.pin_memory() for k, v in host.items()}
+    out_gu = torch.empty((T * TOPK, N1), dtype=torch.bfloat16).pin_memory()
+    out_dn = torch.empty((T, N2), dtype=torch.bfloat16).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+    d2h = out_gu.numel() * 2 + out_dn.numel() * 2
+
+    def e2e_step():
+        for k in dev_in:
+            dev_in[k].copy_(pinned[k], non_blocking=True)
+        gu, dn = step()
+        out_gu.copy_(gu[: T * TOPK], non_blocking=True)
+        out_dn.copy_(dn[:T], non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    s2.record()
+    for _ in range(args.steps):
+        e2e_step()
+    e2.record()
+    torch.cuda.synchronize()
+    e2e_ms = s2.elapsed_time(e2)
+
+    local = torch.tensor([ms_total, e2e_ms, gu_ms, dn_ms], dtype=torch.float64)
+    if world > 1:
+        t = local.to(device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        local = t.cpu()
+    ms_total, e2e_ms, gu_ms, dn_ms = local.tolist()
+    if rank != 0:
+        return None
+
+    ms_step = ms_total / args.steps
+    fl = flops_per_step()
+    value = world * fl * args.steps / (ms_total * 1e-3) / 1e12
+    e2e_value = world * fl * args.steps / (e2e_ms * 1e-3) / 1e12
+    peak, peak_kind = measured_peaks()
+    R = T * TOPK
+    gu_bytes = gemm_bytes(K1, N1, n_active, R, R)
+    dn_bytes = gemm_bytes(K2, N2, n_active, R, T)
+    achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
+    traffic = recorded_traffic()
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4",
+        "data": "synthetic", "config": workload_config(),
+        "hbm_gbs": round(world * step_bytes(n_active) / (ms_step * 1e-3) / 1e9, 1),
+        "frac_of_hbm_roofline": round(step_bytes(n_active) / (ms_step * 1e-3) / 1e9 / peak, 4),
+        "roofline": {
+            "kernel": "nvfp4_gemm_kernel (gate_up grouped launch)", "bound": "hbm",
+            "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": traffic,
+            "algorithmic_bytes_per_launch": int(gu_bytes), "launch_ms": round(gu_ms, 4),
+            "peak_source": f"{peak_kind} hbm_gbs",
+        },
+        "down_launch": {"achieved_gbs": round(dn_bytes / (dn_ms * 1e-3) / 1e9, 1),
+                        "launch_ms": round(dn_ms, 4), "algorithmic_bytes": int(dn_bytes)},
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms / args.steps, 4)},
+        "gpu_launches": 8 * args.steps,
+        "clocks": clocks,
+        "setup_s": round(setup_s, 1),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(W_host_seed=2, budget_s=args.cpu_budget)
+    return line
+
+
+# --------------------------------------------------------------- CPU oracle
+
+def _oracle_sample(experts, seed_base=2, device=None):
+    """One bounded sample of the workload run by the CPU oracle: route, the
+    activation quantisation of the whole batch, and for the given experts
+    the weight quantisation plus their routes' gate_up and down GEMMs and
+    the combine.  Returns the FLOPs of the GEMMs it computed."""
+    import oracle
+    g = inputs.rng(seed_base)
+    x = inputs.normal_bf16(g, (T, K1)).float().numpy()
+    ids = inputs.uniform_topk(g, T, E, TOPK)
+    h = inputs.normal_bf16(inputs.rng(seed_base + 1), (T * TOPK, K2)).float().numpy()
+    wts = inputs.dirichlet_weights(inputs.rng(seed_base + 1), T, TOPK)
+    flops = 0.0
+    t0 = time.perf_counter()
+    off, tok, slot = oracle.route(ids, E)
+    xh = oracle.dequantize(*oracle.quantize(x))
+    hh = oracle.dequantize(*oracle.quantize(h))
+    for e in experts:
+        w1 = _host_weight(seed_base * 100003 + e, (N1, K1))
+        w2 = _host_weight((seed_base + 1) * 100003 + e, (N2, K2))
+        lo, hi = int(off[e]), int(off[e + 1])
+        y1 = xh[tok[lo:hi]] @ oracle.dequantize(*oracle.quantize(w1)).T
+        y2 = hh[lo:hi] @ oracle.dequantize(*oracle.quantize(w2)).T
+        oracle.combine(y2, tok[lo:hi], slot[lo:hi], wts, T)
+        flops += 2.0 * (hi - lo) * (N1 * K1 + N2 * K2)
+        del y1
+    return flops, time.perf_counter() - t0
+
+
+def _host_weight(seed, shape):
+    """The expert weight the device generator draws for `seed`, on the host.
+
+    torch's CPU and CUDA generators differ, so the oracle sample draws its
+    own N(0, 0.02) weights with the host generator: the work is the same
+    size and kind, which is what the baseline times."""
+    return inputs.normal_bf16(inputs.rng(seed), shape, 0.02).float().numpy()
+
+
+def cpu_baseline(W_host_seed=2, budget_s=20.0):
+    experts = []
+    flops, secs = 0.0, 0.0
+    e = 0
+    while secs < budget_s and e < E:
+        f, s = _oracle_sample([e], W_host_seed)
+        flops += f
+        secs += s
+        experts.append(e)
+        e += 1
+    cores = _blas_threads()
+    return {"value": round(flops / secs / 1e12, 6), "unit": UNIT, "cores": cores,
+            "kind": "oracle",
+            "sample": f"experts {experts[0]}..{experts[-1]} of the gate_up+down pass "
+                      f"({len(experts)} of {E}); each sample also routes and quantises the "
+                      f"whole batch; {secs:.1f} s of CPU time"}
+
+
+def _blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    for i in range(args.warmup):
+        _oracle_sample([i % E])
+    times, flops = [], 0.0
+    for i in range(args.steps):
+        f, s = _oracle_sample([(args.warmup + i) % E])
+        times.append(s)
+        flops += f
+    total = sum(times)
+    value = flops / total / 1e12
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * total / args.steps, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(),
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": _blas_threads(),
+                         "kind": "oracle",
+                         "sample": "each step: one expert's gate_up + down GEMMs, its weight "
+                                   "quantisation, and the route + activation quantisation of "
+                                   "the whole batch"},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and args.impl == "ours":
+        torch.distributed.init_process_group(
+            "nccl", device_id=torch.device("cuda", local_rank))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ours(args, rank, world, local_rank)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1 and args.impl == "ours":
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,199 @@
+/*
+ * nvfp4.h -- C ABI of the GB300 (sm_103a) NVFP4 block-scaled GEMM library.
+ *
+ * NVFP4: E2M1 4-bit values (1 sign, 2 exponent, 1 mantissa bit), two per
+ * byte with the lower K index in the low nibble, one FP8-E4M3 block scale per
+ * 16 consecutive K elements and one FP32 global scale per tensor
+ * ("The Blackwell architectural split", Preserving precision -- dual-tier
+ * scale handling).  Dequantised value: x = e2m1 * e4m3(block) * global.
+ *
+ * Conventions shared by every entry point
+ *   - All pointers are DEVICE pointers to caller-owned memory unless stated.
+ *     The library never allocates or frees memory; it keeps only a per-device
+ *     cache of launch attributes and a per-device status word.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is enqueued asynchronously on it.
+ *   - Global scales are device floats, so no call forces a host sync.
+ *   - Host-side argument errors return immediately and enqueue nothing:
+ *       NVFP4_ERR_INVALID_ARG  null pointer, negative size;
+ *       NVFP4_ERR_UNSUPPORTED  shape/alignment/device outside what the
+ *                              kernels implement (K % 64, 16-byte alignment,
+ *                              device not sm_103, workspace too small ...);
+ *       NVFP4_ERR_CUDA         a CUDA call failed (launch error).
+ *   - Device-side failures (a bounded pipeline wait that expired, routing
+ *     offsets that are not monotone, expert ids out of range) are recorded in
+ *     the per-device status word read by nvfp4_device_status(); the kernels
+ *     return early instead of trapping.  No failure leaves an output
+ *     silently unwritten without a non-OK status somewhere: this is the
+ *     lesson of the all-zeros backend in "The SM120 FP4 GEMM Kernel
+ *     Investigation" (The Breaking Point: FlashInfer #2577).
+ */
+#ifndef NVFP4_GB300_H
+#define NVFP4_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum nvfp4_status {
+  NVFP4_OK = 0,
+  NVFP4_ERR_INVALID_ARG = 1,
+  NVFP4_ERR_UNSUPPORTED = 2,
+  NVFP4_ERR_CUDA = 3,
+  NVFP4_ERR_TIMEOUT = 4,       /* a bounded device wait expired            */
+  NVFP4_ERR_DEVICE_CHECK = 5   /* a device-side input check failed         */
+} nvfp4_status;
+
+/* Flags of the quantiser entry points. */
+#define NVFP4_SF_ROWMAJOR   0u  /* scales as uint8 [rows, cols/16]               */
+#define NVFP4_SF_ATOMS      1u  /* scales in the tensor-core atom layout         */
+#define NVFP4_GLOBAL_GIVEN  2u  /* read *global_scale instead of computing it    */
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* nvfp4_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int nvfp4_version(void);
+
+/*
+ * Reads the status word of the current device after synchronising `stream`.
+ * *status_out receives the first device-side error recorded since the last
+ * reset (NVFP4_OK if none).  reset != 0 clears the word afterwards.
+ */
+nvfp4_status nvfp4_device_status(void* stream, int reset, int* status_out);
+
+/* Bounded-wait limit of the pipeline kernels in nanoseconds (default 1 s). */
+nvfp4_status nvfp4_set_timeout_ns(uint64_t ns);
+
+/*
+ * Scale bytes of a [rows, cols] matrix in the tensor-core atom layout:
+ * 512-byte atoms of 128 rows x 4 scale columns (64 K elements), byte
+ * (r % 32) * 16 + ((r % 128) / 32) * 4 + (c % 4), atoms ordered row-tile
+ * major; rows are padded to a multiple of 128.  cols % 64 == 0.
+ */
+size_t nvfp4_atom_scales_bytes(int64_t rows, int64_t cols);
+
+/*
+ * BF16 -> NVFP4 quantiser (per-16 amax, E4M3 block scale, E2M1 round to
+ * nearest even, pack).
+ *   x        BF16 [rows, cols], row stride `ld` elements (ld >= cols);
+ *            cols % 16 == 0 (cols % 64 == 0 with NVFP4_SF_ATOMS).
+ *   packed   uint8 [rows, cols/2] out, row-major, dense.
+ *   scales   uint8 out: [rows, cols/16] row-major, or the atom layout of
+ *            nvfp4_atom_scales_bytes(rows, cols) bytes with NVFP4_SF_ATOMS.
+ *   global_scale  device float: written with g = amax|x| / (6 * 448), or read
+ *            as the global scale when NVFP4_GLOBAL_GIVEN is set.
+ * Every step is IEEE binary32 round-to-nearest-even: s = (amax_b / 6) / g
+ * (0 when g == 0), sf = E4M3_satfinite(s), d = e4m3(sf) * g, and code =
+ * E2M1_satfinite(x / d), or the signed zero code when d == 0.
+ */
+nvfp4_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                            uint8_t* packed, uint8_t* scales, float* global_scale,
+                            uint32_t flags, void* stream);
+
+/*
+ * Rewrites row-major E4M3 scales [rows, kblk] (kblk = K/16, kblk % 4 == 0)
+ * into the atom layout (nvfp4_atom_scales_bytes(rows, 16 * kblk) bytes);
+ * padding rows are written as zero.  Offline step for weights.
+ */
+nvfp4_status nvfp4_prepack_weights(const uint8_t* scales_rowmajor, int64_t rows,
+                                   int64_t kblk, uint8_t* scales_atoms, void* stream);
+
+/*
+ * Single NVFP4 GEMM: C[M, N] (BF16, row stride ldc elements) =
+ * (*gA) * (*gB) * A_hat . B_hat^T, FP32 accumulation in tensor memory,
+ * BF16 round-to-nearest-even output.
+ *   A  packed [M, K/2], sfA atom layout for [M, K];
+ *   B  packed [N, K/2], sfB atom layout for [N, K];
+ *   K % 64 == 0, M, N >= 1, ldc >= N, ldc % 8 == 0, all pointers 16-byte
+ *   aligned.  Small M runs with the operands swapped (weights on the MMA's
+ *   M side); the result is the same.
+ */
+nvfp4_status nvfp4_gemm(const uint8_t* A, const uint8_t* sfA, const float* gA,
+                        const uint8_t* B, const uint8_t* sfB, const float* gB,
+                        void* C, int64_t M, int64_t N, int64_t K, int64_t ldc,
+                        void* stream);
+
+/*
+ * MoE routing prep ("The FP4 Frontier", Finding 5: grouped GEMM batching all
+ * experts): counting sort of the T*topk routes by expert, stable by token.
+ *   topk_ids        int32 [T, topk], values in [0, E)
+ *   expert_offsets  int32 [E+1] out: routes of expert e are positions
+ *                   expert_offsets[e] .. expert_offsets[e+1]-1
+ *   route_token     int32 [T*topk] out: token of each sorted route
+ *   route_slot      int32 [T*topk] out: top-k slot of each sorted route
+ *   route_pos       int32 [T*topk] out (may be NULL): sorted position of the
+ *                   route t*topk + slot
+ * E <= 1024.  An id out of range sets NVFP4_ERR_DEVICE_CHECK on the device
+ * and the route is dropped (expert_offsets[E] < T*topk then).
+ */
+nvfp4_status nvfp4_moe_route(const int32_t* topk_ids, int64_t T, int32_t topk, int32_t E,
+                             int32_t* expert_offsets, int32_t* route_token,
+                             int32_t* route_slot, int32_t* route_pos, void* stream);
+
+/*
+ * Upper bound on the bytes of the grouped scale layout for R routes over E
+ * experts and K: every expert's routes start a fresh 128-row atom tile.
+ */
+size_t nvfp4_grouped_scales_bytes(int64_t R, int32_t E, int64_t K);
+
+/*
+ * Quantise activations straight into route order for the grouped GEMM.
+ *   x           BF16 [rows, K], row stride ld.
+ *   route_pos   int32 [rows * fanout]: destination route of source row i,
+ *               copy j is route_pos[i * fanout + j] (the route_pos output of
+ *               nvfp4_moe_route with fanout = topk).  NULL means the rows are
+ *               already in route order (rows == R, fanout == 1).
+ *   expert_offsets  int32 [E+1] (device), as from nvfp4_moe_route.
+ *   packed      uint8 [R, K/2] out, route order.
+ *   scales      grouped atom layout out, nvfp4_grouped_scales_bytes(R, E, K)
+ *               bytes: route p of expert e is padded row 128 * tb[e] +
+ *               (p - expert_offsets[e]), tb[e] = sum over e' < e of
+ *               ceil(count_e' / 128).
+ *   global_scale  as in nvfp4_quantize (one g over the whole of x).
+ * K % 64 == 0, E <= 1024.
+ */
+nvfp4_status nvfp4_quantize_dispatch(const void* x, int64_t rows, int64_t K, int64_t ld,
+                                     const int32_t* route_pos, int32_t fanout,
+                                     const int32_t* expert_offsets, int32_t E, int64_t R,
+                                     uint8_t* packed, uint8_t* scales, float* global_scale,
+                                     uint32_t flags, void* stream);
+
+/* Bytes of the FP32 combine workspace for T tokens and N outputs. */
+size_t nvfp4_combine_workspace_bytes(int64_t T, int64_t N);
+
+/*
+ * MoE expert grouped GEMM ("The FP4 Frontier", Finding 5 and Finding 7:
+ * small-batch decode is bound by streaming the expert weights).  One
+ * persistent launch covers every (expert, 128-row weight tile, token tile)
+ * unit; experts without routes are skipped and their weights never read.
+ *   A, sfA, gA  route-ordered activations from nvfp4_quantize_dispatch:
+ *               packed [R, K/2], grouped atom scales, device float global.
+ *   W           packed weights [E, N, K/2]; sfW atom layout over [E*N, K];
+ *               gW device float [E], one global per expert.
+ *   expert_offsets  int32 [E+1] (device), R = T * topk routes.
+ *   topk_weights == NULL:  out = BF16 [R, N] in route order,
+ *       out[p, n] = gA * gW[e] * sum_k A_hat[p, k] W_hat[e, n, k].
+ *   topk_weights != NULL (FP32 [T, topk]):  out = BF16 [T, N],
+ *       out[t] = sum over the routes p of t of w[t, slot(p)] * y[p], with
+ *       route_token / route_slot from nvfp4_moe_route and an FP32 workspace
+ *       of nvfp4_combine_workspace_bytes(T, N) bytes (zeroed here).
+ * N % 128 == 0, K % 64 == 0, E <= 1024.
+ */
+nvfp4_status nvfp4_grouped_gemm(const uint8_t* A, const uint8_t* sfA, const float* gA,
+                                const uint8_t* W, const uint8_t* sfW, const float* gW,
+                                const int32_t* expert_offsets, int32_t E,
+                                int64_t T, int32_t topk, int64_t N, int64_t K,
+                                const int32_t* route_token, const int32_t* route_slot,
+                                const float* topk_weights,
+                                void* out, float* workspace, size_t workspace_bytes,
+                                void* stream);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif /* NVFP4_GB300_H */

@@ -1,0 +1,351 @@
+// C ABI of the NVFP4 library: argument validation, tensor-map encoding and
+// launches on the caller's stream.  See include/nvfp4.h for the contract.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/nvfp4.h"
+#include "kernels.h"
+
+namespace {
+
+// Per-device status word of the kernels (first error wins).
+__device__ int g_status_word;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool ready = false;
+  bool sm103 = false;
+  int sms = 0;
+  int* status = nullptr;   // device address of g_status_word
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+std::atomic<uint64_t> g_timeout_ns{1000000000ull};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+nvfp4_status cuda_fail() {
+  cudaGetLastError();   // clear the sticky-free error so later calls can run
+  return NVFP4_ERR_CUDA;
+}
+
+// Looks up (once per device, with that device current) the SM count, the
+// architecture and the device address of the status word, and sets the
+// kernels' shared-memory attributes.
+nvfp4_status device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cuda_fail();
+  if (dev < 0 || dev >= kMaxDevices) return NVFP4_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& d = g_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return cuda_fail();
+    d.sm103 = (major == 10 && minor == 3);
+    d.sms = sms;
+    if (d.sm103) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return cuda_fail();
+      d.status = static_cast<int*>(p);
+      if (nvfp4::init_gemm_attributes() != cudaSuccess) return cuda_fail();
+      if (nvfp4::init_route_attributes() != cudaSuccess) return cuda_fail();
+    }
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                           cudaEnableDefault, &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return cuda_fail();
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    if (const char* env = std::getenv("NVFP4_TIMEOUT_NS")) {
+      const unsigned long long v = std::strtoull(env, nullptr, 10);
+      if (v > 0) g_timeout_ns.store(v);
+    }
+    d.ready = true;
+  }
+  if (!d.sm103) return NVFP4_ERR_UNSUPPORTED;
+  *out = &d;
+  return NVFP4_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 2-D map over a packed operand [rows, row_bytes] (uint8), box of 128 bytes
+// x box_rows rows, 128-byte swizzle.  Out-of-range boxes read zeros.
+nvfp4_status make_operand_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t row_bytes,
+                              uint32_t box_rows) {
+  const cuuint64_t dims[2] = {row_bytes, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {128u, box_rows};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NVFP4_OK : NVFP4_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* nvfp4_status_string(int status) {
+  switch (status) {
+    case NVFP4_OK: return "NVFP4_OK";
+    case NVFP4_ERR_INVALID_ARG: return "NVFP4_ERR_INVALID_ARG";
+    case NVFP4_ERR_UNSUPPORTED: return "NVFP4_ERR_UNSUPPORTED";
+    case NVFP4_ERR_CUDA: return "NVFP4_ERR_CUDA";
+    case NVFP4_ERR_TIMEOUT: return "NVFP4_ERR_TIMEOUT";
+    case NVFP4_ERR_DEVICE_CHECK: return "NVFP4_ERR_DEVICE_CHECK";
+    default: return "NVFP4_ERR_UNKNOWN";
+  }
+}
+
+int nvfp4_version(void) { return 100; }
+
+nvfp4_status nvfp4_set_timeout_ns(uint64_t ns) {
+  if (ns == 0) return NVFP4_ERR_INVALID_ARG;
+  g_timeout_ns.store(ns);
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_device_status(void* stream, int reset, int* status_out) {
+  if (!status_out) return NVFP4_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  nvfp4_status st = device_state(&d);
+  if (st != NVFP4_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int v = 0;
+  if (cudaMemcpyAsync(&v, d->status, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return cuda_fail();
+  if (cudaStreamSynchronize(s) != cudaSuccess) return cuda_fail();
+  if (reset) {
+    if (cudaMemsetAsync(d->status, 0, sizeof(int), s) != cudaSuccess) return cuda_fail();
+    if (cudaStreamSynchronize(s) != cudaSuccess) return cuda_fail();
+  }
+  *status_out = v;
+  return NVFP4_OK;
+}
+
+size_t nvfp4_atom_scales_bytes(int64_t rows, int64_t cols) {
+  if (rows < 0 || cols < 0) return 0;
+  return static_cast<size_t>((rows + 127) / 128 * 128) * static_cast<size_t>(cols / 16);
+}
+
+size_t nvfp4_grouped_scales_bytes(int64_t R, int32_t E, int64_t K) {
+  if (R < 0 || E < 0 || K < 0) return 0;
+  const int64_t nonempty = R < E ? R : E;
+  const int64_t tiles = (R + 127 * nonempty) / 128;
+  return static_cast<size_t>(tiles * 128) * static_cast<size_t>(K / 16);
+}
+
+size_t nvfp4_combine_workspace_bytes(int64_t T, int64_t N) {
+  if (T < 0 || N < 0) return 0;
+  return static_cast<size_t>(T) * static_cast<size_t>(N) * sizeof(float);
+}
+
+nvfp4_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                            uint8_t* packed, uint8_t* scales, float* global_scale,
+                            uint32_t flags, void* stream) {
+  if (rows < 0 || cols < 0 || ld < cols) return NVFP4_ERR_INVALID_ARG;
+  if (flags & ~(NVFP4_SF_ATOMS | NVFP4_GLOBAL_GIVEN)) return NVFP4_ERR_INVALID_ARG;
+  if (!global_scale || (rows > 0 && cols > 0 && (!x || !packed || !scales)))
+    return NVFP4_ERR_INVALID_ARG;
+  if (cols % 16 != 0 || ld % 8 != 0) return NVFP4_ERR_UNSUPPORTED;
+  if ((flags & NVFP4_SF_ATOMS) && cols % 64 != 0) return NVFP4_ERR_UNSUPPORTED;
+  if ((x && !aligned16(x)) || (packed && (reinterpret_cast<uintptr_t>(packed) & 7u)) ||
+      (reinterpret_cast<uintptr_t>(global_scale) & 3u))
+    return NVFP4_ERR_UNSUPPORTED;
+  DeviceState* d = nullptr;
+  nvfp4_status st = device_state(&d);
+  if (st != NVFP4_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const uint16_t* xb = static_cast<const uint16_t*>(x);
+  if (!(flags & NVFP4_GLOBAL_GIVEN)) {
+    if (nvfp4::launch_amax(xb, rows, cols, ld, global_scale, d->sms, s) != cudaSuccess)
+      return cuda_fail();
+  }
+  if (nvfp4::launch_quantize(xb, rows, cols, ld, packed, scales,
+                             (flags & NVFP4_SF_ATOMS) ? 1 : 0, global_scale, d->sms, s) !=
+      cudaSuccess)
+    return cuda_fail();
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_prepack_weights(const uint8_t* scales_rowmajor, int64_t rows, int64_t kblk,
+                                   uint8_t* scales_atoms, void* stream) {
+  if (rows < 0 || kblk < 0) return NVFP4_ERR_INVALID_ARG;
+  if (rows > 0 && kblk > 0 && (!scales_rowmajor || !scales_atoms)) return NVFP4_ERR_INVALID_ARG;
+  if (kblk % 4 != 0) return NVFP4_ERR_UNSUPPORTED;
+  if (scales_atoms && (reinterpret_cast<uintptr_t>(scales_atoms) & 3u)) return NVFP4_ERR_UNSUPPORTED;
+  if (scales_rowmajor && (reinterpret_cast<uintptr_t>(scales_rowmajor) & 3u))
+    return NVFP4_ERR_UNSUPPORTED;
+  DeviceState* d = nullptr;
+  nvfp4_status st = device_state(&d);
+  if (st != NVFP4_OK) return st;
+  if (kblk == 0) return NVFP4_OK;
+  if (nvfp4::launch_prepack(scales_rowmajor, rows, kblk, scales_atoms, d->sms,
+                            static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return cuda_fail();
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_gemm(const uint8_t* A, const uint8_t* sfA, const float* gA,
+                        const uint8_t* B, const uint8_t* sfB, const float* gB,
+                        void* C, int64_t M, int64_t N, int64_t K, int64_t ldc, void* stream) {
+  if (!A || !sfA || !gA || !B || !sfB || !gB || !C) return NVFP4_ERR_INVALID_ARG;
+  if (M <= 0 || N <= 0 || K <= 0 || ldc < N) return NVFP4_ERR_INVALID_ARG;
+  if (K % 64 != 0 || ldc % 8 != 0) return NVFP4_ERR_UNSUPPORTED;
+  if (M > (1LL << 30) || N > (1LL << 30) || K > (1LL << 31)) return NVFP4_ERR_UNSUPPORTED;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(sfA) || !aligned16(sfB) || !aligned16(C))
+    return NVFP4_ERR_UNSUPPORTED;
+  DeviceState* d = nullptr;
+  nvfp4_status st = device_state(&d);
+  if (st != NVFP4_OK) return st;
+  // Small M (decode-like): weights on the MMA's M side, tokens on its N side.
+  const bool swap = M <= 64;
+  const uint8_t* X = swap ? B : A;
+  const uint8_t* Y = swap ? A : B;
+  const int64_t rows_x = swap ? N : M;
+  const int64_t rows_y = swap ? M : N;
+  CUtensorMap tmx, tmy;
+  if (make_operand_map(&tmx, X, rows_x, K / 2, 128) != NVFP4_OK ||
+      make_operand_map(&tmy, Y, rows_y, K / 2, 16) != NVFP4_OK)
+    return NVFP4_ERR_UNSUPPORTED;
+  nvfp4::GemmArgs a{};
+  a.sfx = swap ? sfB : sfA;
+  a.sfy = swap ? sfA : sfB;
+  a.gx = swap ? gB : gA;
+  a.gy = swap ? gA : gB;
+  a.K = K;
+  a.rows_x = static_cast<int32_t>(rows_x);
+  a.rows_y = static_cast<int32_t>(rows_y);
+  a.out = C;
+  a.ldc = ldc;
+  a.status = d->status;
+  a.timeout_ns = g_timeout_ns.load();
+  if (nvfp4::launch_gemm(tmx, tmy, a, swap ? nvfp4::kDenseRowsY : nvfp4::kDenseRowsX, d->sms,
+                         static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return cuda_fail();
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_moe_route(const int32_t* topk_ids, int64_t T, int32_t topk, int32_t E,
+                             int32_t* expert_offsets, int32_t* route_token, int32_t* route_slot,
+                             int32_t* route_pos, void* stream) {
+  if (T < 0 || topk <= 0 || E <= 0 || !expert_offsets) return NVFP4_ERR_INVALID_ARG;
+  if (T > 0 && (!topk_ids || !route_token || !route_slot)) return NVFP4_ERR_INVALID_ARG;
+  if (E > 1024 || T * topk > (1LL << 30)) return NVFP4_ERR_UNSUPPORTED;
+  DeviceState* d = nullptr;
+  nvfp4_status st = device_state(&d);
+  if (st != NVFP4_OK) return st;
+  if (nvfp4::launch_route(topk_ids, T, topk, E, expert_offsets, route_token, route_slot,
+                          route_pos, d->status, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return cuda_fail();
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_quantize_dispatch(const void* x, int64_t rows, int64_t K, int64_t ld,
+                                     const int32_t* route_pos, int32_t fanout,
+                                     const int32_t* expert_offsets, int32_t E, int64_t R,
+                                     uint8_t* packed, uint8_t* scales, float* global_scale,
+                                     uint32_t flags, void* stream) {
+  if (rows < 0 || K <= 0 || ld < K || E <= 0 || R < 0 || fanout <= 0) return NVFP4_ERR_INVALID_ARG;
+  if (flags & ~static_cast<uint32_t>(NVFP4_GLOBAL_GIVEN)) return NVFP4_ERR_INVALID_ARG;
+  if (!expert_offsets || !global_scale || (rows > 0 && (!x || !packed || !scales)))
+    return NVFP4_ERR_INVALID_ARG;
+  if (!route_pos && (fanout != 1 || rows != R)) return NVFP4_ERR_INVALID_ARG;
+  if (K % 64 != 0 || ld % 8 != 0 || E > 1024) return NVFP4_ERR_UNSUPPORTED;
+  if ((x && !aligned16(x)) || (packed && (reinterpret_cast<uintptr_t>(packed) & 7u)))
+    return NVFP4_ERR_UNSUPPORTED;
+  DeviceState* d = nullptr;
+  nvfp4_status st = device_state(&d);
+  if (st != NVFP4_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const uint16_t* xb = static_cast<const uint16_t*>(x);
+  if (!(flags & NVFP4_GLOBAL_GIVEN)) {
+    if (nvfp4::launch_amax(xb, rows, K, ld, global_scale, d->sms, s) != cudaSuccess)
+      return cuda_fail();
+  }
+  if (nvfp4::launch_quantize_dispatch(xb, rows, K, ld, route_pos, fanout, expert_offsets, E, R,
+                                      packed, scales, global_scale, d->status, d->sms, s) !=
+      cudaSuccess)
+    return cuda_fail();
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_grouped_gemm(const uint8_t* A, const uint8_t* sfA, const float* gA,
+                                const uint8_t* W, const uint8_t* sfW, const float* gW,
+                                const int32_t* expert_offsets, int32_t E,
+                                int64_t T, int32_t topk, int64_t N, int64_t K,
+                                const int32_t* route_token, const int32_t* route_slot,
+                                const float* topk_weights,
+                                void* out, float* workspace, size_t workspace_bytes,
+                                void* stream) {
+  if (!A || !sfA || !gA || !W || !sfW || !gW || !expert_offsets || !out)
+    return NVFP4_ERR_INVALID_ARG;
+  if (E <= 0 || T < 0 || topk <= 0 || N <= 0 || K <= 0) return NVFP4_ERR_INVALID_ARG;
+  const bool combine = topk_weights != nullptr;
+  if (combine && (!route_token || !route_slot || !workspace)) return NVFP4_ERR_INVALID_ARG;
+  if (N % 128 != 0 || K % 64 != 0 || E > nvfp4::kGroupedMaxExperts) return NVFP4_ERR_UNSUPPORTED;
+  const int64_t R = T * topk;
+  if (R > (1LL << 30) || static_cast<int64_t>(E) * N > (1LL << 30)) return NVFP4_ERR_UNSUPPORTED;
+  if (combine && workspace_bytes < nvfp4_combine_workspace_bytes(T, N)) return NVFP4_ERR_UNSUPPORTED;
+  if (!aligned16(A) || !aligned16(sfA) || !aligned16(W) || !aligned16(sfW) || !aligned16(out) ||
+      (combine && !aligned16(workspace)))
+    return NVFP4_ERR_UNSUPPORTED;
+  DeviceState* d = nullptr;
+  nvfp4_status st = device_state(&d);
+  if (st != NVFP4_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (R == 0) {
+    if (combine && T > 0 && cudaMemsetAsync(out, 0, T * N * 2, s) != cudaSuccess) return cuda_fail();
+    return NVFP4_OK;
+  }
+  CUtensorMap tmx, tmy;
+  if (make_operand_map(&tmx, W, static_cast<uint64_t>(E) * N, K / 2, 128) != NVFP4_OK ||
+      make_operand_map(&tmy, A, R, K / 2, 16) != NVFP4_OK)
+    return NVFP4_ERR_UNSUPPORTED;
+  nvfp4::GemmArgs a{};
+  a.sfx = sfW;
+  a.sfy = sfA;
+  a.gx = gW;
+  a.gy = gA;
+  a.K = K;
+  a.rows_x = static_cast<int32_t>(E * N);
+  a.rows_y = static_cast<int32_t>(R);
+  a.expert_offsets = expert_offsets;
+  a.E = E;
+  a.n_out = static_cast<int32_t>(N);
+  a.out = out;
+  a.ldc = N;
+  a.route_token = route_token;
+  a.route_slot = route_slot;
+  a.topk_w = topk_weights;
+  a.topk = topk;
+  a.ws = workspace;
+  a.status = d->status;
+  a.timeout_ns = g_timeout_ns.load();
+  if (combine && cudaMemsetAsync(workspace, 0, nvfp4_combine_workspace_bytes(T, N), s) != cudaSuccess)
+    return cuda_fail();
+  if (nvfp4::launch_gemm(tmx, tmy, a, combine ? nvfp4::kGroupedCombine : nvfp4::kGrouped, d->sms,
+                         s) != cudaSuccess)
+    return cuda_fail();
+  if (combine && nvfp4::launch_combine_finalize(workspace, T, N, out, d->sms, s) != cudaSuccess)
+    return cuda_fail();
+  return NVFP4_OK;
+}
+
+}  // extern "C"

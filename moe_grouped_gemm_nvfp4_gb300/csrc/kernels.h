@@ -1,0 +1,69 @@
+// Internal launchers shared between the kernel translation units and the
+// C ABI layer.  Not part of the public interface.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace nvfp4 {
+
+// quantize.cu
+cudaError_t launch_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, float* g,
+                        int sms, cudaStream_t s);
+cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
+                            uint8_t* packed, uint8_t* scales, int sf_atoms, const float* g,
+                            int sms, cudaStream_t s);
+cudaError_t launch_quantize_dispatch(const uint16_t* x, int64_t rows, int64_t K, int64_t ld,
+                                     const int32_t* route_pos, int fanout,
+                                     const int32_t* expert_offsets, int E, int64_t R,
+                                     uint8_t* packed, uint8_t* scales, const float* g,
+                                     int* status, int sms, cudaStream_t s);
+cudaError_t launch_prepack(const uint8_t* src, int64_t rows, int64_t kblk, uint8_t* dst,
+                           int sms, cudaStream_t s);
+
+// route.cu
+cudaError_t init_route_attributes();
+cudaError_t launch_route(const int32_t* ids, int64_t T, int topk, int E, int32_t* offsets,
+                         int32_t* route_token, int32_t* route_slot, int32_t* route_pos,
+                         int* status, cudaStream_t s);
+
+// gemm.cu
+enum GemmMode : int {
+  kDenseRowsX = 0,      // C[x][y]: X = A (M side), Y = B
+  kDenseRowsY = 1,      // C[y][x]: X = B, Y = A (small M)
+  kGrouped = 2,         // out[route][n]
+  kGroupedCombine = 3,  // ws[token][n] += w * y
+};
+
+struct GemmArgs {
+  const uint8_t* sfx;              // X scales, atom layout
+  const uint8_t* sfy;              // Y scales, atom layout (grouped: per-expert tiles)
+  const float* gx;                 // X global (grouped: per expert [E])
+  const float* gy;                 // Y global
+  int64_t K;
+  int32_t rows_x;                  // dense: rows of X
+  int32_t rows_y;                  // dense: rows of Y; grouped: R (rows of A)
+  const int32_t* expert_offsets;   // grouped
+  int32_t E;
+  int32_t n_out;                   // grouped: rows of each expert's W
+  void* out;                       // BF16
+  int64_t ldc;
+  const int32_t* route_token;      // combine
+  const int32_t* route_slot;
+  const float* topk_w;
+  int32_t topk;
+  float* ws;                       // combine: FP32 [T, n_out]
+  int* status;
+  uint64_t timeout_ns;
+};
+
+constexpr int kGroupedMaxExperts = 256;
+
+cudaError_t init_gemm_attributes();
+cudaError_t launch_gemm(const CUtensorMap& tmx, const CUtensorMap& tmy, const GemmArgs& a,
+                        int mode, int sms, cudaStream_t s);
+cudaError_t launch_combine_finalize(const float* ws, int64_t T, int64_t N, void* out, int sms,
+                                    cudaStream_t s);
+
+}  // namespace nvfp4

@@ -1,0 +1,152 @@
+"""MoE expert grouped GEMM on the NVFP4 library: weight preparation and the
+decode/prefill call sequence.
+
+Everything here is argument marshalling around the C ABI; the arithmetic
+runs in the CUDA kernels.  Buffers are allocated once per plan (torch
+device memory) so that a step enqueues kernels only.
+
+Call sequence of one MoE pass ("The FP4 Frontier", Finding 5: grouped GEMM
+over all experts; the activations arrive in BF16 and are quantised on the
+fly, "The SM120 FP4 GEMM Kernel Investigation", The Context):
+    route -> quantise + dispatch to route order -> grouped GEMM
+    [-> weighted combine back to token order for the down projection]
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import nvfp4 as F
+
+
+@dataclass
+class ExpertWeights:
+    """NVFP4 expert weights: packed [E, N, K/2], atom scales over [E*N, K], g [E]."""
+    packed: torch.Tensor
+    sf_atoms: torch.Tensor
+    g: torch.Tensor
+    E: int
+    N: int
+    K: int
+
+
+def quantize_experts(w: torch.Tensor, stream=None) -> ExpertWeights:
+    """BF16 [E, N, K] on the device -> NVFP4 with one global scale per expert."""
+    E, N, K = w.shape
+    dev = w.device
+    packed = torch.empty((E, N, K // 2), dtype=torch.uint8, device=dev)
+    sf_rm = torch.empty((E, N, K // 16), dtype=torch.uint8, device=dev)
+    g = torch.empty(E, dtype=torch.float32, device=dev)
+    for e in range(E):
+        F.nvfp4_quantize(w[e], packed[e], sf_rm[e], g[e:e + 1], 0, stream)
+    sf_atoms = torch.empty(F.nvfp4_atom_scales_bytes(E * N, K), dtype=torch.uint8, device=dev)
+    F.nvfp4_prepack_weights(sf_rm.view(E * N, K // 16), sf_atoms, stream)
+    return ExpertWeights(packed, sf_atoms, g, E, N, K)
+
+
+class GroupedPlan:
+    """Buffers and calls for one grouped-GEMM shape.
+
+    mode "gather": activations [T, K] in token order, each token quantised
+    once and written to its top-k route positions; output [R, N] in route
+    order.  mode "combine": activations [R, K] already in route order;
+    output [T, N] = sum of the token's routes weighted by topk_weights.
+    """
+
+    def __init__(self, w: ExpertWeights, T: int, topk: int, mode: str, device="cuda",
+                 routing_from: "GroupedPlan" = None):
+        assert mode in ("gather", "combine")
+        self.w, self.T, self.topk, self.mode = w, T, topk, mode
+        E, N, K = w.E, w.N, w.K
+        R = T * topk
+        self.R = R
+        dev = torch.device(device)
+        i32 = dict(dtype=torch.int32, device=dev)
+        if routing_from is not None:       # share one routing between two projections
+            assert routing_from.T == T and routing_from.topk == topk and routing_from.w.E == E
+            self.expert_offsets = routing_from.expert_offsets
+            self.route_token = routing_from.route_token
+            self.route_slot = routing_from.route_slot
+            self.route_pos = routing_from.route_pos
+        else:
+            self.expert_offsets = torch.empty(E + 1, **i32)
+            self.route_token = torch.empty(max(R, 1), **i32)
+            self.route_slot = torch.empty(max(R, 1), **i32)
+            self.route_pos = torch.empty(max(R, 1), **i32)
+        self.a_packed = torch.empty((max(R, 1), K // 2), dtype=torch.uint8, device=dev)
+        self.a_sf = torch.empty(max(F.nvfp4_grouped_scales_bytes(R, E, K), 16),
+                                dtype=torch.uint8, device=dev)
+        self.a_g = torch.empty(1, dtype=torch.float32, device=dev)
+        if mode == "gather":
+            self.out = torch.empty((max(R, 1), N), dtype=torch.bfloat16, device=dev)
+            self.workspace = None
+        else:
+            self.out = torch.empty((max(T, 1), N), dtype=torch.bfloat16, device=dev)
+            self.workspace = torch.empty(max(F.nvfp4_combine_workspace_bytes(T, N) // 4, 4),
+                                         dtype=torch.float32, device=dev)
+
+    def route(self, topk_ids, stream=None):
+        F.nvfp4_moe_route(topk_ids, self.w.E, self.expert_offsets, self.route_token,
+                          self.route_slot, self.route_pos, stream)
+
+    def quantize(self, x, stream=None):
+        if self.mode == "gather":
+            F.nvfp4_quantize_dispatch(x, self.route_pos, self.topk, self.expert_offsets,
+                                      self.w.E, self.R, self.a_packed, self.a_sf, self.a_g,
+                                      0, stream)
+        else:
+            F.nvfp4_quantize_dispatch(x, None, 1, self.expert_offsets, self.w.E, self.R,
+                                      self.a_packed, self.a_sf, self.a_g, 0, stream)
+
+    def gemm(self, topk_weights=None, stream=None):
+        w = self.w
+        F.nvfp4_grouped_gemm(self.a_packed, self.a_sf, self.a_g, w.packed, w.sf_atoms, w.g,
+                             self.expert_offsets, w.E, self.T, self.topk, w.N, w.K,
+                             self.route_token, self.route_slot,
+                             topk_weights if self.mode == "combine" else None,
+                             self.out, self.workspace, stream)
+
+    def run(self, x, topk_ids=None, topk_weights=None, stream=None, route=True):
+        """route (optional) -> quantise/dispatch -> grouped GEMM (-> combine)."""
+        if route:
+            self.route(topk_ids, stream)
+        self.quantize(x, stream)
+        self.gemm(topk_weights, stream)
+        return self.out
+
+
+class DecodeLayer:
+    """One MoE pass over a token batch: gate_up (gather) then down (combine).
+
+    The down projection's input is a separate route-ordered BF16 tensor
+    (the SiLU-and-multiply between the two projections is not part of this
+    path), and both projections share one routing.
+    """
+
+    def __init__(self, w_gate_up: ExpertWeights, w_down: ExpertWeights, T: int, topk: int,
+                 device="cuda"):
+        self.gate_up = GroupedPlan(w_gate_up, T, topk, "gather", device)
+        self.down = GroupedPlan(w_down, T, topk, "combine", device, routing_from=self.gate_up)
+
+    def step(self, x, topk_ids, h, topk_weights, stream=None, timing=None):
+        """x [T, K1] BF16, topk_ids [T, k] int32, h [R, K2] BF16 (route order),
+        topk_weights [T, k] FP32 -> (gate_up out [R, N1], down out [T, N2]).
+
+        `timing`, if given, is a pair of (start, end) CUDA-event lists that
+        bracket the two grouped-GEMM calls."""
+        gu, dn = self.gate_up, self.down
+        gu.route(topk_ids, stream)
+        gu.quantize(x, stream)
+        if timing is not None:
+            timing[0][0].record()
+        gu.gemm(None, stream)
+        if timing is not None:
+            timing[0][1].record()
+        dn.quantize(h, stream)
+        if timing is not None:
+            timing[1][0].record()
+        dn.gemm(topk_weights, stream)
+        if timing is not None:
+            timing[1][1].record()
+        return gu.out, dn.out

@@ -1,0 +1,211 @@
+"""Thin Python binding of the C ABI in include/nvfp4.h.
+
+Argument marshalling only: every step runs in the CUDA library.  Functions
+carry the C names; tensors are torch CUDA tensors (torch supplies device
+memory and the current stream).  A missing library or a non-OK status
+raises -- there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+_lib = None
+
+NVFP4_OK = 0
+NVFP4_ERR_INVALID_ARG = 1
+NVFP4_ERR_UNSUPPORTED = 2
+NVFP4_ERR_CUDA = 3
+NVFP4_ERR_TIMEOUT = 4
+NVFP4_ERR_DEVICE_CHECK = 5
+
+NVFP4_SF_ROWMAJOR = 0
+NVFP4_SF_ATOMS = 1
+NVFP4_GLOBAL_GIVEN = 2
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I32 = ctypes.c_int32
+_U32 = ctypes.c_uint32
+_SZ = ctypes.c_size_t
+
+_SIGS = {
+    "nvfp4_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "nvfp4_version": (ctypes.c_int, []),
+    "nvfp4_device_status": (ctypes.c_int, [_P, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]),
+    "nvfp4_set_timeout_ns": (ctypes.c_int, [ctypes.c_uint64]),
+    "nvfp4_atom_scales_bytes": (_SZ, [_I64, _I64]),
+    "nvfp4_quantize": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _P, _U32, _P]),
+    "nvfp4_prepack_weights": (ctypes.c_int, [_P, _I64, _I64, _P, _P]),
+    "nvfp4_gemm": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P]),
+    "nvfp4_moe_route": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _P, _P, _P, _P]),
+    "nvfp4_grouped_scales_bytes": (_SZ, [_I64, _I32, _I64]),
+    "nvfp4_quantize_dispatch": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I32, _P, _I32, _I64,
+                                               _P, _P, _P, _U32, _P]),
+    "nvfp4_combine_workspace_bytes": (_SZ, [_I64, _I64]),
+    "nvfp4_grouped_gemm": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I32, _I64, _I32, _I64,
+                                          _I64, _P, _P, _P, _P, _P, _SZ, _P]),
+}
+
+
+class NVFP4Error(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {nvfp4_status_string(status)} ({status})")
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Loads the in-tree library (building it first if sources are newer)."""
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        if not os.path.exists(path):
+            raise RuntimeError(f"NVFP4 CUDA library missing: {path}")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(lib, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+def _check(fn, st):
+    if st != NVFP4_OK:
+        raise NVFP4Error(fn, st)
+
+
+# ------------------------------------------------------------ C entry points
+
+def nvfp4_status_string(status: int) -> str:
+    return load().nvfp4_status_string(int(status)).decode()
+
+
+def nvfp4_version() -> int:
+    return load().nvfp4_version()
+
+
+def nvfp4_device_status(reset: bool = True, stream=None) -> int:
+    out = ctypes.c_int(0)
+    _check("nvfp4_device_status",
+           load().nvfp4_device_status(_stream(stream), int(reset), ctypes.byref(out)))
+    return out.value
+
+
+def nvfp4_set_timeout_ns(ns: int) -> None:
+    _check("nvfp4_set_timeout_ns", load().nvfp4_set_timeout_ns(int(ns)))
+
+
+def nvfp4_atom_scales_bytes(rows: int, cols: int) -> int:
+    return load().nvfp4_atom_scales_bytes(rows, cols)
+
+
+def nvfp4_grouped_scales_bytes(R: int, E: int, K: int) -> int:
+    return load().nvfp4_grouped_scales_bytes(R, E, K)
+
+
+def nvfp4_combine_workspace_bytes(T: int, N: int) -> int:
+    return load().nvfp4_combine_workspace_bytes(T, N)
+
+
+def nvfp4_quantize(x, packed, scales, global_scale, flags: int = 0, stream=None) -> None:
+    rows, cols = x.shape
+    _check("nvfp4_quantize", load().nvfp4_quantize(
+        _ptr(x), rows, cols, x.stride(0), _ptr(packed), _ptr(scales), _ptr(global_scale),
+        flags, _stream(stream)))
+
+
+def nvfp4_prepack_weights(scales_rowmajor, scales_atoms, stream=None) -> None:
+    rows, kblk = scales_rowmajor.shape
+    _check("nvfp4_prepack_weights", load().nvfp4_prepack_weights(
+        _ptr(scales_rowmajor), rows, kblk, _ptr(scales_atoms), _stream(stream)))
+
+
+def nvfp4_gemm(A, sfA, gA, B, sfB, gB, C, K: int, stream=None) -> None:
+    M, N = C.shape
+    _check("nvfp4_gemm", load().nvfp4_gemm(
+        _ptr(A), _ptr(sfA), _ptr(gA), _ptr(B), _ptr(sfB), _ptr(gB), _ptr(C), M, N, K,
+        C.stride(0), _stream(stream)))
+
+
+def nvfp4_moe_route(topk_ids, E: int, expert_offsets, route_token, route_slot, route_pos=None,
+                    stream=None) -> None:
+    T, topk = topk_ids.shape
+    _check("nvfp4_moe_route", load().nvfp4_moe_route(
+        _ptr(topk_ids), T, topk, E, _ptr(expert_offsets), _ptr(route_token), _ptr(route_slot),
+        _ptr(route_pos), _stream(stream)))
+
+
+def nvfp4_quantize_dispatch(x, route_pos, fanout: int, expert_offsets, E: int, R: int, packed,
+                            scales, global_scale, flags: int = 0, stream=None) -> None:
+    rows, K = x.shape
+    _check("nvfp4_quantize_dispatch", load().nvfp4_quantize_dispatch(
+        _ptr(x), rows, K, x.stride(0), _ptr(route_pos), fanout, _ptr(expert_offsets), E, R,
+        _ptr(packed), _ptr(scales), _ptr(global_scale), flags, _stream(stream)))
+
+
+def nvfp4_grouped_gemm(A, sfA, gA, W, sfW, gW, expert_offsets, E: int, T: int, topk: int,
+                       N: int, K: int, route_token, route_slot, topk_weights, out, workspace,
+                       stream=None) -> None:
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("nvfp4_grouped_gemm", load().nvfp4_grouped_gemm(
+        _ptr(A), _ptr(sfA), _ptr(gA), _ptr(W), _ptr(sfW), _ptr(gW), _ptr(expert_offsets), E,
+        T, topk, N, K, _ptr(route_token), _ptr(route_slot), _ptr(topk_weights), _ptr(out),
+        _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+# ------------------------------------------- allocating conveniences (torch)
+
+def quantize(x, atoms: bool = False, global_scale=None, stream=None):
+    """BF16 [rows, cols] -> (packed, scales, g) with fresh device outputs."""
+    rows, cols = x.shape
+    dev = x.device
+    packed = torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev)
+    if atoms:
+        scales = torch.empty(nvfp4_atom_scales_bytes(rows, cols), dtype=torch.uint8, device=dev)
+    else:
+        scales = torch.empty((rows, cols // 16), dtype=torch.uint8, device=dev)
+    flags = NVFP4_SF_ATOMS if atoms else 0
+    if global_scale is None:
+        g = torch.empty(1, dtype=torch.float32, device=dev)
+    else:
+        g = global_scale
+        flags |= NVFP4_GLOBAL_GIVEN
+    nvfp4_quantize(x, packed, scales, g, flags, stream)
+    return packed, scales, g
+
+
+def moe_route(topk_ids, E: int, stream=None):
+    """int32 [T, topk] -> (expert_offsets [E+1], route_token, route_slot, route_pos)."""
+    T, k = topk_ids.shape
+    dev = topk_ids.device
+    off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    tok = torch.empty(T * k, dtype=torch.int32, device=dev)
+    slot = torch.empty(T * k, dtype=torch.int32, device=dev)
+    pos = torch.empty(T * k, dtype=torch.int32, device=dev)
+    nvfp4_moe_route(topk_ids, E, off, tok, slot, pos, stream)
+    return off, tok, slot, pos

@@ -1,0 +1,71 @@
+"""The C-ABI library builds, loads without a GPU and exports every entry point
+declared in include/nvfp4.h; host-side validation rejects bad arguments
+before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from moe_grouped_gemm_nvfp4_gb300 import build, nvfp4 as F
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "nvfp4.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(nvfp4_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for want in ("nvfp4_quantize", "nvfp4_prepack_weights", "nvfp4_gemm", "nvfp4_grouped_gemm",
+                 "nvfp4_moe_route", "nvfp4_quantize_dispatch"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol():
+    path = build.build()
+    lib = ctypes.CDLL(path)
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+    # and the Python binding wraps every one of them under the same name
+    for n in _declared():
+        assert hasattr(F, n), n
+
+
+def test_pure_host_helpers():
+    assert F.nvfp4_version() == 100
+    assert F.nvfp4_status_string(4) == "NVFP4_ERR_TIMEOUT"
+    assert F.nvfp4_status_string(99) == "NVFP4_ERR_UNKNOWN"
+    assert F.nvfp4_atom_scales_bytes(300, 512) == 384 * 32
+    assert F.nvfp4_atom_scales_bytes(0, 512) == 0
+    assert F.nvfp4_combine_workspace_bytes(256, 6144) == 256 * 6144 * 4
+    # grouped scales: every non-empty expert can waste at most 127 padded rows
+    assert F.nvfp4_grouped_scales_bytes(2048, 128, 6144) == (2048 + 127 * 128) // 128 * 128 * 384
+    assert F.nvfp4_grouped_scales_bytes(1, 128, 64) == 128 * 4
+
+
+def test_host_validation_without_device():
+    lib = F.load()
+    # null operands / bad sizes return INVALID_ARG before any CUDA call
+    assert lib.nvfp4_gemm(None, None, None, None, None, None, None, 16, 16, 64, 16, None) == 1
+    assert lib.nvfp4_quantize(None, -1, 16, 16, None, None, None, 0, None) == 1
+    assert lib.nvfp4_quantize(None, 4, 16, 16, None, None, None, 0, None) == 1
+    assert lib.nvfp4_moe_route(None, 4, 0, 8, None, None, None, None, None) == 1
+    assert lib.nvfp4_grouped_gemm(*([None] * 7), 8, 4, 2, 128, 128, None, None, None, None,
+                                  None, 0, None) == 1
+    assert lib.nvfp4_set_timeout_ns(0) == 1
+    assert lib.nvfp4_device_status(None, 0, None) == 1
+    # unsupported shapes are refused before any CUDA call too
+    p = ctypes.c_void_p(256)
+    assert lib.nvfp4_gemm(p, p, p, p, p, p, p, 16, 16, 48, 16, None) == 2
+    assert lib.nvfp4_quantize(p, 4, 24, 24, p, p, p, 0, None) == 2
+
+
+def test_binding_raises_without_cuda_tensors():
+    import torch
+    x = torch.zeros((4, 16), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        F.quantize(x)

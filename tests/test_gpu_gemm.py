@@ -1,0 +1,131 @@
+"""Single NVFP4 GEMM on tcgen05 against the FP64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_grouped_gemm_nvfp4_gb300 import inputs
+from moe_grouped_gemm_nvfp4_gb300 import nvfp4 as F
+from parity import bf16_to_np, check_gemm, nan_filled
+
+pytestmark = pytest.mark.gpu
+
+
+def _upload_codes(codes, sf_rm, g):
+    """Operands built in code space (not through the quantiser)."""
+    packed = torch.from_numpy(oracle.pack_codes(codes)).cuda()
+    sf = torch.from_numpy(oracle.prepack_scales(sf_rm)).cuda()
+    gd = torch.tensor([g], dtype=torch.float32, device="cuda")
+    return packed, sf, gd
+
+
+def _run(pa, sa, ga, pb, sb, gb, M, N, K):
+    C = nan_filled((M, N))
+    F.nvfp4_gemm(pa, sa, ga, pb, sb, gb, C, K)
+    torch.cuda.synchronize()
+    assert F.nvfp4_device_status() == F.NVFP4_OK
+    return bf16_to_np(C)
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (16, 128, 64), (16, 256, 512)])
+def test_gemm_unit_scales_code_space(M, N, K):
+    """All scales 1.0 and g = 1: checks operand staging and descriptors alone."""
+    g = inputs.rng(M + N + K)
+    ca = g.integers(0, 16, (M, K)).astype(np.uint8)
+    cb = g.integers(0, 16, (N, K)).astype(np.uint8)
+    one = np.full((M, K // 16), 0x38, np.uint8)
+    oneb = np.full((N, K // 16), 0x38, np.uint8)
+    pa, sa, ga = _upload_codes(ca, one, 1.0)
+    pb, sb, gb = _upload_codes(cb, oneb, 1.0)
+    ref = oracle.E2M1_TABLE[ca] @ oracle.E2M1_TABLE[cb].T
+    got = _run(pa, sa, ga, pb, sb, gb, M, N, K)
+    check_gemm(got, ref, "unit-scale")
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (16, 256, 512)])
+def test_gemm_scale_layout_code_space(M, N, K):
+    """Distinct power-of-two scales per (row, block): checks the scale-factor path."""
+    g = inputs.rng(3 * M + N + K)
+    ca = g.integers(0, 16, (M, K)).astype(np.uint8)
+    cb = g.integers(0, 16, (N, K)).astype(np.uint8)
+    sa = (0x30 + 8 * g.integers(0, 3, (M, K // 16))).astype(np.uint8)   # 2^-1, 2^0, 2^1
+    sb = (0x30 + 8 * g.integers(0, 3, (N, K // 16))).astype(np.uint8)
+    pa, sfa, ga = _upload_codes(ca, sa, 1.0)
+    pb, sfb, gb = _upload_codes(cb, sb, 1.0)
+    ref = oracle.gemm(oracle.pack_codes(ca), sa, 1.0, oracle.pack_codes(cb), sb, 1.0)
+    got = _run(pa, sfa, ga, pb, sfb, gb, M, N, K)
+    check_gemm(got, ref, "scale-layout")
+
+
+def _quantized_case(M, N, K, seed):
+    g = inputs.rng(seed)
+    a = inputs.normal_bf16(g, (M, K))
+    b = inputs.normal_bf16(g, (N, K), 0.02)
+    pa, sa, ga = F.quantize(a.cuda(), atoms=True)
+    pb, sb, gb = F.quantize(b.cuda(), atoms=True)
+    pa_r, sa_r, ga_r = oracle.quantize(a.float().numpy())
+    pb_r, sb_r, gb_r = oracle.quantize(b.float().numpy())
+    ref = oracle.gemm(pa_r, sa_r, ga_r, pb_r, sb_r, gb_r)
+    return (pa, sa, ga, pb, sb, gb), ref
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (16, 256, 512),        # the tiny single-GEMM workload
+    (1, 128, 64), (15, 128, 128), (64, 384, 192), (65, 128, 256),
+    (127, 130, 320), (128, 128, 512), (129, 256, 256), (300, 200, 1024), (512, 384, 2048),
+])
+def test_gemm_matches_oracle(M, N, K):
+    ops, ref = _quantized_case(M, N, K, seed=M * 31 + N * 7 + K)
+    got = _run(*ops, M, N, K)
+    check_gemm(got, ref, f"gemm {M}x{N}x{K}")
+
+
+def test_gemm_tiny_workload_seed0():
+    """16x256x512, seed 0: A ~ N(0,1), B ~ N(0,0.02), the configuration's own recipe."""
+    cfg = inputs.CONFIGS["tiny_gemm"]
+    g = inputs.rng(cfg.seed)
+    a = inputs.normal_bf16(g, (cfg.M, cfg.K))
+    b = inputs.normal_bf16(g, (cfg.N, cfg.K), cfg.sigma_w)
+    pa, sa, ga = F.quantize(a.cuda(), atoms=True)
+    pb, sb, gb = F.quantize(b.cuda(), atoms=True)
+    got = _run(pa, sa, ga, pb, sb, gb, cfg.M, cfg.N, cfg.K)
+    ref = oracle.gemm(*oracle.quantize(a.float().numpy()), *oracle.quantize(b.float().numpy()))
+    check_gemm(got, ref, "tiny")
+
+
+def test_gemm_rejects_bad_shapes():
+    z = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    gf = torch.ones(1, dtype=torch.float32, device="cuda")
+    C = torch.empty((4, 8), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(F.NVFP4Error) as ei:
+        F.nvfp4_gemm(z, z, gf, z, z, gf, C, 48)        # K % 64 != 0
+    assert ei.value.status == F.NVFP4_ERR_UNSUPPORTED
+
+
+@pytest.mark.slow
+def test_gemm_8192_cubed_sampled():
+    """M = N = K = 8192 in the launch configuration the benchmark times;
+    checked on sampled rows and columns computed one by one by the oracle."""
+    M = N = K = 8192
+    seed = inputs.CONFIGS["dense_8192"].seed
+    a = inputs.device_normal_bf16((M, K), 1.0, seed, "cuda")
+    b = inputs.device_normal_bf16((N, K), 0.02, seed + 1000, "cuda")
+    pa, sa, ga = F.quantize(a, atoms=True)
+    pb, sb, gb = F.quantize(b, atoms=True)
+    C = nan_filled((M, N))
+    F.nvfp4_gemm(pa, sa, ga, pb, sb, gb, C, K)
+    torch.cuda.synchronize()
+    assert F.nvfp4_device_status() == F.NVFP4_OK
+    assert not torch.isnan(C).any().item()
+    g = inputs.rng(77)
+    rows = np.sort(g.choice(M, 24, replace=False))
+    cols = np.sort(g.choice(N, 256, replace=False))
+    a_h = a.float().cpu().numpy()
+    b_h = b.float().cpu().numpy()
+    ga_r = oracle.global_scale(a_h)
+    gb_r = oracle.global_scale(b_h)
+    pa_r, sa_r, _ = oracle.quantize(a_h[rows], g=ga_r)
+    pb_r, sb_r, _ = oracle.quantize(b_h[cols], g=gb_r)
+    ref = oracle.gemm(pa_r, sa_r, ga_r, pb_r, sb_r, gb_r)
+    got = bf16_to_np(C[torch.from_numpy(rows).cuda()][:, torch.from_numpy(cols).cuda()])
+    check_gemm(got, ref, "8192^3 sampled")

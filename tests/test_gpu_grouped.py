@@ -1,0 +1,93 @@
+"""MoE grouped GEMM (gather and weighted combine) against the FP64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_grouped_gemm_nvfp4_gb300 import inputs, moe
+from moe_grouped_gemm_nvfp4_gb300 import nvfp4 as F
+from parity import bf16_to_np, check_gemm, nan_filled
+
+pytestmark = pytest.mark.gpu
+
+
+def _weights_host(g, E, N, K):
+    return inputs.normal_bf16(g, (E, N, K), 0.02)
+
+
+def _oracle_weights(w_bf16):
+    """Per-expert quantisation in the oracle -> float64 [E, N, K]."""
+    E = w_bf16.shape[0]
+    out = []
+    for e in range(E):
+        p, s, gg = oracle.quantize(w_bf16[e].float().numpy())
+        out.append(oracle.dequantize(p, s, gg))
+    return np.stack(out)
+
+
+def _routing(g, T, E, k, kind):
+    if kind == "zipf":
+        return inputs.zipf_topk(g, T, E, k, n_unused=max(1, E // 16))
+    ids = inputs.uniform_topk(g, T, E, k)
+    return ids
+
+
+@pytest.mark.parametrize("T,E,k,N,K,kind", [
+    (32, 8, 2, 256, 512, "uniform"),
+    (5, 16, 2, 128, 192, "uniform"),      # most experts empty, partial K block
+    (200, 4, 2, 128, 256, "uniform"),     # experts with > 128 routes (several token tiles)
+    (300, 16, 4, 256, 512, "zipf"),       # skewed with empty experts
+])
+def test_grouped_gather_matches_oracle(T, E, k, N, K, kind):
+    g = inputs.rng(T * 13 + E + N + K)
+    x = inputs.normal_bf16(g, (T, K))
+    w = _weights_host(g, E, N, K)
+    ids = _routing(g, T, E, k, kind)
+    W = moe.quantize_experts(w.cuda())
+    plan = moe.GroupedPlan(W, T, k, "gather")
+    plan.out.view(torch.int16).fill_(0x7FC0)
+    out = plan.run(x.cuda(), torch.from_numpy(ids).cuda())
+    torch.cuda.synchronize()
+    assert F.nvfp4_device_status() == F.NVFP4_OK
+    off, tok, slot = oracle.route(ids, E)
+    px, sx, gx = oracle.quantize(x.float().numpy())
+    xh = oracle.dequantize(px, sx, gx)[tok]
+    ref = oracle.grouped_gemm(xh, _oracle_weights(w), off)
+    check_gemm(bf16_to_np(out[: T * k]), ref, "grouped gather")
+
+
+@pytest.mark.parametrize("T,E,k,N,K", [(32, 8, 2, 256, 512), (64, 16, 8, 384, 256),
+                                       (3, 8, 2, 128, 128)])
+def test_grouped_combine_matches_oracle(T, E, k, N, K):
+    g = inputs.rng(T * 17 + E + N + K)
+    ids = inputs.uniform_topk(g, T, E, k)
+    wts = inputs.dirichlet_weights(g, T, k)
+    R = T * k
+    h = inputs.normal_bf16(g, (R, K))          # route-ordered intermediate
+    w = _weights_host(g, E, N, K)
+    W = moe.quantize_experts(w.cuda())
+    plan = moe.GroupedPlan(W, T, k, "combine")
+    plan.out.view(torch.int16).fill_(0x7FC0)
+    out = plan.run(h.cuda(), torch.from_numpy(ids).cuda(), torch.from_numpy(wts).cuda())
+    torch.cuda.synchronize()
+    assert F.nvfp4_device_status() == F.NVFP4_OK
+    off, tok, slot = oracle.route(ids, E)
+    ph, sh, gh = oracle.quantize(h.float().numpy())
+    y = oracle.grouped_gemm(oracle.dequantize(ph, sh, gh), _oracle_weights(w), off)
+    ref = oracle.combine(y, tok, slot, wts, T)
+    check_gemm(bf16_to_np(out[:T]), ref, "grouped combine")
+
+
+def test_grouped_rejects_non_monotone_offsets_on_device():
+    E, N, K, T, k = 4, 128, 128, 4, 1
+    g = inputs.rng(1)
+    W = moe.quantize_experts(_weights_host(g, E, N, K).cuda())
+    plan = moe.GroupedPlan(W, T, k, "gather")
+    x = inputs.normal_bf16(g, (T, K)).cuda()
+    plan.route(torch.zeros((T, k), dtype=torch.int32, device="cuda"))
+    plan.quantize(x)
+    torch.cuda.synchronize()
+    F.nvfp4_device_status(reset=True)
+    plan.expert_offsets.copy_(torch.tensor([0, 3, 1, 4, 4], dtype=torch.int32))
+    plan.gemm()
+    assert F.nvfp4_device_status(reset=True) == F.NVFP4_ERR_DEVICE_CHECK

@@ -38,10 +38,15 @@ from moe_grouped_gemm_nvfp4_gb300 import nvfp4 as F  # noqa: E402
 
 METRIC = "NVFP4 grouped-GEMM TFLOPS & HBM GB/s (frac. of roofline) at 16-64 tok/expert"
 UNIT = "TFLOPS"
-E, TOPK, T = 128, 8, 256
+E, TOPK, T = 128, 8, 256    # T = 2 * E keeps 16 routes per expert (see --experts)
 K1, N1 = 6144, 4096        # gate_up
 K2, N2 = 2048, 6144        # down
 FALLBACK_HBM_GBS = 6800.0
+
+
+def _set_experts(n):
+    global E, T
+    E, T = n, 2 * n
 
 
 def workload_config():
@@ -51,7 +56,8 @@ def workload_config():
         "global_batch": T,
         "weights": "NVFP4 E2M1 + E4M3/16 + FP32 per expert, ~N(0,0.02) before quantisation",
         "activations": "BF16 ~N(0,1), quantised on the fly each step",
-        "l2": "inputs larger than L2 (2.72 GB of expert weights streamed per step)",
+        "l2": f"inputs larger than L2 ({E * (N1 * K1 + N2 * K2) * 0.5625 / 1e9:.2f} GB of "
+              f"expert weights streamed per step)",
         "parallelism": "replicas",
     }
 
@@ -212,11 +218,13 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("timed")
     start.record()
     for i in range(args.steps):
         step(timing=ev[i])
     end.record()
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
@@ -405,7 +413,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--experts", type=int, default=E,
+                    help="experts (tokens scale as 2 per expert); smaller values give the "
+                         "small profiling case of the same kernels")
     args = ap.parse_args()
+    _set_experts(args.experts)
     if args.warmup < 3:
         args.warmup = 3
     world = int(os.environ.get("WORLD_SIZE", "1"))

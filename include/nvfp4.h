@@ -108,9 +108,10 @@ nvfp4_status nvfp4_prepack_weights(const uint8_t* scales_rowmajor, int64_t rows,
  * BF16 round-to-nearest-even output.
  *   A  packed [M, K/2], sfA atom layout for [M, K];
  *   B  packed [N, K/2], sfB atom layout for [N, K];
- *   K % 64 == 0, M, N >= 1, ldc >= N, ldc % 8 == 0, all pointers 16-byte
- *   aligned.  Small M runs with the operands swapped (weights on the MMA's
- *   M side); the result is the same.
+ *   K % 64 == 0, M, N >= 1, ldc >= N; A, B, sfA, sfB 16-byte aligned, C
+ *   2-byte aligned (rows that are 16-byte aligned get vector stores).  Small
+ *   M runs with the operands swapped (weights on the MMA's M side); the
+ *   result is the same.
  */
 nvfp4_status nvfp4_gemm(const uint8_t* A, const uint8_t* sfA, const float* gA,
                         const uint8_t* B, const uint8_t* sfB, const float* gB,

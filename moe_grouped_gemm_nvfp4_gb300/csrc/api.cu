@@ -207,9 +207,10 @@ nvfp4_status nvfp4_gemm(const uint8_t* A, const uint8_t* sfA, const float* gA,
                         void* C, int64_t M, int64_t N, int64_t K, int64_t ldc, void* stream) {
   if (!A || !sfA || !gA || !B || !sfB || !gB || !C) return NVFP4_ERR_INVALID_ARG;
   if (M <= 0 || N <= 0 || K <= 0 || ldc < N) return NVFP4_ERR_INVALID_ARG;
-  if (K % 64 != 0 || ldc % 8 != 0) return NVFP4_ERR_UNSUPPORTED;
+  if (K % 64 != 0) return NVFP4_ERR_UNSUPPORTED;
   if (M > (1LL << 30) || N > (1LL << 30) || K > (1LL << 31)) return NVFP4_ERR_UNSUPPORTED;
-  if (!aligned16(A) || !aligned16(B) || !aligned16(sfA) || !aligned16(sfB) || !aligned16(C))
+  if (!aligned16(A) || !aligned16(B) || !aligned16(sfA) || !aligned16(sfB) ||
+      (reinterpret_cast<uintptr_t>(C) & 1u))
     return NVFP4_ERR_UNSUPPORTED;
   DeviceState* d = nullptr;
   nvfp4_status st = device_state(&d);
@@ -234,6 +235,7 @@ nvfp4_status nvfp4_gemm(const uint8_t* A, const uint8_t* sfA, const float* gA,
   a.rows_y = static_cast<int32_t>(rows_y);
   a.out = C;
   a.ldc = ldc;
+  a.vec_store = (ldc % 8 == 0 && aligned16(C)) ? 1 : 0;
   a.status = d->status;
   a.timeout_ns = g_timeout_ns.load();
   if (nvfp4::launch_gemm(tmx, tmy, a, swap ? nvfp4::kDenseRowsY : nvfp4::kDenseRowsX, d->sms,

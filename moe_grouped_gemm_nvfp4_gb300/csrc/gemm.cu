@@ -320,7 +320,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
           if (xr < a.rows_x) {
             uint16_t* dst = reinterpret_cast<uint16_t*>(a.out) + static_cast<int64_t>(xr) * a.ldc +
                             un.y_row0 + c0;
-            if (nc == 32) {
+            if (nc == 32 && a.vec_store) {
 #pragma unroll
               for (int v = 0; v < 4; ++v) {
                 uint32_t w[4];

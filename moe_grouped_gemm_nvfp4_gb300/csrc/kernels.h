@@ -49,6 +49,7 @@ struct GemmArgs {
   int32_t n_out;                   // grouped: rows of each expert's W
   void* out;                       // BF16
   int64_t ldc;
+  int32_t vec_store;               // rows of C are 16-byte aligned (ldc % 8 == 0)
   const int32_t* route_token;      // combine
   const int32_t* route_slot;
   const float* topk_w;

@@ -405,12 +405,112 @@ def run_reference(args, rank, world):
     }
 
 
+# ------------------------------------------------------ per-configuration table
+
+def _timed(fn, iters, flush):
+    """Mean device time of fn over `iters` runs, L2 flushed before each run."""
+    fn()
+    torch.cuda.synchronize()
+    total = 0.0
+    for _ in range(iters):
+        flush.zero_()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        fn()
+        e.record()
+        torch.cuda.synchronize()
+        total += s.elapsed_time(e)
+    return total / iters
+
+
+def run_configs(args):
+    """One JSON line per workload configuration: kernel time with CUDA events,
+    L2 flushed (256 MB write) before every timed call."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    peak, peak_kind = measured_peaks()
+    bf16_tflops = None
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            bf16_tflops = json.load(f).get("bf16_tflops")
+    fp4_peak = (bf16_tflops or 1900.0) * 6.0      # nominal dense FP4 / BF16 ratio 13.5 / 2.25
+    iters = max(3, min(args.steps, 20))
+    lines = []
+
+    # dense 8192^3: A quantised every call, B prepared offline
+    M = Nn = Kk = 8192
+    a = inputs.device_normal_bf16((M, Kk), 1.0, 1, dev)
+    b = inputs.device_normal_bf16((Nn, Kk), 0.02, 1001, dev)
+    pb, sb, gb = F.quantize(b, atoms=True)
+    pa, sa, ga = F.quantize(a, atoms=True)
+    C = torch.empty((M, Nn), dtype=torch.bfloat16, device=dev)
+    t_gemm = _timed(lambda: F.nvfp4_gemm(pa, sa, ga, pb, sb, gb, C, Kk), iters, flush)
+    t_q = _timed(lambda: F.nvfp4_quantize(a, pa, sa, ga, F.NVFP4_SF_ATOMS), iters, flush)
+    fl = 2.0 * M * Nn * Kk
+    lines.append({"workload": "dense_gemm_8192^3", "gemm_ms": round(t_gemm, 4),
+                  "tflops": round(fl / t_gemm / 1e9, 1),
+                  "frac_of_fp4_peak": round(fl / t_gemm / 1e9 / fp4_peak, 4),
+                  "fp4_peak_tflops": fp4_peak, "quantize_A_ms": round(t_q, 4),
+                  "quantize_A_gbs": round(M * Kk * 2.5625 / t_q / 1e6, 1)})
+    del a, b, pa, sa, pb, sb, C
+
+    # decode down-projection sweep and skewed prefill gate_up
+    for name in ("decode_gate_up", "decode_down_256", "decode_down_512", "decode_down_1024",
+                 "prefill_skewed"):
+        cfg = inputs.CONFIGS[name]
+        g = inputs.rng(cfg.seed)
+        w = torch.empty((cfg.E, cfg.N, cfg.K), dtype=torch.bfloat16, device=dev)
+        for e in range(cfg.E):
+            w[e] = inputs.device_normal_bf16((cfg.N, cfg.K), 0.02, cfg.seed * 100003 + e, dev)
+        W = moe.quantize_experts(w)
+        del w
+        if cfg.kind == "down":
+            ids = inputs.uniform_topk(g, cfg.T, cfg.E, cfg.topk)
+            wts = torch.from_numpy(inputs.dirichlet_weights(g, cfg.T, cfg.topk)).to(dev)
+            xin = inputs.normal_bf16(g, (cfg.T * cfg.topk, cfg.K)).to(dev)
+            plan = moe.GroupedPlan(W, cfg.T, cfg.topk, "combine", dev)
+        else:
+            xf = g.standard_normal((cfg.T, cfg.K), dtype=np.float32)
+            if cfg.outliers:
+                xf = inputs.add_outliers(g, xf)
+            xin = inputs.to_bf16(xf).to(dev)
+            ids = (inputs.zipf_topk(g, cfg.T, cfg.E, cfg.topk) if cfg.routing == "zipf"
+                   else inputs.uniform_topk(g, cfg.T, cfg.E, cfg.topk))
+            wts = None
+            plan = moe.GroupedPlan(W, cfg.T, cfg.topk, "gather", dev)
+        ids_d = torch.from_numpy(ids).to(dev)
+        plan.route(ids_d)
+        plan.quantize(xin)
+        t_gemm = _timed(lambda: plan.gemm(wts), iters, flush)
+        t_all = _timed(lambda: plan.run(xin, ids_d, wts), iters, flush)
+        counts = np.bincount(ids.reshape(-1), minlength=cfg.E)
+        n_act = int(np.count_nonzero(counts))
+        R = cfg.T * cfg.topk
+        fl = 2.0 * R * cfg.N * cfg.K
+        byt = gemm_bytes(cfg.K, cfg.N, n_act, R, cfg.T if cfg.kind == "down" else R)
+        lines.append({"workload": name, "tokens_per_expert": [int(counts.min()), int(counts.max())],
+                      "active_experts": n_act, "gemm_ms": round(t_gemm, 4),
+                      "tflops": round(fl / t_gemm / 1e9, 1), "gbs": round(byt / t_gemm / 1e6, 1),
+                      "frac_of_hbm_roofline": round(byt / t_gemm / 1e6 / peak, 4),
+                      "frac_of_fp4_peak": round(fl / t_gemm / 1e9 / fp4_peak, 4),
+                      "pass_ms_route_quantize_gemm": round(t_all, 4),
+                      "peak_source": f"{peak_kind} hbm_gbs; fp4 = bf16_tflops x 6"})
+        del W, plan
+        torch.cuda.empty_cache()
+    for ln in lines:
+        print(json.dumps(ln), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode_layer", choices=["decode_layer", "configs"],
+                    help="configs: one line per workload configuration (not the headline)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--experts", type=int, default=E,
@@ -426,6 +526,9 @@ def main():
     if world > 1 and args.impl == "ours":
         torch.distributed.init_process_group(
             "nccl", device_id=torch.device("cuda", local_rank))
+    if args.workload == "configs":
+        run_configs(args)
+        return
     if args.impl == "reference":
         line = run_reference(args, rank, world)
     else:

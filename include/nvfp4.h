@@ -136,32 +136,66 @@ nvfp4_status nvfp4_moe_route(const int32_t* topk_ids, int64_t T, int32_t topk, i
                              int32_t* route_slot, int32_t* route_pos, void* stream);
 
 /*
- * Upper bound on the bytes of the grouped scale layout for R routes over E
- * experts and K: every expert's routes start a fresh 128-row atom tile.
+ * Operand tiles: the layout the grouped GEMM copies one pipeline stage from.
+ * A tile covers 128 rows x 256 K elements and is 18432 bytes: 16384 bytes of
+ * packed codes, row r at r * 128 with its 16-byte chunk j stored at chunk
+ * position j ^ (r % 8) (the tensor cores' 128-byte shared-memory swizzle),
+ * then 2048 bytes of scales as four atoms (one per 64 K elements, atom
+ * layout as above).  Tiles are ordered row-tile major, then K block.  Rows
+ * are padded to a multiple of 128 and K to a multiple of 256.
  */
-size_t nvfp4_grouped_scales_bytes(int64_t R, int32_t E, int64_t K);
+size_t nvfp4_operand_tiles_bytes(int64_t rows, int64_t K);
 
 /*
- * Quantise activations straight into route order for the grouped GEMM.
- *   x           BF16 [rows, K], row stride ld.
+ * Offline weight prepack: packed codes [rows, K/2] and row-major scales
+ * [rows, K/16] (as written by nvfp4_quantize) -> operand tiles
+ * (nvfp4_operand_tiles_bytes(rows, K) bytes, padding zero).  For expert
+ * weights [E, N, K] pass rows = E * N with N % 128 == 0, so that every tile
+ * belongs to one expert.  K % 64 == 0; packed and tiles 16-byte aligned.
+ */
+nvfp4_status nvfp4_prepack_weight_tiles(const uint8_t* packed, const uint8_t* scales_rowmajor,
+                                        int64_t rows, int64_t K, uint8_t* tiles, void* stream);
+
+/*
+ * Chunk width (32, 64 or 128 routes) of the grouped activation tiles for R
+ * routes over E experts: about 1.6x the mean routes per expert, rounded up to
+ * the next width.  It is also the grouped GEMM's token-tile width, so that
+ * narrow decode tiles leave shared memory for a deeper pipeline.
+ */
+int nvfp4_grouped_chunk_rows(int64_t R, int32_t E);
+
+/*
+ * Upper bound on the bytes of the grouped activation tiles for R routes over
+ * E experts: every expert's routes are cut into chunks of
+ * nvfp4_grouped_chunk_rows(R, E) rows and each chunk fills its own tile.
+ */
+size_t nvfp4_grouped_tiles_bytes(int64_t R, int32_t E, int64_t K);
+
+/*
+ * Quantise activations straight into route order for the grouped GEMM
+ * ("The FP4 Frontier", Finding 5: grouped GEMM, token counts padded for TMA).
+ *   x           BF16 [rows, K], row stride ld (elements), 16-byte aligned.
  *   route_pos   int32 [rows * fanout]: destination route of source row i,
  *               copy j is route_pos[i * fanout + j] (the route_pos output of
- *               nvfp4_moe_route with fanout = topk).  NULL means the rows are
- *               already in route order (rows == R, fanout == 1).
+ *               nvfp4_moe_route with fanout = topk); negative = dropped.
+ *               NULL means the rows are already in route order (rows == R,
+ *               fanout == 1).
  *   expert_offsets  int32 [E+1] (device), as from nvfp4_moe_route.
- *   packed      uint8 [R, K/2] out, route order.
- *   scales      grouped atom layout out, nvfp4_grouped_scales_bytes(R, E, K)
- *               bytes: route p of expert e is padded row 128 * tb[e] +
- *               (p - expert_offsets[e]), tb[e] = sum over e' < e of
- *               ceil(count_e' / 128).
+ *   tiles       operand tiles out (nvfp4_grouped_tiles_bytes(R, E, K) bytes):
+ *               with c = nvfp4_grouped_chunk_rows(R, E), route p of expert e,
+ *               j = p - expert_offsets[e], is row j % c of tile
+ *               tb[e] + j / c, tb[e] = sum over e' < e of ceil(count_e' / c).
+ *               Rows past a chunk's routes are left unwritten (they only ever
+ *               feed output columns the GEMM does not store).
  *   global_scale  as in nvfp4_quantize (one g over the whole of x).
- * K % 64 == 0, E <= 1024.
+ * K % 64 == 0, E <= 1024.  Offsets that are not monotone or exceed R set
+ * NVFP4_ERR_DEVICE_CHECK and nothing is written.
  */
 nvfp4_status nvfp4_quantize_dispatch(const void* x, int64_t rows, int64_t K, int64_t ld,
                                      const int32_t* route_pos, int32_t fanout,
                                      const int32_t* expert_offsets, int32_t E, int64_t R,
-                                     uint8_t* packed, uint8_t* scales, float* global_scale,
-                                     uint32_t flags, void* stream);
+                                     uint8_t* tiles, float* global_scale, uint32_t flags,
+                                     void* stream);
 
 /* Bytes of the FP32 combine workspace for T tokens and N outputs. */
 size_t nvfp4_combine_workspace_bytes(int64_t T, int64_t N);
@@ -171,21 +205,23 @@ size_t nvfp4_combine_workspace_bytes(int64_t T, int64_t N);
  * small-batch decode is bound by streaming the expert weights).  One
  * persistent launch covers every (expert, 128-row weight tile, token tile)
  * unit; experts without routes are skipped and their weights never read.
- *   A, sfA, gA  route-ordered activations from nvfp4_quantize_dispatch:
- *               packed [R, K/2], grouped atom scales, device float global.
- *   W           packed weights [E, N, K/2]; sfW atom layout over [E*N, K];
- *               gW device float [E], one global per expert.
+ *   A_tiles, gA  route-ordered activation tiles from nvfp4_quantize_dispatch
+ *                and their device float global scale.
+ *   W_tiles      expert weights as operand tiles over [E * N, K]
+ *                (nvfp4_prepack_weight_tiles); gW device float [E], one
+ *                global per expert.
  *   expert_offsets  int32 [E+1] (device), R = T * topk routes.
  *   topk_weights == NULL:  out = BF16 [R, N] in route order,
  *       out[p, n] = gA * gW[e] * sum_k A_hat[p, k] W_hat[e, n, k].
  *   topk_weights != NULL (FP32 [T, topk]):  out = BF16 [T, N],
  *       out[t] = sum over the routes p of t of w[t, slot(p)] * y[p], with
  *       route_token / route_slot from nvfp4_moe_route and an FP32 workspace
- *       of nvfp4_combine_workspace_bytes(T, N) bytes (zeroed here).
- * N % 128 == 0, K % 64 == 0, E <= 1024.
+ *       of nvfp4_combine_workspace_bytes(T, N) bytes (zeroed here).  The FP32
+ *       additions run in no fixed order.
+ * N % 128 == 0, K % 64 == 0, E <= 256; all buffers 16-byte aligned.
  */
-nvfp4_status nvfp4_grouped_gemm(const uint8_t* A, const uint8_t* sfA, const float* gA,
-                                const uint8_t* W, const uint8_t* sfW, const float* gW,
+nvfp4_status nvfp4_grouped_gemm(const uint8_t* A_tiles, const float* gA,
+                                const uint8_t* W_tiles, const float* gW,
                                 const int32_t* expert_offsets, int32_t E,
                                 int64_t T, int32_t topk, int64_t N, int64_t K,
                                 const int32_t* route_token, const int32_t* route_slot,

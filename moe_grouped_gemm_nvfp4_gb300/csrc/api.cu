@@ -144,11 +144,23 @@ size_t nvfp4_atom_scales_bytes(int64_t rows, int64_t cols) {
   return static_cast<size_t>((rows + 127) / 128 * 128) * static_cast<size_t>(cols / 16);
 }
 
-size_t nvfp4_grouped_scales_bytes(int64_t R, int32_t E, int64_t K) {
+size_t nvfp4_operand_tiles_bytes(int64_t rows, int64_t K) {
+  if (rows < 0 || K < 0) return 0;
+  return static_cast<size_t>((rows + 127) / 128) * static_cast<size_t>((K + 255) / 256) *
+         static_cast<size_t>(nvfp4::kOperandTileBytes);
+}
+
+int nvfp4_grouped_chunk_rows(int64_t R, int32_t E) {
+  return nvfp4::grouped_chunk_rows(R < 0 ? 0 : R, E);
+}
+
+size_t nvfp4_grouped_tiles_bytes(int64_t R, int32_t E, int64_t K) {
   if (R < 0 || E < 0 || K < 0) return 0;
+  const int64_t chunk = nvfp4::grouped_chunk_rows(R, E);
   const int64_t nonempty = R < E ? R : E;
-  const int64_t tiles = (R + 127 * nonempty) / 128;
-  return static_cast<size_t>(tiles * 128) * static_cast<size_t>(K / 16);
+  const int64_t tiles = (R + (chunk - 1) * nonempty) / chunk;
+  return static_cast<size_t>(tiles) * static_cast<size_t>((K + 255) / 256) *
+         static_cast<size_t>(nvfp4::kOperandTileBytes);
 }
 
 size_t nvfp4_combine_workspace_bytes(int64_t T, int64_t N) {
@@ -221,9 +233,11 @@ nvfp4_status nvfp4_gemm(const uint8_t* A, const uint8_t* sfA, const float* gA,
   const uint8_t* Y = swap ? A : B;
   const int64_t rows_x = swap ? N : M;
   const int64_t rows_y = swap ? M : N;
+  // Y in one 128-row box per stage when its tiles are full, else 16-row boxes
+  const uint32_t ybox_rows = rows_y >= 128 ? 128u : 16u;
   CUtensorMap tmx, tmy;
   if (make_operand_map(&tmx, X, rows_x, K / 2, 128) != NVFP4_OK ||
-      make_operand_map(&tmy, Y, rows_y, K / 2, 16) != NVFP4_OK)
+      make_operand_map(&tmy, Y, rows_y, K / 2, ybox_rows) != NVFP4_OK)
     return NVFP4_ERR_UNSUPPORTED;
   nvfp4::GemmArgs a{};
   a.sfx = swap ? sfB : sfA;
@@ -236,6 +250,7 @@ nvfp4_status nvfp4_gemm(const uint8_t* A, const uint8_t* sfA, const float* gA,
   a.out = C;
   a.ldc = ldc;
   a.vec_store = (ldc % 8 == 0 && aligned16(C)) ? 1 : 0;
+  a.ybox_rows = static_cast<int32_t>(ybox_rows);
   a.status = d->status;
   a.timeout_ns = g_timeout_ns.load();
   if (nvfp4::launch_gemm(tmx, tmy, a, swap ? nvfp4::kDenseRowsY : nvfp4::kDenseRowsX, d->sms,
@@ -259,19 +274,35 @@ nvfp4_status nvfp4_moe_route(const int32_t* topk_ids, int64_t T, int32_t topk, i
   return NVFP4_OK;
 }
 
+nvfp4_status nvfp4_prepack_weight_tiles(const uint8_t* packed, const uint8_t* scales_rowmajor,
+                                        int64_t rows, int64_t K, uint8_t* tiles, void* stream) {
+  if (rows < 0 || K < 0) return NVFP4_ERR_INVALID_ARG;
+  if (rows > 0 && K > 0 && (!packed || !scales_rowmajor || !tiles)) return NVFP4_ERR_INVALID_ARG;
+  if (K % 64 != 0) return NVFP4_ERR_UNSUPPORTED;
+  if ((packed && !aligned16(packed)) || (tiles && !aligned16(tiles)) ||
+      (scales_rowmajor && (reinterpret_cast<uintptr_t>(scales_rowmajor) & 3u)))
+    return NVFP4_ERR_UNSUPPORTED;
+  DeviceState* d = nullptr;
+  nvfp4_status st = device_state(&d);
+  if (st != NVFP4_OK) return st;
+  if (nvfp4::launch_prepack_tiles(packed, scales_rowmajor, rows, K, tiles, d->sms,
+                                  static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return cuda_fail();
+  return NVFP4_OK;
+}
+
 nvfp4_status nvfp4_quantize_dispatch(const void* x, int64_t rows, int64_t K, int64_t ld,
                                      const int32_t* route_pos, int32_t fanout,
                                      const int32_t* expert_offsets, int32_t E, int64_t R,
-                                     uint8_t* packed, uint8_t* scales, float* global_scale,
-                                     uint32_t flags, void* stream) {
+                                     uint8_t* tiles, float* global_scale, uint32_t flags,
+                                     void* stream) {
   if (rows < 0 || K <= 0 || ld < K || E <= 0 || R < 0 || fanout <= 0) return NVFP4_ERR_INVALID_ARG;
   if (flags & ~static_cast<uint32_t>(NVFP4_GLOBAL_GIVEN)) return NVFP4_ERR_INVALID_ARG;
-  if (!expert_offsets || !global_scale || (rows > 0 && (!x || !packed || !scales)))
+  if (!expert_offsets || !global_scale || (rows > 0 && (!x || !tiles)))
     return NVFP4_ERR_INVALID_ARG;
   if (!route_pos && (fanout != 1 || rows != R)) return NVFP4_ERR_INVALID_ARG;
   if (K % 64 != 0 || ld % 8 != 0 || E > 1024) return NVFP4_ERR_UNSUPPORTED;
-  if ((x && !aligned16(x)) || (packed && (reinterpret_cast<uintptr_t>(packed) & 7u)))
-    return NVFP4_ERR_UNSUPPORTED;
+  if ((x && !aligned16(x)) || (tiles && !aligned16(tiles))) return NVFP4_ERR_UNSUPPORTED;
   DeviceState* d = nullptr;
   nvfp4_status st = device_state(&d);
   if (st != NVFP4_OK) return st;
@@ -282,22 +313,21 @@ nvfp4_status nvfp4_quantize_dispatch(const void* x, int64_t rows, int64_t K, int
       return cuda_fail();
   }
   if (nvfp4::launch_quantize_dispatch(xb, rows, K, ld, route_pos, fanout, expert_offsets, E, R,
-                                      packed, scales, global_scale, d->status, d->sms, s) !=
-      cudaSuccess)
+                                      nvfp4::grouped_chunk_rows(R, E), tiles, global_scale,
+                                      d->status, d->sms, s) != cudaSuccess)
     return cuda_fail();
   return NVFP4_OK;
 }
 
-nvfp4_status nvfp4_grouped_gemm(const uint8_t* A, const uint8_t* sfA, const float* gA,
-                                const uint8_t* W, const uint8_t* sfW, const float* gW,
+nvfp4_status nvfp4_grouped_gemm(const uint8_t* A_tiles, const float* gA,
+                                const uint8_t* W_tiles, const float* gW,
                                 const int32_t* expert_offsets, int32_t E,
                                 int64_t T, int32_t topk, int64_t N, int64_t K,
                                 const int32_t* route_token, const int32_t* route_slot,
                                 const float* topk_weights,
                                 void* out, float* workspace, size_t workspace_bytes,
                                 void* stream) {
-  if (!A || !sfA || !gA || !W || !sfW || !gW || !expert_offsets || !out)
-    return NVFP4_ERR_INVALID_ARG;
+  if (!A_tiles || !gA || !W_tiles || !gW || !expert_offsets || !out) return NVFP4_ERR_INVALID_ARG;
   if (E <= 0 || T < 0 || topk <= 0 || N <= 0 || K <= 0) return NVFP4_ERR_INVALID_ARG;
   const bool combine = topk_weights != nullptr;
   if (combine && (!route_token || !route_slot || !workspace)) return NVFP4_ERR_INVALID_ARG;
@@ -305,7 +335,7 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* A, const uint8_t* sfA, const floa
   const int64_t R = T * topk;
   if (R > (1LL << 30) || static_cast<int64_t>(E) * N > (1LL << 30)) return NVFP4_ERR_UNSUPPORTED;
   if (combine && workspace_bytes < nvfp4_combine_workspace_bytes(T, N)) return NVFP4_ERR_UNSUPPORTED;
-  if (!aligned16(A) || !aligned16(sfA) || !aligned16(W) || !aligned16(sfW) || !aligned16(out) ||
+  if (!aligned16(A_tiles) || !aligned16(W_tiles) || !aligned16(out) ||
       (combine && !aligned16(workspace)))
     return NVFP4_ERR_UNSUPPORTED;
   DeviceState* d = nullptr;
@@ -316,13 +346,11 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* A, const uint8_t* sfA, const floa
     if (combine && T > 0 && cudaMemsetAsync(out, 0, T * N * 2, s) != cudaSuccess) return cuda_fail();
     return NVFP4_OK;
   }
-  CUtensorMap tmx, tmy;
-  if (make_operand_map(&tmx, W, static_cast<uint64_t>(E) * N, K / 2, 128) != NVFP4_OK ||
-      make_operand_map(&tmy, A, R, K / 2, 16) != NVFP4_OK)
-    return NVFP4_ERR_UNSUPPORTED;
+  CUtensorMap unused;                  // the grouped path copies operand tiles, no tensor map
+  std::memset(&unused, 0, sizeof(unused));
   nvfp4::GemmArgs a{};
-  a.sfx = sfW;
-  a.sfy = sfA;
+  a.sfx = W_tiles;
+  a.sfy = A_tiles;
   a.gx = gW;
   a.gy = gA;
   a.K = K;
@@ -333,6 +361,8 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* A, const uint8_t* sfA, const floa
   a.n_out = static_cast<int32_t>(N);
   a.out = out;
   a.ldc = N;
+  a.vec_store = 1;
+  a.ybox_rows = 16;
   a.route_token = route_token;
   a.route_slot = route_slot;
   a.topk_w = topk_weights;
@@ -342,8 +372,8 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* A, const uint8_t* sfA, const floa
   a.timeout_ns = g_timeout_ns.load();
   if (combine && cudaMemsetAsync(workspace, 0, nvfp4_combine_workspace_bytes(T, N), s) != cudaSuccess)
     return cuda_fail();
-  if (nvfp4::launch_gemm(tmx, tmy, a, combine ? nvfp4::kGroupedCombine : nvfp4::kGrouped, d->sms,
-                         s) != cudaSuccess)
+  if (nvfp4::launch_gemm(unused, unused, a, combine ? nvfp4::kGroupedCombine : nvfp4::kGrouped,
+                         d->sms, s) != cudaSuccess)
     return cuda_fail();
   if (combine && nvfp4::launch_combine_finalize(workspace, T, N, out, d->sms, s) != cudaSuccess)
     return cuda_fail();

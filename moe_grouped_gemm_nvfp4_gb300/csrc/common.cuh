@@ -86,6 +86,30 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, CtaCtl*
   return false;
 }
 
+// As mbar_wait, but sleeping between polls.  For waiters off the critical
+// path (the epilogue between accumulators): a warp that spins shares its
+// SM sub-partition's issue slots with the TMA producer or the MMA issuer.
+__device__ __forceinline__ bool mbar_wait_sleepy(uint32_t bar, uint32_t parity, CtaCtl* ctl,
+                                                 int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  uint32_t ns = 32;
+  for (uint32_t i = 1; i < 0x7FFFFFFFu; ++i) {
+    __nanosleep(ns);
+    if (ns < 512) ns <<= 1;
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*reinterpret_cast<volatile uint32_t*>(&ctl->abort)) return false;
+    if (globaltimer() - t0 > ctl->timeout_ns) {
+      *reinterpret_cast<volatile uint32_t*>(&ctl->abort) = 1u;
+      raise_status(status, NVFP4_ERR_TIMEOUT);
+      return false;
+    }
+  }
+  *reinterpret_cast<volatile uint32_t*>(&ctl->abort) = 1u;
+  raise_status(status, NVFP4_ERR_TIMEOUT);
+  return false;
+}
+
 // ---------------------------------------------------------------------------
 // TMA
 // ---------------------------------------------------------------------------

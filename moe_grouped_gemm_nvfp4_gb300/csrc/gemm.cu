@@ -6,12 +6,16 @@
 // Investigation", The Comprehensive Synthesis: A/B FP4 tiles plus their
 // scale-factor tiles staged through shared memory over several stages).
 //
-// Roles of the 192 threads of a CTA (one CTA per SM):
+// Roles of the 224 threads of a CTA (one CTA per SM):
 //   warp 0      TMA producer: operand tiles (128-byte swizzle) and scale
 //               atoms into a ring of shared-memory stages;
 //   warp 1      tensor-memory allocation; lane 0 issues tcgen05.cp (scales
 //               -> tensor memory) and tcgen05.mma kind::mxf4nvf4 into a
 //               double-buffered FP32 accumulator in tensor memory;
+//   warp 6      second MMA issuer for narrow token tiles (odd K steps, own
+//               accumulator): each tcgen05 instruction holds its issuing
+//               thread for ~60-110 cycles, so one thread cannot issue the
+//               12 instructions of a decode stage as fast as HBM delivers it;
 //   warps 2-5   epilogue: tcgen05.ld, global-scale multiply, BF16 store or
 //               weighted FP32 scatter-add (MoE combine).
 // A work unit is one 128-row tile of operand X (the MMA's M side) against up
@@ -29,38 +33,58 @@ namespace nvfp4 {
 
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;                  // 7 warps, roles below
 constexpr int kRowBytes = 128;                 // 256 FP4 values = one swizzle row
 constexpr int kBK = 256;                       // K elements per stage
 constexpr int kXTileBytes = 128 * kRowBytes;   // 16 KB
 constexpr int kSFStageBytes = 4 * 512;         // four scale atoms (K = 256)
 constexpr int kTmemCols = 512;
 
+// Pipeline configuration per token-tile width BN (rows of operand Y, the
+// MMA's N).  Narrow tiles leave shared memory for more stages, i.e. more
+// weight bytes in flight per SM, which is what the decode shapes need: each
+// stage stays occupied for a memory round trip plus the tensor-pipe latency
+// of its scale copies and MMAs.
 template <int BN>
 struct Cfg {
-  static_assert(BN == 128, "tile width");
+  static_assert(BN == 32 || BN == 64 || BN == 128, "tile width");
   static constexpr int kYTileBytes = BN * kRowBytes;
-  static constexpr int kStageBytes = kXTileBytes + kYTileBytes + 2 * kSFStageBytes;
-  static constexpr int kStages = 6;
-  static constexpr int kAccCols = BN;
-  static constexpr int kSfColBase = 2 * BN;    // scale columns follow the accumulators
+  // stage: [X codes 16 KB][X scales 2 KB][Y codes][Y scales 2 KB]; the X part
+  // has the operand-tile layout, so a tile K block lands with one copy
+  static constexpr int kYOffset = kXTileBytes + kSFStageBytes;
+  static constexpr int kStageBytes = kYOffset + kYTileBytes + kSFStageBytes;
+  static_assert(kYOffset % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle alignment");
+  static constexpr int kStages = BN == 32 ? 9 : 6;
+  // Stages are released to the producer in groups with one tcgen05.commit
+  // per group: the tensor pipe does not overlap the operations before a
+  // commit with those after it, so a commit per stage would serialise every
+  // stage's scale copies and MMAs behind the previous stage's.
+  static constexpr int kGroup = 3;
+  static constexpr int kGroups = kStages / kGroup;
+  static_assert(kStages % kGroup == 0, "stage groups");
+  static constexpr int kIssuers = BN <= 64 ? 2 : 1;   // MMA-issuing threads
+  static constexpr int kAccCols = BN;                  // one accumulator
+  // accumulator (buffer b, issuer j) at column (b * kIssuers + j) * BN;
+  // scale columns follow the accumulators
+  static constexpr int kSfColBase = 2 * kIssuers * BN;
   static_assert(kSfColBase + kStages * 32 <= kTmemCols, "tensor memory budget");
-  // barriers: full[S], empty[S], acc_full[2], acc_empty[2], drain
-  static constexpr int kBarBytes = 8 * (2 * kStages + 5);
+  // barriers: full[S], empty[S / G], acc_full[2], acc_empty[2], drain
+  static constexpr int kBarBytes = 8 * (kStages + kGroups + 5);
   static constexpr int kTableInts = 3 * (kGroupedMaxExperts + 1);
   static constexpr int kCtlOffset = kStages * kStageBytes + kBarBytes;
   static constexpr int kTablesOffset = kCtlOffset + 32;
   static constexpr int kSmemBytes = kTablesOffset + 4 * kTableInts + 1024;  // + align slack
+  static_assert(kSmemBytes <= 232448 - 64, "shared memory budget");
 };
 
 struct Unit {
-  int32_t x_row0;     // tensor-map row of the X tile
-  int32_t y_row0;     // tensor-map row of the Y tile
+  int32_t x_row0;     // dense: tensor-map row of the X tile
+  int32_t y_row0;     // dense: tensor-map row of the Y tile; grouped: first route
   int32_t y_rows;     // valid Y rows (1..BN)
   int32_t x_local0;   // first output feature (grouped) / first X row (dense)
   int32_t e;          // expert (grouped)
-  int64_t sfx_off;    // byte offset of the X scale atoms at k-block 0
-  int64_t sfy_off;
+  int64_t sfx_off;    // dense: X scale atoms at k-block 0; grouped: X operand tile
+  int64_t sfy_off;    // dense: Y scale atoms at k-block 0; grouped: Y operand tile
 };
 
 struct Tables {
@@ -90,8 +114,9 @@ __device__ __forceinline__ Unit get_unit(int u, int mode, const GemmArgs& a, con
     un.x_local0 = mt * 128;
     un.y_row0 = t.off[e] + nt * BN;
     un.y_rows = min(BN, cnt - nt * BN);
-    un.sfx_off = static_cast<int64_t>(e * mtiles + mt) * atoms_per_rowtile * 512;
-    un.sfy_off = static_cast<int64_t>(t.tb[e] + nt * (BN / 128)) * atoms_per_rowtile * 512;
+    const int64_t n_kb = (a.K + kBK - 1) / kBK;
+    un.sfx_off = static_cast<int64_t>(e * mtiles + mt) * n_kb * kOperandTileBytes;
+    un.sfy_off = static_cast<int64_t>(t.tb[e] + nt) * n_kb * kOperandTileBytes;
   } else {
     const int tx = u % tiles_x;
     const int ty = u / tiles_x;
@@ -104,6 +129,30 @@ __device__ __forceinline__ Unit get_unit(int u, int mode, const GemmArgs& a, con
     un.sfy_off = static_cast<int64_t>(ty * (BN / 128)) * atoms_per_rowtile * 512;
   }
   return un;
+}
+
+// In-register transpose of a 32 x 32 block held by one warp: lane l's r[i]
+// becomes the value lane i held in r[l].  Five butterfly stages; every
+// register index is a compile-time constant, so r stays in registers.
+__device__ __forceinline__ void warp_transpose32(uint32_t (&r)[32], int lane) {
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) {
+    const bool upper = (lane & s) != 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if ((i & s) == 0) {
+        const uint32_t send = upper ? r[i] : r[i + s];
+        const uint32_t recv = __shfl_xor_sync(0xFFFFFFFFu, send, s);
+        if (upper) r[i] = recv; else r[i + s] = recv;
+      }
+    }
+  }
+}
+
+// Four FP32 additions into global memory in one reduction (16-byte aligned).
+__device__ __forceinline__ void red_add_v4(float* dst, float4 v) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
+               :: "l"(dst), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w) : "memory");
 }
 
 // Waits for a phase regardless of the abort flag (used only to drain copies
@@ -129,10 +178,10 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + C::kStages * C::kStageBytes;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (C::kStages + s); };
-  auto accf_bar = [&](int b) { return bar0 + 8u * (2 * C::kStages + b); };
-  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * C::kStages + 2 + b); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * C::kStages + 4);
+  auto empty_bar = [&](int g) { return bar0 + 8u * (C::kStages + g); };   // per stage group
+  auto accf_bar = [&](int b) { return bar0 + 8u * (C::kStages + C::kGroups + b); };
+  auto acce_bar = [&](int b) { return bar0 + 8u * (C::kStages + C::kGroups + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (C::kStages + C::kGroups + 4);
   CtaCtl* ctl = reinterpret_cast<CtaCtl*>(smem + C::kCtlOffset);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kCtlOffset + 16);
   int32_t* tab = reinterpret_cast<int32_t*>(smem + C::kTablesOffset);
@@ -147,9 +196,13 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
   const int tiles_x = (a.rows_x + 127) >> 7;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::kStages; ++s) { mbar_init(full_bar(s), 1); mbar_init(empty_bar(s), 1); }
-    for (int b = 0; b < 2; ++b) { mbar_init(accf_bar(b), 1); mbar_init(acce_bar(b), 128); }
-    mbar_init(drain_bar, 1);
+    for (int s = 0; s < C::kStages; ++s) mbar_init(full_bar(s), 1);
+    for (int g = 0; g < C::kGroups; ++g) mbar_init(empty_bar(g), C::kIssuers);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf_bar(b), C::kIssuers);
+      mbar_init(acce_bar(b), 128);
+    }
+    mbar_init(drain_bar, C::kIssuers);
     ctl->abort = 0;
     ctl->timeout_ns = a.timeout_ns;
     fence_mbar_init();
@@ -170,7 +223,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
         ok = ok && (c >= 0);
         t.off[e] = o0;
         su += mtiles * ((c + BN - 1) / BN);
-        st += (c + 127) >> 7;
+        st += (c + BN - 1) / BN;
       }
       int32_t iu = su, it = st;
 #pragma unroll
@@ -184,7 +237,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
         const int32_t c = a.expert_offsets[e + 1] - a.expert_offsets[e];
         t.up[e] = pu; t.tb[e] = pt;
         pu += mtiles * ((c + BN - 1) / BN);
-        pt += (c + 127) >> 7;
+        pt += (c + BN - 1) / BN;
       }
       const bool all_ok = __all_sync(0xFFFFFFFFu, ok);
       if (lane == 31) {
@@ -221,24 +274,41 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
       bool alive = true;
       for (int u = blockIdx.x; u < units && alive; u += gridDim.x) {
         const Unit un = get_unit<BN>(u, mode, a, t, tiles_x, atoms_per_rowtile);
-        const int ybox = (un.y_rows + 15) >> 4;
+        const int ybox = (un.y_rows + 15) >> 4;                  // 16-row groups
+        const int ny_loads = (un.y_rows + a.ybox_rows - 1) / a.ybox_rows;
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(empty_bar(stage), phase ^ 1u, ctl, a.status)) { alive = false; break; }
+          // a group of stages is refilled once the MMAs of its previous round completed
+          if (stage % C::kGroup == 0 &&
+              !mbar_wait(empty_bar(stage / C::kGroup), phase ^ 1u, ctl, a.status)) {
+            alive = false;
+            break;
+          }
           const int ksteps = min(4, static_cast<int>((a.K >> 6) - 4 * kb));
           const uint32_t sx = sbase + stage * C::kStageBytes;
-          const uint32_t sy = sx + kXTileBytes;
-          const uint32_t ssfx = sy + C::kYTileBytes;
-          const uint32_t ssfy = ssfx + kSFStageBytes;
-          const uint32_t bytes = kXTileBytes + ybox * 16 * kRowBytes + 2 * ksteps * 512;
+          const uint32_t ssfx = sx + kXTileBytes;
+          const uint32_t sy = sx + C::kYOffset;
+          const uint32_t ssfy = sy + C::kYTileBytes;
+          const uint32_t ybytes = grouped ? ybox * 16 * kRowBytes : ny_loads * a.ybox_rows * kRowBytes;
+          const uint32_t bytes = kXTileBytes + ybytes + 2 * ksteps * 512;
           mbar_arrive_expect_tx(full_bar(stage), bytes);
-          tma_load_2d(sx, &tmx, full_bar(stage), kb * kRowBytes, un.x_row0, pol_x);
-          for (int j = 0; j < ybox; ++j)
-            tma_load_2d(sy + j * 16 * kRowBytes, &tmy, full_bar(stage), kb * kRowBytes,
-                        un.y_row0 + 16 * j, pol_y);
-          bulk_load(ssfx, a.sfx + un.sfx_off + kb * kSFStageBytes, ksteps * 512, full_bar(stage),
-                    pol_x);
-          bulk_load(ssfy, a.sfy + un.sfy_off + kb * kSFStageBytes, ksteps * 512, full_bar(stage),
-                    pol_y);
+          if (grouped) {
+            // operand tiles: X codes + scales in one contiguous copy, Y codes
+            // (only the unit's rows) and Y scales in two more
+            const uint8_t* xt = a.sfx + un.sfx_off + kb * kOperandTileBytes;
+            const uint8_t* yt = a.sfy + un.sfy_off + kb * kOperandTileBytes;
+            bulk_load(sx, xt, kXTileBytes + ksteps * 512, full_bar(stage), pol_x);
+            bulk_load(sy, yt, ybox * 16 * kRowBytes, full_bar(stage), pol_y);
+            bulk_load(ssfy, yt + kXTileBytes, ksteps * 512, full_bar(stage), pol_y);
+          } else {
+            tma_load_2d(sx, &tmx, full_bar(stage), kb * kRowBytes, un.x_row0, pol_x);
+            for (int j = 0; j < ny_loads; ++j)
+              tma_load_2d(sy + j * a.ybox_rows * kRowBytes, &tmy, full_bar(stage), kb * kRowBytes,
+                          un.y_row0 + a.ybox_rows * j, pol_y);
+            bulk_load(ssfx, a.sfx + un.sfx_off + kb * kSFStageBytes, ksteps * 512,
+                      full_bar(stage), pol_x);
+            bulk_load(ssfy, a.sfy + un.sfy_off + kb * kSFStageBytes, ksteps * 512,
+                      full_bar(stage), pol_y);
+          }
           ++issued;
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
         }
@@ -250,8 +320,10 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
                         static_cast<uint32_t>((n / C::kStages) & 1), ctl->timeout_ns);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ----------------------------------------------------------------- MMA
+  } else if (warp == 1 || (C::kIssuers == 2 && warp == 6)) {
+    // ---------------------------------------------------------------- MMA
+    // Issuer j takes the K steps with ks % kIssuers == j of every stage.
+    const int j = (warp == 6) ? 1 : 0;
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
@@ -263,26 +335,32 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
         const uint32_t idesc = idesc_nvf4(static_cast<uint32_t>((un.y_rows + 15) & ~15));
         if (!mbar_wait(acce_bar(abuf), aphase ^ 1u, ctl, a.status)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem + abuf * C::kAccCols;
+        const uint32_t d_tmem = tmem + (abuf * C::kIssuers + j) * C::kAccCols;
         for (int kb = 0; kb < nkb; ++kb) {
+          // The stage's operands arrive by TMA / bulk copy, completing on the
+          // mbarrier; the MMAs read them through the same async proxy, so the
+          // wait alone orders them.  (A tcgen05 thread-sync fence here would
+          // wait for this thread's earlier MMAs and serialise the stages.)
           if (!mbar_wait(full_bar(stage), phase, ctl, a.status)) { alive = false; break; }
-          tc_fence_after();
           const int ksteps = min(4, static_cast<int>((a.K >> 6) - 4 * kb));
           const uint32_t sx = sbase + stage * C::kStageBytes;
-          const uint32_t sy = sx + kXTileBytes;
-          const uint32_t ssfx = sy + C::kYTileBytes;
-          const uint32_t ssfy = ssfx + kSFStageBytes;
+          const uint32_t ssfx = sx + kXTileBytes;
+          const uint32_t sy = sx + C::kYOffset;
+          const uint32_t ssfy = sy + C::kYTileBytes;
           const uint32_t tsfx = tmem + C::kSfColBase + stage * 32;
           const uint32_t tsfy = tsfx + 16;
           const uint64_t dx = sdesc_sw128(sx);
           const uint64_t dy = sdesc_sw128(sy);
-          for (int ks = 0; ks < ksteps; ++ks) {
+          // Every token tile starts at row 0 of its operand tile, so every
+          // scale address handed to the MMA is a multiple of 4 columns (an
+          // address inside an atom's column group faults as misaligned).
+          for (int ks = j; ks < ksteps; ks += C::kIssuers) {
             tc_cp_sf_atom(tsfx + 4 * ks, sdesc_sf_atom(ssfx + 512 * ks));
             tc_cp_sf_atom(tsfy + 4 * ks, sdesc_sf_atom(ssfy + 512 * ks));
             tc_mma_nvf4(d_tmem, dx + 2 * ks, dy + 2 * ks, idesc, tsfx + 4 * ks, tsfy + 4 * ks,
-                        (kb | ks) != 0 ? 1u : 0u);
+                        (kb > 0 || ks >= C::kIssuers) ? 1u : 0u);
           }
-          tc_commit(empty_bar(stage));
+          if (stage % C::kGroup == C::kGroup - 1) tc_commit(empty_bar(stage / C::kGroup));
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
         }
         if (!alive) break;
@@ -295,26 +373,40 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
       mbar_wait_drain(drain_bar, 0, ctl->timeout_ns);
     }
     __syncwarp();
-  } else {
+  } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                       // tensor-memory lane quarter
     const int row = q * 32 + lane;                // row of the X tile
     int abuf = 0;
     uint32_t aphase = 0;
     const float gy = *a.gy;
+    // accumulators that received at least one K step (issuer j's first is ks = j)
+    const int n_acc = (a.K >> 6) < C::kIssuers ? static_cast<int>(a.K >> 6) : C::kIssuers;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const Unit un = get_unit<BN>(u, mode, a, t, tiles_x, atoms_per_rowtile);
-      // all lanes wait, then agree, so the warp-collective loads below stay converged
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(accf_bar(abuf), aphase, ctl, a.status))) break;
+      // all lanes wait (sleeping between polls, see mbar_wait_sleepy), then
+      // agree, so the warp-collective loads below stay converged
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait_sleepy(accf_bar(abuf), aphase, ctl, a.status)))
+        break;
       tc_fence_after();
       const float alpha = __fmul_rn(grouped ? a.gx[un.e] : a.gx[0], gy);
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + abuf * C::kAccCols;
+      const uint32_t taddr =
+          tmem + (static_cast<uint32_t>(q * 32) << 16) + abuf * C::kIssuers * C::kAccCols;
       const int n_valid = un.y_rows;
       const int xr = un.x_local0 + row;            // output feature / X row
       for (int c0 = 0; c0 < n_valid; c0 += 32) {
         uint32_t r[32];
         tmem_ld32(taddr + c0, r);
-        tmem_ld_wait();
+        if (n_acc == 2) {                 // the second issuer's partial sums
+          uint32_t r2[32];
+          tmem_ld32(taddr + C::kAccCols + c0, r2);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            r[i] = __float_as_uint(__fadd_rn(__uint_as_float(r[i]), __uint_as_float(r2[i])));
+        } else {
+          tmem_ld_wait();
+        }
         const int nc = min(32, n_valid - c0);
         if (mode == kDenseRowsX) {
           if (xr < a.rows_x) {
@@ -339,26 +431,49 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
                 if (j < nc) dst[j] = f32_to_bf16_rn(__fmul_rn(__uint_as_float(r[j]), alpha));
             }
           }
-        } else if (mode == kDenseRowsY || mode == kGrouped) {
-          if (mode == kGrouped || xr < a.rows_x) {
-            uint16_t* dst = reinterpret_cast<uint16_t*>(a.out) + xr;
+        } else {
+          // Transposed orientations: lane l takes token column c0 + l and the
+          // 32 features of this warp, so stores and FP32 reductions are vectors.
+          warp_transpose32(r, lane);
+          const int col = c0 + lane;
+          const int f0 = un.x_local0 + q * 32;          // first feature of this warp
+          if (col < n_valid) {
+            const int64_t y = un.y_row0 + col;
+            if (mode == kGroupedCombine) {
+              const int tok = a.route_token[y];
+              const float w = a.topk_w[static_cast<int64_t>(tok) * a.topk + a.route_slot[y]];
+              float* dst = a.ws + static_cast<int64_t>(tok) * a.n_out + f0;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if (j < nc) {
-                const int64_t y = un.y_row0 + c0 + j;
-                dst[y * a.ldc] = f32_to_bf16_rn(__fmul_rn(__uint_as_float(r[j]), alpha));
+              for (int v = 0; v < 8; ++v) {
+                float4 acc4;
+                acc4.x = __fmul_rn(w, __fmul_rn(__uint_as_float(r[4 * v + 0]), alpha));
+                acc4.y = __fmul_rn(w, __fmul_rn(__uint_as_float(r[4 * v + 1]), alpha));
+                acc4.z = __fmul_rn(w, __fmul_rn(__uint_as_float(r[4 * v + 2]), alpha));
+                acc4.w = __fmul_rn(w, __fmul_rn(__uint_as_float(r[4 * v + 3]), alpha));
+                red_add_v4(dst + 4 * v, acc4);
               }
-            }
-          }
-        } else {  // kGroupedCombine
+            } else {
+              uint16_t* dst = reinterpret_cast<uint16_t*>(a.out) + y * a.ldc + f0;
+              const bool full = (mode == kGrouped) || (f0 + 32 <= a.rows_x);
+              if (full && a.vec_store) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (j < nc) {
-              const int p = un.y_row0 + c0 + j;
-              const int tok = a.route_token[p];
-              const float w = a.topk_w[static_cast<int64_t>(tok) * a.topk + a.route_slot[p]];
-              const float v = __fmul_rn(w, __fmul_rn(__uint_as_float(r[j]), alpha));
-              atomicAdd(a.ws + static_cast<int64_t>(tok) * a.n_out + xr, v);
+                for (int v = 0; v < 4; ++v) {
+                  uint32_t w[4];
+#pragma unroll
+                  for (int h = 0; h < 4; ++h) {
+                    const float v0 = __fmul_rn(__uint_as_float(r[8 * v + 2 * h]), alpha);
+                    const float v1 = __fmul_rn(__uint_as_float(r[8 * v + 2 * h + 1]), alpha);
+                    w[h] = static_cast<uint32_t>(f32_to_bf16_rn(v0)) |
+                           (static_cast<uint32_t>(f32_to_bf16_rn(v1)) << 16);
+                  }
+                  reinterpret_cast<uint4*>(dst)[v] = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+              } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (mode == kGrouped || f0 + i < a.rows_x)
+                    dst[i] = f32_to_bf16_rn(__fmul_rn(__uint_as_float(r[i]), alpha));
+              }
             }
           }
         }
@@ -394,9 +509,24 @@ __global__ void __launch_bounds__(256) combine_finalize_kernel(const float* __re
 
 }  // namespace
 
+template <int BN>
+static cudaError_t set_smem_attr() {
+  return cudaFuncSetAttribute(nvfp4_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              Cfg<BN>::kSmemBytes);
+}
+
 cudaError_t init_gemm_attributes() {
-  return cudaFuncSetAttribute(nvfp4_gemm_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              Cfg<128>::kSmemBytes);
+  cudaError_t e = set_smem_attr<32>();
+  if (e == cudaSuccess) e = set_smem_attr<64>();
+  if (e == cudaSuccess) e = set_smem_attr<128>();
+  return e;
+}
+
+template <int BN>
+static cudaError_t launch_bn(const CUtensorMap& tmx, const CUtensorMap& tmy, const GemmArgs& a,
+                             int mode, int grid, cudaStream_t s) {
+  nvfp4_gemm_kernel<BN><<<grid, kThreads, Cfg<BN>::kSmemBytes, s>>>(tmx, tmy, a, mode);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_gemm(const CUtensorMap& tmx, const CUtensorMap& tmy, const GemmArgs& a,
@@ -405,10 +535,14 @@ cudaError_t launch_gemm(const CUtensorMap& tmx, const CUtensorMap& tmy, const Ge
   if (mode == kDenseRowsX || mode == kDenseRowsY) {
     const int64_t units = ((a.rows_x + 127) / 128) * ((a.rows_y + 127) / 128);
     if (units < grid) grid = static_cast<int>(units);
+    if (grid < 1) return cudaSuccess;
+    return launch_bn<128>(tmx, tmy, a, mode, grid, s);
   }
-  if (grid < 1) return cudaSuccess;
-  nvfp4_gemm_kernel<128><<<grid, kThreads, Cfg<128>::kSmemBytes, s>>>(tmx, tmy, a, mode);
-  return cudaGetLastError();
+  switch (grouped_chunk_rows(a.rows_y, a.E)) {
+    case 32: return launch_bn<32>(tmx, tmy, a, mode, grid, s);
+    case 64: return launch_bn<64>(tmx, tmy, a, mode, grid, s);
+    default: return launch_bn<128>(tmx, tmy, a, mode, grid, s);
+  }
 }
 
 cudaError_t launch_combine_finalize(const float* ws, int64_t T, int64_t N, void* out, int sms,

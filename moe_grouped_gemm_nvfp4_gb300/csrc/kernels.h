@@ -17,8 +17,10 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64
 cudaError_t launch_quantize_dispatch(const uint16_t* x, int64_t rows, int64_t K, int64_t ld,
                                      const int32_t* route_pos, int fanout,
                                      const int32_t* expert_offsets, int E, int64_t R,
-                                     uint8_t* packed, uint8_t* scales, const float* g,
-                                     int* status, int sms, cudaStream_t s);
+                                     int chunk_rows, uint8_t* tiles, const float* g, int* status,
+                                     int sms, cudaStream_t s);
+cudaError_t launch_prepack_tiles(const uint8_t* packed, const uint8_t* sf, int64_t rows,
+                                 int64_t K, uint8_t* tiles, int sms, cudaStream_t s);
 cudaError_t launch_prepack(const uint8_t* src, int64_t rows, int64_t kblk, uint8_t* dst,
                            int sms, cudaStream_t s);
 
@@ -37,8 +39,8 @@ enum GemmMode : int {
 };
 
 struct GemmArgs {
-  const uint8_t* sfx;              // X scales, atom layout
-  const uint8_t* sfy;              // Y scales, atom layout (grouped: per-expert tiles)
+  const uint8_t* sfx;              // dense: X scales, atom layout; grouped: X operand tiles
+  const uint8_t* sfy;              // dense: Y scales, atom layout; grouped: Y operand tiles
   const float* gx;                 // X global (grouped: per expert [E])
   const float* gy;                 // Y global
   int64_t K;
@@ -50,6 +52,7 @@ struct GemmArgs {
   void* out;                       // BF16
   int64_t ldc;
   int32_t vec_store;               // rows of C are 16-byte aligned (ldc % 8 == 0)
+  int32_t ybox_rows;               // dense: rows per TMA box of Y (16 or 128)
   const int32_t* route_token;      // combine
   const int32_t* route_slot;
   const float* topk_w;
@@ -60,6 +63,16 @@ struct GemmArgs {
 };
 
 constexpr int kGroupedMaxExperts = 256;
+
+// Token-tile width of the grouped GEMM (32, 64 or 128 routes), a function of
+// the route and expert counts only: ~1.6x the mean routes per expert, so the
+// widest experts of a balanced routing still fit one tile.  The grouped
+// activation layout cuts each expert's routes into chunks of this width.
+inline int grouped_chunk_rows(int64_t routes, int experts) {
+  const int64_t want = experts > 0 ? (routes * 8 + experts * 5 - 1) / (experts * 5) : 128;
+  return want <= 32 ? 32 : (want <= 64 ? 64 : 128);
+}
+constexpr int64_t kOperandTileBytes = 16384 + 2048;   // 128 rows x 256 K: codes + scale atoms
 
 cudaError_t init_gemm_attributes();
 cudaError_t launch_gemm(const CUtensorMap& tmx, const CUtensorMap& tmy, const GemmArgs& a,

@@ -178,51 +178,130 @@ __device__ __forceinline__ int find_expert(const int32_t* off, int E, int32_t p)
   return lo;
 }
 
-// Quantise source rows and write each one to its route positions: packed
-// data in route order [R, K/2], scales in the grouped atom layout (each
-// expert's routes start a fresh 128-row tile).
+// Operand tiles: 128 rows x 256 K-elements per tile, 16384 bytes of codes
+// (row r at r * 128, 16-byte chunk j at position j ^ (r % 8): the 128-byte
+// swizzle the tensor cores read) followed by 2048 bytes of scale atoms; tiles
+// ordered row-tile major, then K block.
+constexpr int64_t kTileBytes = 16384 + 2048;
+
+__device__ __forceinline__ int64_t tile_code_offset(int64_t rt, int r, int64_t kb, int c,
+                                                    int64_t n_kb) {
+  return (rt * n_kb + kb) * kTileBytes + r * 128 + ((((c >> 4) ^ (r & 7))) << 4) + (c & 15);
+}
+
+__device__ __forceinline__ int64_t tile_scale_offset(int64_t rt, int r, int64_t kb, int s,
+                                                     int64_t n_kb) {
+  return (rt * n_kb + kb) * kTileBytes + 16384 + (s >> 2) * 512 + (r & 31) * 16 +
+         ((r >> 5) & 3) * 4 + (s & 3);
+}
+
+// Quantise source rows and write each one to its route positions, in the
+// grouped operand-tile layout: each expert's routes are cut into chunks of
+// `chunk` rows and every chunk starts a fresh row tile (route p, local index
+// j = p - off[e], is row j % chunk of tile tb[e] + j / chunk).
 __global__ void __launch_bounds__(256) quantize_dispatch_kernel(
     const uint16_t* __restrict__ x, int64_t rows, int64_t K, int64_t ld,
     const int32_t* __restrict__ route_pos, int fanout,
-    const int32_t* __restrict__ expert_offsets, int E, int64_t R,
-    uint8_t* __restrict__ packed, uint8_t* __restrict__ scales, const float* g_ptr,
-    int* status) {
+    const int32_t* __restrict__ expert_offsets, int E, int64_t R, int chunk,
+    uint8_t* __restrict__ tiles, const float* g_ptr, int* status) {
   extern __shared__ int32_t sh[];
   int32_t* off = sh;              // [E + 1]
   int32_t* tb = sh + (E + 1);     // [E]
+  __shared__ int32_t s_bad;
   for (int e = threadIdx.x; e <= E; e += blockDim.x) off[e] = expert_offsets[e];
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int32_t acc = 0;
-    bool ok = off[0] == 0 && off[E] <= R;
-    for (int e = 0; e < E; ++e) {
+  // tile prefix: one warp scans the per-expert tile counts
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int per = (E + 31) / 32;
+    const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+    int32_t sum = 0;
+    bool ok = true;
+    for (int e = e0; e < e1; ++e) {
       const int32_t c = off[e + 1] - off[e];
-      if (c < 0) ok = false;
-      tb[e] = acc;
-      acc += (c + 127) >> 7;
+      ok = ok && c >= 0;
+      sum += (c + chunk - 1) / chunk;
     }
-    if (!ok) { raise_status(status, NVFP4_ERR_DEVICE_CHECK); tb[0] = -1; }
+    int32_t incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int32_t acc = incl - sum;
+    for (int e = e0; e < e1; ++e) {
+      tb[e] = acc;
+      acc += (off[e + 1] - off[e] + chunk - 1) / chunk;
+    }
+    const bool all_ok = __all_sync(0xFFFFFFFFu, ok) && off[0] == 0 && off[E] <= R;
+    if (lane == 0) {
+      s_bad = all_ok ? 0 : 1;
+      if (!all_ok) raise_status(status, NVFP4_ERR_DEVICE_CHECK);
+    }
   }
   __syncthreads();
-  if (E > 0 && tb[0] < 0) return;
+  if (s_bad) return;
   const float g = *g_ptr;
   const int64_t bpr = K >> 4;
+  const int64_t n_kb = (K + 255) >> 8;
   const int64_t total = rows * bpr;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  const int64_t ncg = K >> 6;
   const int32_t nroutes = off[E];
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += stride) {
     const int64_t r = i / bpr, b = i - r * bpr;
     const uint4* src = reinterpret_cast<const uint4*>(x + r * ld + b * 16);
     const Block16 q = quantize_block(__ldg(src), __ldg(src + 1), g);
+    const int64_t kb = b >> 4;
+    const int bb = static_cast<int>(b & 15);        // 16-element block inside the K block
     for (int j = 0; j < fanout; ++j) {
       const int32_t p = route_pos ? route_pos[r * fanout + j] : static_cast<int32_t>(r);
       if (p < 0 || p >= nroutes) continue;          // dropped route
-      *reinterpret_cast<uint2*>(packed + static_cast<int64_t>(p) * (K >> 1) + b * 8) = q.packed;
       const int e = find_expert(off, E, p);
-      const int64_t prow = static_cast<int64_t>(tb[e]) * 128 + (p - off[e]);
-      scales[atom_offset(prow, b, ncg)] = static_cast<uint8_t>(q.sf);
+      const int32_t local = p - off[e];
+      const int64_t rt = tb[e] + local / chunk;
+      const int row = local % chunk;
+      *reinterpret_cast<uint2*>(tiles + tile_code_offset(rt, row, kb, bb * 8, n_kb)) = q.packed;
+      tiles[tile_scale_offset(rt, row, kb, bb, n_kb)] = static_cast<uint8_t>(q.sf);
+    }
+  }
+}
+
+// Packed rows [rows, K/2] + row-major scales [rows, K/16] -> operand tiles,
+// rows padded to 128 and K to 256 with zeros.  One thread per 16-byte chunk
+// of codes (and per 4 scale bytes).
+__global__ void __launch_bounds__(256) prepack_tiles_kernel(const uint8_t* __restrict__ packed,
+                                                            const uint8_t* __restrict__ sf,
+                                                            int64_t rows, int64_t K,
+                                                            uint8_t* __restrict__ tiles) {
+  const int64_t rows_pad = (rows + 127) & ~static_cast<int64_t>(127);
+  const int64_t n_kb = (K + 255) >> 8;
+  const int64_t half = K >> 1;
+  const int64_t chunks = n_kb * 8;                  // 16-byte chunks per padded row
+  const int64_t sgroups = n_kb * 4;                 // 4-byte scale groups per padded row
+  const int64_t per_row = chunks + sgroups;
+  const int64_t total = rows_pad * per_row;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += stride) {
+    const int64_t r = i / per_row, w = i - r * per_row;
+    const int64_t rt = r >> 7;
+    const int row = static_cast<int>(r & 127);
+    if (w < chunks) {
+      const int64_t kb = w >> 3;
+      const int c = static_cast<int>(w & 7) * 16;
+      const int64_t byte = kb * 128 + c;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (r < rows && byte < half) v = *reinterpret_cast<const uint4*>(packed + r * half + byte);
+      *reinterpret_cast<uint4*>(tiles + tile_code_offset(rt, row, kb, c, n_kb)) = v;
+    } else {
+      const int64_t gidx = w - chunks;
+      const int64_t kb = gidx >> 2;
+      const int sg = static_cast<int>(gidx & 3) * 4;
+      const int64_t col = kb * 16 + sg;
+      uint32_t v = 0;
+      if (r < rows && col < (K >> 4)) v = *reinterpret_cast<const uint32_t*>(sf + r * (K >> 4) + col);
+      *reinterpret_cast<uint32_t*>(tiles + tile_scale_offset(rt, row, kb, sg, n_kb)) = v;
     }
   }
 }
@@ -280,12 +359,22 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64
 cudaError_t launch_quantize_dispatch(const uint16_t* x, int64_t rows, int64_t K, int64_t ld,
                                      const int32_t* route_pos, int fanout,
                                      const int32_t* expert_offsets, int E, int64_t R,
-                                     uint8_t* packed, uint8_t* scales, const float* g,
-                                     int* status, int sms, cudaStream_t s) {
+                                     int chunk_rows, uint8_t* tiles, const float* g, int* status,
+                                     int sms, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
   const size_t shmem = sizeof(int32_t) * (2 * static_cast<size_t>(E) + 1);
   quantize_dispatch_kernel<<<grid_for(rows * (K >> 4), sms), 256, shmem, s>>>(
-      x, rows, K, ld, route_pos, fanout, expert_offsets, E, R, packed, scales, g, status);
+      x, rows, K, ld, route_pos, fanout, expert_offsets, E, R, chunk_rows, tiles, g, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prepack_tiles(const uint8_t* packed, const uint8_t* sf, int64_t rows,
+                                 int64_t K, uint8_t* tiles, int sms, cudaStream_t s) {
+  const int64_t rows_pad = (rows + 127) & ~static_cast<int64_t>(127);
+  const int64_t n_kb = (K + 255) >> 8;
+  const int64_t work = rows_pad * n_kb * 12;
+  if (work == 0) return cudaSuccess;
+  prepack_tiles_kernel<<<grid_for(work, sms), 256, 0, s>>>(packed, sf, rows, K, tiles);
   return cudaGetLastError();
 }
 

@@ -22,9 +22,8 @@ from . import nvfp4 as F
 
 @dataclass
 class ExpertWeights:
-    """NVFP4 expert weights: packed [E, N, K/2], atom scales over [E*N, K], g [E]."""
-    packed: torch.Tensor
-    sf_atoms: torch.Tensor
+    """NVFP4 expert weights as operand tiles over [E*N, K], one global per expert."""
+    tiles: torch.Tensor
     g: torch.Tensor
     E: int
     N: int
@@ -32,7 +31,7 @@ class ExpertWeights:
 
 
 def quantize_experts(w: torch.Tensor, stream=None) -> ExpertWeights:
-    """BF16 [E, N, K] on the device -> NVFP4 with one global scale per expert."""
+    """BF16 [E, N, K] on the device -> NVFP4 operand tiles, one global per expert."""
     E, N, K = w.shape
     dev = w.device
     packed = torch.empty((E, N, K // 2), dtype=torch.uint8, device=dev)
@@ -40,9 +39,10 @@ def quantize_experts(w: torch.Tensor, stream=None) -> ExpertWeights:
     g = torch.empty(E, dtype=torch.float32, device=dev)
     for e in range(E):
         F.nvfp4_quantize(w[e], packed[e], sf_rm[e], g[e:e + 1], 0, stream)
-    sf_atoms = torch.empty(F.nvfp4_atom_scales_bytes(E * N, K), dtype=torch.uint8, device=dev)
-    F.nvfp4_prepack_weights(sf_rm.view(E * N, K // 16), sf_atoms, stream)
-    return ExpertWeights(packed, sf_atoms, g, E, N, K)
+    tiles = torch.empty(F.nvfp4_operand_tiles_bytes(E * N, K), dtype=torch.uint8, device=dev)
+    F.nvfp4_prepack_weight_tiles(packed.view(E * N, K // 2), sf_rm.view(E * N, K // 16), tiles,
+                                 stream)
+    return ExpertWeights(tiles, g, E, N, K)
 
 
 class GroupedPlan:
@@ -74,9 +74,8 @@ class GroupedPlan:
             self.route_token = torch.empty(max(R, 1), **i32)
             self.route_slot = torch.empty(max(R, 1), **i32)
             self.route_pos = torch.empty(max(R, 1), **i32)
-        self.a_packed = torch.empty((max(R, 1), K // 2), dtype=torch.uint8, device=dev)
-        self.a_sf = torch.empty(max(F.nvfp4_grouped_scales_bytes(R, E, K), 16),
-                                dtype=torch.uint8, device=dev)
+        self.a_tiles = torch.empty(max(F.nvfp4_grouped_tiles_bytes(R, E, K), 16),
+                                   dtype=torch.uint8, device=dev)
         self.a_g = torch.empty(1, dtype=torch.float32, device=dev)
         if mode == "gather":
             self.out = torch.empty((max(R, 1), N), dtype=torch.bfloat16, device=dev)
@@ -93,15 +92,14 @@ class GroupedPlan:
     def quantize(self, x, stream=None):
         if self.mode == "gather":
             F.nvfp4_quantize_dispatch(x, self.route_pos, self.topk, self.expert_offsets,
-                                      self.w.E, self.R, self.a_packed, self.a_sf, self.a_g,
-                                      0, stream)
+                                      self.w.E, self.R, self.a_tiles, self.a_g, 0, stream)
         else:
             F.nvfp4_quantize_dispatch(x, None, 1, self.expert_offsets, self.w.E, self.R,
-                                      self.a_packed, self.a_sf, self.a_g, 0, stream)
+                                      self.a_tiles, self.a_g, 0, stream)
 
     def gemm(self, topk_weights=None, stream=None):
         w = self.w
-        F.nvfp4_grouped_gemm(self.a_packed, self.a_sf, self.a_g, w.packed, w.sf_atoms, w.g,
+        F.nvfp4_grouped_gemm(self.a_tiles, self.a_g, w.tiles, w.g,
                              self.expert_offsets, w.E, self.T, self.topk, w.N, w.K,
                              self.route_token, self.route_slot,
                              topk_weights if self.mode == "combine" else None,

@@ -43,12 +43,15 @@ _SIGS = {
     "nvfp4_prepack_weights": (ctypes.c_int, [_P, _I64, _I64, _P, _P]),
     "nvfp4_gemm": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P]),
     "nvfp4_moe_route": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _P, _P, _P, _P]),
-    "nvfp4_grouped_scales_bytes": (_SZ, [_I64, _I32, _I64]),
+    "nvfp4_operand_tiles_bytes": (_SZ, [_I64, _I64]),
+    "nvfp4_prepack_weight_tiles": (ctypes.c_int, [_P, _P, _I64, _I64, _P, _P]),
+    "nvfp4_grouped_chunk_rows": (ctypes.c_int, [_I64, _I32]),
+    "nvfp4_grouped_tiles_bytes": (_SZ, [_I64, _I32, _I64]),
     "nvfp4_quantize_dispatch": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I32, _P, _I32, _I64,
-                                               _P, _P, _P, _U32, _P]),
+                                               _P, _P, _U32, _P]),
     "nvfp4_combine_workspace_bytes": (_SZ, [_I64, _I64]),
-    "nvfp4_grouped_gemm": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I32, _I64, _I32, _I64,
-                                          _I64, _P, _P, _P, _P, _P, _SZ, _P]),
+    "nvfp4_grouped_gemm": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I64, _I32, _I64, _I64,
+                                          _P, _P, _P, _P, _P, _SZ, _P]),
 }
 
 
@@ -124,8 +127,16 @@ def nvfp4_atom_scales_bytes(rows: int, cols: int) -> int:
     return load().nvfp4_atom_scales_bytes(rows, cols)
 
 
-def nvfp4_grouped_scales_bytes(R: int, E: int, K: int) -> int:
-    return load().nvfp4_grouped_scales_bytes(R, E, K)
+def nvfp4_operand_tiles_bytes(rows: int, K: int) -> int:
+    return load().nvfp4_operand_tiles_bytes(rows, K)
+
+
+def nvfp4_grouped_chunk_rows(R: int, E: int) -> int:
+    return load().nvfp4_grouped_chunk_rows(R, E)
+
+
+def nvfp4_grouped_tiles_bytes(R: int, E: int, K: int) -> int:
+    return load().nvfp4_grouped_tiles_bytes(R, E, K)
 
 
 def nvfp4_combine_workspace_bytes(T: int, N: int) -> int:
@@ -160,21 +171,27 @@ def nvfp4_moe_route(topk_ids, E: int, expert_offsets, route_token, route_slot, r
         _ptr(route_pos), _stream(stream)))
 
 
-def nvfp4_quantize_dispatch(x, route_pos, fanout: int, expert_offsets, E: int, R: int, packed,
-                            scales, global_scale, flags: int = 0, stream=None) -> None:
+def nvfp4_prepack_weight_tiles(packed, scales_rowmajor, tiles, stream=None) -> None:
+    rows, half = packed.shape
+    _check("nvfp4_prepack_weight_tiles", load().nvfp4_prepack_weight_tiles(
+        _ptr(packed), _ptr(scales_rowmajor), rows, 2 * half, _ptr(tiles), _stream(stream)))
+
+
+def nvfp4_quantize_dispatch(x, route_pos, fanout: int, expert_offsets, E: int, R: int, tiles,
+                            global_scale, flags: int = 0, stream=None) -> None:
     rows, K = x.shape
     _check("nvfp4_quantize_dispatch", load().nvfp4_quantize_dispatch(
         _ptr(x), rows, K, x.stride(0), _ptr(route_pos), fanout, _ptr(expert_offsets), E, R,
-        _ptr(packed), _ptr(scales), _ptr(global_scale), flags, _stream(stream)))
+        _ptr(tiles), _ptr(global_scale), flags, _stream(stream)))
 
 
-def nvfp4_grouped_gemm(A, sfA, gA, W, sfW, gW, expert_offsets, E: int, T: int, topk: int,
+def nvfp4_grouped_gemm(A_tiles, gA, W_tiles, gW, expert_offsets, E: int, T: int, topk: int,
                        N: int, K: int, route_token, route_slot, topk_weights, out, workspace,
                        stream=None) -> None:
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check("nvfp4_grouped_gemm", load().nvfp4_grouped_gemm(
-        _ptr(A), _ptr(sfA), _ptr(gA), _ptr(W), _ptr(sfW), _ptr(gW), _ptr(expert_offsets), E,
-        T, topk, N, K, _ptr(route_token), _ptr(route_slot), _ptr(topk_weights), _ptr(out),
+        _ptr(A_tiles), _ptr(gA), _ptr(W_tiles), _ptr(gW), _ptr(expert_offsets), E, T, topk, N,
+        K, _ptr(route_token), _ptr(route_slot), _ptr(topk_weights), _ptr(out),
         _ptr(workspace), ws_bytes, _stream(stream)))
 
 

@@ -31,6 +31,8 @@ __all__ = [
     "global_scale", "quantize", "pack_codes", "unpack_codes", "dequantize",
     "gemm", "route", "grouped_gemm", "combine", "prepack_scales",
     "unprepack_scales", "grouped_sf_layout", "sf_tiles_per_expert",
+    "TILE_BYTES", "operand_tiles", "grouped_operand_tiles", "tile_byte_offset",
+    "tile_scale_offset",
 ]
 
 F32 = np.float32
@@ -277,4 +279,82 @@ def grouped_sf_layout(sf_routes, expert_offsets) -> np.ndarray:
         for p in range(int(off[e]), int(off[e + 1])):
             prow = 128 * int(tb[e]) + (p - int(off[e]))
             out[_atom_offset(prow, np.arange(ks), ks // 4)] = sf[p]
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Operand tiles: the layout a pipeline stage copies in one piece
+# ---------------------------------------------------------------------------
+# A tile covers 128 rows x 256 K-elements.  Its first 16384 bytes are the
+# packed codes, row r at r * 128, with the 16-byte chunk j of a row stored at
+# chunk position j XOR (r % 8) (the 128-byte shared-memory swizzle of the
+# tensor cores); the next 2048 bytes are the tile's scales as four 512-byte
+# atoms, one per 64-element K step.  Tiles are ordered row-tile major, then
+# K block; a tile is 18432 bytes.
+
+TILE_BYTES = 16384 + 2048
+
+
+def tile_byte_offset(rt, r, kb, c, n_kb):
+    """Byte of packed byte c (0..127) of row r in row tile rt, K block kb."""
+    rt, r, kb, c = (np.asarray(v, dtype=np.int64) for v in (rt, r, kb, c))
+    return ((rt * n_kb + kb) * TILE_BYTES + r * 128 + (((c >> 4) ^ (r & 7)) << 4) + (c & 15))
+
+
+def tile_scale_offset(rt, r, kb, s, n_kb):
+    """Byte of scale column s (0..15) of row r in row tile rt, K block kb."""
+    rt, r, kb, s = (np.asarray(v, dtype=np.int64) for v in (rt, r, kb, s))
+    return ((rt * n_kb + kb) * TILE_BYTES + 16384 + (s >> 2) * 512 + (r & 31) * 16
+            + ((r >> 5) & 3) * 4 + (s & 3))
+
+
+def _scatter_rows(out, packed, sf, rows_rt, rows_r, n_kb):
+    """Writes rows (packed [n, K/2], sf [n, K/16]) to row tiles rows_rt, rows rows_r."""
+    n, half = packed.shape
+    c = np.arange(half)
+    out[tile_byte_offset(rows_rt[:, None], rows_r[:, None], c[None, :] // 128,
+                         c[None, :] % 128, n_kb)] = packed
+    s = np.arange(sf.shape[1])
+    out[tile_scale_offset(rows_rt[:, None], rows_r[:, None], s[None, :] // 16,
+                          s[None, :] % 16, n_kb)] = sf
+
+
+def operand_tiles(packed, sf):
+    """Packed [rows, K/2] + row-major scales [rows, K/16] -> tile layout.
+
+    Rows are padded to a multiple of 128 and K to a multiple of 256; padding
+    bytes are zero.
+    """
+    packed = np.asarray(packed, dtype=np.uint8)
+    sf = np.asarray(sf, dtype=np.uint8)
+    rows, half = packed.shape
+    n_rt = -(-rows // 128)
+    n_kb = -(-(2 * half) // 256)
+    out = np.zeros(n_rt * n_kb * TILE_BYTES, dtype=np.uint8)
+    r = np.arange(rows)
+    _scatter_rows(out, packed, sf, r // 128, r % 128, n_kb)
+    return out
+
+
+def grouped_operand_tiles(packed_routes, sf_routes, expert_offsets, chunk_rows=128):
+    """Route-ordered rows -> tiles where each expert's routes are cut into
+    chunks of `chunk_rows` (32, 64 or 128) and every chunk starts a fresh row
+    tile: route p of expert e, local index j = p - offsets[e], is row
+    j % chunk_rows of tile tb[e] + j // chunk_rows, with tb[e] = sum over
+    e' < e of ceil(count_e' / chunk_rows)."""
+    packed = np.asarray(packed_routes, dtype=np.uint8)
+    sf = np.asarray(sf_routes, dtype=np.uint8)
+    R, half = packed.shape
+    off = np.asarray(expert_offsets, dtype=np.int64)
+    counts = off[1:] - off[:-1]
+    chunks = -(-counts // chunk_rows)
+    tb = np.concatenate([[0], np.cumsum(chunks)])
+    n_kb = -(-(2 * half) // 256)
+    out = np.zeros(int(tb[-1]) * n_kb * TILE_BYTES, dtype=np.uint8)
+    for e in range(len(counts)):
+        lo, hi = int(off[e]), int(off[e + 1])
+        if hi > lo:
+            j = np.arange(hi - lo)
+            _scatter_rows(out, packed[lo:hi], sf[lo:hi], tb[e] + j // chunk_rows,
+                          j % chunk_rows, n_kb)
     return out

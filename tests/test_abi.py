@@ -42,9 +42,17 @@ def test_pure_host_helpers():
     assert F.nvfp4_atom_scales_bytes(300, 512) == 384 * 32
     assert F.nvfp4_atom_scales_bytes(0, 512) == 0
     assert F.nvfp4_combine_workspace_bytes(256, 6144) == 256 * 6144 * 4
-    # grouped scales: every non-empty expert can waste at most 127 padded rows
-    assert F.nvfp4_grouped_scales_bytes(2048, 128, 6144) == (2048 + 127 * 128) // 128 * 128 * 384
-    assert F.nvfp4_grouped_scales_bytes(1, 128, 64) == 128 * 4
+    # operand tiles: 18432 bytes per 128 rows x 256 K
+    assert F.nvfp4_operand_tiles_bytes(300, 512) == 3 * 2 * 18432
+    assert F.nvfp4_operand_tiles_bytes(128, 64) == 18432
+    # grouped tiles: chunk width from the mean routes per expert; every non-empty
+    # expert wastes at most chunk - 1 rows
+    assert F.nvfp4_grouped_chunk_rows(2048, 128) == 32        # 16 per expert
+    assert F.nvfp4_grouped_chunk_rows(4096, 128) == 64        # 32 per expert
+    assert F.nvfp4_grouped_chunk_rows(8192, 128) == 128       # 64 per expert
+    assert F.nvfp4_grouped_chunk_rows(65536, 128) == 128
+    assert F.nvfp4_grouped_tiles_bytes(2048, 128, 6144) == (2048 + 31 * 128) // 32 * 24 * 18432
+    assert F.nvfp4_grouped_tiles_bytes(1, 128, 64) == 18432
 
 
 def test_host_validation_without_device():
@@ -54,8 +62,9 @@ def test_host_validation_without_device():
     assert lib.nvfp4_quantize(None, -1, 16, 16, None, None, None, 0, None) == 1
     assert lib.nvfp4_quantize(None, 4, 16, 16, None, None, None, 0, None) == 1
     assert lib.nvfp4_moe_route(None, 4, 0, 8, None, None, None, None, None) == 1
-    assert lib.nvfp4_grouped_gemm(*([None] * 7), 8, 4, 2, 128, 128, None, None, None, None,
+    assert lib.nvfp4_grouped_gemm(*([None] * 5), 8, 4, 2, 128, 128, None, None, None, None,
                                   None, 0, None) == 1
+    assert lib.nvfp4_prepack_weight_tiles(None, None, 4, 64, None, None) == 1
     assert lib.nvfp4_set_timeout_ns(0) == 1
     assert lib.nvfp4_device_status(None, 0, None) == 1
     # unsupported shapes are refused before any CUDA call too

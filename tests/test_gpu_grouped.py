@@ -91,3 +91,41 @@ def test_grouped_rejects_non_monotone_offsets_on_device():
     plan.expert_offsets.copy_(torch.tensor([0, 3, 1, 4, 4], dtype=torch.int32))
     plan.gemm()
     assert F.nvfp4_device_status(reset=True) == F.NVFP4_ERR_DEVICE_CHECK
+
+
+def _hot_expert_routing(g, T, E):
+    """Slot 0 of every token goes to expert 0, slot 1 uniformly to 1..E-1: one
+    expert with T routes among experts with few, so narrow token tiles of the
+    hot expert start at rows 0, 32, 64 and 96 of their operand tiles."""
+    ids = np.empty((T, 2), np.int32)
+    ids[:, 0] = 0
+    ids[:, 1] = g.integers(1, E, T)
+    return ids
+
+
+@pytest.mark.parametrize("T,E,N,K", [(100, 16, 256, 512), (150, 16, 128, 256)])
+def test_grouped_narrow_tiles_hot_expert(T, E, N, K):
+    g = inputs.rng(T + 5 * E)
+    x = inputs.normal_bf16(g, (T, K))
+    w = _weights_host(g, E, N, K)
+    ids = _hot_expert_routing(g, T, E)
+    W = moe.quantize_experts(w.cuda())
+    plan = moe.GroupedPlan(W, T, 2, "gather")
+    plan.out.view(torch.int16).fill_(0x7FC0)
+    out = plan.run(x.cuda(), torch.from_numpy(ids).cuda())
+    torch.cuda.synchronize()
+    assert F.nvfp4_device_status() == F.NVFP4_OK
+    off, tok, slot = oracle.route(ids, E)
+    px, sx, gx = oracle.quantize(x.float().numpy())
+    ref = oracle.grouped_gemm(oracle.dequantize(px, sx, gx)[tok], _oracle_weights(w), off)
+    check_gemm(bf16_to_np(out[: 2 * T]), ref, "hot expert gather")
+    # the same routing through the weighted combine
+    wts = inputs.dirichlet_weights(g, T, 2)
+    h = inputs.normal_bf16(g, (2 * T, K))
+    plan2 = moe.GroupedPlan(W, T, 2, "combine", routing_from=plan)
+    out2 = plan2.run(h.cuda(), None, torch.from_numpy(wts).cuda(), route=False)
+    torch.cuda.synchronize()
+    assert F.nvfp4_device_status() == F.NVFP4_OK
+    ph, sh, gh = oracle.quantize(h.float().numpy())
+    y = oracle.grouped_gemm(oracle.dequantize(ph, sh, gh), _oracle_weights(w), off)
+    check_gemm(bf16_to_np(out2[:T]), oracle.combine(y, tok, slot, wts, T), "hot expert combine")

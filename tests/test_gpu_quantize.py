@@ -112,7 +112,15 @@ def test_route_rejects_bad_ids_on_device():
     assert off[-1].item() == 3
 
 
-@pytest.mark.parametrize("T,E,k,K", [(13, 6, 2, 128), (256, 128, 8, 6144)])
+def _valid_tile_mask(n_rows_routes, K, off, chunk):
+    """Bytes of the grouped tile layout that hold a route's codes or scales."""
+    ones_p = np.full((n_rows_routes, K // 2), 1, np.uint8)
+    ones_s = np.full((n_rows_routes, K // 16), 1, np.uint8)
+    return oracle.grouped_operand_tiles(ones_p, ones_s, off, chunk) == 1
+
+
+@pytest.mark.parametrize("T,E,k,K", [(13, 6, 2, 128), (256, 128, 8, 6144), (300, 4, 2, 320),
+                                     (100, 16, 2, 256)])
 def test_dispatch_gather_bit_exact(T, E, k, K):
     g = inputs.rng(T * 7 + K)
     x = inputs.normal_bf16(g, (T, K))
@@ -120,17 +128,16 @@ def test_dispatch_gather_bit_exact(T, E, k, K):
     ids_d = torch.from_numpy(ids).cuda()
     off, tok, slot, pos = F.moe_route(ids_d, E)
     R = T * k
-    packed = torch.empty((R, K // 2), dtype=torch.uint8, device="cuda")
-    sf = torch.zeros(F.nvfp4_grouped_scales_bytes(R, E, K), dtype=torch.uint8, device="cuda")
+    tiles = torch.zeros(F.nvfp4_grouped_tiles_bytes(R, E, K), dtype=torch.uint8, device="cuda")
     gd = torch.empty(1, dtype=torch.float32, device="cuda")
-    F.nvfp4_quantize_dispatch(x.cuda(), pos, k, off, E, R, packed, sf, gd)
+    F.nvfp4_quantize_dispatch(x.cuda(), pos, k, off, E, R, tiles, gd)
     p_ref, s_ref, g_ref = oracle.quantize(x.float().numpy())
     o_ref, t_ref, _ = oracle.route(ids, E)
     assert np.float32(gd.item()) == g_ref
-    assert np.array_equal(packed.cpu().numpy(), p_ref[t_ref])
-    lay = oracle.grouped_sf_layout(s_ref[t_ref], o_ref)
-    mask = oracle.grouped_sf_layout(np.ones_like(s_ref[t_ref]), o_ref) == 1
-    got = sf.cpu().numpy()[: lay.size]
+    chunk = F.nvfp4_grouped_chunk_rows(R, E)
+    lay = oracle.grouped_operand_tiles(p_ref[t_ref], s_ref[t_ref], o_ref, chunk)
+    mask = _valid_tile_mask(R, K, o_ref, chunk)
+    got = tiles.cpu().numpy()[: lay.size]
     assert np.array_equal(got[mask], lay[mask])
 
 
@@ -141,13 +148,23 @@ def test_dispatch_route_order_input_bit_exact():
     off, tok, slot, pos = F.moe_route(torch.from_numpy(ids).cuda(), E)
     R = T * k
     h = inputs.normal_bf16(g, (R, K))
-    packed = torch.empty((R, K // 2), dtype=torch.uint8, device="cuda")
-    sf = torch.zeros(F.nvfp4_grouped_scales_bytes(R, E, K), dtype=torch.uint8, device="cuda")
+    tiles = torch.zeros(F.nvfp4_grouped_tiles_bytes(R, E, K), dtype=torch.uint8, device="cuda")
     gd = torch.empty(1, dtype=torch.float32, device="cuda")
-    F.nvfp4_quantize_dispatch(h.cuda(), None, 1, off, E, R, packed, sf, gd)
+    F.nvfp4_quantize_dispatch(h.cuda(), None, 1, off, E, R, tiles, gd)
     p_ref, s_ref, g_ref = oracle.quantize(h.float().numpy())
     o_ref, _, _ = oracle.route(ids, E)
-    assert np.array_equal(packed.cpu().numpy(), p_ref)
-    lay = oracle.grouped_sf_layout(s_ref, o_ref)
-    mask = oracle.grouped_sf_layout(np.ones_like(s_ref), o_ref) == 1
-    assert np.array_equal(sf.cpu().numpy()[: lay.size][mask], lay[mask])
+    chunk = F.nvfp4_grouped_chunk_rows(R, E)
+    lay = oracle.grouped_operand_tiles(p_ref, s_ref, o_ref, chunk)
+    mask = _valid_tile_mask(R, K, o_ref, chunk)
+    assert np.array_equal(tiles.cpu().numpy()[: lay.size][mask], lay[mask])
+
+
+@pytest.mark.parametrize("rows,K", [(128, 256), (300, 512), (256, 320)])
+def test_prepack_weight_tiles_matches_oracle(rows, K):
+    g = inputs.rng(rows + K)
+    packed = g.integers(0, 256, (rows, K // 2)).astype(np.uint8)
+    sf = g.integers(0, 256, (rows, K // 16)).astype(np.uint8)
+    out = torch.full((F.nvfp4_operand_tiles_bytes(rows, K),), 0xCD, dtype=torch.uint8,
+                     device="cuda")
+    F.nvfp4_prepack_weight_tiles(torch.from_numpy(packed).cuda(), torch.from_numpy(sf).cuda(), out)
+    assert np.array_equal(out.cpu().numpy(), oracle.operand_tiles(packed, sf))

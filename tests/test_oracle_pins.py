@@ -404,3 +404,77 @@ def test_grouped_sf_layout_padding():
         assert buf[base + 1 * 16 + c] == sf[p, c]
     # expert 3 starts a fresh tile (tile 3)
     assert buf[3 * 512 + 0 * 16 + 2] == sf[133, 2]
+
+
+def test_operand_tile_golden_offsets():
+    rows, K = 300, 512
+    n_kb = K // 256
+    for kind, r, col, off in _read("tile_offsets.txt"):
+        r, col, off = int(r), int(col), int(off)
+        if kind == "b":
+            got = oracle.tile_byte_offset(r // 128, r % 128, col // 128, col % 128, n_kb)
+        else:
+            got = oracle.tile_scale_offset(r // 128, r % 128, col // 16, col % 16, n_kb)
+        assert int(got) == off, (kind, r, col, int(got), off)
+
+
+def test_operand_tiles_bijection_and_swizzle():
+    g = inputs.rng(61)
+    rows, K = 200, 768
+    packed = g.integers(0, 256, (rows, K // 2)).astype(np.uint8)
+    sf = g.integers(0, 256, (rows, K // 16)).astype(np.uint8)
+    buf = oracle.operand_tiles(packed, sf)
+    assert buf.size == 2 * 3 * oracle.TILE_BYTES
+    # every byte of the input lands on a distinct position
+    pos_b = oracle.tile_byte_offset(np.arange(rows)[:, None] // 128, np.arange(rows)[:, None] % 128,
+                                    np.arange(K // 2)[None, :] // 128,
+                                    np.arange(K // 2)[None, :] % 128, 3)
+    pos_s = oracle.tile_scale_offset(np.arange(rows)[:, None] // 128,
+                                     np.arange(rows)[:, None] % 128,
+                                     np.arange(K // 16)[None, :] // 16,
+                                     np.arange(K // 16)[None, :] % 16, 3)
+    allpos = np.concatenate([pos_b.ravel(), pos_s.ravel()])
+    assert np.unique(allpos).size == allpos.size
+    assert np.array_equal(buf[pos_b], packed) and np.array_equal(buf[pos_s], sf)
+    # the scale part of a tile is the atom layout of its 128 rows x 16 scale columns
+    tile0_sf = buf[16384:18432]
+    assert np.array_equal(tile0_sf, oracle.prepack_scales(sf[:128, :16]))
+    # within a tile, a row's 128 bytes are its 8 chunks permuted by XOR with row % 8
+    r = 13
+    row = buf[r * 128:(r + 1) * 128].reshape(8, 16)
+    for j in range(8):
+        assert np.array_equal(row[j ^ (r % 8)], packed[r, 16 * j:16 * (j + 1)])
+
+
+def test_grouped_operand_tiles_layout():
+    g = inputs.rng(62)
+    off = np.array([0, 3, 3, 133, 140], np.int64)
+    R, K = 140, 256
+    packed = g.integers(0, 256, (R, K // 2)).astype(np.uint8)
+    sf = g.integers(0, 256, (R, K // 16)).astype(np.uint8)
+    buf = oracle.grouped_operand_tiles(packed, sf, off)
+    assert buf.size == 4 * oracle.TILE_BYTES
+    # expert 2, local row 129 -> second tile of expert 2 (tile 2), row 1
+    p = 3 + 129
+    t = 2 * oracle.TILE_BYTES
+    assert np.array_equal(buf[t + 128:t + 256].reshape(8, 16)[0 ^ 1], packed[p, :16])
+    assert buf[t + 16384 + 1 * 16 + 0] == sf[p, 0]
+
+
+def test_grouped_operand_tiles_chunks():
+    g = inputs.rng(63)
+    off = np.array([0, 70, 70, 75], np.int64)          # counts 70, 0, 5
+    R, K = 75, 256
+    packed = g.integers(0, 256, (R, K // 2)).astype(np.uint8)
+    sf = g.integers(0, 256, (R, K // 16)).astype(np.uint8)
+    buf = oracle.grouped_operand_tiles(packed, sf, off, chunk_rows=32)
+    assert buf.size == (3 + 1) * oracle.TILE_BYTES       # 70 -> 3 chunks, 5 -> 1 chunk
+    # expert 0, local row 40 -> chunk 1 (tile 1), row 8; its scales are in group 0 of the atom
+    t = oracle.TILE_BYTES
+    assert np.array_equal(buf[t + 8 * 128:t + 9 * 128].reshape(8, 16)[0], packed[40, :16])
+    assert buf[t + 16384 + 8 * 16 + 0] == sf[40, 0]
+    # expert 2 starts tile 3
+    assert buf[3 * t + 16384 + 2 * 16 + 1] == sf[72, 1]
+    # chunk_rows = 128 reproduces the 128-row layout
+    assert np.array_equal(oracle.grouped_operand_tiles(packed, sf, off),
+                          oracle.grouped_operand_tiles(packed, sf, off, chunk_rows=128))

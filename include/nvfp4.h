@@ -229,6 +229,43 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* A_tiles, const float* gA,
                                 void* out, float* workspace, size_t workspace_bytes,
                                 void* stream);
 
+/*
+ * Allocation-free weighted-combine grouped GEMM.  (This entry point is a
+ * library convenience; the pages have no counterpart.)
+ *
+ * Same operation and arguments as nvfp4_grouped_gemm with topk_weights given
+ * (out = BF16 [T, N], out[t] = sum over the routes p of token t of
+ * w[t, slot(p)] * y[p]), except that there is no workspace argument: the FP32
+ * sums go to a fixed workspace inside the library, a device array of
+ * nvfp4_noalloc_workspace_floats() floats (16 MiB) that every GPU loading
+ * the library holds until the process exits.  It serves callers that cannot
+ * allocate device memory at call time and have no workspace to lend: plugin
+ * interfaces that hand a kernel only its inputs and outputs, and serving
+ * loops that forbid the CUDA allocator after start-up (cudaMalloc may
+ * synchronise the device and can fail under memory pressure).  The call
+ * allocates and frees nothing.
+ *
+ *   - T * N must not exceed nvfp4_noalloc_workspace_floats(); larger shapes
+ *     return NVFP4_ERR_UNSUPPORTED before anything is enqueued.
+ *   - The first call on a device looks up the workspace's device address
+ *     (once per device, with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call clears the part of the workspace it uses, then accumulates
+ *     into it.  All calls on a device share the one workspace, so calls that
+ *     overlap on the GPU (different streams without ordering between them)
+ *     race and give wrong sums; serialise them.
+ */
+size_t nvfp4_noalloc_workspace_floats(void);
+
+nvfp4_status nvfp4_grouped_gemm_combine_noalloc(const uint8_t* A_tiles, const float* gA,
+                                                const uint8_t* W_tiles, const float* gW,
+                                                const int32_t* expert_offsets, int32_t E,
+                                                int64_t T, int32_t topk, int64_t N, int64_t K,
+                                                const int32_t* route_token,
+                                                const int32_t* route_slot,
+                                                const float* topk_weights, void* out,
+                                                void* stream);
+
 #ifdef __cplusplus
 }  /* extern "C" */
 #endif

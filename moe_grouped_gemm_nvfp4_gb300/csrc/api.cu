@@ -381,3 +381,105 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* A_tiles, const float* gA,
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of the weighted-combine grouped GEMM.
+// ---------------------------------------------------------------------------
+namespace {
+
+// FP32 combine workspace shared by every call of
+// nvfp4_grouped_gemm_combine_noalloc on a device.  Every GPU that loads this
+// library holds it until the process exits.
+constexpr size_t kNoallocWorkspaceFloats = 4u * 1024u * 1024u;   // 16 MiB
+static __device__ __align__(256) float g_noalloc_workspace[kNoallocWorkspaceFloats];
+
+std::mutex g_noalloc_mu;
+float* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the workspace for the current device.  In host code the
+// array's name only stands in for the symbol, so the address comes from
+// cudaGetSymbolAddress, looked up once per device with that device current.
+nvfp4_status noalloc_workspace(float** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cuda_fail();
+  if (dev < 0 || dev >= kMaxDevices) return NVFP4_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_workspace) != cudaSuccess || !p) return cuda_fail();
+    g_noalloc_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return NVFP4_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t nvfp4_noalloc_workspace_floats(void) { return kNoallocWorkspaceFloats; }
+
+nvfp4_status nvfp4_grouped_gemm_combine_noalloc(const uint8_t* A_tiles, const float* gA,
+                                                const uint8_t* W_tiles, const float* gW,
+                                                const int32_t* expert_offsets, int32_t E,
+                                                int64_t T, int32_t topk, int64_t N, int64_t K,
+                                                const int32_t* route_token,
+                                                const int32_t* route_slot,
+                                                const float* topk_weights, void* out,
+                                                void* stream) {
+  if (!A_tiles || !gA || !W_tiles || !gW || !expert_offsets || !out || !route_token ||
+      !route_slot || !topk_weights)
+    return NVFP4_ERR_INVALID_ARG;
+  if (E <= 0 || T < 0 || topk <= 0 || N <= 0 || K <= 0) return NVFP4_ERR_INVALID_ARG;
+  if (N % 128 != 0 || K % 64 != 0 || E > nvfp4::kGroupedMaxExperts) return NVFP4_ERR_UNSUPPORTED;
+  // the combine workspace holds T x N floats: refuse what does not fit
+  if (T > 0 && static_cast<uint64_t>(T) * static_cast<uint64_t>(N) > kNoallocWorkspaceFloats)
+    return NVFP4_ERR_UNSUPPORTED;
+  const int64_t R = T * topk;
+  if (R > (1LL << 30) || static_cast<int64_t>(E) * N > (1LL << 30)) return NVFP4_ERR_UNSUPPORTED;
+  if (!aligned16(A_tiles) || !aligned16(W_tiles) || !aligned16(out)) return NVFP4_ERR_UNSUPPORTED;
+  DeviceState* d = nullptr;
+  nvfp4_status st = device_state(&d);
+  if (st != NVFP4_OK) return st;
+  float* ws = nullptr;
+  st = noalloc_workspace(&ws);
+  if (st != NVFP4_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (R == 0) {
+    if (T > 0 && cudaMemsetAsync(out, 0, T * N * 2, s) != cudaSuccess) return cuda_fail();
+    return NVFP4_OK;
+  }
+  CUtensorMap unused;
+  std::memset(&unused, 0, sizeof(unused));
+  nvfp4::GemmArgs a{};
+  a.sfx = W_tiles;
+  a.sfy = A_tiles;
+  a.gx = gW;
+  a.gy = gA;
+  a.K = K;
+  a.rows_x = static_cast<int32_t>(E * N);
+  a.rows_y = static_cast<int32_t>(R);
+  a.expert_offsets = expert_offsets;
+  a.E = E;
+  a.n_out = static_cast<int32_t>(N);
+  a.out = out;
+  a.ldc = N;
+  a.vec_store = 1;
+  a.ybox_rows = 16;
+  a.route_token = route_token;
+  a.route_slot = route_slot;
+  a.topk_w = topk_weights;
+  a.topk = topk;
+  a.ws = ws;
+  a.status = d->status;
+  a.timeout_ns = g_timeout_ns.load();
+  // the workspace keeps the previous call's sums: clear the part this call uses
+  if (cudaMemsetAsync(ws, 0, static_cast<size_t>(T) * N * sizeof(float), s) != cudaSuccess)
+    return cuda_fail();
+  if (nvfp4::launch_gemm(unused, unused, a, nvfp4::kGroupedCombine, d->sms, s) != cudaSuccess)
+    return cuda_fail();
+  if (nvfp4::launch_combine_finalize(ws, T, N, out, d->sms, s) != cudaSuccess) return cuda_fail();
+  return NVFP4_OK;
+}
+
+}  // extern "C"

@@ -52,6 +52,9 @@ _SIGS = {
     "nvfp4_combine_workspace_bytes": (_SZ, [_I64, _I64]),
     "nvfp4_grouped_gemm": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I64, _I32, _I64, _I64,
                                           _P, _P, _P, _P, _P, _SZ, _P]),
+    "nvfp4_noalloc_workspace_floats": (_SZ, []),
+    "nvfp4_grouped_gemm_combine_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I64, _I32,
+                                                          _I64, _I64, _P, _P, _P, _P, _P]),
 }
 
 
@@ -193,6 +196,21 @@ def nvfp4_grouped_gemm(A_tiles, gA, W_tiles, gW, expert_offsets, E: int, T: int,
         _ptr(A_tiles), _ptr(gA), _ptr(W_tiles), _ptr(gW), _ptr(expert_offsets), E, T, topk, N,
         K, _ptr(route_token), _ptr(route_slot), _ptr(topk_weights), _ptr(out),
         _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def nvfp4_noalloc_workspace_floats() -> int:
+    return load().nvfp4_noalloc_workspace_floats()
+
+
+def nvfp4_grouped_gemm_combine_noalloc(A_tiles, gA, W_tiles, gW, expert_offsets, E: int, T: int,
+                                       topk: int, N: int, K: int, route_token, route_slot,
+                                       topk_weights, out, stream=None) -> None:
+    """Weighted-combine grouped GEMM using the library's own fixed workspace,
+    for callers that cannot allocate device memory at call time (see the C
+    header for the size limit and the rule that overlapping calls race)."""
+    _check("nvfp4_grouped_gemm_combine_noalloc", load().nvfp4_grouped_gemm_combine_noalloc(
+        _ptr(A_tiles), _ptr(gA), _ptr(W_tiles), _ptr(gW), _ptr(expert_offsets), E, T, topk, N,
+        K, _ptr(route_token), _ptr(route_slot), _ptr(topk_weights), _ptr(out), _stream(stream)))
 
 
 # ------------------------------------------- allocating conveniences (torch)

@@ -86,6 +86,21 @@ def step_bytes(n_active):
     return w + io
 
 
+def max_over_ranks(values, world, device):
+    """Elementwise max of per-rank timings (every rank gets the result)."""
+    local = torch.tensor(values, dtype=torch.float64)
+    if world > 1:
+        t = local.to(device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        local = t.cpu()
+    return local.tolist()
+
+
+def aggregate_tflops(flops_per_rank_step, steps, ms_max, world):
+    """Whole-job throughput: every rank's work over the slowest rank's time."""
+    return world * flops_per_rank_step * steps / (ms_max * 1e-3) / 1e12
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -263,19 +278,15 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_ms = s2.elapsed_time(e2)
 
-    local = torch.tensor([ms_total, e2e_ms, gu_ms, dn_ms], dtype=torch.float64)
-    if world > 1:
-        t = local.to(device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        local = t.cpu()
-    ms_total, e2e_ms, gu_ms, dn_ms = local.tolist()
+    ms_total, e2e_ms, gu_ms, dn_ms = max_over_ranks([ms_total, e2e_ms, gu_ms, dn_ms], world,
+                                                    device)
     if rank != 0:
         return None
 
     ms_step = ms_total / args.steps
     fl = flops_per_step()
-    value = world * fl * args.steps / (ms_total * 1e-3) / 1e12
-    e2e_value = world * fl * args.steps / (e2e_ms * 1e-3) / 1e12
+    value = aggregate_tflops(fl, args.steps, ms_total, world)
+    e2e_value = aggregate_tflops(fl, args.steps, e2e_ms, world)
     peak, peak_kind = measured_peaks()
     R = T * TOPK
     gu_bytes = gemm_bytes(K1, N1, n_active, R, R)

@@ -65,8 +65,19 @@ int nvfp4_version(void);
  */
 nvfp4_status nvfp4_device_status(void* stream, int reset, int* status_out);
 
-/* Bounded-wait limit of the pipeline kernels in nanoseconds (default 1 s). */
+/* Bounded-wait limit of the pipeline kernels in nanoseconds (default 1 s,
+ * or NVFP4_TIMEOUT_NS from the environment at the first call). */
 nvfp4_status nvfp4_set_timeout_ns(uint64_t ns);
+
+/*
+ * Test hook for the failure path of the GEMM kernels (0 = off, the default).
+ * Flag 1: the producer of every CTA leaves its first pipeline stage unfilled,
+ * so the first MMA wait can only end by its time limit; the kernel then
+ * records NVFP4_ERR_TIMEOUT, drains its own copies and MMAs, frees tensor
+ * memory and returns, and the output is incomplete.  Meant for tests, with a
+ * short nvfp4_set_timeout_ns.  Other bits return NVFP4_ERR_INVALID_ARG.
+ */
+nvfp4_status nvfp4_debug_set_flags(uint32_t flags);
 
 /*
  * Scale bytes of a [rows, cols] matrix in the tensor-core atom layout:

@@ -29,6 +29,7 @@ struct DeviceState {
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 std::atomic<uint64_t> g_timeout_ns{1000000000ull};
+std::atomic<uint32_t> g_debug_flags{0u};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 nvfp4_status cuda_fail() {
@@ -118,6 +119,12 @@ int nvfp4_version(void) { return 100; }
 nvfp4_status nvfp4_set_timeout_ns(uint64_t ns) {
   if (ns == 0) return NVFP4_ERR_INVALID_ARG;
   g_timeout_ns.store(ns);
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_debug_set_flags(uint32_t flags) {
+  if (flags & ~nvfp4::kDebugSkipFirstStage) return NVFP4_ERR_INVALID_ARG;
+  g_debug_flags.store(flags);
   return NVFP4_OK;
 }
 
@@ -253,6 +260,7 @@ nvfp4_status nvfp4_gemm(const uint8_t* A, const uint8_t* sfA, const float* gA,
   a.ybox_rows = static_cast<int32_t>(ybox_rows);
   a.status = d->status;
   a.timeout_ns = g_timeout_ns.load();
+  a.debug_flags = g_debug_flags.load();
   if (nvfp4::launch_gemm(tmx, tmy, a, swap ? nvfp4::kDenseRowsY : nvfp4::kDenseRowsX, d->sms,
                          static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return cuda_fail();
@@ -370,6 +378,7 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* A_tiles, const float* gA,
   a.ws = workspace;
   a.status = d->status;
   a.timeout_ns = g_timeout_ns.load();
+  a.debug_flags = g_debug_flags.load();
   if (combine && cudaMemsetAsync(workspace, 0, nvfp4_combine_workspace_bytes(T, N), s) != cudaSuccess)
     return cuda_fail();
   if (nvfp4::launch_gemm(unused, unused, a, combine ? nvfp4::kGroupedCombine : nvfp4::kGrouped,

@@ -288,6 +288,15 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
           const uint32_t ssfx = sx + kXTileBytes;
           const uint32_t sy = sx + C::kYOffset;
           const uint32_t ssfy = sy + C::kYTileBytes;
+          if ((a.debug_flags & kDebugSkipFirstStage) && issued == 0 && stage == 0 && kb == 0 &&
+              u == static_cast<int>(blockIdx.x)) {
+            // test hook: leave stage 0 empty; its consumers' bounded waits expire.
+            // Counted as issued so the drain below keeps stage numbers aligned
+            // (its wait on this stage ends by the time limit too).
+            ++issued;
+            if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+            continue;
+          }
           const uint32_t ybytes = grouped ? ybox * 16 * kRowBytes : ny_loads * a.ybox_rows * kRowBytes;
           const uint32_t bytes = kXTileBytes + ybytes + 2 * ksteps * 512;
           mbar_arrive_expect_tx(full_bar(stage), bytes);

@@ -60,7 +60,12 @@ struct GemmArgs {
   float* ws;                       // combine: FP32 [T, n_out]
   int* status;
   uint64_t timeout_ns;
+  uint32_t debug_flags;            // kDebugSkipFirstStage: test hook, see nvfp4.h
 };
+
+// Test hook: the producer of every CTA leaves its first pipeline stage
+// unfilled, so the first MMA wait can only end by its time limit.
+constexpr uint32_t kDebugSkipFirstStage = 1u;
 
 constexpr int kGroupedMaxExperts = 256;
 

@@ -38,6 +38,7 @@ _SIGS = {
     "nvfp4_version": (ctypes.c_int, []),
     "nvfp4_device_status": (ctypes.c_int, [_P, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]),
     "nvfp4_set_timeout_ns": (ctypes.c_int, [ctypes.c_uint64]),
+    "nvfp4_debug_set_flags": (ctypes.c_int, [ctypes.c_uint32]),
     "nvfp4_atom_scales_bytes": (_SZ, [_I64, _I64]),
     "nvfp4_quantize": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _P, _U32, _P]),
     "nvfp4_prepack_weights": (ctypes.c_int, [_P, _I64, _I64, _P, _P]),
@@ -124,6 +125,10 @@ def nvfp4_device_status(reset: bool = True, stream=None) -> int:
 
 def nvfp4_set_timeout_ns(ns: int) -> None:
     _check("nvfp4_set_timeout_ns", load().nvfp4_set_timeout_ns(int(ns)))
+
+
+def nvfp4_debug_set_flags(flags: int) -> None:
+    _check("nvfp4_debug_set_flags", load().nvfp4_debug_set_flags(int(flags)))
 
 
 def nvfp4_atom_scales_bytes(rows: int, cols: int) -> int:

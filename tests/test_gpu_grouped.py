@@ -129,3 +129,36 @@ def test_grouped_narrow_tiles_hot_expert(T, E, N, K):
     ph, sh, gh = oracle.quantize(h.float().numpy())
     y = oracle.grouped_gemm(oracle.dequantize(ph, sh, gh), _oracle_weights(w), off)
     check_gemm(bf16_to_np(out2[:T]), oracle.combine(y, tok, slot, wts, T), "hot expert combine")
+
+
+def test_bounded_wait_expires_reports_timeout_and_context_survives():
+    """Failure path: a stage that never fills (test hook) makes the MMA wait run
+    out; the kernel records NVFP4_ERR_TIMEOUT and returns, and the next call on
+    the same context computes the right result."""
+    T, E, k, N, K = 16, 4, 2, 128, 256
+    g = inputs.rng(9)
+    x = inputs.normal_bf16(g, (T, K)).cuda()
+    w = _weights_host(g, E, N, K)
+    ids = torch.from_numpy(inputs.uniform_topk(g, T, E, k)).cuda()
+    W = moe.quantize_experts(w.cuda())
+    plan = moe.GroupedPlan(W, T, k, "gather")
+    plan.route(ids)
+    plan.quantize(x)
+    torch.cuda.synchronize()
+    F.nvfp4_device_status(reset=True)
+    F.nvfp4_set_timeout_ns(20_000_000)                 # 20 ms
+    F.nvfp4_debug_set_flags(1)
+    try:
+        plan.gemm()
+        assert F.nvfp4_device_status(reset=True) == F.NVFP4_ERR_TIMEOUT
+    finally:
+        F.nvfp4_debug_set_flags(0)
+        F.nvfp4_set_timeout_ns(1_000_000_000)
+    plan.out.view(torch.int16).fill_(0x7FC0)
+    plan.gemm()
+    torch.cuda.synchronize()
+    assert F.nvfp4_device_status() == F.NVFP4_OK
+    off, tok, _ = oracle.route(ids.cpu().numpy(), E)
+    px, sx, gx = oracle.quantize(x.float().cpu().numpy())
+    ref = oracle.grouped_gemm(oracle.dequantize(px, sx, gx)[tok], _oracle_weights(w), off)
+    check_gemm(bf16_to_np(plan.out[: T * k]), ref, "after timeout")

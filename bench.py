@@ -246,9 +246,36 @@ def run_ours(args, rank, world, local_rank):
     status = F.nvfp4_device_status(reset=True)
     if status != F.NVFP4_OK:
         raise RuntimeError(f"device status {F.nvfp4_status_string(status)} during the timed run")
-    ms_total = start.elapsed_time(end)
+    eager_ms_total = start.elapsed_time(end)
     gu_ms = statistics.mean(e[0][0].elapsed_time(e[0][1]) for e in ev)
     dn_ms = statistics.mean(e[1][0].elapsed_time(e[1][1]) for e in ev)
+
+    # The same step recorded in a CUDA graph (one launch per step): the way a
+    # server runs a fixed-shape decode step.  This is the headline figure.
+    captured = moe.CapturedStep(layer, dev_in["x"], dev_in["ids"], dev_in["h"], dev_in["wts"])
+    for _ in range(args.warmup):
+        captured.replay()
+    torch.cuda.synchronize()
+    sampler2 = ClockSampler(local_rank)
+    sampler2.start()
+    gs, ge = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("timed_graph")
+    gs.record()
+    for _ in range(args.steps):
+        captured.replay()
+    ge.record()
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks_graph = sampler2.stop()
+    status = F.nvfp4_device_status(reset=True)
+    if status != F.NVFP4_OK:
+        raise RuntimeError(f"device status {F.nvfp4_status_string(status)} during the graph run")
+    ms_total = gs.elapsed_time(ge)
 
     # end to end through the public API with host buffers: H2D of the step's
     # inputs from pinned memory, the step, D2H of both outputs
@@ -261,7 +288,7 @@ def run_ours(args, rank, world, local_rank):
     def e2e_step():
         for k in dev_in:
             dev_in[k].copy_(pinned[k], non_blocking=True)
-        gu, dn = step()
+        gu, dn = captured.replay()
         out_gu.copy_(gu[: T * TOPK], non_blocking=True)
         out_dn.copy_(dn[:T], non_blocking=True)
 
@@ -278,8 +305,8 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_ms = s2.elapsed_time(e2)
 
-    ms_total, e2e_ms, gu_ms, dn_ms = max_over_ranks([ms_total, e2e_ms, gu_ms, dn_ms], world,
-                                                    device)
+    ms_total, eager_ms_total, e2e_ms, gu_ms, dn_ms = max_over_ranks(
+        [ms_total, eager_ms_total, e2e_ms, gu_ms, dn_ms], world, device)
     if rank != 0:
         return None
 
@@ -312,7 +339,13 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms / args.steps, 4)},
         "gpu_launches": 8 * args.steps,
-        "clocks": clocks,
+        "step_mode": "CUDA graph replay of the whole step (one graph launch per step)",
+        "eager": {"ms_per_step": round(eager_ms_total / args.steps, 4),
+                  "value": round(aggregate_tflops(fl, args.steps, eager_ms_total, world), 2),
+                  "note": "same step launched kernel by kernel; the per-launch CUDA events of "
+                          "this pass give roofline.launch_ms and down_launch"},
+        "clocks": clocks_graph or clocks,
+        "clocks_eager": clocks,
         "setup_s": round(setup_s, 1),
     }
     if world == 1 and not args.no_cpu_baseline:

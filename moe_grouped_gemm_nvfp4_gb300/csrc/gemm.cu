@@ -47,27 +47,33 @@ constexpr int kTmemCols = 512;
 // of its scale copies and MMAs.
 template <int BN>
 struct Cfg {
-  static_assert(BN == 32 || BN == 64 || BN == 128, "tile width");
+  static_assert(BN == 32 || BN == 64 || BN == 128 || BN == 256, "tile width");
   static constexpr int kYTileBytes = BN * kRowBytes;
-  // stage: [X codes 16 KB][X scales 2 KB][Y codes][Y scales 2 KB]; the X part
-  // has the operand-tile layout, so a tile K block lands with one copy
+  static constexpr int kSfyAtomsPerStep = BN == 256 ? 2 : 1;   // 128-row scale atoms of Y
+  static constexpr int kSfyStageBytes = kSfyAtomsPerStep * kSFStageBytes;
+  // stage: [X codes 16 KB][X scales 2 KB][Y codes][Y scales]; the X part has
+  // the operand-tile layout, so a tile K block lands with one copy
   static constexpr int kYOffset = kXTileBytes + kSFStageBytes;
-  static constexpr int kStageBytes = kYOffset + kYTileBytes + kSFStageBytes;
+  static constexpr int kStageBytes = kYOffset + kYTileBytes + kSfyStageBytes;
   static_assert(kYOffset % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle alignment");
-  static constexpr int kStages = BN == 32 ? 9 : 6;
+  static constexpr int kStages = BN == 32 ? 9 : (BN == 256 ? 4 : 6);
   // Stages are released to the producer in groups with one tcgen05.commit
-  // per group: the tensor pipe does not overlap the operations before a
-  // commit with those after it, so a commit per stage would serialise every
-  // stage's scale copies and MMAs behind the previous stage's.
-  static constexpr int kGroup = 3;
+  // per group (fewer tcgen05 instructions per stage).
+  static constexpr int kGroup = BN == 256 ? 2 : 3;
   static constexpr int kGroups = kStages / kGroup;
   static_assert(kStages % kGroup == 0, "stage groups");
   static constexpr int kIssuers = BN <= 64 ? 2 : 1;   // MMA-issuing threads
+  // accumulator buffers: two (the epilogue of one tile overlaps the next
+  // tile's MMAs), except for 256-wide tiles, whose one accumulator already
+  // takes half of tensor memory
+  static constexpr int kAccBufs = BN == 256 ? 1 : 2;
   static constexpr int kAccCols = BN;                  // one accumulator
   // accumulator (buffer b, issuer j) at column (b * kIssuers + j) * BN;
-  // scale columns follow the accumulators
-  static constexpr int kSfColBase = 2 * kIssuers * BN;
-  static_assert(kSfColBase + kStages * 32 <= kTmemCols, "tensor memory budget");
+  // scale columns follow the accumulators: per stage 16 for X, 16 or 32 for Y
+  static constexpr int kSfColBase = kAccBufs * kIssuers * BN;
+  static constexpr int kSfyColsPerStep = 4 * kSfyAtomsPerStep;
+  static constexpr int kSfColsPerStage = 16 + 4 * kSfyColsPerStep;
+  static_assert(kSfColBase + kStages * kSfColsPerStage <= kTmemCols, "tensor memory budget");
   // barriers: full[S], empty[S / G], acc_full[2], acc_empty[2], drain
   static constexpr int kBarBytes = 8 * (kStages + kGroups + 5);
   static constexpr int kTableInts = 3 * (kGroupedMaxExperts + 1);
@@ -85,6 +91,8 @@ struct Unit {
   int32_t e;          // expert (grouped)
   int64_t sfx_off;    // dense: X scale atoms at k-block 0; grouped: X operand tile
   int64_t sfy_off;    // dense: Y scale atoms at k-block 0; grouped: Y operand tile
+  int32_t x_reused;   // grouped: the expert has more than one token tile, so its
+                      // weight tiles are read again by other units
 };
 
 struct Tables {
@@ -117,6 +125,7 @@ __device__ __forceinline__ Unit get_unit(int u, int mode, const GemmArgs& a, con
     const int64_t n_kb = (a.K + kBK - 1) / kBK;
     un.sfx_off = static_cast<int64_t>(e * mtiles + mt) * n_kb * kOperandTileBytes;
     un.sfy_off = static_cast<int64_t>(t.tb[e] + nt) * n_kb * kOperandTileBytes;
+    un.x_reused = cnt > BN;
   } else {
     const int tx = u % tiles_x;
     const int ty = u / tiles_x;
@@ -127,6 +136,7 @@ __device__ __forceinline__ Unit get_unit(int u, int mode, const GemmArgs& a, con
     un.y_rows = min(BN, a.rows_y - ty * BN);
     un.sfx_off = static_cast<int64_t>(tx) * atoms_per_rowtile * 512;
     un.sfy_off = static_cast<int64_t>(ty * (BN / 128)) * atoms_per_rowtile * 512;
+    un.x_reused = 1;
   }
   return un;
 }
@@ -266,7 +276,10 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint64_t pol_x = grouped ? l2_policy_evict_first() : l2_policy_evict_last();
+      // Weights read by a single unit stream through L2 (evict first); weights
+      // that other token tiles of the same expert read again stay (normal).
+      const uint64_t pol_once = l2_policy_evict_first();
+      const uint64_t pol_again = grouped ? l2_policy_evict_normal() : l2_policy_evict_last();
       const uint64_t pol_y = l2_policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
@@ -274,6 +287,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
       bool alive = true;
       for (int u = blockIdx.x; u < units && alive; u += gridDim.x) {
         const Unit un = get_unit<BN>(u, mode, a, t, tiles_x, atoms_per_rowtile);
+        const uint64_t pol_x = un.x_reused ? pol_again : pol_once;
         const int ybox = (un.y_rows + 15) >> 4;                  // 16-row groups
         const int ny_loads = (un.y_rows + a.ybox_rows - 1) / a.ybox_rows;
         for (int kb = 0; kb < nkb; ++kb) {
@@ -298,7 +312,10 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
             continue;
           }
           const uint32_t ybytes = grouped ? ybox * 16 * kRowBytes : ny_loads * a.ybox_rows * kRowBytes;
-          const uint32_t bytes = kXTileBytes + ybytes + 2 * ksteps * 512;
+          // the second 128-row scale group of a 256-wide Y tile exists only when
+          // the tile has more than 128 rows
+          const int sfy_groups = (C::kSfyAtomsPerStep == 2 && un.y_rows > 128) ? 2 : 1;
+          const uint32_t bytes = kXTileBytes + ybytes + (1 + sfy_groups) * ksteps * 512;
           mbar_arrive_expect_tx(full_bar(stage), bytes);
           if (grouped) {
             // operand tiles: X codes + scales in one contiguous copy, Y codes
@@ -317,6 +334,10 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
                       full_bar(stage), pol_x);
             bulk_load(ssfy, a.sfy + un.sfy_off + kb * kSFStageBytes, ksteps * 512,
                       full_bar(stage), pol_y);
+            if (sfy_groups == 2)
+              bulk_load(ssfy + kSFStageBytes,
+                        a.sfy + un.sfy_off + atoms_per_rowtile * 512 + kb * kSFStageBytes,
+                        ksteps * 512, full_bar(stage), pol_y);
           }
           ++issued;
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
@@ -356,7 +377,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
           const uint32_t ssfx = sx + kXTileBytes;
           const uint32_t sy = sx + C::kYOffset;
           const uint32_t ssfy = sy + C::kYTileBytes;
-          const uint32_t tsfx = tmem + C::kSfColBase + stage * 32;
+          const uint32_t tsfx = tmem + C::kSfColBase + stage * C::kSfColsPerStage;
           const uint32_t tsfy = tsfx + 16;
           const uint64_t dx = sdesc_sw128(sx);
           const uint64_t dy = sdesc_sw128(sy);
@@ -364,9 +385,14 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
           // scale address handed to the MMA is a multiple of 4 columns (an
           // address inside an atom's column group faults as misaligned).
           for (int ks = j; ks < ksteps; ks += C::kIssuers) {
+            const uint32_t tsfy_ks = tsfy + C::kSfyColsPerStep * ks;
             tc_cp_sf_atom(tsfx + 4 * ks, sdesc_sf_atom(ssfx + 512 * ks));
-            tc_cp_sf_atom(tsfy + 4 * ks, sdesc_sf_atom(ssfy + 512 * ks));
-            tc_mma_nvf4(d_tmem, dx + 2 * ks, dy + 2 * ks, idesc, tsfx + 4 * ks, tsfy + 4 * ks,
+            tc_cp_sf_atom(tsfy_ks, sdesc_sf_atom(ssfy + 512 * ks));
+            // rows 128-255 of a 256-wide Y tile: the next 4 columns (the MMA
+            // reads the scales of row n from column base + n / 32)
+            if (C::kSfyAtomsPerStep == 2 && un.y_rows > 128)
+              tc_cp_sf_atom(tsfy_ks + 4, sdesc_sf_atom(ssfy + kSFStageBytes + 512 * ks));
+            tc_mma_nvf4(d_tmem, dx + 2 * ks, dy + 2 * ks, idesc, tsfx + 4 * ks, tsfy_ks,
                         (kb > 0 || ks >= C::kIssuers) ? 1u : 0u);
           }
           if (stage % C::kGroup == C::kGroup - 1) tc_commit(empty_bar(stage / C::kGroup));
@@ -374,8 +400,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
         }
         if (!alive) break;
         tc_commit(accf_bar(abuf));
-        abuf ^= 1;
-        if (abuf == 0) aphase ^= 1u;
+        if (++abuf == C::kAccBufs) { abuf = 0; aphase ^= 1u; }
       }
       // Drain: wait for every MMA and copy issued above before teardown.
       tc_commit(drain_bar);
@@ -393,6 +418,24 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
     const int n_acc = (a.K >> 6) < C::kIssuers ? static_cast<int>(a.K >> 6) : C::kIssuers;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const Unit un = get_unit<BN>(u, mode, a, t, tiles_x, atoms_per_rowtile);
+      // Combine: fetch this lane's tokens and routing weights (one token per
+      // lane per 32-column chunk) before waiting, so the dependent L2 round
+      // trips overlap the MMAs instead of following them.
+      int c_tok[BN / 32];
+      float c_w[BN / 32];
+      if (mode == kGroupedCombine) {
+#pragma unroll
+        for (int ci = 0; ci < BN / 32; ++ci) {
+          const int col = ci * 32 + lane;
+          c_tok[ci] = 0;
+          c_w[ci] = 0.0f;
+          if (col < un.y_rows) {
+            const int p = un.y_row0 + col;
+            c_tok[ci] = a.route_token[p];
+            c_w[ci] = a.topk_w[static_cast<int64_t>(c_tok[ci]) * a.topk + a.route_slot[p]];
+          }
+        }
+      }
       // all lanes wait (sleeping between polls, see mbar_wait_sleepy), then
       // agree, so the warp-collective loads below stay converged
       if (!__all_sync(0xFFFFFFFFu, mbar_wait_sleepy(accf_bar(abuf), aphase, ctl, a.status)))
@@ -449,8 +492,11 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
           if (col < n_valid) {
             const int64_t y = un.y_row0 + col;
             if (mode == kGroupedCombine) {
-              const int tok = a.route_token[y];
-              const float w = a.topk_w[static_cast<int64_t>(tok) * a.topk + a.route_slot[y]];
+              int tok = c_tok[0];
+              float w = c_w[0];
+#pragma unroll
+              for (int ci = 1; ci < BN / 32; ++ci)
+                if (c0 == ci * 32) { tok = c_tok[ci]; w = c_w[ci]; }
               float* dst = a.ws + static_cast<int64_t>(tok) * a.n_out + f0;
 #pragma unroll
               for (int v = 0; v < 8; ++v) {
@@ -489,8 +535,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
       }
       tc_fence_before();
       mbar_arrive(acce_bar(abuf));
-      abuf ^= 1;
-      if (abuf == 0) aphase ^= 1u;
+      if (++abuf == C::kAccBufs) { abuf = 0; aphase ^= 1u; }
     }
   }
 
@@ -528,6 +573,7 @@ cudaError_t init_gemm_attributes() {
   cudaError_t e = set_smem_attr<32>();
   if (e == cudaSuccess) e = set_smem_attr<64>();
   if (e == cudaSuccess) e = set_smem_attr<128>();
+  if (e == cudaSuccess) e = set_smem_attr<256>();
   return e;
 }
 
@@ -542,10 +588,14 @@ cudaError_t launch_gemm(const CUtensorMap& tmx, const CUtensorMap& tmy, const Ge
                         int mode, int sms, cudaStream_t s) {
   int grid = sms;
   if (mode == kDenseRowsX || mode == kDenseRowsY) {
-    const int64_t units = ((a.rows_x + 127) / 128) * ((a.rows_y + 127) / 128);
+    // 256-wide Y tiles when Y is large: each MMA instruction then covers
+    // 128 x 256 x 64 and a K block moves 1.33x fewer bytes per FLOP
+    const int bn = (mode == kDenseRowsX && a.rows_y >= 256) ? 256 : 128;
+    const int64_t units = ((a.rows_x + 127) / 128) * ((a.rows_y + bn - 1) / bn);
     if (units < grid) grid = static_cast<int>(units);
     if (grid < 1) return cudaSuccess;
-    return launch_bn<128>(tmx, tmy, a, mode, grid, s);
+    return bn == 256 ? launch_bn<256>(tmx, tmy, a, mode, grid, s)
+                     : launch_bn<128>(tmx, tmy, a, mode, grid, s);
   }
   switch (grouped_chunk_rows(a.rows_y, a.E)) {
     case 32: return launch_bn<32>(tmx, tmy, a, mode, grid, s);

@@ -70,12 +70,15 @@ constexpr uint32_t kDebugSkipFirstStage = 1u;
 constexpr int kGroupedMaxExperts = 256;
 
 // Token-tile width of the grouped GEMM (32, 64 or 128 routes), a function of
-// the route and expert counts only: ~1.6x the mean routes per expert, so the
-// widest experts of a balanced routing still fit one tile.  The grouped
+// the route and expert counts only.  With want = ~1.6x the mean routes per
+// expert: 32 when the widest experts of a balanced routing fit 32 rows, 64 up
+// to a mean of ~80 routes (an expert that needs a second 64-row tile re-reads
+// its weight tile from L2 within the same wave, while 64-row tiles keep two
+// MMA issuers and a double-buffered accumulator), else 128.  The grouped
 // activation layout cuts each expert's routes into chunks of this width.
 inline int grouped_chunk_rows(int64_t routes, int experts) {
   const int64_t want = experts > 0 ? (routes * 8 + experts * 5 - 1) / (experts * 5) : 128;
-  return want <= 32 ? 32 : (want <= 64 ? 64 : 128);
+  return want <= 32 ? 32 : (want <= 128 ? 64 : 128);
 }
 constexpr int64_t kOperandTileBytes = 16384 + 2048;   // 128 rows x 256 K: codes + scale atoms
 

@@ -148,3 +148,27 @@ class DecodeLayer:
         if timing is not None:
             timing[1][1].record()
         return gu.out, dn.out
+
+
+class CapturedStep:
+    """A DecodeLayer step recorded once into a CUDA graph over fixed input
+    buffers; replay() re-runs every kernel of the step with one launch.
+
+    The library's per-device set-up runs on the first eager call, so call
+    the layer's step() at least once before capturing.
+    """
+
+    def __init__(self, layer: DecodeLayer, x, topk_ids, h, topk_weights):
+        self.inputs = (x, topk_ids, h, topk_weights)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            layer.step(*self.inputs)
+        torch.cuda.current_stream().wait_stream(side)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.outputs = layer.step(*self.inputs)
+
+    def replay(self):
+        self.graph.replay()
+        return self.outputs

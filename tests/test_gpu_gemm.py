@@ -73,6 +73,7 @@ def _quantized_case(M, N, K, seed):
     (16, 256, 512),        # the tiny single-GEMM workload
     (1, 128, 64), (15, 128, 128), (64, 384, 192), (65, 128, 256),
     (127, 130, 320), (128, 128, 512), (129, 256, 256), (300, 200, 1024), (512, 384, 2048),
+    (256, 448, 512), (200, 700, 320),     # 256-wide tiles with ragged last tiles
 ])
 def test_gemm_matches_oracle(M, N, K):
     ops, ref = _quantized_case(M, N, K, seed=M * 31 + N * 7 + K)

@@ -103,7 +103,8 @@ def _hot_expert_routing(g, T, E):
     return ids
 
 
-@pytest.mark.parametrize("T,E,N,K", [(100, 16, 256, 512), (150, 16, 128, 256)])
+@pytest.mark.parametrize("T,E,N,K", [(100, 16, 256, 512), (150, 16, 128, 256),
+                                     (150, 8, 128, 256)])     # 32-, 32- and 64-row tiles
 def test_grouped_narrow_tiles_hot_expert(T, E, N, K):
     g = inputs.rng(T + 5 * E)
     x = inputs.normal_bf16(g, (T, K))

@@ -50,6 +50,9 @@ struct Cfg {
   static_assert(BN == 32 || BN == 64 || BN == 128 || BN == 256, "tile width");
   static constexpr int kYTileBytes = BN * kRowBytes;
   static constexpr int kSfyAtomsPerStep = BN == 256 ? 2 : 1;   // 128-row scale atoms of Y
+  // rows of one grouped operand tile / layout chunk: a 256-row token tile
+  // spans two consecutive 128-row operand tiles
+  static constexpr int kLayoutRows = BN < 128 ? BN : 128;
   static constexpr int kSfyStageBytes = kSfyAtomsPerStep * kSFStageBytes;
   // stage: [X codes 16 KB][X scales 2 KB][Y codes][Y scales]; the X part has
   // the operand-tile layout, so a tile K block lands with one copy
@@ -124,7 +127,8 @@ __device__ __forceinline__ Unit get_unit(int u, int mode, const GemmArgs& a, con
     un.y_rows = min(BN, cnt - nt * BN);
     const int64_t n_kb = (a.K + kBK - 1) / kBK;
     un.sfx_off = static_cast<int64_t>(e * mtiles + mt) * n_kb * kOperandTileBytes;
-    un.sfy_off = static_cast<int64_t>(t.tb[e] + nt) * n_kb * kOperandTileBytes;
+    un.sfy_off =
+        static_cast<int64_t>(t.tb[e] + nt * (BN / Cfg<BN>::kLayoutRows)) * n_kb * kOperandTileBytes;
     un.x_reused = cnt > BN;
   } else {
     const int tx = u % tiles_x;
@@ -233,7 +237,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
         ok = ok && (c >= 0);
         t.off[e] = o0;
         su += mtiles * ((c + BN - 1) / BN);
-        st += (c + BN - 1) / BN;
+        st += (c + C::kLayoutRows - 1) / C::kLayoutRows;
       }
       int32_t iu = su, it = st;
 #pragma unroll
@@ -247,7 +251,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
         const int32_t c = a.expert_offsets[e + 1] - a.expert_offsets[e];
         t.up[e] = pu; t.tb[e] = pt;
         pu += mtiles * ((c + BN - 1) / BN);
-        pt += (c + BN - 1) / BN;
+        pt += (c + C::kLayoutRows - 1) / C::kLayoutRows;
       }
       const bool all_ok = __all_sync(0xFFFFFFFFu, ok);
       if (lane == 31) {
@@ -315,6 +319,8 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
           // the second 128-row scale group of a 256-wide Y tile exists only when
           // the tile has more than 128 rows
           const int sfy_groups = (C::kSfyAtomsPerStep == 2 && un.y_rows > 128) ? 2 : 1;
+          // grouped 256-row tiles: codes of rows 0-127 and 128+ come from two tiles
+          const int ybox_lo = min(ybox, 8), ybox_hi = ybox - ybox_lo;
           const uint32_t bytes = kXTileBytes + ybytes + (1 + sfy_groups) * ksteps * 512;
           mbar_arrive_expect_tx(full_bar(stage), bytes);
           if (grouped) {
@@ -323,8 +329,14 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
             const uint8_t* xt = a.sfx + un.sfx_off + kb * kOperandTileBytes;
             const uint8_t* yt = a.sfy + un.sfy_off + kb * kOperandTileBytes;
             bulk_load(sx, xt, kXTileBytes + ksteps * 512, full_bar(stage), pol_x);
-            bulk_load(sy, yt, ybox * 16 * kRowBytes, full_bar(stage), pol_y);
+            bulk_load(sy, yt, ybox_lo * 16 * kRowBytes, full_bar(stage), pol_y);
             bulk_load(ssfy, yt + kXTileBytes, ksteps * 512, full_bar(stage), pol_y);
+            if (ybox_hi > 0) {               // second operand tile of a 256-row token tile
+              const uint8_t* yt2 = yt + static_cast<int64_t>((a.K + kBK - 1) / kBK) * kOperandTileBytes;
+              bulk_load(sy + 128 * kRowBytes, yt2, ybox_hi * 16 * kRowBytes, full_bar(stage), pol_y);
+              bulk_load(ssfy + kSFStageBytes, yt2 + kXTileBytes, ksteps * 512, full_bar(stage),
+                        pol_y);
+            }
           } else {
             tma_load_2d(sx, &tmx, full_bar(stage), kb * kRowBytes, un.x_row0, pol_x);
             for (int j = 0; j < ny_loads; ++j)
@@ -597,10 +609,11 @@ cudaError_t launch_gemm(const CUtensorMap& tmx, const CUtensorMap& tmy, const Ge
     return bn == 256 ? launch_bn<256>(tmx, tmy, a, mode, grid, s)
                      : launch_bn<128>(tmx, tmy, a, mode, grid, s);
   }
-  switch (grouped_chunk_rows(a.rows_y, a.E)) {
+  switch (grouped_tile_width(a.rows_y, a.E)) {
     case 32: return launch_bn<32>(tmx, tmy, a, mode, grid, s);
     case 64: return launch_bn<64>(tmx, tmy, a, mode, grid, s);
-    default: return launch_bn<128>(tmx, tmy, a, mode, grid, s);
+    case 128: return launch_bn<128>(tmx, tmy, a, mode, grid, s);
+    default: return launch_bn<256>(tmx, tmy, a, mode, grid, s);
   }
 }
 

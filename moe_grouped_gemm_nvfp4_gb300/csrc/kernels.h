@@ -80,6 +80,14 @@ inline int grouped_chunk_rows(int64_t routes, int experts) {
   const int64_t want = experts > 0 ? (routes * 8 + experts * 5 - 1) / (experts * 5) : 128;
   return want <= 32 ? 32 : (want <= 128 ? 64 : 128);
 }
+
+// Token-tile width of the grouped GEMM itself: the chunk width, or 256 when
+// experts average well over 160 routes (prefill).  A 256-row token tile spans
+// two consecutive 128-row operand tiles of the layout above.
+inline int grouped_tile_width(int64_t routes, int experts) {
+  const int64_t want = experts > 0 ? (routes * 8 + experts * 5 - 1) / (experts * 5) : 128;
+  return want > 256 ? 256 : grouped_chunk_rows(routes, experts);
+}
 constexpr int64_t kOperandTileBytes = 16384 + 2048;   // 128 rows x 256 K: codes + scale atoms
 
 cudaError_t init_gemm_attributes();

@@ -81,7 +81,11 @@ struct Cfg {
   static constexpr int kBarBytes = 8 * (kStages + kGroups + 5);
   static constexpr int kTableInts = 3 * (kGroupedMaxExperts + 1);
   static constexpr int kCtlOffset = kStages * kStageBytes + kBarBytes;
-  static constexpr int kTablesOffset = kCtlOffset + 32;
+  // ring of per-unit token-row counts published by the producer (see below)
+  static constexpr int kUnitRing = 16;
+  static_assert(kUnitRing > kStages + 1, "unit ring depth");
+  static constexpr int kRingOffset = kCtlOffset + 32;
+  static constexpr int kTablesOffset = kRingOffset + 4 * kUnitRing;
   static constexpr int kSmemBytes = kTablesOffset + 4 * kTableInts + 1024;  // + align slack
   static_assert(kSmemBytes <= 232448 - 64, "shared memory budget");
 };
@@ -199,6 +203,13 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
   CtaCtl* ctl = reinterpret_cast<CtaCtl*>(smem + C::kCtlOffset);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kCtlOffset + 16);
   int32_t* tab = reinterpret_cast<int32_t*>(smem + C::kTablesOffset);
+  // The producer decodes every unit anyway; it publishes the unit's token-row
+  // count here before arriving on the unit's first full barrier, and the MMA
+  // issuers read it after waiting on that barrier, which keeps the unit
+  // decoding (binary search, divisions) off their critical path.  The
+  // producer runs at most kStages stages ahead, so a slot is never rewritten
+  // before it is read.
+  volatile int32_t* unit_rows = reinterpret_cast<volatile int32_t*>(smem + C::kRingOffset);
   Tables t{tab, tab + (kGroupedMaxExperts + 1), tab + 2 * (kGroupedMaxExperts + 1)};
   __shared__ int32_t s_units;
 
@@ -289,8 +300,10 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
       uint32_t phase = 0;
       int64_t issued = 0;
       bool alive = true;
-      for (int u = blockIdx.x; u < units && alive; u += gridDim.x) {
+      int uidx = 0;
+      for (int u = blockIdx.x; u < units && alive; u += gridDim.x, ++uidx) {
         const Unit un = get_unit<BN>(u, mode, a, t, tiles_x, atoms_per_rowtile);
+        unit_rows[uidx & (C::kUnitRing - 1)] = un.y_rows;
         const uint64_t pol_x = un.x_reused ? pol_again : pol_once;
         const int ybox = (un.y_rows + 15) >> 4;                  // 16-row groups
         const int ny_loads = (un.y_rows + a.ybox_rows - 1) / a.ybox_rows;
@@ -372,9 +385,10 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
       int abuf = 0;
       uint32_t aphase = 0;
       bool alive = true;
-      for (int u = blockIdx.x; u < units && alive; u += gridDim.x) {
-        const Unit un = get_unit<BN>(u, mode, a, t, tiles_x, atoms_per_rowtile);
-        const uint32_t idesc = idesc_nvf4(static_cast<uint32_t>((un.y_rows + 15) & ~15));
+      int uidx = 0;
+      for (int u = blockIdx.x; u < units && alive; u += gridDim.x, ++uidx) {
+        int y_rows = 0;
+        uint32_t idesc = 0;
         if (!mbar_wait(acce_bar(abuf), aphase ^ 1u, ctl, a.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + (abuf * C::kIssuers + j) * C::kAccCols;
@@ -384,6 +398,10 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
           // wait alone orders them.  (A tcgen05 thread-sync fence here would
           // wait for this thread's earlier MMAs and serialise the stages.)
           if (!mbar_wait(full_bar(stage), phase, ctl, a.status)) { alive = false; break; }
+          if (kb == 0) {
+            y_rows = unit_rows[uidx & (C::kUnitRing - 1)];
+            idesc = idesc_nvf4(static_cast<uint32_t>((y_rows + 15) & ~15));
+          }
           const int ksteps = min(4, static_cast<int>((a.K >> 6) - 4 * kb));
           const uint32_t sx = sbase + stage * C::kStageBytes;
           const uint32_t ssfx = sx + kXTileBytes;
@@ -402,7 +420,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
             tc_cp_sf_atom(tsfy_ks, sdesc_sf_atom(ssfy + 512 * ks));
             // rows 128-255 of a 256-wide Y tile: the next 4 columns (the MMA
             // reads the scales of row n from column base + n / 32)
-            if (C::kSfyAtomsPerStep == 2 && un.y_rows > 128)
+            if (C::kSfyAtomsPerStep == 2 && y_rows > 128)
               tc_cp_sf_atom(tsfy_ks + 4, sdesc_sf_atom(ssfy + kSFStageBytes + 512 * ks));
             tc_mma_nvf4(d_tmem, dx + 2 * ks, dy + 2 * ks, idesc, tsfx + 4 * ks, tsfy_ks,
                         (kb > 0 || ks >= C::kIssuers) ? 1u : 0u);

@@ -45,9 +45,13 @@ constexpr int kTmemCols = 512;
 // weight bytes in flight per SM, which is what the decode shapes need: each
 // stage stays occupied for a memory round trip plus the tensor-pipe latency
 // of its scale copies and MMAs.
-template <int BN>
+template <int BN, int MT = 1>
 struct Cfg {
   static_assert(BN == 32 || BN == 64 || BN == 128 || BN == 256, "tile width");
+  // MT 128-row X tiles per unit (2 only for 32-row token tiles: two MMAs per
+  // K step share the token operand, halving the units, the token re-reads
+  // and the scale copies of Y per weight byte)
+  static_assert(MT == 1 || (MT == 2 && BN == 32), "unit height");
   static constexpr int kYTileBytes = BN * kRowBytes;
   static constexpr int kSfyAtomsPerStep = BN == 256 ? 2 : 1;   // 128-row scale atoms of Y
   // rows of one grouped operand tile / layout chunk: a 256-row token tile
@@ -56,13 +60,14 @@ struct Cfg {
   static constexpr int kSfyStageBytes = kSfyAtomsPerStep * kSFStageBytes;
   // stage: [X codes 16 KB][X scales 2 KB][Y codes][Y scales]; the X part has
   // the operand-tile layout, so a tile K block lands with one copy
-  static constexpr int kYOffset = kXTileBytes + kSFStageBytes;
+  static constexpr int kXPartBytes = kXTileBytes + kSFStageBytes;   // codes + scales
+  static constexpr int kYOffset = MT * kXPartBytes;
   static constexpr int kStageBytes = kYOffset + kYTileBytes + kSfyStageBytes;
   static_assert(kYOffset % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle alignment");
-  static constexpr int kStages = BN == 32 ? 9 : (BN == 256 ? 4 : 6);
+  static constexpr int kStages = MT == 2 ? 5 : (BN == 32 ? 9 : (BN == 256 ? 4 : 6));
   // Stages are released to the producer in groups with one tcgen05.commit
   // per group (fewer tcgen05 instructions per stage).
-  static constexpr int kGroup = BN == 256 ? 2 : 3;
+  static constexpr int kGroup = MT == 2 ? 1 : (BN == 256 ? 2 : 3);
   static constexpr int kGroups = kStages / kGroup;
   static_assert(kStages % kGroup == 0, "stage groups");
   static constexpr int kIssuers = BN <= 64 ? 2 : 1;   // MMA-issuing threads
@@ -71,11 +76,12 @@ struct Cfg {
   // takes half of tensor memory
   static constexpr int kAccBufs = BN == 256 ? 1 : 2;
   static constexpr int kAccCols = BN;                  // one accumulator
-  // accumulator (buffer b, issuer j) at column (b * kIssuers + j) * BN;
-  // scale columns follow the accumulators: per stage 16 for X, 16 or 32 for Y
-  static constexpr int kSfColBase = kAccBufs * kIssuers * BN;
+  // accumulator (buffer b, X tile x, issuer j) at column ((b * MT + x) *
+  // kIssuers + j) * BN; scale columns follow the accumulators: per stage 16
+  // for each X tile, 16 or 32 for Y
+  static constexpr int kSfColBase = kAccBufs * MT * kIssuers * BN;
   static constexpr int kSfyColsPerStep = 4 * kSfyAtomsPerStep;
-  static constexpr int kSfColsPerStage = 16 + 4 * kSfyColsPerStep;
+  static constexpr int kSfColsPerStage = 16 * MT + 4 * kSfyColsPerStep;
   static_assert(kSfColBase + kStages * kSfColsPerStage <= kTmemCols, "tensor memory budget");
   // barriers: full[S], empty[S / G], acc_full[2], acc_empty[2], drain
   static constexpr int kBarBytes = 8 * (kStages + kGroups + 5);
@@ -108,7 +114,7 @@ struct Tables {
   int32_t* tb;        // [E+1] scale-tile prefix
 };
 
-template <int BN>
+template <int BN, int MT>
 __device__ __forceinline__ Unit get_unit(int u, int mode, const GemmArgs& a, const Tables& t,
                                          int tiles_x, int64_t atoms_per_rowtile) {
   Unit un;
@@ -120,9 +126,10 @@ __device__ __forceinline__ Unit get_unit(int u, int mode, const GemmArgs& a, con
     }
     const int e = lo;
     const int mtiles = a.n_out >> 7;
+    const int munits = mtiles / MT;               // units per token tile
     const int local = u - t.up[e];
-    const int mt = local % mtiles;
-    const int nt = local / mtiles;
+    const int mt = (local % munits) * MT;         // first X tile of the unit
+    const int nt = local / munits;
     const int cnt = t.off[e + 1] - t.off[e];
     un.e = e;
     un.x_row0 = e * a.n_out + mt * 128;
@@ -132,7 +139,7 @@ __device__ __forceinline__ Unit get_unit(int u, int mode, const GemmArgs& a, con
     const int64_t n_kb = (a.K + kBK - 1) / kBK;
     un.sfx_off = static_cast<int64_t>(e * mtiles + mt) * n_kb * kOperandTileBytes;
     un.sfy_off =
-        static_cast<int64_t>(t.tb[e] + nt * (BN / Cfg<BN>::kLayoutRows)) * n_kb * kOperandTileBytes;
+        static_cast<int64_t>(t.tb[e] + nt * (BN / Cfg<BN, MT>::kLayoutRows)) * n_kb * kOperandTileBytes;
     un.x_reused = cnt > BN;
   } else {
     const int tx = u % tiles_x;
@@ -185,11 +192,11 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, u
   return false;
 }
 
-template <int BN>
+template <int BN, int MT>
 __global__ void __launch_bounds__(kThreads, 1)
 nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmy,
                   const GemmArgs a, int mode) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, MT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -239,7 +246,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
       const int E = a.E;
       const int per = (E + 31) / 32;
       const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
-      const int mtiles = a.n_out >> 7;
+      const int mtiles = (a.n_out >> 7) / MT;       // units per token tile
       int32_t su = 0, st = 0;
       bool ok = true;
       for (int e = e0; e < e1; ++e) {
@@ -302,7 +309,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
       bool alive = true;
       int uidx = 0;
       for (int u = blockIdx.x; u < units && alive; u += gridDim.x, ++uidx) {
-        const Unit un = get_unit<BN>(u, mode, a, t, tiles_x, atoms_per_rowtile);
+        const Unit un = get_unit<BN, MT>(u, mode, a, t, tiles_x, atoms_per_rowtile);
         unit_rows[uidx & (C::kUnitRing - 1)] = un.y_rows;
         const uint64_t pol_x = un.x_reused ? pol_again : pol_once;
         const int ybox = (un.y_rows + 15) >> 4;                  // 16-row groups
@@ -334,7 +341,8 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
           const int sfy_groups = (C::kSfyAtomsPerStep == 2 && un.y_rows > 128) ? 2 : 1;
           // grouped 256-row tiles: codes of rows 0-127 and 128+ come from two tiles
           const int ybox_lo = min(ybox, 8), ybox_hi = ybox - ybox_lo;
-          const uint32_t bytes = kXTileBytes + ybytes + (1 + sfy_groups) * ksteps * 512;
+          const uint32_t bytes =
+              MT * (kXTileBytes + ksteps * 512) + ybytes + sfy_groups * ksteps * 512;
           mbar_arrive_expect_tx(full_bar(stage), bytes);
           if (grouped) {
             // operand tiles: X codes + scales in one contiguous copy, Y codes
@@ -342,6 +350,10 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
             const uint8_t* xt = a.sfx + un.sfx_off + kb * kOperandTileBytes;
             const uint8_t* yt = a.sfy + un.sfy_off + kb * kOperandTileBytes;
             bulk_load(sx, xt, kXTileBytes + ksteps * 512, full_bar(stage), pol_x);
+            if (MT == 2)                   // the unit's second weight tile
+              bulk_load(sx + C::kXPartBytes,
+                        xt + static_cast<int64_t>((a.K + kBK - 1) / kBK) * kOperandTileBytes,
+                        kXTileBytes + ksteps * 512, full_bar(stage), pol_x);
             bulk_load(sy, yt, ybox_lo * 16 * kRowBytes, full_bar(stage), pol_y);
             bulk_load(ssfy, yt + kXTileBytes, ksteps * 512, full_bar(stage), pol_y);
             if (ybox_hi > 0) {               // second operand tile of a 256-row token tile
@@ -391,7 +403,8 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
         uint32_t idesc = 0;
         if (!mbar_wait(acce_bar(abuf), aphase ^ 1u, ctl, a.status)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem + (abuf * C::kIssuers + j) * C::kAccCols;
+        // accumulator of X tile x: column ((abuf * MT + x) * kIssuers + j) * BN
+        const uint32_t d_tmem = tmem + (abuf * MT * C::kIssuers + j) * C::kAccCols;
         for (int kb = 0; kb < nkb; ++kb) {
           // The stage's operands arrive by TMA / bulk copy, completing on the
           // mbarrier; the MMAs read them through the same async proxy, so the
@@ -408,7 +421,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
           const uint32_t sy = sx + C::kYOffset;
           const uint32_t ssfy = sy + C::kYTileBytes;
           const uint32_t tsfx = tmem + C::kSfColBase + stage * C::kSfColsPerStage;
-          const uint32_t tsfy = tsfx + 16;
+          const uint32_t tsfy = tsfx + 16 * MT;
           const uint64_t dx = sdesc_sw128(sx);
           const uint64_t dy = sdesc_sw128(sy);
           // Every token tile starts at row 0 of its operand tile, so every
@@ -424,6 +437,12 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
               tc_cp_sf_atom(tsfy_ks + 4, sdesc_sf_atom(ssfy + kSFStageBytes + 512 * ks));
             tc_mma_nvf4(d_tmem, dx + 2 * ks, dy + 2 * ks, idesc, tsfx + 4 * ks, tsfy_ks,
                         (kb > 0 || ks >= C::kIssuers) ? 1u : 0u);
+            if (MT == 2) {                 // second weight tile, same token operand
+              tc_cp_sf_atom(tsfx + 16 + 4 * ks, sdesc_sf_atom(ssfx + C::kXPartBytes + 512 * ks));
+              tc_mma_nvf4(d_tmem + C::kIssuers * C::kAccCols,
+                          sdesc_sw128(sx + C::kXPartBytes) + 2 * ks, dy + 2 * ks, idesc,
+                          tsfx + 16 + 4 * ks, tsfy_ks, (kb > 0 || ks >= C::kIssuers) ? 1u : 0u);
+            }
           }
           if (stage % C::kGroup == C::kGroup - 1) tc_commit(empty_bar(stage / C::kGroup));
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
@@ -447,7 +466,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
     // accumulators that received at least one K step (issuer j's first is ks = j)
     const int n_acc = (a.K >> 6) < C::kIssuers ? static_cast<int>(a.K >> 6) : C::kIssuers;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
-      const Unit un = get_unit<BN>(u, mode, a, t, tiles_x, atoms_per_rowtile);
+      const Unit un = get_unit<BN, MT>(u, mode, a, t, tiles_x, atoms_per_rowtile);
       // Combine: fetch this lane's tokens and routing weights (one token per
       // lane per 32-column chunk) before waiting, so the dependent L2 round
       // trips overlap the MMAs instead of following them.
@@ -472,10 +491,12 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
         break;
       tc_fence_after();
       const float alpha = __fmul_rn(grouped ? a.gx[un.e] : a.gx[0], gy);
-      const uint32_t taddr =
-          tmem + (static_cast<uint32_t>(q * 32) << 16) + abuf * C::kIssuers * C::kAccCols;
       const int n_valid = un.y_rows;
-      const int xr = un.x_local0 + row;            // output feature / X row
+#pragma unroll 1
+      for (int xt = 0; xt < MT; ++xt) {           // the unit's X tiles
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) +
+                             (abuf * MT + xt) * C::kIssuers * C::kAccCols;
+      const int xr = un.x_local0 + xt * 128 + row;  // output feature / X row
       for (int c0 = 0; c0 < n_valid; c0 += 32) {
         uint32_t r[32];
         tmem_ld32(taddr + c0, r);
@@ -518,7 +539,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
           // 32 features of this warp, so stores and FP32 reductions are vectors.
           warp_transpose32(r, lane);
           const int col = c0 + lane;
-          const int f0 = un.x_local0 + q * 32;          // first feature of this warp
+          const int f0 = un.x_local0 + xt * 128 + q * 32;  // first feature of this warp
           if (col < n_valid) {
             const int64_t y = un.y_row0 + col;
             if (mode == kGroupedCombine) {
@@ -563,6 +584,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
           }
         }
       }
+      }  // X tiles
       tc_fence_before();
       mbar_arrive(acce_bar(abuf));
       if (++abuf == C::kAccBufs) { abuf = 0; aphase ^= 1u; }
@@ -593,24 +615,25 @@ __global__ void __launch_bounds__(256) combine_finalize_kernel(const float* __re
 
 }  // namespace
 
-template <int BN>
+template <int BN, int MT = 1>
 static cudaError_t set_smem_attr() {
-  return cudaFuncSetAttribute(nvfp4_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              Cfg<BN>::kSmemBytes);
+  return cudaFuncSetAttribute(nvfp4_gemm_kernel<BN, MT>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN, MT>::kSmemBytes);
 }
 
 cudaError_t init_gemm_attributes() {
   cudaError_t e = set_smem_attr<32>();
+  if (e == cudaSuccess) e = set_smem_attr<32, 2>();
   if (e == cudaSuccess) e = set_smem_attr<64>();
   if (e == cudaSuccess) e = set_smem_attr<128>();
   if (e == cudaSuccess) e = set_smem_attr<256>();
   return e;
 }
 
-template <int BN>
+template <int BN, int MT = 1>
 static cudaError_t launch_bn(const CUtensorMap& tmx, const CUtensorMap& tmy, const GemmArgs& a,
                              int mode, int grid, cudaStream_t s) {
-  nvfp4_gemm_kernel<BN><<<grid, kThreads, Cfg<BN>::kSmemBytes, s>>>(tmx, tmy, a, mode);
+  nvfp4_gemm_kernel<BN, MT><<<grid, kThreads, Cfg<BN, MT>::kSmemBytes, s>>>(tmx, tmy, a, mode);
   return cudaGetLastError();
 }
 
@@ -628,7 +651,9 @@ cudaError_t launch_gemm(const CUtensorMap& tmx, const CUtensorMap& tmy, const Ge
                      : launch_bn<128>(tmx, tmy, a, mode, grid, s);
   }
   switch (grouped_tile_width(a.rows_y, a.E)) {
-    case 32: return launch_bn<32>(tmx, tmy, a, mode, grid, s);
+    case 32:   // two weight tiles per unit when the expert's rows pair up
+      return (a.n_out / 128) % 2 == 0 ? launch_bn<32, 2>(tmx, tmy, a, mode, grid, s)
+                                       : launch_bn<32>(tmx, tmy, a, mode, grid, s);
     case 64: return launch_bn<64>(tmx, tmy, a, mode, grid, s);
     case 128: return launch_bn<128>(tmx, tmy, a, mode, grid, s);
     default: return launch_bn<256>(tmx, tmy, a, mode, grid, s);

@@ -389,72 +389,78 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
     __syncwarp();
   } else if (warp == 1 || (C::kIssuers == 2 && warp == 6)) {
     // ---------------------------------------------------------------- MMA
-    // Issuer j takes the K steps with ks % kIssuers == j of every stage.
+    // Issuer j takes the K steps with ks % kIssuers == j of every stage.  The
+    // whole warp runs the loop (every lane waits on the barriers, so the
+    // control flow stays converged and uniform); one elected lane issues each
+    // tcgen05 instruction.
     const int j = (warp == 6) ? 1 : 0;
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      int abuf = 0;
-      uint32_t aphase = 0;
-      bool alive = true;
-      int uidx = 0;
-      for (int u = blockIdx.x; u < units && alive; u += gridDim.x, ++uidx) {
-        int y_rows = 0;
-        uint32_t idesc = 0;
-        if (!mbar_wait(acce_bar(abuf), aphase ^ 1u, ctl, a.status)) break;
-        tc_fence_after();
-        // accumulator of X tile x: column ((abuf * MT + x) * kIssuers + j) * BN
-        const uint32_t d_tmem = tmem + (abuf * MT * C::kIssuers + j) * C::kAccCols;
-        for (int kb = 0; kb < nkb; ++kb) {
-          // The stage's operands arrive by TMA / bulk copy, completing on the
-          // mbarrier; the MMAs read them through the same async proxy, so the
-          // wait alone orders them.  (A tcgen05 thread-sync fence here would
-          // wait for this thread's earlier MMAs and serialise the stages.)
-          if (!mbar_wait(full_bar(stage), phase, ctl, a.status)) { alive = false; break; }
-          if (kb == 0) {
-            y_rows = unit_rows[uidx & (C::kUnitRing - 1)];
-            idesc = idesc_nvf4(static_cast<uint32_t>((y_rows + 15) & ~15));
-          }
-          const int ksteps = min(4, static_cast<int>((a.K >> 6) - 4 * kb));
-          const uint32_t sx = sbase + stage * C::kStageBytes;
-          const uint32_t ssfx = sx + kXTileBytes;
-          const uint32_t sy = sx + C::kYOffset;
-          const uint32_t ssfy = sy + C::kYTileBytes;
-          const uint32_t tsfx = tmem + C::kSfColBase + stage * C::kSfColsPerStage;
-          const uint32_t tsfy = tsfx + 16 * MT;
-          const uint64_t dx = sdesc_sw128(sx);
-          const uint64_t dy = sdesc_sw128(sy);
-          // Every token tile starts at row 0 of its operand tile, so every
-          // scale address handed to the MMA is a multiple of 4 columns (an
-          // address inside an atom's column group faults as misaligned).
-          for (int ks = j; ks < ksteps; ks += C::kIssuers) {
-            const uint32_t tsfy_ks = tsfy + C::kSfyColsPerStep * ks;
-            tc_cp_sf_atom(tsfx + 4 * ks, sdesc_sf_atom(ssfx + 512 * ks));
-            tc_cp_sf_atom(tsfy_ks, sdesc_sf_atom(ssfy + 512 * ks));
-            // rows 128-255 of a 256-wide Y tile: the next 4 columns (the MMA
-            // reads the scales of row n from column base + n / 32)
-            if (C::kSfyAtomsPerStep == 2 && y_rows > 128)
-              tc_cp_sf_atom(tsfy_ks + 4, sdesc_sf_atom(ssfy + kSFStageBytes + 512 * ks));
-            tc_mma_nvf4(d_tmem, dx + 2 * ks, dy + 2 * ks, idesc, tsfx + 4 * ks, tsfy_ks,
-                        (kb > 0 || ks >= C::kIssuers) ? 1u : 0u);
-            if (MT == 2) {                 // second weight tile, same token operand
-              tc_cp_sf_atom(tsfx + 16 + 4 * ks, sdesc_sf_atom(ssfx + C::kXPartBytes + 512 * ks));
-              tc_mma_nvf4(d_tmem + C::kIssuers * C::kAccCols,
-                          sdesc_sw128(sx + C::kXPartBytes) + 2 * ks, dy + 2 * ks, idesc,
-                          tsfx + 16 + 4 * ks, tsfy_ks, (kb > 0 || ks >= C::kIssuers) ? 1u : 0u);
-            }
-          }
-          if (stage % C::kGroup == C::kGroup - 1) tc_commit(empty_bar(stage / C::kGroup));
-          if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+    int stage = 0;
+    uint32_t phase = 0;
+    int abuf = 0;
+    uint32_t aphase = 0;
+    bool alive = true;
+    int uidx = 0;
+    for (int u = blockIdx.x; u < units && alive; u += gridDim.x, ++uidx) {
+      int y_rows = 0;
+      uint32_t idesc = 0;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(acce_bar(abuf), aphase ^ 1u, ctl, a.status))) break;
+      tc_fence_after();
+      // accumulator of X tile x: column ((abuf * MT + x) * kIssuers + j) * BN
+      const uint32_t d_tmem = tmem + (abuf * MT * C::kIssuers + j) * C::kAccCols;
+      for (int kb = 0; kb < nkb; ++kb) {
+        // The stage's operands arrive by TMA / bulk copy, completing on the
+        // mbarrier; the MMAs read them through the same async proxy, so the
+        // wait alone orders them.  (A tcgen05 thread-sync fence here would
+        // wait for this thread's earlier MMAs and serialise the stages.)
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(full_bar(stage), phase, ctl, a.status))) {
+          alive = false;
+          break;
         }
-        if (!alive) break;
-        tc_commit(accf_bar(abuf));
-        if (++abuf == C::kAccBufs) { abuf = 0; aphase ^= 1u; }
+        if (kb == 0) {
+          y_rows = unit_rows[uidx & (C::kUnitRing - 1)];
+          idesc = idesc_nvf4(static_cast<uint32_t>((y_rows + 15) & ~15));
+        }
+        const int ksteps = min(4, static_cast<int>((a.K >> 6) - 4 * kb));
+        const uint32_t sx = sbase + stage * C::kStageBytes;
+        const uint32_t ssfx = sx + kXTileBytes;
+        const uint32_t sy = sx + C::kYOffset;
+        const uint32_t ssfy = sy + C::kYTileBytes;
+        const uint32_t tsfx = tmem + C::kSfColBase + stage * C::kSfColsPerStage;
+        const uint32_t tsfy = tsfx + 16 * MT;
+        const uint64_t dx = sdesc_sw128(sx);
+        const uint64_t dy = sdesc_sw128(sy);
+        // Every token tile starts at row 0 of its operand tile, so every
+        // scale address handed to the MMA is a multiple of 4 columns (an
+        // address inside an atom's column group faults as misaligned).
+        for (int ks = j; ks < ksteps; ks += C::kIssuers) {
+          const uint32_t tsfy_ks = tsfy + C::kSfyColsPerStep * ks;
+          tc_cp_sf_atom_elect(tsfx + 4 * ks, sdesc_sf_atom(ssfx + 512 * ks));
+          tc_cp_sf_atom_elect(tsfy_ks, sdesc_sf_atom(ssfy + 512 * ks));
+          // rows 128-255 of a 256-wide Y tile: the next 4 columns (the MMA
+          // reads the scales of row n from column base + n / 32)
+          if (C::kSfyAtomsPerStep == 2 && y_rows > 128)
+            tc_cp_sf_atom_elect(tsfy_ks + 4, sdesc_sf_atom(ssfy + kSFStageBytes + 512 * ks));
+          tc_mma_nvf4_elect(d_tmem, dx + 2 * ks, dy + 2 * ks, idesc, tsfx + 4 * ks, tsfy_ks,
+                            (kb > 0 || ks >= C::kIssuers) ? 1u : 0u);
+          if (MT == 2) {                 // second weight tile, same token operand
+            tc_cp_sf_atom_elect(tsfx + 16 + 4 * ks,
+                                sdesc_sf_atom(ssfx + C::kXPartBytes + 512 * ks));
+            tc_mma_nvf4_elect(d_tmem + C::kIssuers * C::kAccCols,
+                              sdesc_sw128(sx + C::kXPartBytes) + 2 * ks, dy + 2 * ks, idesc,
+                              tsfx + 16 + 4 * ks, tsfy_ks,
+                              (kb > 0 || ks >= C::kIssuers) ? 1u : 0u);
+          }
+        }
+        if (stage % C::kGroup == C::kGroup - 1) tc_commit_elect(empty_bar(stage / C::kGroup));
+        if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
       }
-      // Drain: wait for every MMA and copy issued above before teardown.
-      tc_commit(drain_bar);
-      mbar_wait_drain(drain_bar, 0, ctl->timeout_ns);
+      if (!alive) break;
+      tc_commit_elect(accf_bar(abuf));
+      if (++abuf == C::kAccBufs) { abuf = 0; aphase ^= 1u; }
     }
+    // Drain: wait for every MMA and copy issued above before teardown.
+    tc_commit_elect(drain_bar);
+    if (lane == 0) mbar_wait_drain(drain_bar, 0, ctl->timeout_ns);
     __syncwarp();
   } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------ epilogue

@@ -70,7 +70,13 @@ struct Cfg {
   static constexpr int kGroup = MT == 2 ? 1 : (BN == 256 ? 2 : 3);
   static constexpr int kGroups = kStages / kGroup;
   static_assert(kStages % kGroup == 0, "stage groups");
-  static constexpr int kIssuers = BN <= 64 ? 2 : 1;   // MMA-issuing threads
+  static constexpr int kIssuers = BN <= 64 ? 2 : 1;   // MMA-issuing warps
+  // With one MMA warp, warp 6 becomes a scale warp: it copies the stage's Y
+  // scales (and for 128-wide tiles the X scales too) into tensor memory and
+  // signals the MMA warp, so the two warps issue tcgen05 instructions in
+  // parallel (each warp's issue rate, not the tensor pipe, bounds a stage).
+  static constexpr bool kSplit = kIssuers == 1;
+  static constexpr bool kXsfOnScaleWarp = kSplit && BN == 128;
   // accumulator buffers: two (the epilogue of one tile overlaps the next
   // tile's MMAs), except for 256-wide tiles, whose one accumulator already
   // takes half of tensor memory
@@ -83,8 +89,9 @@ struct Cfg {
   static constexpr int kSfyColsPerStep = 4 * kSfyAtomsPerStep;
   static constexpr int kSfColsPerStage = 16 * MT + 4 * kSfyColsPerStep;
   static_assert(kSfColBase + kStages * kSfColsPerStage <= kTmemCols, "tensor memory budget");
-  // barriers: full[S], empty[S / G], acc_full[2], acc_empty[2], drain
-  static constexpr int kBarBytes = 8 * (kStages + kGroups + 5);
+  // barriers: full[S], empty[S / G], acc_full[2], acc_empty[2], drain,
+  // scales_ready[S] (split issue only)
+  static constexpr int kBarBytes = 8 * (kStages + kGroups + 5 + (kSplit ? kStages : 0));
   static constexpr int kTableInts = 3 * (kGroupedMaxExperts + 1);
   static constexpr int kCtlOffset = kStages * kStageBytes + kBarBytes;
   // ring of per-unit token-row counts published by the producer (see below)
@@ -207,6 +214,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
   auto accf_bar = [&](int b) { return bar0 + 8u * (C::kStages + C::kGroups + b); };
   auto acce_bar = [&](int b) { return bar0 + 8u * (C::kStages + C::kGroups + 2 + b); };
   const uint32_t drain_bar = bar0 + 8u * (C::kStages + C::kGroups + 4);
+  auto sfr_bar = [&](int s) { return bar0 + 8u * (C::kStages + C::kGroups + 5 + s); };
   CtaCtl* ctl = reinterpret_cast<CtaCtl*>(smem + C::kCtlOffset);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kCtlOffset + 16);
   int32_t* tab = reinterpret_cast<int32_t*>(smem + C::kTablesOffset);
@@ -234,7 +242,9 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
       mbar_init(accf_bar(b), C::kIssuers);
       mbar_init(acce_bar(b), 128);
     }
-    mbar_init(drain_bar, C::kIssuers);
+    mbar_init(drain_bar, C::kSplit ? 2 : C::kIssuers);
+    if (C::kSplit)
+      for (int s = 0; s < C::kStages; ++s) mbar_init(sfr_bar(s), 1);
     ctl->abort = 0;
     ctl->timeout_ns = a.timeout_ns;
     fence_mbar_init();
@@ -387,6 +397,46 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
                         static_cast<uint32_t>((n / C::kStages) & 1), ctl->timeout_ns);
     }
     __syncwarp();
+  } else if (C::kSplit && warp == 6) {
+    // ---------------------------------------------------------- scale warp
+    // Copies each stage's Y scale atoms (and X's for 128-wide tiles) into the
+    // stage's tensor-memory columns once the stage has landed, then commits
+    // to the stage's scales-ready barrier, on which the MMA warp waits.  A
+    // stage's columns are rewritten only after its refill, which follows the
+    // completion of the MMAs that read them.
+    int stage = 0;
+    uint32_t phase = 0;
+    bool alive = true;
+    int uidx = 0;
+    for (int u = blockIdx.x; u < units && alive; u += gridDim.x, ++uidx) {
+      int y_rows = 0;
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(full_bar(stage), phase, ctl, a.status))) {
+          alive = false;
+          break;
+        }
+        if (kb == 0) y_rows = unit_rows[uidx & (C::kUnitRing - 1)];
+        const int ksteps = min(4, static_cast<int>((a.K >> 6) - 4 * kb));
+        const uint32_t sx = sbase + stage * C::kStageBytes;
+        const uint32_t ssfx = sx + kXTileBytes;
+        const uint32_t ssfy = sx + C::kYOffset + C::kYTileBytes;
+        const uint32_t tsfx = tmem + C::kSfColBase + stage * C::kSfColsPerStage;
+        const uint32_t tsfy = tsfx + 16 * MT;
+        for (int ks = 0; ks < ksteps; ++ks) {
+          if (C::kXsfOnScaleWarp)
+            tc_cp_sf_atom_elect(tsfx + 4 * ks, sdesc_sf_atom(ssfx + 512 * ks));
+          tc_cp_sf_atom_elect(tsfy + C::kSfyColsPerStep * ks, sdesc_sf_atom(ssfy + 512 * ks));
+          if (C::kSfyAtomsPerStep == 2 && y_rows > 128)
+            tc_cp_sf_atom_elect(tsfy + C::kSfyColsPerStep * ks + 4,
+                                sdesc_sf_atom(ssfy + kSFStageBytes + 512 * ks));
+        }
+        tc_commit_elect(sfr_bar(stage));
+        if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+      }
+    }
+    tc_commit_elect(drain_bar);
+    if (lane == 0) mbar_wait_drain(drain_bar, 0, ctl->timeout_ns);
+    __syncwarp();
   } else if (warp == 1 || (C::kIssuers == 2 && warp == 6)) {
     // ---------------------------------------------------------------- MMA
     // Issuer j takes the K steps with ks % kIssuers == j of every stage.  The
@@ -412,7 +462,10 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
         // mbarrier; the MMAs read them through the same async proxy, so the
         // wait alone orders them.  (A tcgen05 thread-sync fence here would
         // wait for this thread's earlier MMAs and serialise the stages.)
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(full_bar(stage), phase, ctl, a.status))) {
+        // split issue: the scales-ready barrier completes after the stage
+        // landed (the scale warp waited for it) and its scale copies ran
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(C::kSplit ? sfr_bar(stage) : full_bar(stage),
+                                               phase, ctl, a.status))) {
           alive = false;
           break;
         }
@@ -434,12 +487,15 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
         // address inside an atom's column group faults as misaligned).
         for (int ks = j; ks < ksteps; ks += C::kIssuers) {
           const uint32_t tsfy_ks = tsfy + C::kSfyColsPerStep * ks;
-          tc_cp_sf_atom_elect(tsfx + 4 * ks, sdesc_sf_atom(ssfx + 512 * ks));
-          tc_cp_sf_atom_elect(tsfy_ks, sdesc_sf_atom(ssfy + 512 * ks));
-          // rows 128-255 of a 256-wide Y tile: the next 4 columns (the MMA
-          // reads the scales of row n from column base + n / 32)
-          if (C::kSfyAtomsPerStep == 2 && y_rows > 128)
-            tc_cp_sf_atom_elect(tsfy_ks + 4, sdesc_sf_atom(ssfy + kSFStageBytes + 512 * ks));
+          if (!C::kXsfOnScaleWarp)
+            tc_cp_sf_atom_elect(tsfx + 4 * ks, sdesc_sf_atom(ssfx + 512 * ks));
+          if (!C::kSplit) {
+            tc_cp_sf_atom_elect(tsfy_ks, sdesc_sf_atom(ssfy + 512 * ks));
+            // rows 128-255 of a 256-wide Y tile: the next 4 columns (the MMA
+            // reads the scales of row n from column base + n / 32)
+            if (C::kSfyAtomsPerStep == 2 && y_rows > 128)
+              tc_cp_sf_atom_elect(tsfy_ks + 4, sdesc_sf_atom(ssfy + kSFStageBytes + 512 * ks));
+          }
           tc_mma_nvf4_elect(d_tmem, dx + 2 * ks, dy + 2 * ks, idesc, tsfx + 4 * ks, tsfy_ks,
                             (kb > 0 || ks >= C::kIssuers) ? 1u : 0u);
           if (MT == 2) {                 // second weight tile, same token operand

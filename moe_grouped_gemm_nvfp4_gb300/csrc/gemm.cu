@@ -66,8 +66,10 @@ struct Cfg {
   static_assert(kYOffset % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle alignment");
   static constexpr int kStages = MT == 2 ? 5 : (BN == 32 ? 9 : (BN == 256 ? 4 : 6));
   // Stages are released to the producer in groups with one tcgen05.commit
-  // per group (fewer tcgen05 instructions per stage).
-  static constexpr int kGroup = MT == 2 ? 1 : (BN == 256 ? 2 : 3);
+  // per group.  One stage per group: a commit completes ~1000 cycles after it
+  // is issued, and releasing stages one by one keeps more of the ring in
+  // flight across that latency than saving the commits does.
+  static constexpr int kGroup = 1;
   static constexpr int kGroups = kStages / kGroup;
   static_assert(kStages % kGroup == 0, "stage groups");
   static constexpr int kIssuers = BN <= 64 ? 2 : 1;   // MMA-issuing warps
@@ -400,8 +402,8 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
   } else if (C::kSplit && warp == 6) {
     // ---------------------------------------------------------- scale warp
     // Copies each stage's Y scale atoms (and X's for 128-wide tiles) into the
-    // stage's tensor-memory columns once the stage has landed, then commits
-    // to the stage's scales-ready barrier, on which the MMA warp waits.  A
+    // stage's tensor-memory columns once the stage has landed, then arrives
+    // on the stage's scales-ready barrier, on which the MMA warp waits.  A
     // stage's columns are rewritten only after its refill, which follows the
     // completion of the MMAs that read them.
     int stage = 0;
@@ -430,7 +432,12 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
             tc_cp_sf_atom_elect(tsfy + C::kSfyColsPerStep * ks + 4,
                                 sdesc_sf_atom(ssfy + kSFStageBytes + 512 * ks));
         }
-        tc_commit_elect(sfr_bar(stage));
+        // The MMA warp issues after this arrive and its after-sync fence, and
+        // copies followed by MMAs that read their columns execute in that
+        // order, so no commit (and its completion latency) is needed here.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sfr_bar(stage));
         if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
       }
     }
@@ -463,12 +470,14 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
         // wait alone orders them.  (A tcgen05 thread-sync fence here would
         // wait for this thread's earlier MMAs and serialise the stages.)
         // split issue: the scales-ready barrier completes after the stage
-        // landed (the scale warp waited for it) and its scale copies ran
+        // landed (the scale warp waited for it) and its scale copies were
+        // issued; the fence orders these MMAs after those copies
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(C::kSplit ? sfr_bar(stage) : full_bar(stage),
                                                phase, ctl, a.status))) {
           alive = false;
           break;
         }
+        if (C::kSplit) tc_fence_after();
         if (kb == 0) {
           y_rows = unit_rows[uidx & (C::kUnitRing - 1)];
           idesc = idesc_nvf4(static_cast<uint32_t>((y_rows + 15) & ~15));
@@ -554,6 +563,64 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
       tc_fence_after();
       const float alpha = __fmul_rn(grouped ? a.gx[un.e] : a.gx[0], gy);
       const int n_valid = un.y_rows;
+      if (C::kAccBufs == 1 && mode != kGroupedCombine) {
+        // One accumulator: the next unit's MMAs wait for it.  Read all of it
+        // into registers as BF16 first, hand it back, then store, so the
+        // stores overlap the next unit's MMAs.
+        uint32_t pk[BN / 32][16];                 // BF16 pairs of alpha * acc
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll
+        for (int ci = 0; ci < BN / 32; ++ci) {
+          if (ci * 32 < n_valid) {
+            uint32_t r[32];
+            tmem_ld32(taddr + ci * 32, r);
+            tmem_ld_wait();
+            if (mode != kDenseRowsX) warp_transpose32(r, lane);
+#pragma unroll
+            for (int h = 0; h < 16; ++h)
+              pk[ci][h] =
+                  static_cast<uint32_t>(f32_to_bf16_rn(__fmul_rn(__uint_as_float(r[2 * h]), alpha))) |
+                  (static_cast<uint32_t>(
+                       f32_to_bf16_rn(__fmul_rn(__uint_as_float(r[2 * h + 1]), alpha))) << 16);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(acce_bar(abuf));
+        if (++abuf == C::kAccBufs) { abuf = 0; aphase ^= 1u; }
+#pragma unroll
+        for (int ci = 0; ci < BN / 32; ++ci) {
+          const int c0 = ci * 32;
+          if (c0 >= n_valid) continue;
+          uint16_t* dst;
+          bool vec;
+          int lim;                                 // valid elements of this lane's 32
+          if (mode == kDenseRowsX) {
+            const int xr = un.x_local0 + row;
+            if (xr >= a.rows_x) continue;
+            dst = reinterpret_cast<uint16_t*>(a.out) + static_cast<int64_t>(xr) * a.ldc +
+                  un.y_row0 + c0;
+            lim = min(32, n_valid - c0);
+          } else {
+            const int col = c0 + lane;
+            if (col >= n_valid) continue;
+            const int f0 = un.x_local0 + q * 32;
+            dst = reinterpret_cast<uint16_t*>(a.out) + (un.y_row0 + col) * a.ldc + f0;
+            lim = (mode == kGrouped) ? 32 : min(32, a.rows_x - f0);
+          }
+          vec = (lim == 32) && a.vec_store;
+          if (vec) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              reinterpret_cast<uint4*>(dst)[v] =
+                  make_uint4(pk[ci][4 * v], pk[ci][4 * v + 1], pk[ci][4 * v + 2], pk[ci][4 * v + 3]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (i < lim) dst[i] = static_cast<uint16_t>(pk[ci][i >> 1] >> (16 * (i & 1)));
+          }
+        }
+        continue;
+      }
 #pragma unroll 1
       for (int xt = 0; xt < MT; ++xt) {           // the unit's X tiles
       const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) +

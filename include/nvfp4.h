@@ -170,7 +170,7 @@ nvfp4_status nvfp4_prepack_weight_tiles(const uint8_t* packed, const uint8_t* sc
 /*
  * Chunk width (32, 64 or 128 routes) of the grouped activation tiles for R
  * routes over E experts: with want = ceil(1.6 x R / E), 32 if want <= 32, 64 if
- * want <= 128, else 128.  It is also the grouped GEMM's token-tile width, so
+ * want <= 80, else 128.  It is also the grouped GEMM's token-tile width, so
  * that narrow decode tiles leave shared memory for a deeper pipeline.
  */
 int nvfp4_grouped_chunk_rows(int64_t R, int32_t E);

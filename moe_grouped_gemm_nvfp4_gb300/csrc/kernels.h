@@ -72,13 +72,14 @@ constexpr int kGroupedMaxExperts = 256;
 // Token-tile width of the grouped GEMM (32, 64 or 128 routes), a function of
 // the route and expert counts only.  With want = ~1.6x the mean routes per
 // expert: 32 when the widest experts of a balanced routing fit 32 rows, 64 up
-// to a mean of ~80 routes (an expert that needs a second 64-row tile re-reads
-// its weight tile from L2 within the same wave, while 64-row tiles keep two
-// MMA issuers and a double-buffered accumulator), else 128.  The grouped
+// to want = 80 (a mean of ~50 routes), else 128.  Past that point too many
+// experts need a second 64-row tile, whose unit streams the weight tile again
+// and pays a second epilogue (at a mean of 64 routes, 128-row tiles took the
+// down projection from 0.239 to 0.197 ms).  The grouped
 // activation layout cuts each expert's routes into chunks of this width.
 inline int grouped_chunk_rows(int64_t routes, int experts) {
   const int64_t want = experts > 0 ? (routes * 8 + experts * 5 - 1) / (experts * 5) : 128;
-  return want <= 32 ? 32 : (want <= 128 ? 64 : 128);
+  return want <= 32 ? 32 : (want <= 80 ? 64 : 128);
 }
 
 // Token-tile width of the grouped GEMM itself: the chunk width, or 256 when

@@ -49,7 +49,8 @@ def test_pure_host_helpers():
     # expert wastes at most chunk - 1 rows
     assert F.nvfp4_grouped_chunk_rows(2048, 128) == 32        # 16 per expert
     assert F.nvfp4_grouped_chunk_rows(4096, 128) == 64        # 32 per expert
-    assert F.nvfp4_grouped_chunk_rows(8192, 128) == 64        # 64 per expert
+    assert F.nvfp4_grouped_chunk_rows(6144, 128) == 64        # 48 per expert
+    assert F.nvfp4_grouped_chunk_rows(8192, 128) == 128       # 64 per expert
     assert F.nvfp4_grouped_chunk_rows(12288, 128) == 128      # 96 per expert
     assert F.nvfp4_grouped_chunk_rows(65536, 128) == 128
     assert F.nvfp4_grouped_tiles_bytes(2048, 128, 6144) == (2048 + 31 * 128) // 32 * 24 * 18432

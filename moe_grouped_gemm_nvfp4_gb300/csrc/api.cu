@@ -240,8 +240,10 @@ nvfp4_status nvfp4_gemm(const uint8_t* A, const uint8_t* sfA, const float* gA,
   const uint8_t* Y = swap ? A : B;
   const int64_t rows_x = swap ? N : M;
   const int64_t rows_y = swap ? M : N;
-  // Y in one 128-row box per stage when its tiles are full, else 16-row boxes
-  const uint32_t ybox_rows = rows_y >= 128 ? 128u : 16u;
+  // Y in one box per stage: 256 rows for the 256-wide tiles the launch picks
+  // when Y has at least 256 rows (kDenseRowsX), 128 rows when its tiles are
+  // full, else 16-row boxes
+  const uint32_t ybox_rows = (!swap && rows_y >= 256) ? 256u : (rows_y >= 128 ? 128u : 16u);
   CUtensorMap tmx, tmy;
   if (make_operand_map(&tmx, X, rows_x, K / 2, 128) != NVFP4_OK ||
       make_operand_map(&tmy, Y, rows_y, K / 2, ybox_rows) != NVFP4_OK)

@@ -309,90 +309,95 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      // Weights read by a single unit stream through L2 (evict first); weights
-      // that other token tiles of the same expert read again stay (normal).
-      const uint64_t pol_once = l2_policy_evict_first();
-      const uint64_t pol_again = grouped ? l2_policy_evict_normal() : l2_policy_evict_last();
-      const uint64_t pol_y = l2_policy_evict_last();
-      int stage = 0;
-      uint32_t phase = 0;
-      int64_t issued = 0;
-      bool alive = true;
-      int uidx = 0;
-      for (int u = blockIdx.x; u < units && alive; u += gridDim.x, ++uidx) {
-        const Unit un = get_unit<BN, MT>(u, mode, a, t, tiles_x, atoms_per_rowtile);
-        unit_rows[uidx & (C::kUnitRing - 1)] = un.y_rows;
-        const uint64_t pol_x = un.x_reused ? pol_again : pol_once;
-        const int ybox = (un.y_rows + 15) >> 4;                  // 16-row groups
-        const int ny_loads = (un.y_rows + a.ybox_rows - 1) / a.ybox_rows;
-        for (int kb = 0; kb < nkb; ++kb) {
-          // a group of stages is refilled once the MMAs of its previous round completed
-          if (stage % C::kGroup == 0 &&
-              !mbar_wait(empty_bar(stage / C::kGroup), phase ^ 1u, ctl, a.status)) {
-            alive = false;
-            break;
-          }
-          const int ksteps = min(4, static_cast<int>((a.K >> 6) - 4 * kb));
-          const uint32_t sx = sbase + stage * C::kStageBytes;
-          const uint32_t ssfx = sx + kXTileBytes;
-          const uint32_t sy = sx + C::kYOffset;
-          const uint32_t ssfy = sy + C::kYTileBytes;
-          if ((a.debug_flags & kDebugSkipFirstStage) && issued == 0 && stage == 0 && kb == 0 &&
-              u == static_cast<int>(blockIdx.x)) {
-            // test hook: leave stage 0 empty; its consumers' bounded waits expire.
-            // Counted as issued so the drain below keeps stage numbers aligned
-            // (its wait on this stage ends by the time limit too).
-            ++issued;
-            if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
-            continue;
-          }
-          const uint32_t ybytes = grouped ? ybox * 16 * kRowBytes : ny_loads * a.ybox_rows * kRowBytes;
-          // the second 128-row scale group of a 256-wide Y tile exists only when
-          // the tile has more than 128 rows
-          const int sfy_groups = (C::kSfyAtomsPerStep == 2 && un.y_rows > 128) ? 2 : 1;
-          // grouped 256-row tiles: codes of rows 0-127 and 128+ come from two tiles
-          const int ybox_lo = min(ybox, 8), ybox_hi = ybox - ybox_lo;
-          const uint32_t bytes =
-              MT * (kXTileBytes + ksteps * 512) + ybytes + sfy_groups * ksteps * 512;
-          mbar_arrive_expect_tx(full_bar(stage), bytes);
-          if (grouped) {
-            // operand tiles: X codes + scales in one contiguous copy, Y codes
-            // (only the unit's rows) and Y scales in two more
-            const uint8_t* xt = a.sfx + un.sfx_off + kb * kOperandTileBytes;
-            const uint8_t* yt = a.sfy + un.sfy_off + kb * kOperandTileBytes;
-            bulk_load(sx, xt, kXTileBytes + ksteps * 512, full_bar(stage), pol_x);
-            if (MT == 2)                   // the unit's second weight tile
-              bulk_load(sx + C::kXPartBytes,
-                        xt + static_cast<int64_t>((a.K + kBK - 1) / kBK) * kOperandTileBytes,
-                        kXTileBytes + ksteps * 512, full_bar(stage), pol_x);
-            bulk_load(sy, yt, ybox_lo * 16 * kRowBytes, full_bar(stage), pol_y);
-            bulk_load(ssfy, yt + kXTileBytes, ksteps * 512, full_bar(stage), pol_y);
-            if (ybox_hi > 0) {               // second operand tile of a 256-row token tile
-              const uint8_t* yt2 = yt + static_cast<int64_t>((a.K + kBK - 1) / kBK) * kOperandTileBytes;
-              bulk_load(sy + 128 * kRowBytes, yt2, ybox_hi * 16 * kRowBytes, full_bar(stage), pol_y);
-              bulk_load(ssfy + kSFStageBytes, yt2 + kXTileBytes, ksteps * 512, full_bar(stage),
-                        pol_y);
-            }
-          } else {
-            tma_load_2d(sx, &tmx, full_bar(stage), kb * kRowBytes, un.x_row0, pol_x);
-            for (int j = 0; j < ny_loads; ++j)
-              tma_load_2d(sy + j * a.ybox_rows * kRowBytes, &tmy, full_bar(stage), kb * kRowBytes,
-                          un.y_row0 + a.ybox_rows * j, pol_y);
-            bulk_load(ssfx, a.sfx + un.sfx_off + kb * kSFStageBytes, ksteps * 512,
-                      full_bar(stage), pol_x);
-            bulk_load(ssfy, a.sfy + un.sfy_off + kb * kSFStageBytes, ksteps * 512,
-                      full_bar(stage), pol_y);
-            if (sfy_groups == 2)
-              bulk_load(ssfy + kSFStageBytes,
-                        a.sfy + un.sfy_off + atoms_per_rowtile * 512 + kb * kSFStageBytes,
-                        ksteps * 512, full_bar(stage), pol_y);
-          }
+    // The whole warp runs the loop (uniform control flow); one elected lane
+    // issues each copy, as in the MMA warp.
+    // Weights read by a single unit stream through L2 (evict first); weights
+    // that other token tiles of the same expert read again stay (normal).
+    const uint64_t pol_once = l2_policy_evict_first();
+    const uint64_t pol_again = grouped ? l2_policy_evict_normal() : l2_policy_evict_last();
+    const uint64_t pol_y = l2_policy_evict_last();
+    int stage = 0;
+    uint32_t phase = 0;
+    int64_t issued = 0;
+    bool alive = true;
+    int uidx = 0;
+    for (int u = blockIdx.x; u < units && alive; u += gridDim.x, ++uidx) {
+      const Unit un = get_unit<BN, MT>(u, mode, a, t, tiles_x, atoms_per_rowtile);
+      if (lane == 0) unit_rows[uidx & (C::kUnitRing - 1)] = un.y_rows;
+      __syncwarp();
+      const uint64_t pol_x = un.x_reused ? pol_again : pol_once;
+      const int ybox = (un.y_rows + 15) >> 4;                  // 16-row groups
+      const int ny_loads = (un.y_rows + a.ybox_rows - 1) / a.ybox_rows;
+      for (int kb = 0; kb < nkb; ++kb) {
+        // a group of stages is refilled once the MMAs of its previous round completed
+        if (stage % C::kGroup == 0 &&
+            !__all_sync(0xFFFFFFFFu, mbar_wait(empty_bar(stage / C::kGroup), phase ^ 1u, ctl,
+                                               a.status))) {
+          alive = false;
+          break;
+        }
+        const int ksteps = min(4, static_cast<int>((a.K >> 6) - 4 * kb));
+        const uint32_t sx = sbase + stage * C::kStageBytes;
+        const uint32_t ssfx = sx + kXTileBytes;
+        const uint32_t sy = sx + C::kYOffset;
+        const uint32_t ssfy = sy + C::kYTileBytes;
+        if ((a.debug_flags & kDebugSkipFirstStage) && issued == 0 && stage == 0 && kb == 0 &&
+            u == static_cast<int>(blockIdx.x)) {
+          // test hook: leave stage 0 empty; its consumers' bounded waits expire.
+          // Counted as issued so the drain below keeps stage numbers aligned
+          // (its wait on this stage ends by the time limit too).
           ++issued;
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+          continue;
         }
+        const uint32_t ybytes = grouped ? ybox * 16 * kRowBytes : ny_loads * a.ybox_rows * kRowBytes;
+        // the second 128-row scale group of a 256-wide Y tile exists only when
+        // the tile has more than 128 rows
+        const int sfy_groups = (C::kSfyAtomsPerStep == 2 && un.y_rows > 128) ? 2 : 1;
+        // grouped 256-row tiles: codes of rows 0-127 and 128+ come from two tiles
+        const int ybox_lo = min(ybox, 8), ybox_hi = ybox - ybox_lo;
+        const uint32_t bytes =
+            MT * (kXTileBytes + ksteps * 512) + ybytes + sfy_groups * ksteps * 512;
+        mbar_arrive_expect_tx_elect(full_bar(stage), bytes);
+        if (grouped) {
+          // operand tiles: X codes + scales in one contiguous copy, Y codes
+          // (only the unit's rows) and Y scales in two more
+          const uint8_t* xt = a.sfx + un.sfx_off + kb * kOperandTileBytes;
+          const uint8_t* yt = a.sfy + un.sfy_off + kb * kOperandTileBytes;
+          bulk_load_elect(sx, xt, kXTileBytes + ksteps * 512, full_bar(stage), pol_x);
+          if (MT == 2)                   // the unit's second weight tile
+            bulk_load_elect(sx + C::kXPartBytes,
+                            xt + static_cast<int64_t>((a.K + kBK - 1) / kBK) * kOperandTileBytes,
+                            kXTileBytes + ksteps * 512, full_bar(stage), pol_x);
+          bulk_load_elect(sy, yt, ybox_lo * 16 * kRowBytes, full_bar(stage), pol_y);
+          bulk_load_elect(ssfy, yt + kXTileBytes, ksteps * 512, full_bar(stage), pol_y);
+          if (ybox_hi > 0) {               // second operand tile of a 256-row token tile
+            const uint8_t* yt2 = yt + static_cast<int64_t>((a.K + kBK - 1) / kBK) * kOperandTileBytes;
+            bulk_load_elect(sy + 128 * kRowBytes, yt2, ybox_hi * 16 * kRowBytes, full_bar(stage),
+                            pol_y);
+            bulk_load_elect(ssfy + kSFStageBytes, yt2 + kXTileBytes, ksteps * 512, full_bar(stage),
+                            pol_y);
+          }
+        } else {
+          tma_load_2d_elect(sx, &tmx, full_bar(stage), kb * kRowBytes, un.x_row0, pol_x);
+          for (int j = 0; j < ny_loads; ++j)
+            tma_load_2d_elect(sy + j * a.ybox_rows * kRowBytes, &tmy, full_bar(stage),
+                              kb * kRowBytes, un.y_row0 + a.ybox_rows * j, pol_y);
+          bulk_load_elect(ssfx, a.sfx + un.sfx_off + kb * kSFStageBytes, ksteps * 512,
+                          full_bar(stage), pol_x);
+          bulk_load_elect(ssfy, a.sfy + un.sfy_off + kb * kSFStageBytes, ksteps * 512,
+                          full_bar(stage), pol_y);
+          if (sfy_groups == 2)
+            bulk_load_elect(ssfy + kSFStageBytes,
+                            a.sfy + un.sfy_off + atoms_per_rowtile * 512 + kb * kSFStageBytes,
+                            ksteps * 512, full_bar(stage), pol_y);
+        }
+        ++issued;
+        if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
       }
-      // Drain: every copy this thread issued must land before the CTA exits.
+    }
+    // Drain: every copy this warp issued must land before the CTA exits.
+    if (lane == 0) {
       const int64_t first = issued > C::kStages ? issued - C::kStages : 0;
       for (int64_t n = first; n < issued; ++n)
         mbar_wait_drain(full_bar(static_cast<int>(n % C::kStages)),

@@ -574,19 +574,26 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
         // stores overlap the next unit's MMAs.
         uint32_t pk[BN / 32][16];                 // BF16 pairs of alpha * acc
         const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+        // two 32-column loads in flight per wait (the load latency, not the
+        // conversion, sets the drain time)
 #pragma unroll
-        for (int ci = 0; ci < BN / 32; ++ci) {
-          if (ci * 32 < n_valid) {
-            uint32_t r[32];
-            tmem_ld32(taddr + ci * 32, r);
+        for (int cp2 = 0; cp2 < BN / 64; ++cp2) {
+          if (cp2 * 64 < n_valid) {
+            uint32_t r[2][32];
+            tmem_ld32(taddr + cp2 * 64, r[0]);
+            tmem_ld32(taddr + cp2 * 64 + 32, r[1]);
             tmem_ld_wait();
-            if (mode != kDenseRowsX) warp_transpose32(r, lane);
 #pragma unroll
-            for (int h = 0; h < 16; ++h)
-              pk[ci][h] =
-                  static_cast<uint32_t>(f32_to_bf16_rn(__fmul_rn(__uint_as_float(r[2 * h]), alpha))) |
-                  (static_cast<uint32_t>(
-                       f32_to_bf16_rn(__fmul_rn(__uint_as_float(r[2 * h + 1]), alpha))) << 16);
+            for (int hh = 0; hh < 2; ++hh) {
+              const int ci = 2 * cp2 + hh;
+              if (mode != kDenseRowsX) warp_transpose32(r[hh], lane);
+#pragma unroll
+              for (int h = 0; h < 16; ++h)
+                pk[ci][h] = static_cast<uint32_t>(
+                                f32_to_bf16_rn(__fmul_rn(__uint_as_float(r[hh][2 * h]), alpha))) |
+                            (static_cast<uint32_t>(f32_to_bf16_rn(
+                                 __fmul_rn(__uint_as_float(r[hh][2 * h + 1]), alpha))) << 16);
+            }
           }
         }
         tc_fence_before();

@@ -176,9 +176,11 @@ nvfp4_status nvfp4_prepack_weight_tiles(const uint8_t* packed, const uint8_t* sc
 int nvfp4_grouped_chunk_rows(int64_t R, int32_t E);
 
 /*
- * Upper bound on the bytes of the grouped activation tiles for R routes over
- * E experts: every expert's routes are cut into chunks of
- * nvfp4_grouped_chunk_rows(R, E) rows and each chunk fills its own tile.
+ * Bytes of the grouped activation tile buffer for R routes over E experts:
+ * an upper bound on the tiles (every expert's routes are cut into chunks of
+ * nvfp4_grouped_chunk_rows(R, E) rows and each chunk fills its own tile),
+ * plus 16 KiB of scratch at the end in which nvfp4_quantize_dispatch keeps
+ * the tensor amax's per-block maxima between its two kernels.
  */
 size_t nvfp4_grouped_tiles_bytes(int64_t R, int32_t E, int64_t K);
 

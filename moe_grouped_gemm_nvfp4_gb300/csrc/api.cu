@@ -83,6 +83,17 @@ nvfp4_status device_state(DeviceState** out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The grouped activation tiles proper, and the scratch after them that holds
+// the tensor amax's per-block maxima between the amax and dispatch kernels.
+size_t grouped_tiles_body_bytes(int64_t R, int32_t E, int64_t K) {
+  const int64_t chunk = nvfp4::grouped_chunk_rows(R, E);
+  const int64_t nonempty = R < E ? R : E;
+  const int64_t tiles = (R + (chunk - 1) * nonempty) / chunk;
+  return static_cast<size_t>(tiles) * static_cast<size_t>((K + 255) / 256) *
+         static_cast<size_t>(nvfp4::kOperandTileBytes);
+}
+constexpr size_t kAmaxScratchBytes = 16384;
+
 // 2-D map over a packed operand [rows, row_bytes] (uint8), box of 128 bytes
 // x box_rows rows, 128-byte swizzle.  Out-of-range boxes read zeros.
 nvfp4_status make_operand_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t row_bytes,
@@ -163,11 +174,7 @@ int nvfp4_grouped_chunk_rows(int64_t R, int32_t E) {
 
 size_t nvfp4_grouped_tiles_bytes(int64_t R, int32_t E, int64_t K) {
   if (R < 0 || E < 0 || K < 0) return 0;
-  const int64_t chunk = nvfp4::grouped_chunk_rows(R, E);
-  const int64_t nonempty = R < E ? R : E;
-  const int64_t tiles = (R + (chunk - 1) * nonempty) / chunk;
-  return static_cast<size_t>(tiles) * static_cast<size_t>((K + 255) / 256) *
-         static_cast<size_t>(nvfp4::kOperandTileBytes);
+  return grouped_tiles_body_bytes(R, E, K) + kAmaxScratchBytes;
 }
 
 size_t nvfp4_combine_workspace_bytes(int64_t T, int64_t N) {
@@ -318,13 +325,25 @@ nvfp4_status nvfp4_quantize_dispatch(const void* x, int64_t rows, int64_t K, int
   if (st != NVFP4_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const uint16_t* xb = static_cast<const uint16_t*>(x);
+  uint32_t* partials = nullptr;
+  int n_partials = 0;
   if (!(flags & NVFP4_GLOBAL_GIVEN)) {
-    if (nvfp4::launch_amax(xb, rows, K, ld, global_scale, d->sms, s) != cudaSuccess)
+    if (rows == 0) {                     // nothing to quantise: g = 0
+      if (cudaMemsetAsync(global_scale, 0, sizeof(float), s) != cudaSuccess) return cuda_fail();
+      return NVFP4_OK;
+    }
+    // per-block maxima go to the scratch after the tiles; the dispatch
+    // kernel reduces them and stores g
+    n_partials = nvfp4::amax_partials_count(rows, K, d->sms);
+    if (static_cast<size_t>(n_partials) * sizeof(uint32_t) > kAmaxScratchBytes)
+      return NVFP4_ERR_UNSUPPORTED;
+    partials = reinterpret_cast<uint32_t*>(tiles + grouped_tiles_body_bytes(R, E, K));
+    if (nvfp4::launch_amax_partials(xb, rows, K, ld, partials, d->sms, s) != cudaSuccess)
       return cuda_fail();
   }
   if (nvfp4::launch_quantize_dispatch(xb, rows, K, ld, route_pos, fanout, expert_offsets, E, R,
                                       nvfp4::grouped_chunk_rows(R, E), tiles, global_scale,
-                                      d->status, d->sms, s) != cudaSuccess)
+                                      partials, n_partials, d->status, d->sms, s) != cudaSuccess)
     return cuda_fail();
   return NVFP4_OK;
 }

@@ -14,10 +14,18 @@ cudaError_t launch_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t l
 cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
                             uint8_t* packed, uint8_t* scales, int sf_atoms, const float* g,
                             int sms, cudaStream_t s);
+// Per-block maxima of |x| (magnitude bits) into partials[0, count) for a
+// later quantize_dispatch launch to reduce.
+int amax_partials_count(int64_t rows, int64_t cols, int sms);
+cudaError_t launch_amax_partials(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
+                                 uint32_t* partials, int sms, cudaStream_t s);
+// With partials, every block derives g from them and block 0 stores it in
+// *g; without, g is read from *g.
 cudaError_t launch_quantize_dispatch(const uint16_t* x, int64_t rows, int64_t K, int64_t ld,
                                      const int32_t* route_pos, int fanout,
                                      const int32_t* expert_offsets, int E, int64_t R,
-                                     int chunk_rows, uint8_t* tiles, const float* g, int* status,
+                                     int chunk_rows, uint8_t* tiles, float* g,
+                                     const uint32_t* partials, int n_partials, int* status,
                                      int sms, cudaStream_t s);
 cudaError_t launch_prepack_tiles(const uint8_t* packed, const uint8_t* sf, int64_t rows,
                                  int64_t K, uint8_t* tiles, int sms, cudaStream_t s);

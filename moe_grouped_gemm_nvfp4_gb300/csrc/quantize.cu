@@ -57,12 +57,14 @@ __device__ __forceinline__ uint32_t e2m1_mag_code(float a) {
 // Tensor amax -> global scale
 // ---------------------------------------------------------------------------
 // Each block reduces |x| over a grid-stride slice (BF16 magnitudes compare as
-// integers), turns its maximum into g_b = amax_b / 2688 and folds it into
-// *g with an integer atomicMax on the float bits (valid for g_b >= 0).
-// Division by a positive constant is monotone, so max_b(g_b) = max(amax)/2688.
+// integers).  With `g`, it turns its maximum into g_b = amax_b / 2688 and
+// folds it into *g with an integer atomicMax on the float bits (valid for
+// g_b >= 0; *g starts at 0).  Division by a positive constant is monotone, so
+// max_b(g_b) = max(amax)/2688.  With `partials`, it stores its maximum's
+// magnitude bits in partials[block] and a later kernel reduces them.
 __global__ void __launch_bounds__(256) amax_kernel(const uint16_t* __restrict__ x,
                                                    int64_t rows, int64_t cols, int64_t ld,
-                                                   float* g) {
+                                                   float* g, uint32_t* partials) {
   uint32_t m = 0;
   const bool vec = ((cols & 7) == 0) && ((ld & 7) == 0) &&
                    ((reinterpret_cast<uintptr_t>(x) & 15) == 0);
@@ -95,8 +97,12 @@ __global__ void __launch_bounds__(256) amax_kernel(const uint16_t* __restrict__ 
   __syncthreads();
   if (threadIdx.x == 0) {
     for (int w = 1; w < (blockDim.x >> 5); ++w) m = max(m, wm[w]);
-    const float gb = __fdiv_rn(bf16_bits_to_f32(m), 2688.0f);
-    atomicMax(reinterpret_cast<unsigned int*>(g), __float_as_uint(gb));
+    if (partials) {
+      partials[blockIdx.x] = m;
+    } else {
+      const float gb = __fdiv_rn(bf16_bits_to_f32(m), 2688.0f);
+      atomicMax(reinterpret_cast<unsigned int*>(g), __float_as_uint(gb));
+    }
   }
 }
 
@@ -203,12 +209,23 @@ __global__ void __launch_bounds__(256) quantize_dispatch_kernel(
     const uint16_t* __restrict__ x, int64_t rows, int64_t K, int64_t ld,
     const int32_t* __restrict__ route_pos, int fanout,
     const int32_t* __restrict__ expert_offsets, int E, int64_t R, int chunk,
-    uint8_t* __restrict__ tiles, const float* g_ptr, int* status) {
+    uint8_t* __restrict__ tiles, float* g_ptr, const uint32_t* __restrict__ partials,
+    int n_partials, int* status) {
   extern __shared__ int32_t sh[];
   int32_t* off = sh;              // [E + 1]
   int32_t* tb = sh + (E + 1);     // [E]
   __shared__ int32_t s_bad;
+  __shared__ uint32_t s_wmax[8];
   for (int e = threadIdx.x; e <= E; e += blockDim.x) off[e] = expert_offsets[e];
+  // tensor amax: every block reduces the amax kernel's per-block maxima
+  // itself (a few KB from L2), so no reset or atomic sits between the calls
+  if (partials) {
+    uint32_t m = 0;
+    for (int i = threadIdx.x; i < n_partials; i += blockDim.x) m = max(m, partials[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if ((threadIdx.x & 31) == 0) s_wmax[threadIdx.x >> 5] = m;
+  }
   __syncthreads();
   // tile prefix: one warp scans the per-expert tile counts
   if (threadIdx.x < 32) {
@@ -240,8 +257,16 @@ __global__ void __launch_bounds__(256) quantize_dispatch_kernel(
     }
   }
   __syncthreads();
+  float g;
+  if (partials) {
+    uint32_t m = s_wmax[0];
+    for (int w = 1; w < (blockDim.x >> 5); ++w) m = max(m, s_wmax[w]);
+    g = __fdiv_rn(bf16_bits_to_f32(m), 2688.0f);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *g_ptr = g;
+  } else {
+    g = *g_ptr;
+  }
   if (s_bad) return;
-  const float g = *g_ptr;
   const int64_t bpr = K >> 4;
   const int64_t n_kb = (K + 255) >> 8;
   const int64_t total = rows * bpr;
@@ -343,7 +368,18 @@ cudaError_t launch_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t l
   cudaError_t err = cudaMemsetAsync(g, 0, sizeof(float), s);
   if (err != cudaSuccess) return err;
   if (rows == 0 || cols == 0) return cudaSuccess;
-  amax_kernel<<<grid_for(rows * cols / 8, sms), 256, 0, s>>>(x, rows, cols, ld, g);
+  amax_kernel<<<grid_for(rows * cols / 8, sms), 256, 0, s>>>(x, rows, cols, ld, g, nullptr);
+  return cudaGetLastError();
+}
+
+int amax_partials_count(int64_t rows, int64_t cols, int sms) {
+  return grid_for(rows * cols / 8, sms);
+}
+
+cudaError_t launch_amax_partials(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
+                                 uint32_t* partials, int sms, cudaStream_t s) {
+  amax_kernel<<<amax_partials_count(rows, cols, sms), 256, 0, s>>>(x, rows, cols, ld, nullptr,
+                                                                 partials);
   return cudaGetLastError();
 }
 
@@ -359,12 +395,14 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64
 cudaError_t launch_quantize_dispatch(const uint16_t* x, int64_t rows, int64_t K, int64_t ld,
                                      const int32_t* route_pos, int fanout,
                                      const int32_t* expert_offsets, int E, int64_t R,
-                                     int chunk_rows, uint8_t* tiles, const float* g, int* status,
+                                     int chunk_rows, uint8_t* tiles, float* g,
+                                     const uint32_t* partials, int n_partials, int* status,
                                      int sms, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
   const size_t shmem = sizeof(int32_t) * (2 * static_cast<size_t>(E) + 1);
   quantize_dispatch_kernel<<<grid_for(rows * (K >> 4), sms), 256, shmem, s>>>(
-      x, rows, K, ld, route_pos, fanout, expert_offsets, E, R, chunk_rows, tiles, g, status);
+      x, rows, K, ld, route_pos, fanout, expert_offsets, E, R, chunk_rows, tiles, g, partials,
+      n_partials, status);
   return cudaGetLastError();
 }
 

@@ -53,8 +53,10 @@ def test_pure_host_helpers():
     assert F.nvfp4_grouped_chunk_rows(8192, 128) == 128       # 64 per expert
     assert F.nvfp4_grouped_chunk_rows(12288, 128) == 128      # 96 per expert
     assert F.nvfp4_grouped_chunk_rows(65536, 128) == 128
-    assert F.nvfp4_grouped_tiles_bytes(2048, 128, 6144) == (2048 + 31 * 128) // 32 * 24 * 18432
-    assert F.nvfp4_grouped_tiles_bytes(1, 128, 64) == 18432
+    # tiles proper + 16 KB of scratch for the tensor amax's per-block maxima
+    assert F.nvfp4_grouped_tiles_bytes(2048, 128, 6144) == \
+        (2048 + 31 * 128) // 32 * 24 * 18432 + 16384
+    assert F.nvfp4_grouped_tiles_bytes(1, 128, 64) == 18432 + 16384
 
 
 def test_host_validation_without_device():

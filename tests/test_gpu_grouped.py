@@ -69,15 +69,17 @@ def test_grouped_combine_matches_oracle(T, E, k, N, K):
     w = _weights_host(g, E, N, K)
     W = moe.quantize_experts(w.cuda())
     plan = moe.GroupedPlan(W, T, k, "combine")
-    plan.out.view(torch.int16).fill_(0x7FC0)
-    out = plan.run(h.cuda(), torch.from_numpy(ids).cuda(), torch.from_numpy(wts).cuda())
-    torch.cuda.synchronize()
-    assert F.nvfp4_device_status() == F.NVFP4_OK
     off, tok, slot = oracle.route(ids, E)
     ph, sh, gh = oracle.quantize(h.float().numpy())
     y = oracle.grouped_gemm(oracle.dequantize(ph, sh, gh), _oracle_weights(w), off)
     ref = oracle.combine(y, tok, slot, wts, T)
-    check_gemm(bf16_to_np(out[:T]), ref, "grouped combine")
+    # twice on one workspace: each call must leave it cleared for the next
+    for call in range(2):
+        plan.out.view(torch.int16).fill_(0x7FC0)
+        out = plan.run(h.cuda(), torch.from_numpy(ids).cuda(), torch.from_numpy(wts).cuda())
+        torch.cuda.synchronize()
+        assert F.nvfp4_device_status() == F.NVFP4_OK
+        check_gemm(bf16_to_np(out[:T]), ref, f"grouped combine, call {call}")
 
 
 def test_grouped_rejects_non_monotone_offsets_on_device():

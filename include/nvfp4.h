@@ -94,7 +94,8 @@ size_t nvfp4_atom_scales_bytes(int64_t rows, int64_t cols);
  *            cols % 16 == 0 (cols % 64 == 0 with NVFP4_SF_ATOMS).
  *   packed   uint8 [rows, cols/2] out, row-major, dense.
  *   scales   uint8 out: [rows, cols/16] row-major, or the atom layout of
- *            nvfp4_atom_scales_bytes(rows, cols) bytes with NVFP4_SF_ATOMS.
+ *            nvfp4_atom_scales_bytes(rows, cols) bytes with NVFP4_SF_ATOMS
+ *            (then 4-byte aligned; padding rows are left unwritten).
  *   global_scale  device float: written with g = amax|x| / (6 * 448), or read
  *            as the global scale when NVFP4_GLOBAL_GIVEN is set.
  * Every step is IEEE binary32 round-to-nearest-even: s = (amax_b / 6) / g

@@ -190,7 +190,9 @@ nvfp4_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t l
   if (!global_scale || (rows > 0 && cols > 0 && (!x || !packed || !scales)))
     return NVFP4_ERR_INVALID_ARG;
   if (cols % 16 != 0 || ld % 8 != 0) return NVFP4_ERR_UNSUPPORTED;
-  if ((flags & NVFP4_SF_ATOMS) && cols % 64 != 0) return NVFP4_ERR_UNSUPPORTED;
+  if ((flags & NVFP4_SF_ATOMS) &&
+      (cols % 64 != 0 || (scales && (reinterpret_cast<uintptr_t>(scales) & 3u))))
+    return NVFP4_ERR_UNSUPPORTED;
   if ((x && !aligned16(x)) || (packed && (reinterpret_cast<uintptr_t>(packed) & 7u)) ||
       (reinterpret_cast<uintptr_t>(global_scale) & 3u))
     return NVFP4_ERR_UNSUPPORTED;

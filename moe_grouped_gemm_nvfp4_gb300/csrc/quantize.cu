@@ -43,57 +43,50 @@ __device__ __forceinline__ float f32_from_e4m3(uint32_t c) {
   return (c & 0x80u) ? -mag : mag;
 }
 
-// |q| -> E2M1 magnitude code with round to nearest even and saturation to 6:
-// each threshold is a midpoint between neighbouring magnitudes, inclusive
-// when the upper neighbour has the even code.
-__device__ __forceinline__ uint32_t e2m1_mag_code(float a) {
-  return static_cast<uint32_t>(a > 0.25f) + static_cast<uint32_t>(a >= 0.75f) +
-         static_cast<uint32_t>(a > 1.25f) + static_cast<uint32_t>(a >= 1.75f) +
-         static_cast<uint32_t>(a > 2.5f) + static_cast<uint32_t>(a >= 3.5f) +
-         static_cast<uint32_t>(a > 5.0f);
-}
-
 // ---------------------------------------------------------------------------
 // Tensor amax -> global scale
 // ---------------------------------------------------------------------------
-// Each block reduces |x| over a grid-stride slice (BF16 magnitudes compare as
-// integers).  With `g`, it turns its maximum into g_b = amax_b / 2688 and
-// folds it into *g with an integer atomicMax on the float bits (valid for
-// g_b >= 0; *g starts at 0).  Division by a positive constant is monotone, so
-// max_b(g_b) = max(amax)/2688.  With `partials`, it stores its maximum's
-// magnitude bits in partials[block] and a later kernel reduces them.
+// Each block reduces |x| over its share of the tensor (BF16 magnitudes
+// compare as integers).  Work item: a warp reads 128 consecutive 16-byte
+// vectors of one row (four loads in flight per lane); one integer division
+// per item maps it to its row.  With `g`, the block turns its maximum into
+// g_b = amax_b / 2688 and folds it into *g with an integer atomicMax on the
+// float bits (valid for g_b >= 0; *g starts at 0).  Division by a positive
+// constant is monotone, so max_b(g_b) = max(amax)/2688.  With `partials`, it
+// stores its maximum's magnitude bits in partials[block] and a later kernel
+// reduces them.  Rows must be 16-byte aligned with cols % 8 == 0.
 __global__ void __launch_bounds__(256) amax_kernel(const uint16_t* __restrict__ x,
                                                    int64_t rows, int64_t cols, int64_t ld,
                                                    float* g, uint32_t* partials) {
   uint32_t m = 0;
-  const bool vec = ((cols & 7) == 0) && ((ld & 7) == 0) &&
-                   ((reinterpret_cast<uintptr_t>(x) & 15) == 0);
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (vec) {
-    const int64_t vpr = cols >> 3;
-    const int64_t total = rows * vpr;
-    for (int64_t i = tid; i < total; i += stride) {
-      const int64_t r = i / vpr, v = i - r * vpr;
-      const uint4 q = __ldg(reinterpret_cast<const uint4*>(x + r * ld) + v);
-      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  const int lane = threadIdx.x & 31;
+  const uint32_t vpr = static_cast<uint32_t>(cols >> 3);          // vectors per row
+  const uint32_t segs = (vpr + 127u) / 128u;                       // items per row
+  const uint64_t items = static_cast<uint64_t>(rows) * segs;
+  const uint64_t wstride = static_cast<uint64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (uint64_t it = static_cast<uint64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       it < items; it += wstride) {
+    const uint64_t r = it / segs;
+    const uint32_t v0 = static_cast<uint32_t>(it - r * segs) * 128u + lane;
+    const uint4* row = reinterpret_cast<const uint4*>(x + r * ld);
+    uint4 q[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      q[k] = (v0 + 32u * k < vpr) ? __ldg(row + v0 + 32u * k) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t w[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         m = max(m, w[j] & 0x7FFFu);
         m = max(m, (w[j] >> 16) & 0x7FFFu);
       }
     }
-  } else {
-    const int64_t total = rows * cols;
-    for (int64_t i = tid; i < total; i += stride) {
-      const int64_t r = i / cols, c = i - r * cols;
-      m = max(m, static_cast<uint32_t>(x[r * ld + c]) & 0x7FFFu);
-    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
   __shared__ uint32_t wm[8];
-  if ((threadIdx.x & 31) == 0) wm[threadIdx.x >> 5] = m;
+  if (lane == 0) wm[threadIdx.x >> 5] = m;
   __syncthreads();
   if (threadIdx.x == 0) {
     for (int w = 1; w < (blockDim.x >> 5); ++w) m = max(m, wm[w]);
@@ -106,6 +99,15 @@ __global__ void __launch_bounds__(256) amax_kernel(const uint16_t* __restrict__ 
   }
 }
 
+// Lane 4j of a warp returns the bytes of lanes 4j..4j+3 as one little-endian
+// word (for scale bytes that sit four to an aligned word).
+__device__ __forceinline__ uint32_t gather4_bytes(uint32_t byte) {
+  const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, byte, 1);
+  const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, byte, 2);
+  const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, byte, 3);
+  return (byte & 0xFFu) | ((b1 & 0xFFu) << 8) | ((b2 & 0xFFu) << 16) | ((b3 & 0xFFu) << 24);
+}
+
 // ---------------------------------------------------------------------------
 // Quantise one 16-element block
 // ---------------------------------------------------------------------------
@@ -113,6 +115,22 @@ struct Block16 {
   uint2 packed;     // 16 codes, low nibble = lower K index
   uint32_t sf;      // E4M3 code
 };
+
+// Eight binary32 values -> eight E2M1 codes in one word (value 2i in the low
+// nibble of byte i, value 2i+1 in its high nibble), each rounded to nearest
+// even and saturated to +-6 by the hardware conversion.
+__device__ __forceinline__ uint32_t e2m1x8_rn_satfinite(const float* q) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(q[0]), "f"(q[1]), "f"(q[2]), "f"(q[3]), "f"(q[4]), "f"(q[5]), "f"(q[6]), "f"(q[7]));
+  return r;
+}
 
 __device__ __forceinline__ Block16 quantize_block(const uint4 lo, const uint4 hi, float g) {
   uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
@@ -126,22 +144,25 @@ __device__ __forceinline__ Block16 quantize_block(const uint4 lo, const uint4 hi
   const float s = (g > 0.0f) ? __fdiv_rn(__fdiv_rn(amax_b, 6.0f), g) : 0.0f;
   const uint32_t sf = e4m3_from_f32(s);
   const float d = __fmul_rn(f32_from_e4m3(sf), g);
-  uint32_t out[2] = {0u, 0u};
+  // q = x / d in binary32 (d == 0: a signed zero), then E2M1; the sign bit
+  // of every code is set from x itself, so values that round to zero keep
+  // their sign whatever the conversion does with negative zeros.
+  float q[16];
+  uint32_t sgn[2] = {0u, 0u};
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const uint32_t bits = (w[j] >> (16 * h)) & 0xFFFFu;
-      const uint32_t sign = (bits >> 15) << 3;
-      uint32_t code = sign;
-      if (d != 0.0f) {
-        const float q = __fdiv_rn(bf16_bits_to_f32(bits), d);
-        code |= e2m1_mag_code(fabsf(q));
-      }
+      const float xv = bf16_bits_to_f32(bits);
       const int e = 2 * j + h;                 // element index 0..15
-      out[e >> 3] |= code << (4 * (e & 7));
+      q[e] = (d != 0.0f) ? __fdiv_rn(xv, d) : __fmul_rn(xv, 0.0f);
+      sgn[e >> 3] |= (bits >> 15) << (4 * (e & 7) + 3);
     }
   }
+  uint32_t out[2];
+  out[0] = e2m1x8_rn_satfinite(q) | sgn[0];
+  out[1] = e2m1x8_rn_satfinite(q + 8) | sgn[1];
   Block16 b;
   b.packed = make_uint2(out[0], out[1]);
   b.sf = sf;
@@ -152,24 +173,44 @@ __device__ __forceinline__ int64_t atom_offset(int64_t r, int64_t c, int64_t n_c
   return ((r >> 7) * n_cgroups + (c >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (c & 3);
 }
 
-// One thread per 16-element block of x [rows, cols].
+// Work item: a warp quantises 32 consecutive 16-element blocks of one row
+// (lane l takes block 32 * seg + l): one division per item, 1 KB of
+// coalesced loads, 256 contiguous bytes of codes.  Atom-layout scales leave
+// as one word per four blocks.
 __global__ void __launch_bounds__(256) quantize_kernel(const uint16_t* __restrict__ x,
                                                        int64_t rows, int64_t cols, int64_t ld,
                                                        uint8_t* __restrict__ packed,
                                                        uint8_t* __restrict__ scales,
                                                        int sf_atoms, const float* g_ptr) {
   const float g = *g_ptr;
-  const int64_t bpr = cols >> 4;
-  const int64_t total = rows * bpr;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-       i += stride) {
-    const int64_t r = i / bpr, b = i - r * bpr;
-    const uint4* src = reinterpret_cast<const uint4*>(x + r * ld + b * 16);
-    const Block16 q = quantize_block(__ldg(src), __ldg(src + 1), g);
-    *reinterpret_cast<uint2*>(packed + r * (cols >> 1) + b * 8) = q.packed;
-    const int64_t so = sf_atoms ? atom_offset(r, b, cols >> 6) : r * bpr + b;
-    scales[so] = static_cast<uint8_t>(q.sf);
+  const int lane = threadIdx.x & 31;
+  const uint32_t bpr = static_cast<uint32_t>(cols >> 4);
+  const uint32_t segs = (bpr + 31u) / 32u;
+  const uint64_t items = static_cast<uint64_t>(rows) * segs;
+  const uint64_t wstride = static_cast<uint64_t>(gridDim.x) * (blockDim.x >> 5);
+  const int64_t ncg = (cols + 63) >> 6;                 // 4-block scale groups per row
+  for (uint64_t it = static_cast<uint64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       it < items; it += wstride) {
+    const int64_t r = static_cast<int64_t>(it / segs);
+    const uint32_t b = static_cast<uint32_t>(it - static_cast<uint64_t>(r) * segs) * 32u + lane;
+    const bool valid = b < bpr;
+    Block16 q;
+    q.packed = make_uint2(0u, 0u);
+    q.sf = 0u;
+    if (valid) {
+      const uint4* src = reinterpret_cast<const uint4*>(x + r * ld + b * 16);
+      q = quantize_block(__ldg(src), __ldg(src + 1), g);
+      *reinterpret_cast<uint2*>(packed + r * (cols >> 1) + b * 8) = q.packed;
+    }
+    if (sf_atoms) {
+      // blocks 4j..4j+3 of the item share one word of an atom (padding
+      // columns past the row end get zero scales)
+      const uint32_t word = gather4_bytes(q.sf);
+      if ((lane & 3) == 0 && b < static_cast<uint32_t>(ncg * 4))
+        *reinterpret_cast<uint32_t*>(scales + atom_offset(r, b, ncg)) = word;
+    } else if (valid) {
+      scales[r * bpr + b] = static_cast<uint8_t>(q.sf);
+    }
   }
 }
 
@@ -267,27 +308,44 @@ __global__ void __launch_bounds__(256) quantize_dispatch_kernel(
     g = *g_ptr;
   }
   if (s_bad) return;
-  const int64_t bpr = K >> 4;
+  // Work item: a warp quantises 32 consecutive 16-element blocks of one
+  // source row (K % 64 == 0, so every group of four blocks is whole) and
+  // writes them to each of the row's routes: 256 bytes of codes and one
+  // scale word per four blocks per route.
+  const int lane = threadIdx.x & 31;
+  const uint32_t bpr = static_cast<uint32_t>(K >> 4);
+  const uint32_t segs = (bpr + 31u) / 32u;
   const int64_t n_kb = (K + 255) >> 8;
-  const int64_t total = rows * bpr;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const uint64_t items = static_cast<uint64_t>(rows) * segs;
+  const uint64_t wstride = static_cast<uint64_t>(gridDim.x) * (blockDim.x >> 5);
   const int32_t nroutes = off[E];
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-       i += stride) {
-    const int64_t r = i / bpr, b = i - r * bpr;
-    const uint4* src = reinterpret_cast<const uint4*>(x + r * ld + b * 16);
-    const Block16 q = quantize_block(__ldg(src), __ldg(src + 1), g);
+  for (uint64_t it = static_cast<uint64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       it < items; it += wstride) {
+    const int64_t r = static_cast<int64_t>(it / segs);
+    const uint32_t b = static_cast<uint32_t>(it - static_cast<uint64_t>(r) * segs) * 32u + lane;
+    const bool valid = b < bpr;
+    Block16 q;
+    q.packed = make_uint2(0u, 0u);
+    q.sf = 0u;
+    if (valid) {
+      const uint4* src = reinterpret_cast<const uint4*>(x + r * ld + static_cast<int64_t>(b) * 16);
+      q = quantize_block(__ldg(src), __ldg(src + 1), g);
+    }
+    const uint32_t word = gather4_bytes(q.sf);
     const int64_t kb = b >> 4;
     const int bb = static_cast<int>(b & 15);        // 16-element block inside the K block
-    for (int j = 0; j < fanout; ++j) {
+    for (int j = 0; j < fanout; ++j) {              // the row's routes (warp-uniform)
       const int32_t p = route_pos ? route_pos[r * fanout + j] : static_cast<int32_t>(r);
       if (p < 0 || p >= nroutes) continue;          // dropped route
       const int e = find_expert(off, E, p);
       const int32_t local = p - off[e];
       const int64_t rt = tb[e] + local / chunk;
       const int row = local % chunk;
-      *reinterpret_cast<uint2*>(tiles + tile_code_offset(rt, row, kb, bb * 8, n_kb)) = q.packed;
-      tiles[tile_scale_offset(rt, row, kb, bb, n_kb)] = static_cast<uint8_t>(q.sf);
+      if (valid) {
+        *reinterpret_cast<uint2*>(tiles + tile_code_offset(rt, row, kb, bb * 8, n_kb)) = q.packed;
+        if ((lane & 3) == 0)
+          *reinterpret_cast<uint32_t*>(tiles + tile_scale_offset(rt, row, kb, bb, n_kb)) = word;
+      }
     }
   }
 }
@@ -363,17 +421,45 @@ static int grid_for(int64_t work, int sms) {
   return blocks < 1 ? 1 : static_cast<int>(blocks);
 }
 
+// Blocks of 256 threads (8 warps) for `items` warp work items, capped at what
+// the GPU holds at once (one wave, so no block waits for a second one).  The
+// resident count per SM comes from the occupancy calculator, once per kernel.
+template <typename Kernel>
+static int grid_for_items(Kernel kernel, size_t smem, int64_t items, int sms) {
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, 256, smem) != cudaSuccess ||
+        n < 1)
+      n = 1;
+    per_sm = n;
+  }
+  int64_t blocks = (items + 7) / 8;
+  const int64_t cap = static_cast<int64_t>(per_sm) * sms;
+  if (blocks > cap) blocks = cap;
+  return blocks < 1 ? 1 : static_cast<int>(blocks);
+}
+
+static int amax_grid(int64_t rows, int64_t cols, int sms) {
+  const int64_t segs = ((cols >> 3) + 127) / 128;
+  return grid_for_items(amax_kernel, 0, rows * segs, sms);
+}
+
+// Dispatch shared memory is at most 2 * 1024 + 1 ints (E <= 1024); the
+// occupancy is taken at that size.
+constexpr size_t kDispatchSmemMax = sizeof(int32_t) * (2 * 1024 + 1);
+
 cudaError_t launch_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, float* g,
                         int sms, cudaStream_t s) {
   cudaError_t err = cudaMemsetAsync(g, 0, sizeof(float), s);
   if (err != cudaSuccess) return err;
   if (rows == 0 || cols == 0) return cudaSuccess;
-  amax_kernel<<<grid_for(rows * cols / 8, sms), 256, 0, s>>>(x, rows, cols, ld, g, nullptr);
+  amax_kernel<<<amax_grid(rows, cols, sms), 256, 0, s>>>(x, rows, cols, ld, g, nullptr);
   return cudaGetLastError();
 }
 
 int amax_partials_count(int64_t rows, int64_t cols, int sms) {
-  return grid_for(rows * cols / 8, sms);
+  return amax_grid(rows, cols, sms);
 }
 
 cudaError_t launch_amax_partials(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
@@ -387,8 +473,9 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64
                             uint8_t* packed, uint8_t* scales, int sf_atoms, const float* g,
                             int sms, cudaStream_t s) {
   if (rows == 0 || cols == 0) return cudaSuccess;
-  quantize_kernel<<<grid_for(rows * (cols >> 4), sms), 256, 0, s>>>(x, rows, cols, ld, packed,
-                                                                   scales, sf_atoms, g);
+  const int64_t items = rows * (((cols >> 4) + 31) / 32);
+  quantize_kernel<<<grid_for_items(quantize_kernel, 0, items, sms), 256, 0, s>>>(
+      x, rows, cols, ld, packed, scales, sf_atoms, g);
   return cudaGetLastError();
 }
 
@@ -400,7 +487,9 @@ cudaError_t launch_quantize_dispatch(const uint16_t* x, int64_t rows, int64_t K,
                                      int sms, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
   const size_t shmem = sizeof(int32_t) * (2 * static_cast<size_t>(E) + 1);
-  quantize_dispatch_kernel<<<grid_for(rows * (K >> 4), sms), 256, shmem, s>>>(
+  const int64_t items = rows * (((K >> 4) + 31) / 32);
+  quantize_dispatch_kernel<<<grid_for_items(quantize_dispatch_kernel, kDispatchSmemMax, items, sms),
+                             256, shmem, s>>>(
       x, rows, K, ld, route_pos, fanout, expert_offsets, E, R, chunk_rows, tiles, g, partials,
       n_partials, status);
   return cudaGetLastError();

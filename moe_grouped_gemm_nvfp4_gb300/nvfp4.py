@@ -85,6 +85,12 @@ def load() -> ctypes.CDLL:
     return _lib
 
 
+def _row_stride(x):
+    """Row stride in elements; a single row may carry any stride in torch
+    (0 for a broadcast view), and its stride is never used, so pass the width."""
+    return x.stride(0) if x.shape[0] > 1 else x.shape[1]
+
+
 def _ptr(t):
     if t is None:
         return None
@@ -154,7 +160,7 @@ def nvfp4_combine_workspace_bytes(T: int, N: int) -> int:
 def nvfp4_quantize(x, packed, scales, global_scale, flags: int = 0, stream=None) -> None:
     rows, cols = x.shape
     _check("nvfp4_quantize", load().nvfp4_quantize(
-        _ptr(x), rows, cols, x.stride(0), _ptr(packed), _ptr(scales), _ptr(global_scale),
+        _ptr(x), rows, cols, _row_stride(x), _ptr(packed), _ptr(scales), _ptr(global_scale),
         flags, _stream(stream)))
 
 
@@ -189,7 +195,7 @@ def nvfp4_quantize_dispatch(x, route_pos, fanout: int, expert_offsets, E: int, R
                             global_scale, flags: int = 0, stream=None) -> None:
     rows, K = x.shape
     _check("nvfp4_quantize_dispatch", load().nvfp4_quantize_dispatch(
-        _ptr(x), rows, K, x.stride(0), _ptr(route_pos), fanout, _ptr(expert_offsets), E, R,
+        _ptr(x), rows, K, _row_stride(x), _ptr(route_pos), fanout, _ptr(expert_offsets), E, R,
         _ptr(tiles), _ptr(global_scale), flags, _stream(stream)))
 
 

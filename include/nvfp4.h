@@ -244,6 +244,34 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* A_tiles, const float* gA,
                                 void* stream);
 
 /*
+ * Fused expert MLP front half: the gate_up grouped GEMM, SiLU(gate) * up,
+ * and the NVFP4 quantisation of the product, in one launch ("The FP4
+ * Frontier", Finding 5: persistent grouped GEMM; the activation between the
+ * two projections never goes to memory in BF16).
+ *   A_tiles, gA, W_tiles, gW, expert_offsets, E, T, topk, K  as in
+ *       nvfp4_grouped_gemm (gather orientation: A in route order).
+ *   N         rows of each expert's W: rows [0, N/2) are the gate projection,
+ *             rows [N/2, N) the up projection of the same N/2 features.
+ *   g_h       device float: the global scale of h (given, for instance
+ *             calibrated offline as amax(h) / (6 * 448)).
+ *   h_tiles   out: h = SiLU(g) * u per route and feature, with
+ *             g = gA * gW[e] * sum_k A_hat W_hat[e, f, :] and u the same for row
+ *             N/2 + f, SiLU(z) = z / (1 + exp(-z)), all in binary32; quantised
+ *             per 16 features with g_h exactly as nvfp4_quantize does, into the
+ *             grouped tile layout nvfp4_quantize_dispatch writes for R routes,
+ *             E experts and K = N/2 (nvfp4_grouped_tiles_bytes(R, E, N/2)
+ *             bytes).  Feed it to nvfp4_grouped_gemm as A_tiles with gA = g_h.
+ * N % 256 == 0, K % 64 == 0, E <= 256, and the decode regime: the token-tile
+ * width nvfp4_grouped_chunk_rows(R, E) must be 32 (NVFP4_ERR_UNSUPPORTED
+ * otherwise).
+ */
+nvfp4_status nvfp4_moe_gate_up_silu(const uint8_t* A_tiles, const float* gA,
+                                    const uint8_t* W_tiles, const float* gW,
+                                    const int32_t* expert_offsets, int32_t E, int64_t T,
+                                    int32_t topk, int64_t N, int64_t K, const float* g_h,
+                                    uint8_t* h_tiles, void* stream);
+
+/*
  * Allocation-free weighted-combine grouped GEMM.  (This entry point is a
  * library convenience; the pages have no counterpart.)
  *

@@ -28,6 +28,7 @@
 // its own copies and MMAs, frees tensor memory and exits.
 #include "common.cuh"
 #include "kernels.h"
+#include "format.cuh"
 
 namespace nvfp4 {
 
@@ -115,6 +116,8 @@ struct Unit {
   int64_t sfy_off;    // dense: Y scale atoms at k-block 0; grouped: Y operand tile
   int32_t x_reused;   // grouped: the expert has more than one token tile, so its
                       // weight tiles are read again by other units
+  int32_t x_pair;     // grouped, MT == 2: row tiles from the first X tile to the second
+  int32_t y_tile;     // grouped: first operand tile of the unit's token tile
 };
 
 struct Tables {
@@ -127,7 +130,7 @@ template <int BN, int MT>
 __device__ __forceinline__ Unit get_unit(int u, int mode, const GemmArgs& a, const Tables& t,
                                          int tiles_x, int64_t atoms_per_rowtile) {
   Unit un;
-  if (mode == kGrouped || mode == kGroupedCombine) {
+  if (mode == kGrouped || mode == kGroupedCombine || mode == kGroupedSiluMul) {
     int lo = 0, hi = a.E;
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -137,7 +140,10 @@ __device__ __forceinline__ Unit get_unit(int u, int mode, const GemmArgs& a, con
     const int mtiles = a.n_out >> 7;
     const int munits = mtiles / MT;               // units per token tile
     const int local = u - t.up[e];
-    const int mt = (local % munits) * MT;         // first X tile of the unit
+    // SiLU-mul: X tile m (gate rows) pairs with X tile m + mtiles / 2 (the
+    // up rows of the same features); otherwise a unit's X tiles are adjacent
+    const bool glu = mode == kGroupedSiluMul;
+    const int mt = glu ? (local % munits) : (local % munits) * MT;   // first X tile
     const int nt = local / munits;
     const int cnt = t.off[e + 1] - t.off[e];
     un.e = e;
@@ -147,9 +153,10 @@ __device__ __forceinline__ Unit get_unit(int u, int mode, const GemmArgs& a, con
     un.y_rows = min(BN, cnt - nt * BN);
     const int64_t n_kb = (a.K + kBK - 1) / kBK;
     un.sfx_off = static_cast<int64_t>(e * mtiles + mt) * n_kb * kOperandTileBytes;
-    un.sfy_off =
-        static_cast<int64_t>(t.tb[e] + nt * (BN / Cfg<BN, MT>::kLayoutRows)) * n_kb * kOperandTileBytes;
+    un.y_tile = t.tb[e] + nt * (BN / Cfg<BN, MT>::kLayoutRows);
+    un.sfy_off = static_cast<int64_t>(un.y_tile) * n_kb * kOperandTileBytes;
     un.x_reused = cnt > BN;
+    un.x_pair = glu ? mtiles / 2 : 1;
   } else {
     const int tx = u % tiles_x;
     const int ty = u / tiles_x;
@@ -161,6 +168,8 @@ __device__ __forceinline__ Unit get_unit(int u, int mode, const GemmArgs& a, con
     un.sfx_off = static_cast<int64_t>(tx) * atoms_per_rowtile * 512;
     un.sfy_off = static_cast<int64_t>(ty * (BN / 128)) * atoms_per_rowtile * 512;
     un.x_reused = 1;
+    un.x_pair = 1;
+    un.y_tile = 0;
   }
   return un;
 }
@@ -232,7 +241,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const bool grouped = (mode == kGrouped || mode == kGroupedCombine);
+  const bool grouped = (mode == kGrouped || mode == kGroupedCombine || mode == kGroupedSiluMul);
   const int64_t atoms_per_rowtile = a.K >> 6;
   const int nkb = static_cast<int>((a.K + kBK - 1) / kBK);
   const int tiles_x = (a.rows_x + 127) >> 7;
@@ -367,7 +376,8 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
           bulk_load_elect(sx, xt, kXTileBytes + ksteps * 512, full_bar(stage), pol_x);
           if (MT == 2)                   // the unit's second weight tile
             bulk_load_elect(sx + C::kXPartBytes,
-                            xt + static_cast<int64_t>((a.K + kBK - 1) / kBK) * kOperandTileBytes,
+                            xt + static_cast<int64_t>(un.x_pair) * ((a.K + kBK - 1) / kBK) *
+                                     kOperandTileBytes,
                             kXTileBytes + ksteps * 512, full_bar(stage), pol_x);
           bulk_load_elect(sy, yt, ybox_lo * 16 * kRowBytes, full_bar(stage), pol_y);
           bulk_load_elect(ssfy, yt + kXTileBytes, ksteps * 512, full_bar(stage), pol_y);
@@ -568,7 +578,60 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
       tc_fence_after();
       const float alpha = __fmul_rn(grouped ? a.gx[un.e] : a.gx[0], gy);
       const int n_valid = un.y_rows;
-      if (C::kAccBufs == 1 && mode != kGroupedCombine) {
+      if (MT == 2 && mode == kGroupedSiluMul) {
+        // Gate (X tile 0) and up (X tile 1) accumulators of the same 128
+        // features: h = SiLU(alpha * gate) * (alpha * up) in FP32, quantised
+        // per 16 features with the given global of h and written as NVFP4
+        // into h's operand tiles (the layout the dispatch quantiser writes
+        // for K = n_out / 2), row = the route's row in its token tile.
+        const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16) +
+                            abuf * MT * C::kIssuers * C::kAccCols;
+        // one X tile's accumulator, the two MMA warps' partial sums added
+        auto load_acc = [&](uint32_t ta, uint32_t (&r)[32]) {
+          uint32_t r2[32];
+          tmem_ld32(ta, r);
+          if (n_acc == 2) tmem_ld32(ta + C::kAccCols, r2);
+          tmem_ld_wait();
+          if (n_acc == 2) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              r[i] = __float_as_uint(__fadd_rn(__uint_as_float(r[i]), __uint_as_float(r2[i])));
+          }
+        };
+        uint32_t rg[32], ru[32];
+        load_acc(tq, rg);
+        load_acc(tq + C::kIssuers * C::kAccCols, ru);
+        tc_fence_before();
+        mbar_arrive(acce_bar(abuf));               // both accumulators are in registers
+        if (++abuf == C::kAccBufs) { abuf = 0; aphase ^= 1u; }
+        warp_transpose32(rg, lane);                // lane = token, 32 features of quarter q
+        warp_transpose32(ru, lane);
+        if (lane < n_valid) {
+          const float gh = *a.g_h;
+          float h[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float gz = __fmul_rn(__uint_as_float(rg[i]), alpha);
+            const float uz = __fmul_rn(__uint_as_float(ru[i]), alpha);
+            h[i] = __fmul_rn(__fdiv_rn(gz, __fadd_rn(1.0f, expf(-gz))), uz);
+          }
+          const Block16 b0 = quantize16(h, gh);
+          const Block16 b1 = quantize16(h + 16, gh);
+          const int f0 = un.x_local0 + q * 32;     // first feature of h in this lane
+          const int row = lane;                    // token tile = one layout chunk (BN = 32)
+          const int64_t tile = (static_cast<int64_t>(un.y_tile) * a.h_nkb + (f0 >> 8)) *
+                               kOperandTileBytes;
+          const int chunk = (f0 & 255) >> 5;       // 16-byte chunk of the 128-byte row
+          *reinterpret_cast<uint4*>(a.h_tiles + tile + row * 128 + ((chunk ^ (row & 7)) << 4)) =
+              make_uint4(b0.packed.x, b0.packed.y, b1.packed.x, b1.packed.y);
+          const int sc = (f0 & 255) >> 4;          // scale column (even)
+          *reinterpret_cast<uint16_t*>(a.h_tiles + tile + kXTileBytes + (sc >> 2) * 512 +
+                                       (row & 31) * 16 + ((row >> 5) & 3) * 4 + (sc & 3)) =
+              static_cast<uint16_t>(b0.sf | (b1.sf << 8));
+        }
+        continue;
+      }
+      if (C::kAccBufs == 1 && mode != kGroupedCombine && mode != kGroupedSiluMul) {
         // One accumulator: the next unit's MMAs wait for it.  Read all of it
         // into registers as BF16 first, hand it back, then store, so the
         // stores overlap the next unit's MMAs.
@@ -791,6 +854,8 @@ cudaError_t launch_gemm(const CUtensorMap& tmx, const CUtensorMap& tmy, const Ge
     return bn == 256 ? launch_bn<256>(tmx, tmy, a, mode, grid, s)
                      : launch_bn<128>(tmx, tmy, a, mode, grid, s);
   }
+  if (mode == kGroupedSiluMul)      // gate and up tiles pair up in one 32-route unit
+    return launch_bn<32, 2>(tmx, tmy, a, mode, grid, s);
   switch (grouped_tile_width(a.rows_y, a.E)) {
     case 32:   // two weight tiles per unit when the expert's rows pair up
       return (a.n_out / 128) % 2 == 0 ? launch_bn<32, 2>(tmx, tmy, a, mode, grid, s)

@@ -44,6 +44,7 @@ enum GemmMode : int {
   kDenseRowsY = 1,      // C[y][x]: X = B, Y = A (small M)
   kGrouped = 2,         // out[route][n]
   kGroupedCombine = 3,  // ws[token][n] += w * y
+  kGroupedSiluMul = 4,  // h[route][f] = SiLU(gate) * up, quantised into h_tiles
 };
 
 struct GemmArgs {
@@ -69,6 +70,9 @@ struct GemmArgs {
   int* status;
   uint64_t timeout_ns;
   uint32_t debug_flags;            // kDebugSkipFirstStage: test hook, see nvfp4.h
+  uint8_t* h_tiles;                // SiLU-mul: NVFP4 operand tiles of h (K = n_out / 2)
+  const float* g_h;                // SiLU-mul: global scale of h (given)
+  int32_t h_nkb;                   // SiLU-mul: 256-element K blocks of h
 };
 
 // Test hook: the producer of every CTA leaves its first pipeline stage

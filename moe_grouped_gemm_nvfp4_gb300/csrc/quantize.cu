@@ -8,40 +8,9 @@
 // s = (amax_b / 6) / g, each step binary32 round-to-nearest-even.
 #include "common.cuh"
 #include "kernels.h"
+#include "format.cuh"
 
 namespace nvfp4 {
-
-// ---------------------------------------------------------------------------
-// Number formats (implemented from the format definitions)
-// ---------------------------------------------------------------------------
-
-// binary32 (s >= 0, finite) -> E4M3 code, round to nearest even, saturating
-// at 448 (0x7E).  Normal range: keep 3 mantissa bits with RNE (a carry into
-// the exponent is the correct next code).  Below 2^-6: subnormal quantum
-// 2^-9, so the code is s * 2^9 rounded to the nearest even integer.
-__device__ __forceinline__ uint32_t e4m3_from_f32(float s) {
-  if (!(s < 448.0f)) return 0x7Eu;
-  const uint32_t b = __float_as_uint(s);
-  const uint32_t exp = (b >> 23) & 0xFFu;
-  if (exp >= 121u) {                       // s >= 2^-6
-    const uint32_t mant = b & 0x7FFFFFu;
-    const uint32_t keep = mant >> 20;
-    const uint32_t rest = mant & 0xFFFFFu;
-    uint32_t v = ((exp - 120u) << 3) | keep;
-    if (rest > 0x80000u || (rest == 0x80000u && (keep & 1u))) v += 1u;
-    return v;
-  }
-  return __float2uint_rn(s * 512.0f);      // 0..8; 8 is the smallest normal
-}
-
-// E4M3 code (never NaN here) -> binary32, exact.
-__device__ __forceinline__ float f32_from_e4m3(uint32_t c) {
-  const uint32_t e = (c >> 3) & 0xFu;
-  const uint32_t m = c & 7u;
-  const float mag = (e == 0u) ? static_cast<float>(m) * 0.001953125f
-                              : __uint_as_float(((e + 120u) << 23) | (m << 20));
-  return (c & 0x80u) ? -mag : mag;
-}
 
 // ---------------------------------------------------------------------------
 // Tensor amax -> global scale
@@ -108,65 +77,19 @@ __device__ __forceinline__ uint32_t gather4_bytes(uint32_t byte) {
   return (byte & 0xFFu) | ((b1 & 0xFFu) << 8) | ((b2 & 0xFFu) << 16) | ((b3 & 0xFFu) << 24);
 }
 
-// ---------------------------------------------------------------------------
-// Quantise one 16-element block
-// ---------------------------------------------------------------------------
-struct Block16 {
-  uint2 packed;     // 16 codes, low nibble = lower K index
-  uint32_t sf;      // E4M3 code
-};
-
-// Eight binary32 values -> eight E2M1 codes in one word (value 2i in the low
-// nibble of byte i, value 2i+1 in its high nibble), each rounded to nearest
-// even and saturated to +-6 by the hardware conversion.
-__device__ __forceinline__ uint32_t e2m1x8_rn_satfinite(const float* q) {
-  uint32_t r;
-  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
-      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
-      : "=r"(r)
-      : "f"(q[0]), "f"(q[1]), "f"(q[2]), "f"(q[3]), "f"(q[4]), "f"(q[5]), "f"(q[6]), "f"(q[7]));
-  return r;
-}
-
+// One 16-element block of BF16 (two 16-byte vectors) -> codes + scale.  BF16
+// magnitudes compare as integers, so the block maximum needs no conversion.
 __device__ __forceinline__ Block16 quantize_block(const uint4 lo, const uint4 hi, float g) {
-  uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+  const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
   uint32_t amax_bits = 0;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     amax_bits = max(amax_bits, w[j] & 0x7FFFu);
     amax_bits = max(amax_bits, (w[j] >> 16) & 0x7FFFu);
   }
-  const float amax_b = bf16_bits_to_f32(amax_bits);
-  const float s = (g > 0.0f) ? __fdiv_rn(__fdiv_rn(amax_b, 6.0f), g) : 0.0f;
-  const uint32_t sf = e4m3_from_f32(s);
-  const float d = __fmul_rn(f32_from_e4m3(sf), g);
-  // q = x / d in binary32 (d == 0: a signed zero), then E2M1; the sign bit
-  // of every code is set from x itself, so values that round to zero keep
-  // their sign whatever the conversion does with negative zeros.
-  float q[16];
-  uint32_t sgn[2] = {0u, 0u};
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint32_t bits = (w[j] >> (16 * h)) & 0xFFFFu;
-      const float xv = bf16_bits_to_f32(bits);
-      const int e = 2 * j + h;                 // element index 0..15
-      q[e] = (d != 0.0f) ? __fdiv_rn(xv, d) : __fmul_rn(xv, 0.0f);
-      sgn[e >> 3] |= (bits >> 15) << (4 * (e & 7) + 3);
-    }
-  }
-  uint32_t out[2];
-  out[0] = e2m1x8_rn_satfinite(q) | sgn[0];
-  out[1] = e2m1x8_rn_satfinite(q + 8) | sgn[1];
-  Block16 b;
-  b.packed = make_uint2(out[0], out[1]);
-  b.sf = sf;
-  return b;
+  return quantize16_with(bf16_bits_to_f32(amax_bits), g, [&](int e) {
+    return bf16_bits_to_f32((w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu);
+  });
 }
 
 __device__ __forceinline__ int64_t atom_offset(int64_t r, int64_t c, int64_t n_cgroups) {

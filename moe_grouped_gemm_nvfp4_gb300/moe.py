@@ -55,7 +55,7 @@ class GroupedPlan:
     """
 
     def __init__(self, w: ExpertWeights, T: int, topk: int, mode: str, device="cuda",
-                 routing_from: "GroupedPlan" = None):
+                 routing_from: "GroupedPlan" = None, out: bool = True):
         assert mode in ("gather", "combine")
         self.w, self.T, self.topk, self.mode = w, T, topk, mode
         E, N, K = w.E, w.N, w.K
@@ -78,7 +78,10 @@ class GroupedPlan:
                                    dtype=torch.uint8, device=dev)
         self.a_g = torch.empty(1, dtype=torch.float32, device=dev)
         if mode == "gather":
-            self.out = torch.empty((max(R, 1), N), dtype=torch.bfloat16, device=dev)
+            # out=False: the plan only routes and quantises (its GEMM output
+            # goes elsewhere, e.g. the fused MLP's h tiles)
+            self.out = (torch.empty((max(R, 1), N), dtype=torch.bfloat16, device=dev)
+                        if out else None)
             self.workspace = None
         else:
             self.out = torch.empty((max(T, 1), N), dtype=torch.bfloat16, device=dev)
@@ -148,6 +151,35 @@ class DecodeLayer:
         if timing is not None:
             timing[1][1].record()
         return gu.out, dn.out
+
+
+class FusedMLP:
+    """One expert MLP pass, decode regime: route, quantise + dispatch x, then
+    gate_up, SiLU(gate) * up and the NVFP4 quantisation of h in one grouped
+    GEMM launch (nvfp4_moe_gate_up_silu), then the down projection with the
+    weighted combine.  h never exists in BF16; its global scale g_h is given
+    (a device float, calibrated by the caller).
+    """
+
+    def __init__(self, w_gate_up: ExpertWeights, w_down: ExpertWeights, T: int, topk: int,
+                 g_h: torch.Tensor, device="cuda"):
+        assert w_gate_up.E == w_down.E and w_gate_up.N == 2 * w_down.K
+        self.w1, self.w2, self.T, self.topk, self.g_h = w_gate_up, w_down, T, topk, g_h
+        self.gate_up = GroupedPlan(w_gate_up, T, topk, "gather", device, out=False)
+        self.down = GroupedPlan(w_down, T, topk, "combine", device, routing_from=self.gate_up)
+
+    def step(self, x, topk_ids, topk_weights, stream=None):
+        """x [T, K1] BF16, topk_ids [T, k] int32, topk_weights [T, k] FP32 ->
+        out [T, N2] BF16 (the down plan's output buffer)."""
+        gu, dn, w1, w2 = self.gate_up, self.down, self.w1, self.w2
+        gu.route(topk_ids, stream)
+        gu.quantize(x, stream)
+        F.nvfp4_moe_gate_up_silu(gu.a_tiles, gu.a_g, w1.tiles, w1.g, gu.expert_offsets, w1.E,
+                                 self.T, self.topk, w1.N, w1.K, self.g_h, dn.a_tiles, stream)
+        F.nvfp4_grouped_gemm(dn.a_tiles, self.g_h, w2.tiles, w2.g, dn.expert_offsets, w2.E,
+                             self.T, self.topk, w2.N, w2.K, dn.route_token, dn.route_slot,
+                             topk_weights, dn.out, dn.workspace, stream)
+        return dn.out
 
 
 class CapturedStep:

@@ -53,6 +53,8 @@ _SIGS = {
     "nvfp4_combine_workspace_bytes": (_SZ, [_I64, _I64]),
     "nvfp4_grouped_gemm": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I64, _I32, _I64, _I64,
                                           _P, _P, _P, _P, _P, _SZ, _P]),
+    "nvfp4_moe_gate_up_silu": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I64, _I32, _I64, _I64,
+                                              _P, _P, _P]),
     "nvfp4_noalloc_workspace_floats": (_SZ, []),
     "nvfp4_grouped_gemm_combine_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I64, _I32,
                                                           _I64, _I64, _P, _P, _P, _P, _P]),
@@ -197,6 +199,13 @@ def nvfp4_quantize_dispatch(x, route_pos, fanout: int, expert_offsets, E: int, R
     _check("nvfp4_quantize_dispatch", load().nvfp4_quantize_dispatch(
         _ptr(x), rows, K, _row_stride(x), _ptr(route_pos), fanout, _ptr(expert_offsets), E, R,
         _ptr(tiles), _ptr(global_scale), flags, _stream(stream)))
+
+
+def nvfp4_moe_gate_up_silu(A_tiles, gA, W_tiles, gW, expert_offsets, E: int, T: int, topk: int,
+                           N: int, K: int, g_h, h_tiles, stream=None) -> None:
+    _check("nvfp4_moe_gate_up_silu", load().nvfp4_moe_gate_up_silu(
+        _ptr(A_tiles), _ptr(gA), _ptr(W_tiles), _ptr(gW), _ptr(expert_offsets), E, T, topk, N, K,
+        _ptr(g_h), _ptr(h_tiles), _stream(stream)))
 
 
 def nvfp4_grouped_gemm(A_tiles, gA, W_tiles, gW, expert_offsets, E: int, T: int, topk: int,

@@ -32,7 +32,7 @@ __all__ = [
     "gemm", "route", "grouped_gemm", "combine", "prepack_scales",
     "unprepack_scales", "grouped_sf_layout", "sf_tiles_per_expert",
     "TILE_BYTES", "operand_tiles", "grouped_operand_tiles", "tile_byte_offset",
-    "tile_scale_offset",
+    "tile_scale_offset", "grouped_operand_rows", "silu", "silu_mul",
 ]
 
 F32 = np.float32
@@ -213,6 +213,24 @@ def grouped_gemm(a_hat_rows, w_hat, expert_offsets) -> np.ndarray:
     return y
 
 
+def silu(z) -> np.ndarray:
+    """SiLU(z) = z * sigmoid(z) = z / (1 + exp(-z)), in float64 (the usual
+    definition; the pages name the gated MLP, not its formula)."""
+    z = np.asarray(z, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return z / (1.0 + np.exp(-z))
+
+
+def silu_mul(y_gate_up) -> np.ndarray:
+    """Expert MLP gate: y [R, N] -> h [R, N/2] = SiLU(y[:, :N/2]) * y[:, N/2:]
+    (rows [0, N/2) of the gate_up weight are the gate projection, rows
+    [N/2, N) the up projection of the same features), float64.  The fused
+    step between the two projections of "The FP4 Frontier", Finding 5."""
+    y = np.asarray(y_gate_up, dtype=np.float64)
+    half = y.shape[1] // 2
+    return silu(y[:, :half]) * y[:, half:]
+
+
 def combine(y, route_token, route_slot, topk_weights, T) -> np.ndarray:
     """out[t] = sum over the routes p of token t of w[t, slot(p)] * y[p] (float64)."""
     w = np.asarray(topk_weights, dtype=np.float64)
@@ -358,3 +376,28 @@ def grouped_operand_tiles(packed_routes, sf_routes, expert_offsets, chunk_rows=1
             _scatter_rows(out, packed[lo:hi], sf[lo:hi], tb[e] + j // chunk_rows,
                           j % chunk_rows, n_kb)
     return out
+
+
+def grouped_operand_rows(buf, expert_offsets, K, chunk_rows):
+    """Inverse of grouped_operand_tiles: the tile buffer -> (packed [R, K/2],
+    scales [R, K/16]) of the routes, read back from the same positions."""
+    buf = np.asarray(buf, dtype=np.uint8)
+    off = np.asarray(expert_offsets, dtype=np.int64)
+    counts = off[1:] - off[:-1]
+    chunks = -(-counts // chunk_rows)
+    tb = np.concatenate([[0], np.cumsum(chunks)])
+    n_kb = -(-K // 256)
+    R = int(off[-1])
+    packed = np.zeros((R, K // 2), np.uint8)
+    sf = np.zeros((R, K // 16), np.uint8)
+    c = np.arange(K // 2)
+    sc = np.arange(K // 16)
+    for e in range(len(counts)):
+        lo, hi = int(off[e]), int(off[e + 1])
+        if hi > lo:
+            j = np.arange(hi - lo)
+            rt = (tb[e] + j // chunk_rows)[:, None]
+            r = (j % chunk_rows)[:, None]
+            packed[lo:hi] = buf[tile_byte_offset(rt, r, c[None, :] // 128, c[None, :] % 128, n_kb)]
+            sf[lo:hi] = buf[tile_scale_offset(rt, r, sc[None, :] // 16, sc[None, :] % 16, n_kb)]
+    return packed, sf

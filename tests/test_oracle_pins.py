@@ -478,3 +478,41 @@ def test_grouped_operand_tiles_chunks():
     # chunk_rows = 128 reproduces the 128-row layout
     assert np.array_equal(oracle.grouped_operand_tiles(packed, sf, off),
                           oracle.grouped_operand_tiles(packed, sf, off, chunk_rows=128))
+
+
+def test_grouped_operand_rows_inverts_the_layout():
+    """Reading the tiles back at the same byte positions returns every route's
+    codes and scales (chunks of 32 and 128, an empty expert, a ragged K block)."""
+    g = inputs.rng(64)
+    off = np.array([0, 5, 5, 45, 46], np.int64)
+    R, K = 46, 320
+    packed = g.integers(0, 256, (R, K // 2)).astype(np.uint8)
+    sf = g.integers(0, 256, (R, K // 16)).astype(np.uint8)
+    for chunk in (32, 128):
+        buf = oracle.grouped_operand_tiles(packed, sf, off, chunk_rows=chunk)
+        p2, s2 = oracle.grouped_operand_rows(buf, off, K, chunk)
+        assert np.array_equal(p2, packed) and np.array_equal(s2, sf)
+
+
+def test_silu_closed_forms():
+    """sigmoid(ln 3) = 3/4, so SiLU(ln 3) = (3/4) ln 3; SiLU(z) - SiLU(-z) = z
+    because sigmoid(-z) = 1 - sigmoid(z); SiLU(0) = 0; SiLU(z) -> z and -> 0
+    for large |z| (no overflow warning at the far end)."""
+    ln3 = np.log(3.0)
+    assert abs(oracle.silu(ln3) - 0.75 * ln3) <= 4 * np.finfo(np.float64).eps
+    z = np.linspace(-20.0, 20.0, 41)
+    assert np.allclose(oracle.silu(z) - oracle.silu(-z), z, rtol=0, atol=1e-13)
+    assert oracle.silu(0.0) == 0.0
+    assert oracle.silu(800.0) == 800.0 and oracle.silu(-800.0) == 0.0
+
+
+def test_silu_mul_uses_the_first_half_as_gate():
+    """y = [gate | up]: with up = 1 the product is SiLU(gate); swapping the
+    halves changes it (a transposed gate/up reading fails here)."""
+    gate = np.array([[-2.0, 0.5, 3.0]])
+    up = np.array([[1.0, 1.0, 1.0]])
+    h = oracle.silu_mul(np.concatenate([gate, up], axis=1))
+    assert np.allclose(h, oracle.silu(gate), rtol=0, atol=0)
+    h2 = oracle.silu_mul(np.concatenate([up, gate], axis=1))
+    assert not np.allclose(h2, h)
+    assert np.allclose(h2, oracle.silu(1.0) * gate)

@@ -39,6 +39,7 @@ def _routing(g, T, E, k, kind):
     (300, 16, 4, 256, 512, "zipf"),       # skewed with empty experts
     (400, 4, 2, 256, 512, "uniform"),     # 256-row token tiles spanning two operand tiles
     (900, 3, 2, 128, 320, "uniform"),     # several 256-row tiles per expert, ragged K block
+    (256, 32, 2, 1280, 256, "uniform"),   # more two-tile units than CTAs
 ])
 def test_grouped_gather_matches_oracle(T, E, k, N, K, kind):
     g = inputs.rng(T * 13 + E + N + K)
@@ -59,7 +60,8 @@ def test_grouped_gather_matches_oracle(T, E, k, N, K, kind):
 
 
 @pytest.mark.parametrize("T,E,k,N,K", [(32, 8, 2, 256, 512), (64, 16, 8, 384, 256),
-                                       (3, 8, 2, 128, 128), (400, 4, 2, 128, 256)])
+                                       (3, 8, 2, 128, 128), (400, 4, 2, 128, 256),
+                                       (256, 32, 2, 1280, 256)])   # units > CTAs
 def test_grouped_combine_matches_oracle(T, E, k, N, K):
     g = inputs.rng(T * 17 + E + N + K)
     ids = inputs.uniform_topk(g, T, E, k)

@@ -34,7 +34,7 @@ namespace nvfp4 {
 
 namespace {
 
-constexpr int kThreads = 224;                  // 7 warps, roles below
+// 7 warps (11 for 256-wide tiles: Cfg::kThreads), roles below
 constexpr int kRowBytes = 128;                 // 256 FP4 values = one swizzle row
 constexpr int kBK = 256;                       // K elements per stage
 constexpr int kXTileBytes = 128 * kRowBytes;   // 16 KB
@@ -85,6 +85,11 @@ struct Cfg {
   // takes half of tensor memory
   static constexpr int kAccBufs = BN == 256 ? 1 : 2;
   static constexpr int kAccCols = BN;                  // one accumulator
+  // Epilogue warp groups: 256-wide tiles hold their single accumulator until
+  // the epilogue has read it, so a second group of four warps (warps 7-10)
+  // takes the upper half of its columns and halves that wait.
+  static constexpr int kEpiGroups = BN == 256 ? 2 : 1;
+  static constexpr int kThreads = (7 + 4 * (kEpiGroups - 1)) * 32;
   // accumulator (buffer b, X tile x, issuer j) at column ((b * MT + x) *
   // kIssuers + j) * BN; scale columns follow the accumulators: per stage 16
   // for each X tile, 16 or 32 for Y
@@ -211,7 +216,7 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, u
 }
 
 template <int BN, int MT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<BN, MT>::kThreads, 1)
 nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmy,
                   const GemmArgs a, int mode) {
   using C = Cfg<BN, MT>;
@@ -251,7 +256,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
     for (int g = 0; g < C::kGroups; ++g) mbar_init(empty_bar(g), C::kIssuers);
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), C::kIssuers);
-      mbar_init(acce_bar(b), 128);
+      mbar_init(acce_bar(b), 128 * C::kEpiGroups);
     }
     mbar_init(drain_bar, C::kSplit ? 2 : C::kIssuers);
     if (C::kSplit)
@@ -542,9 +547,13 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
     tc_commit_elect(drain_bar);
     if (lane == 0) mbar_wait_drain(drain_bar, 0, ctl->timeout_ns);
     __syncwarp();
-  } else if (warp >= 2 && warp <= 5) {
+  } else if ((warp >= 2 && warp <= 5) || warp >= 7) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                       // tensor-memory lane quarter
+    // columns of the accumulator this warp's group reads
+    const int grp = warp >= 7 ? 1 : 0;
+    constexpr int kGrpCols = BN / C::kEpiGroups;
+    const int gc0 = grp * kGrpCols;
     const int row = q * 32 + lane;                // row of the X tile
     int abuf = 0;
     uint32_t aphase = 0;
@@ -635,13 +644,13 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
         // One accumulator: the next unit's MMAs wait for it.  Read all of it
         // into registers as BF16 first, hand it back, then store, so the
         // stores overlap the next unit's MMAs.
-        uint32_t pk[BN / 32][16];                 // BF16 pairs of alpha * acc
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+        uint32_t pk[kGrpCols / 32][16];           // BF16 pairs of alpha * acc
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + gc0;
         // two 32-column loads in flight per wait (the load latency, not the
         // conversion, sets the drain time)
 #pragma unroll
-        for (int cp2 = 0; cp2 < BN / 64; ++cp2) {
-          if (cp2 * 64 < n_valid) {
+        for (int cp2 = 0; cp2 < kGrpCols / 64; ++cp2) {
+          if (gc0 + cp2 * 64 < n_valid) {
             uint32_t r[2][32];
             tmem_ld32(taddr + cp2 * 64, r[0]);
             tmem_ld32(taddr + cp2 * 64 + 32, r[1]);
@@ -663,8 +672,8 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
         mbar_arrive(acce_bar(abuf));
         if (++abuf == C::kAccBufs) { abuf = 0; aphase ^= 1u; }
 #pragma unroll
-        for (int ci = 0; ci < BN / 32; ++ci) {
-          const int c0 = ci * 32;
+        for (int ci = 0; ci < kGrpCols / 32; ++ci) {
+          const int c0 = gc0 + ci * 32;
           if (c0 >= n_valid) continue;
           uint16_t* dst;
           bool vec;
@@ -701,7 +710,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
       const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) +
                              (abuf * MT + xt) * C::kIssuers * C::kAccCols;
       const int xr = un.x_local0 + xt * 128 + row;  // output feature / X row
-      for (int c0 = 0; c0 < n_valid; c0 += 32) {
+      for (int c0 = gc0; c0 < min(n_valid, gc0 + kGrpCols); c0 += 32) {
         uint32_t r[32];
         tmem_ld32(taddr + c0, r);
         if (n_acc == 2) {                 // the second issuer's partial sums
@@ -837,7 +846,8 @@ cudaError_t init_gemm_attributes() {
 template <int BN, int MT = 1>
 static cudaError_t launch_bn(const CUtensorMap& tmx, const CUtensorMap& tmy, const GemmArgs& a,
                              int mode, int grid, cudaStream_t s) {
-  nvfp4_gemm_kernel<BN, MT><<<grid, kThreads, Cfg<BN, MT>::kSmemBytes, s>>>(tmx, tmy, a, mode);
+  nvfp4_gemm_kernel<BN, MT><<<grid, Cfg<BN, MT>::kThreads, Cfg<BN, MT>::kSmemBytes, s>>>(
+      tmx, tmy, a, mode);
   return cudaGetLastError();
 }
 

@@ -273,13 +273,16 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
       const int per = (E + 31) / 32;
       const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
       const int mtiles = (a.n_out >> 7) / MT;       // units per token tile
+      // the offsets arrive with coalesced loads (all in flight at once);
+      // the scan below reads them from shared memory
+#pragma unroll 4
+      for (int i = lane; i <= E; i += 32) t.off[i] = a.expert_offsets[i];
+      __syncwarp();
       int32_t su = 0, st = 0;
       bool ok = true;
       for (int e = e0; e < e1; ++e) {
-        const int32_t o0 = a.expert_offsets[e], o1 = a.expert_offsets[e + 1];
-        const int32_t c = o1 - o0;
+        const int32_t c = t.off[e + 1] - t.off[e];
         ok = ok && (c >= 0);
-        t.off[e] = o0;
         su += mtiles * ((c + BN - 1) / BN);
         st += (c + C::kLayoutRows - 1) / C::kLayoutRows;
       }
@@ -292,18 +295,17 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
       }
       int32_t pu = iu - su, pt = it - st;
       for (int e = e0; e < e1; ++e) {
-        const int32_t c = a.expert_offsets[e + 1] - a.expert_offsets[e];
+        const int32_t c = t.off[e + 1] - t.off[e];
         t.up[e] = pu; t.tb[e] = pt;
         pu += mtiles * ((c + BN - 1) / BN);
         pt += (c + C::kLayoutRows - 1) / C::kLayoutRows;
       }
       const bool all_ok = __all_sync(0xFFFFFFFFu, ok);
       if (lane == 31) {
-        const int32_t oE = a.expert_offsets[E];
-        t.off[E] = oE;
+        const int32_t oE = t.off[E];
         t.up[E] = iu;
         t.tb[E] = it;
-        const bool good = all_ok && a.expert_offsets[0] == 0 && oE <= a.rows_y;
+        const bool good = all_ok && t.off[0] == 0 && oE <= a.rows_y;
         if (!good) raise_status(a.status, NVFP4_ERR_DEVICE_CHECK);
         s_units = good ? iu : 0;
       }

@@ -65,6 +65,14 @@ int nvfp4_version(void);
  */
 nvfp4_status nvfp4_device_status(void* stream, int reset, int* status_out);
 
+/*
+ * Reads the calling device's status word without clearing it, after
+ * synchronising `stream`: NVFP4_OK, or the first device-side error recorded
+ * since the last reset (or an error of the read itself).  The same word as
+ * nvfp4_device_status(stream, 0, &status).
+ */
+nvfp4_status nvfp4_last_device_status(void* stream);
+
 /* Bounded-wait limit of the pipeline kernels in nanoseconds (default 1 s,
  * or NVFP4_TIMEOUT_NS from the environment at the first call). */
 nvfp4_status nvfp4_set_timeout_ns(uint64_t ns);
@@ -86,6 +94,12 @@ nvfp4_status nvfp4_debug_set_flags(uint32_t flags);
  * major; rows are padded to a multiple of 128.  cols % 64 == 0.
  */
 size_t nvfp4_atom_scales_bytes(int64_t rows, int64_t cols);
+
+/*
+ * Bytes of the atom-layout scales for rows x kblk row-major scales (kblk =
+ * K/16): what nvfp4_prepack_weights writes, rows padded to 128 and kblk to 4.
+ */
+size_t nvfp4_prepacked_scales_bytes(int64_t rows, int64_t kblk);
 
 /*
  * BF16 -> NVFP4 quantiser (per-16 amax, E4M3 block scale, E2M1 round to
@@ -213,6 +227,9 @@ nvfp4_status nvfp4_quantize_dispatch(const void* x, int64_t rows, int64_t K, int
 
 /* Bytes of the FP32 combine workspace for T tokens and N outputs. */
 size_t nvfp4_combine_workspace_bytes(int64_t T, int64_t N);
+
+/* The same as nvfp4_combine_workspace_bytes(T, N): FP32 [T, N]. */
+size_t nvfp4_grouped_gemm_workspace_bytes(int64_t T, int64_t N);
 
 /*
  * MoE expert grouped GEMM ("The FP4 Frontier", Finding 5 and Finding 7:

@@ -157,6 +157,21 @@ nvfp4_status nvfp4_device_status(void* stream, int reset, int* status_out) {
   return NVFP4_OK;
 }
 
+nvfp4_status nvfp4_last_device_status(void* stream) {
+  int v = 0;
+  const nvfp4_status st = nvfp4_device_status(stream, 0, &v);
+  return st != NVFP4_OK ? st : static_cast<nvfp4_status>(v);
+}
+
+size_t nvfp4_prepacked_scales_bytes(int64_t rows, int64_t kblk) {
+  if (rows < 0 || kblk < 0) return 0;
+  return nvfp4_atom_scales_bytes(rows, 16 * ((kblk + 3) / 4 * 4));
+}
+
+size_t nvfp4_grouped_gemm_workspace_bytes(int64_t T, int64_t N) {
+  return nvfp4_combine_workspace_bytes(T, N);
+}
+
 size_t nvfp4_atom_scales_bytes(int64_t rows, int64_t cols) {
   if (rows < 0 || cols < 0) return 0;
   return static_cast<size_t>((rows + 127) / 128 * 128) * static_cast<size_t>(cols / 16);

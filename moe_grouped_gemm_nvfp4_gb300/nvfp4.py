@@ -40,6 +40,9 @@ _SIGS = {
     "nvfp4_set_timeout_ns": (ctypes.c_int, [ctypes.c_uint64]),
     "nvfp4_debug_set_flags": (ctypes.c_int, [ctypes.c_uint32]),
     "nvfp4_atom_scales_bytes": (_SZ, [_I64, _I64]),
+    "nvfp4_last_device_status": (ctypes.c_int, [_P]),
+    "nvfp4_prepacked_scales_bytes": (_SZ, [_I64, _I64]),
+    "nvfp4_grouped_gemm_workspace_bytes": (_SZ, [_I64, _I64]),
     "nvfp4_quantize": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _P, _U32, _P]),
     "nvfp4_prepack_weights": (ctypes.c_int, [_P, _I64, _I64, _P, _P]),
     "nvfp4_gemm": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P]),
@@ -137,6 +140,19 @@ def nvfp4_set_timeout_ns(ns: int) -> None:
 
 def nvfp4_debug_set_flags(flags: int) -> None:
     _check("nvfp4_debug_set_flags", load().nvfp4_debug_set_flags(int(flags)))
+
+
+def nvfp4_last_device_status(stream=None) -> int:
+    """The device status word (not cleared); see nvfp4_device_status."""
+    return load().nvfp4_last_device_status(_stream(stream))
+
+
+def nvfp4_prepacked_scales_bytes(rows: int, kblk: int) -> int:
+    return load().nvfp4_prepacked_scales_bytes(rows, kblk)
+
+
+def nvfp4_grouped_gemm_workspace_bytes(T: int, N: int) -> int:
+    return load().nvfp4_grouped_gemm_workspace_bytes(T, N)
 
 
 def nvfp4_atom_scales_bytes(rows: int, cols: int) -> int:

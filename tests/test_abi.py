@@ -42,6 +42,9 @@ def test_pure_host_helpers():
     assert F.nvfp4_atom_scales_bytes(300, 512) == 384 * 32
     assert F.nvfp4_atom_scales_bytes(0, 512) == 0
     assert F.nvfp4_combine_workspace_bytes(256, 6144) == 256 * 6144 * 4
+    assert F.nvfp4_grouped_gemm_workspace_bytes(256, 6144) == 256 * 6144 * 4
+    assert F.nvfp4_prepacked_scales_bytes(300, 32) == F.nvfp4_atom_scales_bytes(300, 512)
+    assert F.nvfp4_prepacked_scales_bytes(1, 3) == 128 * 4      # kblk padded to 4
     # operand tiles: 18432 bytes per 128 rows x 256 K
     assert F.nvfp4_operand_tiles_bytes(300, 512) == 3 * 2 * 18432
     assert F.nvfp4_operand_tiles_bytes(128, 64) == 18432

@@ -138,7 +138,9 @@ def test_route_rejects_bad_ids_on_device():
     ids = torch.tensor([[0, 1], [5, 2]], dtype=torch.int32, device="cuda")
     F.nvfp4_device_status(reset=True)
     off, tok, slot, pos = F.moe_route(ids, 4)
+    assert F.nvfp4_last_device_status() == F.NVFP4_ERR_DEVICE_CHECK   # read, not cleared
     assert F.nvfp4_device_status(reset=True) == F.NVFP4_ERR_DEVICE_CHECK
+    assert F.nvfp4_last_device_status() == F.NVFP4_OK
     assert off[-1].item() == 3
 
 

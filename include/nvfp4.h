@@ -51,6 +51,8 @@ typedef enum nvfp4_status {
 #define NVFP4_SF_ROWMAJOR   0u  /* scales as uint8 [rows, cols/16]               */
 #define NVFP4_SF_ATOMS      1u  /* scales in the tensor-core atom layout         */
 #define NVFP4_GLOBAL_GIVEN  2u  /* read *global_scale instead of computing it    */
+#define NVFP4_AMAX_DONE     4u  /* dispatch: amax maxima already in the tiles'   */
+                                /* scratch (nvfp4_amax_partials)                 */
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* nvfp4_status_string(int status);
@@ -216,6 +218,10 @@ size_t nvfp4_grouped_tiles_bytes(int64_t R, int32_t E, int64_t K);
  *               Rows past a chunk's routes are left unwritten (they only ever
  *               feed output columns the GEMM does not store).
  *   global_scale  as in nvfp4_quantize (one g over the whole of x).
+ *   flags       NVFP4_GLOBAL_GIVEN: use *global_scale; NVFP4_AMAX_DONE: the
+ *               tensor amax's per-block maxima of this x are already in the
+ *               tiles' scratch (nvfp4_amax_partials, same x, rows, K, R, E and
+ *               device), so only the quantise-and-dispatch kernel runs.
  * K % 64 == 0, E <= 1024.  Offsets that are not monotone or exceed R set
  * NVFP4_ERR_DEVICE_CHECK and nothing is written.
  */
@@ -224,6 +230,16 @@ nvfp4_status nvfp4_quantize_dispatch(const void* x, int64_t rows, int64_t K, int
                                      const int32_t* expert_offsets, int32_t E, int64_t R,
                                      uint8_t* tiles, float* global_scale, uint32_t flags,
                                      void* stream);
+
+/*
+ * The first half of nvfp4_quantize_dispatch: the tensor amax of x as
+ * per-block maxima in the scratch at the end of `tiles` (sized by
+ * nvfp4_grouped_tiles_bytes(R, E, K)).  It needs no routing, so it can run
+ * on another stream while nvfp4_moe_route runs; then call
+ * nvfp4_quantize_dispatch with NVFP4_AMAX_DONE after both.
+ */
+nvfp4_status nvfp4_amax_partials(const void* x, int64_t rows, int64_t K, int64_t ld, int64_t R,
+                                 int32_t E, uint8_t* tiles, void* stream);
 
 /* Bytes of the FP32 combine workspace for T tokens and N outputs. */
 size_t nvfp4_combine_workspace_bytes(int64_t T, int64_t N);

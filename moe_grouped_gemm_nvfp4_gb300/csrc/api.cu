@@ -331,7 +331,9 @@ nvfp4_status nvfp4_quantize_dispatch(const void* x, int64_t rows, int64_t K, int
                                      uint8_t* tiles, float* global_scale, uint32_t flags,
                                      void* stream) {
   if (rows < 0 || K <= 0 || ld < K || E <= 0 || R < 0 || fanout <= 0) return NVFP4_ERR_INVALID_ARG;
-  if (flags & ~static_cast<uint32_t>(NVFP4_GLOBAL_GIVEN)) return NVFP4_ERR_INVALID_ARG;
+  if (flags & ~static_cast<uint32_t>(NVFP4_GLOBAL_GIVEN | NVFP4_AMAX_DONE))
+    return NVFP4_ERR_INVALID_ARG;
+  if ((flags & NVFP4_GLOBAL_GIVEN) && (flags & NVFP4_AMAX_DONE)) return NVFP4_ERR_INVALID_ARG;
   if (!expert_offsets || !global_scale || (rows > 0 && (!x || !tiles)))
     return NVFP4_ERR_INVALID_ARG;
   if (!route_pos && (fanout != 1 || rows != R)) return NVFP4_ERR_INVALID_ARG;
@@ -355,12 +357,34 @@ nvfp4_status nvfp4_quantize_dispatch(const void* x, int64_t rows, int64_t K, int
     if (static_cast<size_t>(n_partials) * sizeof(uint32_t) > kAmaxScratchBytes)
       return NVFP4_ERR_UNSUPPORTED;
     partials = reinterpret_cast<uint32_t*>(tiles + grouped_tiles_body_bytes(R, E, K));
-    if (nvfp4::launch_amax_partials(xb, rows, K, ld, partials, d->sms, s) != cudaSuccess)
+    // NVFP4_AMAX_DONE: nvfp4_amax_partials already left them there
+    if (!(flags & NVFP4_AMAX_DONE) &&
+        nvfp4::launch_amax_partials(xb, rows, K, ld, partials, d->sms, s) != cudaSuccess)
       return cuda_fail();
   }
   if (nvfp4::launch_quantize_dispatch(xb, rows, K, ld, route_pos, fanout, expert_offsets, E, R,
                                       nvfp4::grouped_chunk_rows(R, E), tiles, global_scale,
                                       partials, n_partials, d->status, d->sms, s) != cudaSuccess)
+    return cuda_fail();
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_amax_partials(const void* x, int64_t rows, int64_t K, int64_t ld, int64_t R,
+                                 int32_t E, uint8_t* tiles, void* stream) {
+  if (rows < 0 || K <= 0 || ld < K || E <= 0 || R < 0) return NVFP4_ERR_INVALID_ARG;
+  if (rows > 0 && (!x || !tiles)) return NVFP4_ERR_INVALID_ARG;
+  if (K % 64 != 0 || ld % 8 != 0 || E > 1024) return NVFP4_ERR_UNSUPPORTED;
+  if ((x && !aligned16(x)) || (tiles && !aligned16(tiles))) return NVFP4_ERR_UNSUPPORTED;
+  DeviceState* d = nullptr;
+  nvfp4_status st = device_state(&d);
+  if (st != NVFP4_OK) return st;
+  if (rows == 0) return NVFP4_OK;
+  const int n_partials = nvfp4::amax_partials_count(rows, K, d->sms);
+  if (static_cast<size_t>(n_partials) * sizeof(uint32_t) > kAmaxScratchBytes)
+    return NVFP4_ERR_UNSUPPORTED;
+  uint32_t* partials = reinterpret_cast<uint32_t*>(tiles + grouped_tiles_body_bytes(R, E, K));
+  if (nvfp4::launch_amax_partials(static_cast<const uint16_t*>(x), rows, K, ld, partials, d->sms,
+                                  static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return cuda_fail();
   return NVFP4_OK;
 }

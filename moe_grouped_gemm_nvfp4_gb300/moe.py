@@ -92,13 +92,18 @@ class GroupedPlan:
         F.nvfp4_moe_route(topk_ids, self.w.E, self.expert_offsets, self.route_token,
                           self.route_slot, self.route_pos, stream)
 
-    def quantize(self, x, stream=None):
+    def amax(self, x, stream=None):
+        """The tensor amax half of quantize(); needs no routing."""
+        F.nvfp4_amax_partials(x, self.R, self.w.E, self.a_tiles, stream)
+
+    def quantize(self, x, stream=None, amax_done: bool = False):
+        flags = F.NVFP4_AMAX_DONE if amax_done else 0
         if self.mode == "gather":
             F.nvfp4_quantize_dispatch(x, self.route_pos, self.topk, self.expert_offsets,
-                                      self.w.E, self.R, self.a_tiles, self.a_g, 0, stream)
+                                      self.w.E, self.R, self.a_tiles, self.a_g, flags, stream)
         else:
             F.nvfp4_quantize_dispatch(x, None, 1, self.expert_offsets, self.w.E, self.R,
-                                      self.a_tiles, self.a_g, 0, stream)
+                                      self.a_tiles, self.a_g, flags, stream)
 
     def gemm(self, topk_weights=None, stream=None):
         w = self.w
@@ -117,6 +122,18 @@ class GroupedPlan:
         return self.out
 
 
+def _route_and_amax(plan: "GroupedPlan", x, topk_ids, side, stream=None):
+    """Routing and the amax of x need nothing from each other: the amax runs
+    on `side` while the routing runs on the step's stream, which then waits
+    for it (fork and join by events, which CUDA graph capture records)."""
+    main = torch.cuda.current_stream() if stream is None else stream
+    side.wait_stream(main)
+    with torch.cuda.stream(side):
+        plan.amax(x, side)
+    plan.route(topk_ids, main)
+    main.wait_stream(side)
+
+
 class DecodeLayer:
     """One MoE pass over a token batch: gate_up (gather) then down (combine).
 
@@ -129,6 +146,7 @@ class DecodeLayer:
                  device="cuda"):
         self.gate_up = GroupedPlan(w_gate_up, T, topk, "gather", device)
         self.down = GroupedPlan(w_down, T, topk, "combine", device, routing_from=self.gate_up)
+        self._side = torch.cuda.Stream(device=torch.device(device))
 
     def step(self, x, topk_ids, h, topk_weights, stream=None, timing=None):
         """x [T, K1] BF16, topk_ids [T, k] int32, h [R, K2] BF16 (route order),
@@ -137,8 +155,8 @@ class DecodeLayer:
         `timing`, if given, is a pair of (start, end) CUDA-event lists that
         bracket the two grouped-GEMM calls."""
         gu, dn = self.gate_up, self.down
-        gu.route(topk_ids, stream)
-        gu.quantize(x, stream)
+        _route_and_amax(gu, x, topk_ids, self._side, stream)
+        gu.quantize(x, stream, amax_done=True)
         if timing is not None:
             timing[0][0].record()
         gu.gemm(None, stream)
@@ -167,13 +185,14 @@ class FusedMLP:
         self.w1, self.w2, self.T, self.topk, self.g_h = w_gate_up, w_down, T, topk, g_h
         self.gate_up = GroupedPlan(w_gate_up, T, topk, "gather", device, out=False)
         self.down = GroupedPlan(w_down, T, topk, "combine", device, routing_from=self.gate_up)
+        self._side = torch.cuda.Stream(device=torch.device(device))
 
     def step(self, x, topk_ids, topk_weights, stream=None):
         """x [T, K1] BF16, topk_ids [T, k] int32, topk_weights [T, k] FP32 ->
         out [T, N2] BF16 (the down plan's output buffer)."""
         gu, dn, w1, w2 = self.gate_up, self.down, self.w1, self.w2
-        gu.route(topk_ids, stream)
-        gu.quantize(x, stream)
+        _route_and_amax(gu, x, topk_ids, self._side, stream)
+        gu.quantize(x, stream, amax_done=True)
         F.nvfp4_moe_gate_up_silu(gu.a_tiles, gu.a_g, w1.tiles, w1.g, gu.expert_offsets, w1.E,
                                  self.T, self.topk, w1.N, w1.K, self.g_h, dn.a_tiles, stream)
         F.nvfp4_grouped_gemm(dn.a_tiles, self.g_h, w2.tiles, w2.g, dn.expert_offsets, w2.E,

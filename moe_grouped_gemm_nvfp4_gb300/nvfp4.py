@@ -26,6 +26,7 @@ NVFP4_ERR_DEVICE_CHECK = 5
 NVFP4_SF_ROWMAJOR = 0
 NVFP4_SF_ATOMS = 1
 NVFP4_GLOBAL_GIVEN = 2
+NVFP4_AMAX_DONE = 4
 
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
@@ -53,6 +54,7 @@ _SIGS = {
     "nvfp4_grouped_tiles_bytes": (_SZ, [_I64, _I32, _I64]),
     "nvfp4_quantize_dispatch": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I32, _P, _I32, _I64,
                                                _P, _P, _U32, _P]),
+    "nvfp4_amax_partials": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, _I32, _P, _P]),
     "nvfp4_combine_workspace_bytes": (_SZ, [_I64, _I64]),
     "nvfp4_grouped_gemm": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I64, _I32, _I64, _I64,
                                           _P, _P, _P, _P, _P, _SZ, _P]),
@@ -222,6 +224,12 @@ def nvfp4_moe_gate_up_silu(A_tiles, gA, W_tiles, gW, expert_offsets, E: int, T: 
     _check("nvfp4_moe_gate_up_silu", load().nvfp4_moe_gate_up_silu(
         _ptr(A_tiles), _ptr(gA), _ptr(W_tiles), _ptr(gW), _ptr(expert_offsets), E, T, topk, N, K,
         _ptr(g_h), _ptr(h_tiles), _stream(stream)))
+
+
+def nvfp4_amax_partials(x, R: int, E: int, tiles, stream=None) -> None:
+    rows, K = x.shape
+    _check("nvfp4_amax_partials", load().nvfp4_amax_partials(
+        _ptr(x), rows, K, _row_stride(x), R, E, _ptr(tiles), _stream(stream)))
 
 
 def nvfp4_grouped_gemm(A_tiles, gA, W_tiles, gW, expert_offsets, E: int, T: int, topk: int,

@@ -169,3 +169,35 @@ def test_bounded_wait_expires_reports_timeout_and_context_survives():
     px, sx, gx = oracle.quantize(x.float().cpu().numpy())
     ref = oracle.grouped_gemm(oracle.dequantize(px, sx, gx)[tok], _oracle_weights(w), off)
     check_gemm(bf16_to_np(plan.out[: T * k]), ref, "after timeout")
+
+
+def test_layer_step_overlapping_route_and_amax_matches_sequential_calls():
+    """DecodeLayer.step runs the amax of x on a side stream beside the routing
+    (NVFP4_AMAX_DONE for the dispatch); eagerly and replayed from a CUDA graph
+    it must give the bytes the plain sequence route -> quantize -> GEMM gives."""
+    T, E, k, K1, N1, K2, N2 = 48, 8, 2, 256, 256, 128, 256
+    g = inputs.rng(4242)
+    x = inputs.normal_bf16(g, (T, K1)).cuda()
+    h = inputs.normal_bf16(g, (T * k, K2)).cuda()
+    ids = torch.from_numpy(inputs.uniform_topk(g, T, E, k)).cuda()
+    wts = torch.from_numpy(inputs.dirichlet_weights(g, T, k)).cuda()
+    W1 = moe.quantize_experts(_weights_host(g, E, N1, K1).cuda())
+    W2 = moe.quantize_experts(_weights_host(g, E, N2, K2).cuda())
+    ref = moe.GroupedPlan(W1, T, k, "gather")
+    ref_out = ref.run(x, ids).clone()
+    ref_dn = moe.GroupedPlan(W2, T, k, "combine", routing_from=ref)
+    ref_dn_out = ref_dn.run(h, None, wts, route=False).clone()
+    layer = moe.DecodeLayer(W1, W2, T, k)
+    gu_out, dn_out = layer.step(x, ids, h, wts)
+    torch.cuda.synchronize()
+    assert F.nvfp4_device_status() == F.NVFP4_OK
+    assert torch.equal(layer.gate_up.a_g, ref.a_g)
+    assert torch.equal(gu_out[:T * k], ref_out[:T * k])
+    assert torch.equal(dn_out[:T].float(), ref_dn_out[:T].float()) or \
+        torch.allclose(dn_out[:T].float(), ref_dn_out[:T].float(), rtol=1e-2, atol=1e-3)
+    cap = moe.CapturedStep(layer, x, ids, h, wts)
+    gu_out.zero_()
+    cap.replay()
+    torch.cuda.synchronize()
+    assert F.nvfp4_device_status() == F.NVFP4_OK
+    assert torch.equal(gu_out[:T * k], ref_out[:T * k])

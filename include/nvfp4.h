@@ -295,7 +295,7 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* A_tiles, const float* gA,
  *             E experts and K = N/2 (nvfp4_grouped_tiles_bytes(R, E, N/2)
  *             bytes).  Feed it to nvfp4_grouped_gemm as A_tiles with gA = g_h.
  * N % 256 == 0, K % 64 == 0, E <= 256, and the decode regime: the token-tile
- * width nvfp4_grouped_chunk_rows(R, E) must be 32 (NVFP4_ERR_UNSUPPORTED
+ * width nvfp4_grouped_chunk_rows(R, E) must be 32 or 64 (NVFP4_ERR_UNSUPPORTED
  * otherwise).
  */
 nvfp4_status nvfp4_moe_gate_up_silu(const uint8_t* A_tiles, const float* gA,

@@ -463,8 +463,9 @@ nvfp4_status nvfp4_moe_gate_up_silu(const uint8_t* A_tiles, const float* gA,
   const int64_t R = T * topk;
   if (R > (1LL << 30) || static_cast<int64_t>(E) * N > (1LL << 30)) return NVFP4_ERR_UNSUPPORTED;
   // the fused epilogue pairs each gate tile with its up tile in one unit,
-  // which the 32-route token tiles of the decode regime provide
-  if (nvfp4::grouped_tile_width(R, E) != 32) return NVFP4_ERR_UNSUPPORTED;
+  // which the 32- and 64-route token tiles of the decode regime provide
+  const int tw = nvfp4::grouped_tile_width(R, E);
+  if (tw != 32 && tw != 64) return NVFP4_ERR_UNSUPPORTED;
   if (!aligned16(A_tiles) || !aligned16(W_tiles) || !aligned16(h_tiles) ||
       (reinterpret_cast<uintptr_t>(g_h) & 3u))
     return NVFP4_ERR_UNSUPPORTED;

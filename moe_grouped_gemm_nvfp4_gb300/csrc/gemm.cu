@@ -52,7 +52,8 @@ struct Cfg {
   // MT 128-row X tiles per unit (2 only for 32-row token tiles: two MMAs per
   // K step share the token operand, halving the units, the token re-reads
   // and the scale copies of Y per weight byte)
-  static_assert(MT == 1 || (MT == 2 && BN == 32), "unit height");
+  // (64-row tiles with two X tiles serve only the fused SiLU-mul epilogue)
+  static_assert(MT == 1 || (MT == 2 && (BN == 32 || BN == 64)), "unit height");
   static constexpr int kYTileBytes = BN * kRowBytes;
   static constexpr int kSfyAtomsPerStep = BN == 256 ? 2 : 1;   // 128-row scale atoms of Y
   // rows of one grouped operand tile / layout chunk: a 256-row token tile
@@ -65,7 +66,7 @@ struct Cfg {
   static constexpr int kYOffset = MT * kXPartBytes;
   static constexpr int kStageBytes = kYOffset + kYTileBytes + kSfyStageBytes;
   static_assert(kYOffset % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle alignment");
-  static constexpr int kStages = MT == 2 ? 5 : (BN == 32 ? 9 : (BN == 256 ? 4 : 6));
+  static constexpr int kStages = MT == 2 ? (BN == 32 ? 5 : 4) : (BN == 32 ? 9 : (BN == 256 ? 4 : 6));
   // Stages are released to the producer in groups with one tcgen05.commit
   // per group.  One stage per group: a commit completes ~1000 cycles after it
   // is issued, and releasing stages one by one keeps more of the ring in
@@ -83,7 +84,7 @@ struct Cfg {
   // accumulator buffers: two (the epilogue of one tile overlaps the next
   // tile's MMAs), except for 256-wide tiles, whose one accumulator already
   // takes half of tensor memory
-  static constexpr int kAccBufs = BN == 256 ? 1 : 2;
+  static constexpr int kAccBufs = (BN == 256 || (MT == 2 && BN == 64)) ? 1 : 2;
   static constexpr int kAccCols = BN;                  // one accumulator
   // Epilogue warp groups: 256-wide tiles hold their single accumulator until
   // the epilogue has read it, so a second group of four warps (warps 7-10)
@@ -609,27 +610,37 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
               r[i] = __float_as_uint(__fadd_rn(__uint_as_float(r[i]), __uint_as_float(r2[i])));
           }
         };
-        uint32_t rg[32], ru[32];
-        load_acc(tq, rg);
-        load_acc(tq + C::kIssuers * C::kAccCols, ru);
+        // every 32-token chunk of the tile (all of it in registers before the
+        // accumulators go back to the MMA warps)
+        uint32_t rg[BN / 32][32], ru[BN / 32][32];
+#pragma unroll
+        for (int ci = 0; ci < BN / 32; ++ci) {
+          if (ci * 32 < n_valid) {
+            load_acc(tq + ci * 32, rg[ci]);
+            load_acc(tq + C::kIssuers * C::kAccCols + ci * 32, ru[ci]);
+          }
+        }
         tc_fence_before();
         mbar_arrive(acce_bar(abuf));               // both accumulators are in registers
         if (++abuf == C::kAccBufs) { abuf = 0; aphase ^= 1u; }
-        warp_transpose32(rg, lane);                // lane = token, 32 features of quarter q
-        warp_transpose32(ru, lane);
-        if (lane < n_valid) {
+#pragma unroll
+        for (int ci = 0; ci < BN / 32; ++ci) {
+        if (ci * 32 >= n_valid) continue;
+        warp_transpose32(rg[ci], lane);            // lane = token, 32 features of quarter q
+        warp_transpose32(ru[ci], lane);
+        if (ci * 32 + lane < n_valid) {
           const float gh = *a.g_h;
           float h[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const float gz = __fmul_rn(__uint_as_float(rg[i]), alpha);
-            const float uz = __fmul_rn(__uint_as_float(ru[i]), alpha);
+            const float gz = __fmul_rn(__uint_as_float(rg[ci][i]), alpha);
+            const float uz = __fmul_rn(__uint_as_float(ru[ci][i]), alpha);
             h[i] = __fmul_rn(__fdiv_rn(gz, __fadd_rn(1.0f, expf(-gz))), uz);
           }
           const Block16 b0 = quantize16(h, gh);
           const Block16 b1 = quantize16(h + 16, gh);
           const int f0 = un.x_local0 + q * 32;     // first feature of h in this lane
-          const int row = lane;                    // token tile = one layout chunk (BN = 32)
+          const int row = ci * 32 + lane;          // token tile = one layout chunk (BN <= 64)
           const int64_t tile = (static_cast<int64_t>(un.y_tile) * a.h_nkb + (f0 >> 8)) *
                                kOperandTileBytes;
           const int chunk = (f0 & 255) >> 5;       // 16-byte chunk of the 128-byte row
@@ -639,6 +650,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
           *reinterpret_cast<uint16_t*>(a.h_tiles + tile + kXTileBytes + (sc >> 2) * 512 +
                                        (row & 31) * 16 + ((row >> 5) & 3) * 4 + (sc & 3)) =
               static_cast<uint16_t>(b0.sf | (b1.sf << 8));
+        }
         }
         continue;
       }
@@ -839,6 +851,7 @@ static cudaError_t set_smem_attr() {
 cudaError_t init_gemm_attributes() {
   cudaError_t e = set_smem_attr<32>();
   if (e == cudaSuccess) e = set_smem_attr<32, 2>();
+  if (e == cudaSuccess) e = set_smem_attr<64, 2>();
   if (e == cudaSuccess) e = set_smem_attr<64>();
   if (e == cudaSuccess) e = set_smem_attr<128>();
   if (e == cudaSuccess) e = set_smem_attr<256>();
@@ -866,8 +879,11 @@ cudaError_t launch_gemm(const CUtensorMap& tmx, const CUtensorMap& tmy, const Ge
     return bn == 256 ? launch_bn<256>(tmx, tmy, a, mode, grid, s)
                      : launch_bn<128>(tmx, tmy, a, mode, grid, s);
   }
-  if (mode == kGroupedSiluMul)      // gate and up tiles pair up in one 32-route unit
-    return launch_bn<32, 2>(tmx, tmy, a, mode, grid, s);
+  // gate and up tiles pair up in one unit of 32 or 64 routes (<64, 2> serves
+  // only this mode: its single accumulator buffer has no other epilogue)
+  if (mode == kGroupedSiluMul)
+    return grouped_tile_width(a.rows_y, a.E) == 32 ? launch_bn<32, 2>(tmx, tmy, a, mode, grid, s)
+                                                   : launch_bn<64, 2>(tmx, tmy, a, mode, grid, s);
   switch (grouped_tile_width(a.rows_y, a.E)) {
     case 32:   // two weight tiles per unit when the expert's rows pair up
       return (a.n_out / 128) % 2 == 0 ? launch_bn<32, 2>(tmx, tmy, a, mode, grid, s)

@@ -179,8 +179,9 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
 
 
-def build_problem(device, seed_base=2):
+def build_problem(device, seed_base=2, tokens=None):
     """Resident NVFP4 weights and one batch of per-step inputs (seeded)."""
+    T = globals()["T"] if tokens is None else tokens
     t0 = time.time()
     w1 = torch.empty((E, N1, K1), dtype=torch.bfloat16, device=device)
     w2 = torch.empty((E, N2, K2), dtype=torch.bfloat16, device=device)
@@ -580,29 +581,31 @@ def run_configs(args):
         torch.cuda.empty_cache()
 
     # decode expert MLP: the fused path (gate_up + SiLU * up + NVFP4 h in one
-    # launch) against the same pass with h quantised by its own kernels
-    W1, W2, w1, w2, host, _ = build_problem(dev)
-    del w1, w2
-    torch.cuda.empty_cache()
-    d = {k: v.to(dev) for k, v in host.items()}
-    layer = moe.DecodeLayer(W1, W2, T, TOPK, dev)
-    gu_out, _ = layer.step(d["x"], d["ids"], d["h"], d["wts"])
-    # calibration of h's global (set-up, outside the timed region): amax of
-    # SiLU(gate) * up over this batch
-    gate, up = gu_out.float().split(N1 // 2, dim=1)
-    g_h = (torch.nn.functional.silu(gate) * up).abs().amax().reshape(1) / 2688.0
-    mlp = moe.FusedMLP(W1, W2, T, TOPK, g_h.to(torch.float32), dev)
-    t_fused = _timed(lambda: mlp.step(d["x"], d["ids"], d["wts"]), iters, flush)
-    t_split = _timed(lambda: layer.step(d["x"], d["ids"], d["h"], d["wts"]), iters, flush)
-    fl = 2.0 * T * TOPK * (N1 * K1 + N2 * K2)
-    lines.append({"workload": "decode_mlp_fused", "pass_ms": round(t_fused, 4),
-                  "tflops": round(fl / t_fused / 1e9, 1),
-                  "unfused_pass_ms": round(t_split, 4),
-                  "note": "route + quantise x + fused gate_up/SiLU/quantise-h + down with combine; "
-                          "unfused = the same pass with a BF16 gate_up output and h quantised by "
-                          "its own kernels (h drawn at random there)"})
-    del layer, mlp, W1, W2
-    torch.cuda.empty_cache()
+    # launch) against the same pass with h quantised by its own kernels, at
+    # 16 and 32 routes per expert (32- and 64-route token tiles)
+    for tokens in (T, 2 * T):
+        W1, W2, w1, w2, host, _ = build_problem(dev, tokens=tokens)
+        del w1, w2
+        torch.cuda.empty_cache()
+        d = {k: v.to(dev) for k, v in host.items()}
+        layer = moe.DecodeLayer(W1, W2, tokens, TOPK, dev)
+        gu_out, _ = layer.step(d["x"], d["ids"], d["h"], d["wts"])
+        # calibration of h's global (set-up, outside the timed region): amax of
+        # SiLU(gate) * up over this batch
+        gate, up = gu_out.float().split(N1 // 2, dim=1)
+        g_h = (torch.nn.functional.silu(gate) * up).abs().amax().reshape(1) / 2688.0
+        mlp = moe.FusedMLP(W1, W2, tokens, TOPK, g_h.to(torch.float32), dev)
+        t_fused = _timed(lambda: mlp.step(d["x"], d["ids"], d["wts"]), iters, flush)
+        t_split = _timed(lambda: layer.step(d["x"], d["ids"], d["h"], d["wts"]), iters, flush)
+        fl = 2.0 * tokens * TOPK * (N1 * K1 + N2 * K2)
+        lines.append({"workload": f"decode_mlp_fused_T{tokens}", "pass_ms": round(t_fused, 4),
+                      "tflops": round(fl / t_fused / 1e9, 1),
+                      "unfused_pass_ms": round(t_split, 4),
+                      "note": "route + quantise x + fused gate_up/SiLU/quantise-h + down with "
+                              "combine; unfused = the same pass with a BF16 gate_up output and h "
+                              "quantised by its own kernels (h drawn at random there)"})
+        del layer, mlp, W1, W2, d, gu_out, gate, up
+        torch.cuda.empty_cache()
     for ln in lines:
         print(json.dumps(ln), flush=True)
 

@@ -74,17 +74,20 @@ struct Cfg {
   static constexpr int kGroup = 1;
   static constexpr int kGroups = kStages / kGroup;
   static_assert(kStages % kGroup == 0, "stage groups");
-  static constexpr int kIssuers = BN <= 64 ? 2 : 1;   // MMA-issuing warps
+  // MMA-issuing warps: two for narrow tiles, except the fused two-tile units
+  // of 64 routes, whose accumulators (gate and up) then fit twice in tensor
+  // memory so the epilogue overlaps the next unit
+  static constexpr int kIssuers = (BN <= 64 && !(MT == 2 && BN == 64)) ? 2 : 1;
   // With one MMA warp, warp 6 becomes a scale warp: it copies the stage's Y
   // scales (and for 128-wide tiles the X scales too) into tensor memory and
   // signals the MMA warp, so the two warps issue tcgen05 instructions in
   // parallel (each warp's issue rate, not the tensor pipe, bounds a stage).
   static constexpr bool kSplit = kIssuers == 1;
-  static constexpr bool kXsfOnScaleWarp = kSplit && BN == 128;
+  static constexpr bool kXsfOnScaleWarp = kSplit && (BN == 128 || MT == 2);
   // accumulator buffers: two (the epilogue of one tile overlaps the next
   // tile's MMAs), except for 256-wide tiles, whose one accumulator already
   // takes half of tensor memory
-  static constexpr int kAccBufs = (BN == 256 || (MT == 2 && BN == 64)) ? 1 : 2;
+  static constexpr int kAccBufs = BN == 256 ? 1 : 2;
   static constexpr int kAccCols = BN;                  // one accumulator
   // Epilogue warp groups: 256-wide tiles hold their single accumulator until
   // the epilogue has read it, so a second group of four warps (warps 7-10)
@@ -448,8 +451,12 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
         const uint32_t tsfx = tmem + C::kSfColBase + stage * C::kSfColsPerStage;
         const uint32_t tsfy = tsfx + 16 * MT;
         for (int ks = 0; ks < ksteps; ++ks) {
-          if (C::kXsfOnScaleWarp)
+          if (C::kXsfOnScaleWarp) {
             tc_cp_sf_atom_elect(tsfx + 4 * ks, sdesc_sf_atom(ssfx + 512 * ks));
+            if (MT == 2)                 // the unit's second X tile
+              tc_cp_sf_atom_elect(tsfx + 16 + 4 * ks,
+                                  sdesc_sf_atom(ssfx + C::kXPartBytes + 512 * ks));
+          }
           tc_cp_sf_atom_elect(tsfy + C::kSfyColsPerStep * ks, sdesc_sf_atom(ssfy + 512 * ks));
           if (C::kSfyAtomsPerStep == 2 && y_rows > 128)
             tc_cp_sf_atom_elect(tsfy + C::kSfyColsPerStep * ks + 4,
@@ -531,8 +538,9 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
           tc_mma_nvf4_elect(d_tmem, dx + 2 * ks, dy + 2 * ks, idesc, tsfx + 4 * ks, tsfy_ks,
                             (kb > 0 || ks >= C::kIssuers) ? 1u : 0u);
           if (MT == 2) {                 // second weight tile, same token operand
-            tc_cp_sf_atom_elect(tsfx + 16 + 4 * ks,
-                                sdesc_sf_atom(ssfx + C::kXPartBytes + 512 * ks));
+            if (!C::kXsfOnScaleWarp)
+              tc_cp_sf_atom_elect(tsfx + 16 + 4 * ks,
+                                  sdesc_sf_atom(ssfx + C::kXPartBytes + 512 * ks));
             tc_mma_nvf4_elect(d_tmem + C::kIssuers * C::kAccCols,
                               sdesc_sw128(sx + C::kXPartBytes) + 2 * ks, dy + 2 * ks, idesc,
                               tsfx + 16 + 4 * ks, tsfy_ks,
@@ -610,31 +618,24 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
               r[i] = __float_as_uint(__fadd_rn(__uint_as_float(r[i]), __uint_as_float(r2[i])));
           }
         };
-        // every 32-token chunk of the tile (all of it in registers before the
-        // accumulators go back to the MMA warps)
-        uint32_t rg[BN / 32][32], ru[BN / 32][32];
-#pragma unroll
+        // one 32-token chunk at a time; the accumulator buffer goes back to
+        // the MMA warps after the last chunk (the other buffer keeps them busy)
+        static_assert(MT != 2 || C::kAccBufs == 2, "fused epilogue: double-buffered accumulator");
+#pragma unroll 1
         for (int ci = 0; ci < BN / 32; ++ci) {
-          if (ci * 32 < n_valid) {
-            load_acc(tq + ci * 32, rg[ci]);
-            load_acc(tq + C::kIssuers * C::kAccCols + ci * 32, ru[ci]);
-          }
-        }
-        tc_fence_before();
-        mbar_arrive(acce_bar(abuf));               // both accumulators are in registers
-        if (++abuf == C::kAccBufs) { abuf = 0; aphase ^= 1u; }
-#pragma unroll
-        for (int ci = 0; ci < BN / 32; ++ci) {
-        if (ci * 32 >= n_valid) continue;
-        warp_transpose32(rg[ci], lane);            // lane = token, 32 features of quarter q
-        warp_transpose32(ru[ci], lane);
+        if (ci * 32 >= n_valid) break;
+        uint32_t rg[32], ru[32];
+        load_acc(tq + ci * 32, rg);
+        load_acc(tq + C::kIssuers * C::kAccCols + ci * 32, ru);
+        warp_transpose32(rg, lane);                // lane = token, 32 features of quarter q
+        warp_transpose32(ru, lane);
         if (ci * 32 + lane < n_valid) {
           const float gh = *a.g_h;
           float h[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const float gz = __fmul_rn(__uint_as_float(rg[ci][i]), alpha);
-            const float uz = __fmul_rn(__uint_as_float(ru[ci][i]), alpha);
+            const float gz = __fmul_rn(__uint_as_float(rg[i]), alpha);
+            const float uz = __fmul_rn(__uint_as_float(ru[i]), alpha);
             h[i] = __fmul_rn(__fdiv_rn(gz, __fadd_rn(1.0f, expf(-gz))), uz);
           }
           const Block16 b0 = quantize16(h, gh);
@@ -652,6 +653,9 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
               static_cast<uint16_t>(b0.sf | (b1.sf << 8));
         }
         }
+        tc_fence_before();
+        mbar_arrive(acce_bar(abuf));               // both accumulators have been read
+        if (++abuf == C::kAccBufs) { abuf = 0; aphase ^= 1u; }
         continue;
       }
       if (C::kAccBufs == 1 && mode != kGroupedCombine && mode != kGroupedSiluMul) {

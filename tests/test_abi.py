@@ -74,10 +74,20 @@ def test_host_validation_without_device():
     assert lib.nvfp4_prepack_weight_tiles(None, None, 4, 64, None, None) == 1
     assert lib.nvfp4_set_timeout_ns(0) == 1
     assert lib.nvfp4_device_status(None, 0, None) == 1
+    assert lib.nvfp4_amax_partials(None, 4, 64, 64, 8, 2, None, None) == 1
+    assert lib.nvfp4_moe_gate_up_silu(*([None] * 5), 4, 8, 2, 256, 128, None, None, None) == 1
+    assert lib.nvfp4_grouped_gemm_combine_noalloc(*([None] * 5), 4, 8, 2, 128, 128,
+                                                  None, None, None, None, None) == 1
     # unsupported shapes are refused before any CUDA call too
     p = ctypes.c_void_p(256)
     assert lib.nvfp4_gemm(p, p, p, p, p, p, p, 16, 16, 48, 16, None) == 2
     assert lib.nvfp4_quantize(p, 4, 24, 24, p, p, p, 0, None) == 2
+    assert lib.nvfp4_amax_partials(p, 4, 48, 48, 8, 2, p, None) == 2            # K % 64
+    # fused MLP: N must split into gate and up halves of whole 128-row tiles
+    assert lib.nvfp4_moe_gate_up_silu(p, p, p, p, p, 4, 8, 2, 384, 128, p, p, None) == 2
+    # conflicting quantiser flags: a given global and amax maxima already present
+    assert lib.nvfp4_quantize_dispatch(p, 4, 64, 64, p, 2, p, 4, 8, p, p,
+                                       F.NVFP4_GLOBAL_GIVEN | F.NVFP4_AMAX_DONE, None) == 1
 
 
 def test_binding_raises_without_cuda_tensors():

@@ -74,17 +74,39 @@ __device__ __forceinline__ Block16 quantize16_with(float amax_b, float g, Get ge
   const float s = (g > 0.0f) ? __fdiv_rn(__fdiv_rn(amax_b, 6.0f), g) : 0.0f;
   const uint32_t sf = e4m3_from_f32(s);
   const float d = __fmul_rn(f32_from_e4m3(sf), g);
-  float q[16];
   uint32_t sgn[2] = {0u, 0u};
+#pragma unroll
+  for (int e = 0; e < 16; ++e) sgn[e >> 3] |= (__float_as_uint(get(e)) >> 31) << (4 * (e & 7) + 3);
+  Block16 b;
+  b.sf = sf;
+  // Fast path: q1 = v * RN(1/d) is within 2^-23 (relative) of v / d, and the
+  // correctly rounded quotient within 2^-24 of that, so both lie between
+  // q1 (1 - 2^-20) and q1 (1 + 2^-20).  The E2M1 conversion is monotone, so
+  // when the two bounds give the same codes those are the codes of the
+  // rounded quotient.  Otherwise (a quotient within ~2^-20 of a rounding
+  // boundary, or 1/d out of range) every code comes from the exact division.
+  const float inv = __frcp_rn(d);
+  if (d != 0.0f && inv < 3.0e38f) {
+    float lo[16], hi[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const float q1 = __fmul_rn(get(e), inv);
+      lo[e] = __fmul_rn(q1, 0.99999904632568359375f);    // 1 - 2^-20
+      hi[e] = __fmul_rn(q1, 1.00000095367431640625f);    // 1 + 2^-20
+    }
+    const uint32_t c0 = e2m1x8_rn_satfinite(lo), c1 = e2m1x8_rn_satfinite(lo + 8);
+    if (c0 == e2m1x8_rn_satfinite(hi) && c1 == e2m1x8_rn_satfinite(hi + 8)) {
+      b.packed = make_uint2(c0 | sgn[0], c1 | sgn[1]);
+      return b;
+    }
+  }
+  float q[16];
 #pragma unroll
   for (int e = 0; e < 16; ++e) {
     const float v = get(e);
     q[e] = (d != 0.0f) ? __fdiv_rn(v, d) : __fmul_rn(v, 0.0f);
-    sgn[e >> 3] |= (__float_as_uint(v) >> 31) << (4 * (e & 7) + 3);
   }
-  Block16 b;
   b.packed = make_uint2(e2m1x8_rn_satfinite(q) | sgn[0], e2m1x8_rn_satfinite(q + 8) | sgn[1]);
-  b.sf = sf;
   return b;
 }
 

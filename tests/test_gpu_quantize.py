@@ -54,32 +54,36 @@ def test_quantize_atom_layout_bit_exact(rows, cols):
     assert np.array_equal(got[mask], ref[mask])
 
 
-def test_quantize_e2m1_rounding_at_unit_step():
-    """With g = 2^-8 and a 6 in every block, s = 256 is an exact E4M3 value and
-    d = 1, so x / d = x: every E2M1 midpoint is hit exactly (ties go to the
-    even code) and so are its BF16 neighbours on both sides, with both signs."""
-    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], np.float32)
+@pytest.mark.parametrize("dstep,amax,scode", [(1.0, 6.0, 0x78), (1.5, 9.0, 0x7C)])
+def test_quantize_e2m1_rounding_at_exact_ties(dstep, amax, scode):
+    """With g = 2^-8 and a block maximum `amax`, s = amax / 6 / g is an exact
+    E4M3 value and d = dstep, so x = midpoint * dstep makes x / d an exact E2M1
+    tie (ties go to the even code); the BF16 neighbours of those x fall just
+    either side.  Both signs.  (d = 1.5 puts the quotients at the ties without
+    d being a power of two, where a shortcut through 1/d must defer to the
+    exact division.)"""
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], np.float32) * np.float32(dstep)
     bits = inputs.to_bf16(mids).view(torch.int16).numpy().astype(np.int32)
     vals = []
-    for b in bits:                                   # the midpoint and its two BF16 neighbours
+    for b in bits:                                   # the tie and its two BF16 neighbours
         for db in (-1, 0, 1):
             vals.append(np.array([b + db], np.int32).astype(np.int16).view(np.uint16)[0])
     v = torch.from_numpy(np.array(vals, np.uint16).view(np.int16)).view(torch.bfloat16).float()
     v = v.numpy()
-    tail = np.array([0.0, -0.0, 6.0, -6.0, 1e-3, -1e-3, 0.1, -0.1], np.float32)
+    tail = np.array([0.0, -0.0, amax, -amax, 1e-3, -1e-3, 0.1, -0.1], np.float32)
     pool = np.concatenate([v, -v, tail])             # 50 values
     rows = []
-    for i in range(0, len(pool), 15):                # 15 values + a 6.0 per block
+    for i in range(0, len(pool), 15):                # 15 values + the block maximum
         blk = np.full(16, 0.0, np.float32)
         chunk = pool[i:i + 15]
         blk[:len(chunk)] = chunk
-        blk[15] = 6.0
+        blk[15] = amax
         rows.append(blk)
-    x = inputs.to_bf16(np.concatenate(rows)[None, :])
+    x = inputs.to_bf16(np.concatenate(rows).reshape(1, -1))
     gg = torch.tensor([2.0 ** -8], dtype=torch.float32, device="cuda")
     packed, scales, _ = F.quantize(x.cuda(), global_scale=gg)
     p_ref, s_ref, _ = oracle.quantize(x.float().numpy(), g=np.float32(2.0 ** -8))
-    assert (s_ref == 0x78).all()                     # s = 256 -> d = 1
+    assert (s_ref == scode).all()                    # d = dstep in every block
     assert np.array_equal(scales.cpu().numpy(), s_ref)
     assert np.array_equal(packed.cpu().numpy(), p_ref)
 

@@ -341,6 +341,73 @@ nvfp4_status nvfp4_grouped_gemm_combine_noalloc(const uint8_t* A_tiles, const fl
                                                 const float* topk_weights, void* out,
                                                 void* stream);
 
+/*
+ * 2:4-sparse NVFP4 weights ("The FP4 Frontier", Finding 6: structured 2:4
+ * sparsity halves the bits of an NVFP4 weight; the experts of an MoE model
+ * can be pruned independently).  The unit of sparsity is the packed byte,
+ * i.e. the pair of E2M1 values at K = 2i, 2i+1: in every aligned group of
+ * four bytes (eight K elements) at most two bytes are non-zero.  Preparing
+ * weights: nvfp4_prune_2of4 on the BF16 weights, nvfp4_quantize of the pruned
+ * tensor (one global per expert, as for dense weights), then
+ * nvfp4_prepack_sparse_weight_tiles; multiply with nvfp4_grouped_gemm_sparse.
+ */
+
+/*
+ * Magnitude pruning of BF16 weights [rows, cols] (row stride ld elements) to
+ * 2:4 over element pairs.  In each group of four pairs, pair i scores
+ * |w[2i]| + |w[2i+1]| (one binary32 addition); the two highest scores stay,
+ * equal scores favouring the lower position; the other two pairs are written
+ * as +0.  out [rows, cols] (row stride ld_out) may be w itself (ld_out == ld).
+ * cols, ld and ld_out % 8 == 0; both buffers 16-byte aligned.
+ */
+nvfp4_status nvfp4_prune_2of4(const void* w, int64_t rows, int64_t cols, int64_t ld, void* out,
+                              int64_t ld_out, void* stream);
+
+/* Bytes of the sparse operand tiles of rows x K weights:
+ * ceil(rows / 128) x ceil(K / 256) tiles of 12288 bytes. */
+size_t nvfp4_sparse_tiles_bytes(int64_t rows, int64_t K);
+
+/*
+ * Packed codes [rows, K/2] (2:4 over bytes) + row-major E4M3 scales
+ * [rows, K/16] -> sparse operand tiles (nvfp4_sparse_tiles_bytes(rows, K)
+ * bytes, caller-owned).  Tile (rt, kb) covers rows 128 rt .. 128 rt + 127 and
+ * K 256 kb .. 256 kb + 255, at byte (rt * ceil(K / 256) + kb) * 12288:
+ *   [0, 8192)       kept bytes: per group the two kept bytes in position
+ *                   order; 64-K slice j of row r at j * 2048 + r * 16;
+ *   [8192, 10240)   combination indices, 4 bits per group, numbering the
+ *                   kept positions (i0 < i1) lexicographically: (0,1) (0,2)
+ *                   (0,3) (1,2) (1,3) (2,3) -> 0..5; a group with fewer than
+ *                   two non-zero bytes keeps the lowest zero positions; the 16
+ *                   groups of 128-K half h of row r at 8192 + h * 1024 + r * 8,
+ *                   group g in byte g / 2, low nibble for even g;
+ *   [10240, 12288)  the scales as four 512-byte atoms, as in the dense tile.
+ * Padding rows and K are zero.  A group with more than two non-zero bytes
+ * sets NVFP4_ERR_DEVICE_CHECK in the device status word (the tile is then
+ * not a faithful copy).  K % 64 == 0; packed and tiles 16-byte aligned,
+ * scales 4-byte aligned.
+ */
+nvfp4_status nvfp4_prepack_sparse_weight_tiles(const uint8_t* packed,
+                                               const uint8_t* scales_rowmajor, int64_t rows,
+                                               int64_t K, uint8_t* tiles, void* stream);
+
+/*
+ * nvfp4_grouped_gemm over 2:4-sparse expert weights: the same operation,
+ * arguments, orientations (route-ordered out or weighted combine), limits
+ * and errors, with W_sparse_tiles = nvfp4_prepack_sparse_weight_tiles over
+ * [E * N, K].  The result equals that of nvfp4_grouped_gemm on the dense
+ * tiles of the same pruned weights: the kernel streams the sparse tiles (two
+ * thirds of the dense bytes) and expands them in shared memory before the
+ * block-scaled MMAs.
+ */
+nvfp4_status nvfp4_grouped_gemm_sparse(const uint8_t* A_tiles, const float* gA,
+                                       const uint8_t* W_sparse_tiles, const float* gW,
+                                       const int32_t* expert_offsets, int32_t E,
+                                       int64_t T, int32_t topk, int64_t N, int64_t K,
+                                       const int32_t* route_token, const int32_t* route_slot,
+                                       const float* topk_weights,
+                                       void* out, float* workspace, size_t workspace_bytes,
+                                       void* stream);
+
 #ifdef __cplusplus
 }  /* extern "C" */
 #endif

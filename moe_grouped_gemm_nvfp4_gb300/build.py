@@ -1,6 +1,6 @@
 """Builds the in-tree CUDA library `_lib/libnvfp4_gb300.so` for sm_103a.
 
-The four translation units compile in parallel with nvcc, then link into
+The translation units compile in parallel with nvcc, then link into
 one shared object with the CUDA runtime linked statically.  A build is
 skipped when the library is newer than every source and header.
 """
@@ -16,8 +16,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(OUT_DIR, "libnvfp4_gb300.so")
-SOURCES = ["api.cu", "quantize.cu", "route.cu", "gemm.cu"]
-HEADERS = [os.path.join(CSRC, h) for h in ("common.cuh", "kernels.h")] + [
+SOURCES = ["api.cu", "quantize.cu", "route.cu", "gemm.cu", "sparse.cu"]
+HEADERS = [os.path.join(CSRC, h) for h in ("common.cuh", "kernels.h", "format.cuh")] + [
     os.path.join(ROOT, "include", "nvfp4.h")]
 
 NVCC_FLAGS = [

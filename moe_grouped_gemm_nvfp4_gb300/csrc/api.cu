@@ -389,14 +389,14 @@ nvfp4_status nvfp4_amax_partials(const void* x, int64_t rows, int64_t K, int64_t
   return NVFP4_OK;
 }
 
-nvfp4_status nvfp4_grouped_gemm(const uint8_t* A_tiles, const float* gA,
-                                const uint8_t* W_tiles, const float* gW,
-                                const int32_t* expert_offsets, int32_t E,
-                                int64_t T, int32_t topk, int64_t N, int64_t K,
-                                const int32_t* route_token, const int32_t* route_slot,
-                                const float* topk_weights,
-                                void* out, float* workspace, size_t workspace_bytes,
-                                void* stream) {
+static nvfp4_status grouped_gemm_impl(const uint8_t* A_tiles, const float* gA,
+                                      const uint8_t* W_tiles, const float* gW,
+                                      const int32_t* expert_offsets, int32_t E,
+                                      int64_t T, int32_t topk, int64_t N, int64_t K,
+                                      const int32_t* route_token, const int32_t* route_slot,
+                                      const float* topk_weights,
+                                      void* out, float* workspace, size_t workspace_bytes,
+                                      bool sparse_w, void* stream) {
   if (!A_tiles || !gA || !W_tiles || !gW || !expert_offsets || !out) return NVFP4_ERR_INVALID_ARG;
   if (E <= 0 || T < 0 || topk <= 0 || N <= 0 || K <= 0) return NVFP4_ERR_INVALID_ARG;
   const bool combine = topk_weights != nullptr;
@@ -441,12 +441,79 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* A_tiles, const float* gA,
   a.status = d->status;
   a.timeout_ns = g_timeout_ns.load();
   a.debug_flags = g_debug_flags.load();
+  a.sparse_w = sparse_w ? 1 : 0;
   if (combine && cudaMemsetAsync(workspace, 0, nvfp4_combine_workspace_bytes(T, N), s) != cudaSuccess)
     return cuda_fail();
   if (nvfp4::launch_gemm(unused, unused, a, combine ? nvfp4::kGroupedCombine : nvfp4::kGrouped,
                          d->sms, s) != cudaSuccess)
     return cuda_fail();
   if (combine && nvfp4::launch_combine_finalize(workspace, T, N, out, d->sms, s) != cudaSuccess)
+    return cuda_fail();
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_grouped_gemm(const uint8_t* A_tiles, const float* gA,
+                                const uint8_t* W_tiles, const float* gW,
+                                const int32_t* expert_offsets, int32_t E,
+                                int64_t T, int32_t topk, int64_t N, int64_t K,
+                                const int32_t* route_token, const int32_t* route_slot,
+                                const float* topk_weights,
+                                void* out, float* workspace, size_t workspace_bytes,
+                                void* stream) {
+  return grouped_gemm_impl(A_tiles, gA, W_tiles, gW, expert_offsets, E, T, topk, N, K,
+                           route_token, route_slot, topk_weights, out, workspace,
+                           workspace_bytes, false, stream);
+}
+
+nvfp4_status nvfp4_grouped_gemm_sparse(const uint8_t* A_tiles, const float* gA,
+                                       const uint8_t* W_sparse_tiles, const float* gW,
+                                       const int32_t* expert_offsets, int32_t E,
+                                       int64_t T, int32_t topk, int64_t N, int64_t K,
+                                       const int32_t* route_token, const int32_t* route_slot,
+                                       const float* topk_weights,
+                                       void* out, float* workspace, size_t workspace_bytes,
+                                       void* stream) {
+  return grouped_gemm_impl(A_tiles, gA, W_sparse_tiles, gW, expert_offsets, E, T, topk, N, K,
+                           route_token, route_slot, topk_weights, out, workspace,
+                           workspace_bytes, true, stream);
+}
+
+size_t nvfp4_sparse_tiles_bytes(int64_t rows, int64_t K) {
+  if (rows < 0 || K < 0) return 0;
+  return static_cast<size_t>((rows + 127) / 128) * static_cast<size_t>((K + 255) / 256) *
+         static_cast<size_t>(nvfp4::kSparseTileBytes);
+}
+
+nvfp4_status nvfp4_prune_2of4(const void* w, int64_t rows, int64_t cols, int64_t ld, void* out,
+                              int64_t ld_out, void* stream) {
+  if (rows < 0 || cols < 0 || ld < cols || ld_out < cols) return NVFP4_ERR_INVALID_ARG;
+  if (rows > 0 && cols > 0 && (!w || !out)) return NVFP4_ERR_INVALID_ARG;
+  if (cols % 8 != 0 || ld % 8 != 0 || ld_out % 8 != 0) return NVFP4_ERR_UNSUPPORTED;
+  if ((w && !aligned16(w)) || (out && !aligned16(out))) return NVFP4_ERR_UNSUPPORTED;
+  DeviceState* d = nullptr;
+  nvfp4_status st = device_state(&d);
+  if (st != NVFP4_OK) return st;
+  if (nvfp4::launch_prune_2of4(static_cast<const uint16_t*>(w), rows, cols, ld,
+                               static_cast<uint16_t*>(out), ld_out, d->sms,
+                               static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return cuda_fail();
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_prepack_sparse_weight_tiles(const uint8_t* packed,
+                                               const uint8_t* scales_rowmajor, int64_t rows,
+                                               int64_t K, uint8_t* tiles, void* stream) {
+  if (rows < 0 || K < 0) return NVFP4_ERR_INVALID_ARG;
+  if (rows > 0 && K > 0 && (!packed || !scales_rowmajor || !tiles)) return NVFP4_ERR_INVALID_ARG;
+  if (K % 64 != 0) return NVFP4_ERR_UNSUPPORTED;
+  if ((packed && !aligned16(packed)) || (tiles && !aligned16(tiles)) ||
+      (scales_rowmajor && (reinterpret_cast<uintptr_t>(scales_rowmajor) & 3u)))
+    return NVFP4_ERR_UNSUPPORTED;
+  DeviceState* d = nullptr;
+  nvfp4_status st = device_state(&d);
+  if (st != NVFP4_OK) return st;
+  if (nvfp4::launch_prepack_sparse_tiles(packed, scales_rowmajor, rows, K, tiles, d->status,
+                                         d->sms, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return cuda_fail();
   return NVFP4_OK;
 }

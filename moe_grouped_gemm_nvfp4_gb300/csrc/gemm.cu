@@ -46,7 +46,7 @@ constexpr int kTmemCols = 512;
 // weight bytes in flight per SM, which is what the decode shapes need: each
 // stage stays occupied for a memory round trip plus the tensor-pipe latency
 // of its scale copies and MMAs.
-template <int BN, int MT = 1>
+template <int BN, int MT = 1, bool SP = false>
 struct Cfg {
   static_assert(BN == 32 || BN == 64 || BN == 128 || BN == 256, "tile width");
   // MT 128-row X tiles per unit (2 only for 32-row token tiles: two MMAs per
@@ -54,19 +54,32 @@ struct Cfg {
   // and the scale copies of Y per weight byte)
   // (64-row tiles with two X tiles serve only the fused SiLU-mul epilogue)
   static_assert(MT == 1 || (MT == 2 && (BN == 32 || BN == 64)), "unit height");
+  // SP: X (the weights) arrives as 2:4-sparse tiles and is expanded in shared
+  // memory by the decompression warps before the MMAs read it
+  static_assert(!SP || (MT == 1 && BN <= 128), "sparse weights: one X tile, token tiles <= 128");
   static constexpr int kYTileBytes = BN * kRowBytes;
   static constexpr int kSfyAtomsPerStep = BN == 256 ? 2 : 1;   // 128-row scale atoms of Y
   // rows of one grouped operand tile / layout chunk: a 256-row token tile
   // spans two consecutive 128-row operand tiles
   static constexpr int kLayoutRows = BN < 128 ? BN : 128;
   static constexpr int kSfyStageBytes = kSfyAtomsPerStep * kSFStageBytes;
-  // stage: [X codes 16 KB][X scales 2 KB][Y codes][Y scales]; the X part has
-  // the operand-tile layout, so a tile K block lands with one copy
-  static constexpr int kXPartBytes = kXTileBytes + kSFStageBytes;   // codes + scales
+  // stage: [X part][Y codes][Y scales]; the X part has the operand-tile
+  // layout (dense: codes 16 KB + scales 2 KB; sparse: kept bytes 8 KB +
+  // combination indices 2 KB + scales 2 KB), so a tile K block lands with
+  // one copy
+  static constexpr int kXPartBytes = SP ? static_cast<int>(kSparseTileBytes)
+                                        : kXTileBytes + kSFStageBytes;
+  static constexpr int kXsfOffset = SP ? kSparseScaleOffset : kXTileBytes;  // X scales in the part
   static constexpr int kYOffset = MT * kXPartBytes;
   static constexpr int kStageBytes = kYOffset + kYTileBytes + kSfyStageBytes;
   static_assert(kYOffset % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle alignment");
-  static constexpr int kStages = MT == 2 ? (BN == 32 ? 5 : 4) : (BN == 32 ? 9 : (BN == 256 ? 4 : 6));
+  static constexpr int kStages = SP ? (BN == 32 ? 7 : (BN == 64 ? 6 : 5))
+                                    : MT == 2 ? (BN == 32 ? 5 : 4)
+                                              : (BN == 32 ? 9 : (BN == 256 ? 4 : 6));
+  // sparse: ring of expanded (dense) X code tiles, written by the
+  // decompression warps, read by the MMAs
+  static constexpr int kDStages = SP ? (BN == 32 ? 4 : 3) : 0;
+  static constexpr int kDecWarps = SP ? 8 : 0;
   // Stages are released to the producer in groups with one tcgen05.commit
   // per group.  One stage per group: a commit completes ~1000 cycles after it
   // is issued, and releasing stages one by one keeps more of the ring in
@@ -93,7 +106,9 @@ struct Cfg {
   // the epilogue has read it, so a second group of four warps (warps 7-10)
   // takes the upper half of its columns and halves that wait.
   static constexpr int kEpiGroups = BN == 256 ? 2 : 1;
-  static constexpr int kThreads = (7 + 4 * (kEpiGroups - 1)) * 32;
+  // decompression warps (sparse) follow the epilogue warps: warps 7-14
+  static constexpr int kDecWarp0 = 7 + 4 * (kEpiGroups - 1);
+  static constexpr int kThreads = (kDecWarp0 + kDecWarps) * 32;
   // accumulator (buffer b, X tile x, issuer j) at column ((b * MT + x) *
   // kIssuers + j) * BN; scale columns follow the accumulators: per stage 16
   // for each X tile, 16 or 32 for Y
@@ -101,11 +116,15 @@ struct Cfg {
   static constexpr int kSfyColsPerStep = 4 * kSfyAtomsPerStep;
   static constexpr int kSfColsPerStage = 16 * MT + 4 * kSfyColsPerStep;
   static_assert(kSfColBase + kStages * kSfColsPerStage <= kTmemCols, "tensor memory budget");
+  static constexpr int kDenseOffset = kStages * kStageBytes;     // expanded X ring (sparse)
   // barriers: full[S], empty[S / G], acc_full[2], acc_empty[2], drain,
-  // scales_ready[S] (split issue only)
-  static constexpr int kBarBytes = 8 * (kStages + kGroups + 5 + (kSplit ? kStages : 0));
+  // scales_ready[S] (split issue only), dense_ready[D] and dense_free[D]
+  // (sparse only)
+  static constexpr int kBarOffset = kDenseOffset + kDStages * kXTileBytes;
+  static constexpr int kBarBytes =
+      8 * (kStages + kGroups + 5 + (kSplit ? kStages : 0) + 2 * kDStages);
   static constexpr int kTableInts = 3 * (kGroupedMaxExperts + 1);
-  static constexpr int kCtlOffset = kStages * kStageBytes + kBarBytes;
+  static constexpr int kCtlOffset = kBarOffset + kBarBytes;
   // ring of per-unit token-row counts published by the producer (see below)
   static constexpr int kUnitRing = 16;
   static_assert(kUnitRing > kStages + 1, "unit ring depth");
@@ -135,7 +154,7 @@ struct Tables {
   int32_t* tb;        // [E+1] scale-tile prefix
 };
 
-template <int BN, int MT>
+template <int BN, int MT, bool SP = false>
 __device__ __forceinline__ Unit get_unit(int u, int mode, const GemmArgs& a, const Tables& t,
                                          int tiles_x, int64_t atoms_per_rowtile) {
   Unit un;
@@ -161,7 +180,8 @@ __device__ __forceinline__ Unit get_unit(int u, int mode, const GemmArgs& a, con
     un.y_row0 = t.off[e] + nt * BN;
     un.y_rows = min(BN, cnt - nt * BN);
     const int64_t n_kb = (a.K + kBK - 1) / kBK;
-    un.sfx_off = static_cast<int64_t>(e * mtiles + mt) * n_kb * kOperandTileBytes;
+    un.sfx_off = static_cast<int64_t>(e * mtiles + mt) * n_kb *
+                 (SP ? kSparseTileBytes : kOperandTileBytes);
     un.y_tile = t.tb[e] + nt * (BN / Cfg<BN, MT>::kLayoutRows);
     un.sfy_off = static_cast<int64_t>(un.y_tile) * n_kb * kOperandTileBytes;
     un.x_reused = cnt > BN;
@@ -201,6 +221,66 @@ __device__ __forceinline__ void warp_transpose32(uint32_t (&r)[32], int lane) {
   }
 }
 
+// ---------------------------------------------------------------- 2:4 sparse
+// A sparse weight group is four packed bytes (eight K elements) of which two
+// are kept; its 4-bit combination index c numbers the kept positions
+// (i0 < i1) in lexicographic order: (0,1) (0,2) (0,3) (1,2) (1,3) (2,3).
+// Expanding a group is one byte permute of the word holding its two kept
+// bytes (in bytes 0 and 1) and a zero word: output byte p takes byte 0 if
+// p == i0, byte 1 if p == i1, else byte 4 (zero).  sp_selector(c) is that
+// 16-bit permute selector; indices 6 and 7 never occur (all-zero selector).
+__host__ __device__ constexpr uint32_t sp_selector(int c) {
+  int i0 = 0, i1 = 1, n = 0;
+  for (int x = 0; x < 4; ++x)
+    for (int y = x + 1; y < 4; ++y) {
+      if (n == c) { i0 = x; i1 = y; }
+      ++n;
+    }
+  if (c >= 6) return 0x4444u;
+  uint32_t sel = 0;
+  for (int p = 0; p < 4; ++p) sel |= (p == i0 ? 0u : (p == i1 ? 1u : 4u)) << (4 * p);
+  return sel;
+}
+// Byte-permute lookup tables: byte b of word (lo, 0) / (lo, 1) is the low
+// selector byte of combination b / 4 + b, likewise (hi, *) the high byte, so
+// one permute turns four combination nibbles into four selector bytes.
+__host__ __device__ constexpr uint32_t sp_table(int hi, int upper) {
+  uint32_t w = 0;
+  for (int b = 0; b < 4; ++b) w |= ((sp_selector(4 * upper + b) >> (8 * hi)) & 0xFFu) << (8 * b);
+  return w;
+}
+
+// Expands K elements 128h .. 128h + 127 of row r of one sparse X tile at
+// `sp` (shared memory, the sparse tile layout: kept bytes of 64-K slice j of
+// row r at j * 2048 + r * 16, combination nibbles of 128-K half h at 8192 +
+// h * 1024 + r * 8) into the dense code tile at `dn` (row r at r * 128,
+// 16-byte chunk c at position c ^ (r % 8)): four 16-byte chunks.
+__device__ __forceinline__ void sp_expand_row_half(const uint8_t* sp, uint8_t* dn, int r, int h) {
+  constexpr uint32_t kLoA = sp_table(0, 0), kLoB = sp_table(0, 1);
+  constexpr uint32_t kHiA = sp_table(1, 0), kHiB = sp_table(1, 1);
+  const uint4 k0 = *reinterpret_cast<const uint4*>(sp + (2 * h) * 2048 + r * 16);
+  const uint4 k1 = *reinterpret_cast<const uint4*>(sp + (2 * h + 1) * 2048 + r * 16);
+  const uint2 m = *reinterpret_cast<const uint2*>(sp + kSparseComboOffset + h * 1024 + r * 8);
+  // word k holds the kept bytes of groups 2k and 2k + 1 of the half
+  const uint32_t w[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {                  // dense chunk 4h + q: groups 4q .. 4q + 3
+    const uint32_t mw = q < 2 ? m.x : m.y;
+    const uint32_t m16 = (q & 1) ? (mw >> 16) : mw;   // the permutes read 16 selector bits
+    const uint32_t lo = __byte_perm(kLoA, kLoB, m16);
+    const uint32_t hi = __byte_perm(kHiA, kHiB, m16);
+    const uint32_t s01 = __byte_perm(lo, hi, 0x5140);  // selectors of groups 4q, 4q + 1
+    const uint32_t s23 = __byte_perm(lo, hi, 0x7362);  // groups 4q + 2, 4q + 3
+    uint4 d;
+    d.x = __byte_perm(w[2 * q], 0u, s01);
+    d.y = __byte_perm(w[2 * q] >> 16, 0u, s01 >> 16);
+    d.z = __byte_perm(w[2 * q + 1], 0u, s23);
+    d.w = __byte_perm(w[2 * q + 1] >> 16, 0u, s23 >> 16);
+    const int c = 4 * h + q;
+    *reinterpret_cast<uint4*>(dn + r * kRowBytes + ((c ^ (r & 7)) << 4)) = d;
+  }
+}
+
 // Four FP32 additions into global memory in one reduction (16-byte aligned).
 __device__ __forceinline__ void red_add_v4(float* dst, float4 v) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
@@ -219,22 +299,26 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, u
   return false;
 }
 
-template <int BN, int MT>
-__global__ void __launch_bounds__(Cfg<BN, MT>::kThreads, 1)
+template <int BN, int MT, bool SP>
+__global__ void __launch_bounds__(Cfg<BN, MT, SP>::kThreads, 1)
 nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmy,
                   const GemmArgs a, int mode) {
-  using C = Cfg<BN, MT>;
+  using C = Cfg<BN, MT, SP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t bar0 = sbase + C::kStages * C::kStageBytes;
+  const uint32_t bar0 = sbase + C::kBarOffset;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int g) { return bar0 + 8u * (C::kStages + g); };   // per stage group
   auto accf_bar = [&](int b) { return bar0 + 8u * (C::kStages + C::kGroups + b); };
   auto acce_bar = [&](int b) { return bar0 + 8u * (C::kStages + C::kGroups + 2 + b); };
   const uint32_t drain_bar = bar0 + 8u * (C::kStages + C::kGroups + 4);
   auto sfr_bar = [&](int s) { return bar0 + 8u * (C::kStages + C::kGroups + 5 + s); };
+  // sparse: an expanded X tile is ready for the MMAs / free for the next expansion
+  constexpr int kDBar0 = C::kStages + C::kGroups + 5 + (C::kSplit ? C::kStages : 0);
+  auto dready_bar = [&](int d) { return bar0 + 8u * (kDBar0 + d); };
+  auto dfree_bar = [&](int d) { return bar0 + 8u * (kDBar0 + C::kDStages + d); };
   CtaCtl* ctl = reinterpret_cast<CtaCtl*>(smem + C::kCtlOffset);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kCtlOffset + 16);
   int32_t* tab = reinterpret_cast<int32_t*>(smem + C::kTablesOffset);
@@ -265,6 +349,10 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
     mbar_init(drain_bar, C::kSplit ? 2 : C::kIssuers);
     if (C::kSplit)
       for (int s = 0; s < C::kStages; ++s) mbar_init(sfr_bar(s), 1);
+    for (int d = 0; d < C::kDStages; ++d) {
+      mbar_init(dready_bar(d), C::kDecWarps);
+      mbar_init(dfree_bar(d), C::kIssuers);
+    }
     ctl->abort = 0;
     ctl->timeout_ns = a.timeout_ns;
     fence_mbar_init();
@@ -342,7 +430,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
     bool alive = true;
     int uidx = 0;
     for (int u = blockIdx.x; u < units && alive; u += gridDim.x, ++uidx) {
-      const Unit un = get_unit<BN, MT>(u, mode, a, t, tiles_x, atoms_per_rowtile);
+      const Unit un = get_unit<BN, MT, SP>(u, mode, a, t, tiles_x, atoms_per_rowtile);
       if (lane == 0) unit_rows[uidx & (C::kUnitRing - 1)] = un.y_rows;
       __syncwarp();
       const uint64_t pol_x = un.x_reused ? pol_again : pol_once;
@@ -376,20 +464,22 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
         const int sfy_groups = (C::kSfyAtomsPerStep == 2 && un.y_rows > 128) ? 2 : 1;
         // grouped 256-row tiles: codes of rows 0-127 and 128+ come from two tiles
         const int ybox_lo = min(ybox, 8), ybox_hi = ybox - ybox_lo;
-        const uint32_t bytes =
-            MT * (kXTileBytes + ksteps * 512) + ybytes + sfy_groups * ksteps * 512;
+        // X part: codes (dense) or kept bytes + combination indices (sparse),
+        // then the scale atoms of the block's K steps
+        const uint32_t xbytes = C::kXsfOffset + ksteps * 512;
+        const uint32_t bytes = MT * xbytes + ybytes + sfy_groups * ksteps * 512;
         mbar_arrive_expect_tx_elect(full_bar(stage), bytes);
         if (grouped) {
           // operand tiles: X codes + scales in one contiguous copy, Y codes
           // (only the unit's rows) and Y scales in two more
-          const uint8_t* xt = a.sfx + un.sfx_off + kb * kOperandTileBytes;
+          const uint8_t* xt = a.sfx + un.sfx_off + kb * (SP ? kSparseTileBytes : kOperandTileBytes);
           const uint8_t* yt = a.sfy + un.sfy_off + kb * kOperandTileBytes;
-          bulk_load_elect(sx, xt, kXTileBytes + ksteps * 512, full_bar(stage), pol_x);
+          bulk_load_elect(sx, xt, xbytes, full_bar(stage), pol_x);
           if (MT == 2)                   // the unit's second weight tile
             bulk_load_elect(sx + C::kXPartBytes,
                             xt + static_cast<int64_t>(un.x_pair) * ((a.K + kBK - 1) / kBK) *
                                      kOperandTileBytes,
-                            kXTileBytes + ksteps * 512, full_bar(stage), pol_x);
+                            xbytes, full_bar(stage), pol_x);
           bulk_load_elect(sy, yt, ybox_lo * 16 * kRowBytes, full_bar(stage), pol_y);
           bulk_load_elect(ssfy, yt + kXTileBytes, ksteps * 512, full_bar(stage), pol_y);
           if (ybox_hi > 0) {               // second operand tile of a 256-row token tile
@@ -446,7 +536,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
         if (kb == 0) y_rows = unit_rows[uidx & (C::kUnitRing - 1)];
         const int ksteps = min(4, static_cast<int>((a.K >> 6) - 4 * kb));
         const uint32_t sx = sbase + stage * C::kStageBytes;
-        const uint32_t ssfx = sx + kXTileBytes;
+        const uint32_t ssfx = sx + C::kXsfOffset;
         const uint32_t ssfy = sx + C::kYOffset + C::kYTileBytes;
         const uint32_t tsfx = tmem + C::kSfColBase + stage * C::kSfColsPerStage;
         const uint32_t tsfy = tsfx + 16 * MT;
@@ -483,6 +573,8 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
     const int j = (warp == 6) ? 1 : 0;
     int stage = 0;
     uint32_t phase = 0;
+    int dstage = 0;                     // sparse: expanded X tile ring
+    uint32_t dphase = 0;
     int abuf = 0;
     uint32_t aphase = 0;
     bool alive = true;
@@ -507,6 +599,13 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
           alive = false;
           break;
         }
+        // sparse: the decompression warps expanded this stage's X tile (they
+        // waited for the stage too; their proxy fence orders their writes
+        // before these MMAs' operand reads)
+        if (SP && !__all_sync(0xFFFFFFFFu, mbar_wait(dready_bar(dstage), dphase, ctl, a.status))) {
+          alive = false;
+          break;
+        }
         if (C::kSplit) tc_fence_after();
         if (kb == 0) {
           y_rows = unit_rows[uidx & (C::kUnitRing - 1)];
@@ -514,12 +613,13 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
         }
         const int ksteps = min(4, static_cast<int>((a.K >> 6) - 4 * kb));
         const uint32_t sx = sbase + stage * C::kStageBytes;
-        const uint32_t ssfx = sx + kXTileBytes;
+        const uint32_t ssfx = sx + C::kXsfOffset;
         const uint32_t sy = sx + C::kYOffset;
         const uint32_t ssfy = sy + C::kYTileBytes;
         const uint32_t tsfx = tmem + C::kSfColBase + stage * C::kSfColsPerStage;
         const uint32_t tsfy = tsfx + 16 * MT;
-        const uint64_t dx = sdesc_sw128(sx);
+        const uint64_t dx =
+            sdesc_sw128(SP ? sbase + C::kDenseOffset + dstage * kXTileBytes : sx);
         const uint64_t dy = sdesc_sw128(sy);
         // Every token tile starts at row 0 of its operand tile, so every
         // scale address handed to the MMA is a multiple of 4 columns (an
@@ -549,6 +649,10 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
         }
         if (stage % C::kGroup == C::kGroup - 1) tc_commit_elect(empty_bar(stage / C::kGroup));
         if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+        if (SP) {                        // the expanded tile is free once these MMAs complete
+          tc_commit_elect(dfree_bar(dstage));
+          if (++dstage == C::kDStages) { dstage = 0; dphase ^= 1u; }
+        }
       }
       if (!alive) break;
       tc_commit_elect(accf_bar(abuf));
@@ -558,7 +662,35 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
     tc_commit_elect(drain_bar);
     if (lane == 0) mbar_wait_drain(drain_bar, 0, ctl->timeout_ns);
     __syncwarp();
-  } else if ((warp >= 2 && warp <= 5) || warp >= 7) {
+  } else if (SP && warp >= C::kDecWarp0) {
+    // ------------------------------------------------------- decompression
+    // Eight warps; thread (row r, half h) expands K elements 128h .. 128h +
+    // 127 of row r of every stage's sparse X tile into the next free tile of
+    // the expanded ring, then the warp hands the tile to the MMA warps.
+    static_assert(!SP || C::kDecWarps == 8, "one thread per row half");
+    const int dt = threadIdx.x - C::kDecWarp0 * 32;
+    const int r = dt & 127, h = dt >> 7;
+    int stage = 0, dstage = 0;
+    uint32_t phase = 0, dphase = 0;
+    bool alive = true;
+    for (int u = blockIdx.x; u < units && alive; u += gridDim.x) {
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(full_bar(stage), phase, ctl, a.status)) ||
+            !__all_sync(0xFFFFFFFFu,
+                        mbar_wait(dfree_bar(dstage), dphase ^ 1u, ctl, a.status))) {
+          alive = false;
+          break;
+        }
+        sp_expand_row_half(smem + stage * C::kStageBytes,
+                           smem + C::kDenseOffset + dstage * kXTileBytes, r, h);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(dready_bar(dstage));
+        if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+        if (++dstage == C::kDStages) { dstage = 0; dphase ^= 1u; }
+      }
+    }
+  } else if ((warp >= 2 && warp <= 5) || (C::kEpiGroups == 2 && warp >= 7)) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                       // tensor-memory lane quarter
     // columns of the accumulator this warp's group reads
@@ -572,7 +704,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
     // accumulators that received at least one K step (issuer j's first is ks = j)
     const int n_acc = (a.K >> 6) < C::kIssuers ? static_cast<int>(a.K >> 6) : C::kIssuers;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
-      const Unit un = get_unit<BN, MT>(u, mode, a, t, tiles_x, atoms_per_rowtile);
+      const Unit un = get_unit<BN, MT, SP>(u, mode, a, t, tiles_x, atoms_per_rowtile);
       // Combine: fetch this lane's tokens and routing weights (one token per
       // lane per 32-column chunk) before waiting, so the dependent L2 round
       // trips overlap the MMAs instead of following them.
@@ -846,10 +978,11 @@ __global__ void __launch_bounds__(256) combine_finalize_kernel(const float* __re
 
 }  // namespace
 
-template <int BN, int MT = 1>
+template <int BN, int MT = 1, bool SP = false>
 static cudaError_t set_smem_attr() {
-  return cudaFuncSetAttribute(nvfp4_gemm_kernel<BN, MT>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN, MT>::kSmemBytes);
+  return cudaFuncSetAttribute(nvfp4_gemm_kernel<BN, MT, SP>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              Cfg<BN, MT, SP>::kSmemBytes);
 }
 
 cudaError_t init_gemm_attributes() {
@@ -859,14 +992,17 @@ cudaError_t init_gemm_attributes() {
   if (e == cudaSuccess) e = set_smem_attr<64>();
   if (e == cudaSuccess) e = set_smem_attr<128>();
   if (e == cudaSuccess) e = set_smem_attr<256>();
+  if (e == cudaSuccess) e = set_smem_attr<32, 1, true>();
+  if (e == cudaSuccess) e = set_smem_attr<64, 1, true>();
+  if (e == cudaSuccess) e = set_smem_attr<128, 1, true>();
   return e;
 }
 
-template <int BN, int MT = 1>
+template <int BN, int MT = 1, bool SP = false>
 static cudaError_t launch_bn(const CUtensorMap& tmx, const CUtensorMap& tmy, const GemmArgs& a,
                              int mode, int grid, cudaStream_t s) {
-  nvfp4_gemm_kernel<BN, MT><<<grid, Cfg<BN, MT>::kThreads, Cfg<BN, MT>::kSmemBytes, s>>>(
-      tmx, tmy, a, mode);
+  nvfp4_gemm_kernel<BN, MT, SP>
+      <<<grid, Cfg<BN, MT, SP>::kThreads, Cfg<BN, MT, SP>::kSmemBytes, s>>>(tmx, tmy, a, mode);
   return cudaGetLastError();
 }
 
@@ -885,6 +1021,15 @@ cudaError_t launch_gemm(const CUtensorMap& tmx, const CUtensorMap& tmy, const Ge
   }
   // gate and up tiles pair up in one unit of 32 or 64 routes (<64, 2> serves
   // only this mode: its single accumulator buffer has no other epilogue)
+  // 2:4-sparse weights (gather or combine): one weight tile per unit, token
+  // tiles of the activation layout's chunk width (128 for prefill shapes)
+  if (a.sparse_w) {
+    switch (grouped_chunk_rows(a.rows_y, a.E)) {
+      case 32: return launch_bn<32, 1, true>(tmx, tmy, a, mode, grid, s);
+      case 64: return launch_bn<64, 1, true>(tmx, tmy, a, mode, grid, s);
+      default: return launch_bn<128, 1, true>(tmx, tmy, a, mode, grid, s);
+    }
+  }
   if (mode == kGroupedSiluMul)
     return grouped_tile_width(a.rows_y, a.E) == 32 ? launch_bn<32, 2>(tmx, tmy, a, mode, grid, s)
                                                    : launch_bn<64, 2>(tmx, tmy, a, mode, grid, s);

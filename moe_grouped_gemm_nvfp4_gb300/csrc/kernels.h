@@ -32,6 +32,13 @@ cudaError_t launch_prepack_tiles(const uint8_t* packed, const uint8_t* sf, int64
 cudaError_t launch_prepack(const uint8_t* src, int64_t rows, int64_t kblk, uint8_t* dst,
                            int sms, cudaStream_t s);
 
+// sparse.cu
+cudaError_t launch_prune_2of4(const uint16_t* w, int64_t rows, int64_t cols, int64_t ld,
+                              uint16_t* out, int64_t ld_out, int sms, cudaStream_t s);
+cudaError_t launch_prepack_sparse_tiles(const uint8_t* packed, const uint8_t* sf, int64_t rows,
+                                        int64_t K, uint8_t* tiles, int* status, int sms,
+                                        cudaStream_t s);
+
 // route.cu
 cudaError_t init_route_attributes();
 cudaError_t launch_route(const int32_t* ids, int64_t T, int topk, int E, int32_t* offsets,
@@ -73,6 +80,7 @@ struct GemmArgs {
   uint8_t* h_tiles;                // SiLU-mul: NVFP4 operand tiles of h (K = n_out / 2)
   const float* g_h;                // SiLU-mul: global scale of h (given)
   int32_t h_nkb;                   // SiLU-mul: 256-element K blocks of h
+  int32_t sparse_w;                // grouped: X operand tiles are 2:4-sparse tiles
 };
 
 // Test hook: the producer of every CTA leaves its first pipeline stage
@@ -102,6 +110,12 @@ inline int grouped_tile_width(int64_t routes, int experts) {
   return want > 256 ? 256 : grouped_chunk_rows(routes, experts);
 }
 constexpr int64_t kOperandTileBytes = 16384 + 2048;   // 128 rows x 256 K: codes + scale atoms
+// 2:4-sparse weight tile, same 128 rows x 256 K: kept bytes (four 64-K slices
+// of 16 bytes per row), 4-bit combination indices (two 128-K halves of 8
+// bytes per row), scale atoms as in the dense tile
+constexpr int64_t kSparseTileBytes = 8192 + 2048 + 2048;
+constexpr int kSparseComboOffset = 8192;
+constexpr int kSparseScaleOffset = 10240;
 
 cudaError_t init_gemm_attributes();
 cudaError_t launch_gemm(const CUtensorMap& tmx, const CUtensorMap& tmy, const GemmArgs& a,

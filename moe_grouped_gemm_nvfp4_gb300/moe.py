@@ -28,6 +28,7 @@ class ExpertWeights:
     E: int
     N: int
     K: int
+    sparse: bool = False      # tiles are 2:4-sparse tiles (nvfp4_grouped_gemm_sparse)
 
 
 def quantize_experts(w: torch.Tensor, stream=None) -> ExpertWeights:
@@ -43,6 +44,27 @@ def quantize_experts(w: torch.Tensor, stream=None) -> ExpertWeights:
     F.nvfp4_prepack_weight_tiles(packed.view(E * N, K // 2), sf_rm.view(E * N, K // 16), tiles,
                                  stream)
     return ExpertWeights(tiles, g, E, N, K)
+
+
+def quantize_experts_sparse(w: torch.Tensor, stream=None, pruned: bool = False) -> ExpertWeights:
+    """BF16 [E, N, K] on the device -> 2:4-sparse NVFP4 tiles ("The FP4
+    Frontier", Finding 6): each expert pruned to 2:4 over element pairs (unless
+    `pruned` says it already is), quantised with its own global, packed as
+    sparse tiles (two thirds of the dense bytes)."""
+    E, N, K = w.shape
+    dev = w.device
+    if not pruned:
+        w = w.contiguous().clone()
+        F.nvfp4_prune_2of4(w.view(E * N, K), w.view(E * N, K), stream)
+    packed = torch.empty((E, N, K // 2), dtype=torch.uint8, device=dev)
+    sf_rm = torch.empty((E, N, K // 16), dtype=torch.uint8, device=dev)
+    g = torch.empty(E, dtype=torch.float32, device=dev)
+    for e in range(E):
+        F.nvfp4_quantize(w[e], packed[e], sf_rm[e], g[e:e + 1], 0, stream)
+    tiles = torch.empty(F.nvfp4_sparse_tiles_bytes(E * N, K), dtype=torch.uint8, device=dev)
+    F.nvfp4_prepack_sparse_weight_tiles(packed.view(E * N, K // 2), sf_rm.view(E * N, K // 16),
+                                        tiles, stream)
+    return ExpertWeights(tiles, g, E, N, K, sparse=True)
 
 
 class GroupedPlan:
@@ -107,7 +129,8 @@ class GroupedPlan:
 
     def gemm(self, topk_weights=None, stream=None):
         w = self.w
-        F.nvfp4_grouped_gemm(self.a_tiles, self.a_g, w.tiles, w.g,
+        fn = F.nvfp4_grouped_gemm_sparse if w.sparse else F.nvfp4_grouped_gemm
+        fn(self.a_tiles, self.a_g, w.tiles, w.g,
                              self.expert_offsets, w.E, self.T, self.topk, w.N, w.K,
                              self.route_token, self.route_slot,
                              topk_weights if self.mode == "combine" else None,

@@ -61,6 +61,11 @@ _SIGS = {
     "nvfp4_moe_gate_up_silu": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I64, _I32, _I64, _I64,
                                               _P, _P, _P]),
     "nvfp4_noalloc_workspace_floats": (_SZ, []),
+    "nvfp4_prune_2of4": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I64, _P]),
+    "nvfp4_sparse_tiles_bytes": (_SZ, [_I64, _I64]),
+    "nvfp4_prepack_sparse_weight_tiles": (ctypes.c_int, [_P, _P, _I64, _I64, _P, _P]),
+    "nvfp4_grouped_gemm_sparse": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I64, _I32, _I64,
+                                                 _I64, _P, _P, _P, _P, _P, _SZ, _P]),
     "nvfp4_grouped_gemm_combine_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I64, _I32,
                                                           _I64, _I64, _P, _P, _P, _P, _P]),
 }
@@ -239,6 +244,33 @@ def nvfp4_grouped_gemm(A_tiles, gA, W_tiles, gW, expert_offsets, E: int, T: int,
     _check("nvfp4_grouped_gemm", load().nvfp4_grouped_gemm(
         _ptr(A_tiles), _ptr(gA), _ptr(W_tiles), _ptr(gW), _ptr(expert_offsets), E, T, topk, N,
         K, _ptr(route_token), _ptr(route_slot), _ptr(topk_weights), _ptr(out),
+        _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def nvfp4_prune_2of4(w, out, stream=None) -> None:
+    """2:4 magnitude pruning over element pairs of BF16 [rows, cols]; out may be w."""
+    rows, cols = w.shape
+    _check("nvfp4_prune_2of4", load().nvfp4_prune_2of4(
+        _ptr(w), rows, cols, _row_stride(w), _ptr(out), _row_stride(out), _stream(stream)))
+
+
+def nvfp4_sparse_tiles_bytes(rows: int, K: int) -> int:
+    return load().nvfp4_sparse_tiles_bytes(rows, K)
+
+
+def nvfp4_prepack_sparse_weight_tiles(packed, scales_rowmajor, tiles, stream=None) -> None:
+    rows, half = packed.shape
+    _check("nvfp4_prepack_sparse_weight_tiles", load().nvfp4_prepack_sparse_weight_tiles(
+        _ptr(packed), _ptr(scales_rowmajor), rows, 2 * half, _ptr(tiles), _stream(stream)))
+
+
+def nvfp4_grouped_gemm_sparse(A_tiles, gA, W_sparse_tiles, gW, expert_offsets, E: int, T: int,
+                              topk: int, N: int, K: int, route_token, route_slot, topk_weights,
+                              out, workspace, stream=None) -> None:
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("nvfp4_grouped_gemm_sparse", load().nvfp4_grouped_gemm_sparse(
+        _ptr(A_tiles), _ptr(gA), _ptr(W_sparse_tiles), _ptr(gW), _ptr(expert_offsets), E, T,
+        topk, N, K, _ptr(route_token), _ptr(route_slot), _ptr(topk_weights), _ptr(out),
         _ptr(workspace), ws_bytes, _stream(stream)))
 
 

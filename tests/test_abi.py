@@ -60,6 +60,11 @@ def test_pure_host_helpers():
     assert F.nvfp4_grouped_tiles_bytes(2048, 128, 6144) == \
         (2048 + 31 * 128) // 32 * 24 * 18432 + 16384
     assert F.nvfp4_grouped_tiles_bytes(1, 128, 64) == 18432 + 16384
+    # 2:4-sparse tiles: 12288 bytes per 128 rows x 256 K, two thirds of a dense tile
+    assert F.nvfp4_sparse_tiles_bytes(300, 512) == 3 * 2 * 12288
+    assert F.nvfp4_sparse_tiles_bytes(128 * 4096, 6144) * 3 == \
+        F.nvfp4_operand_tiles_bytes(128 * 4096, 6144) * 2
+    assert F.nvfp4_sparse_tiles_bytes(-1, 64) == 0
 
 
 def test_host_validation_without_device():
@@ -78,11 +83,20 @@ def test_host_validation_without_device():
     assert lib.nvfp4_moe_gate_up_silu(*([None] * 5), 4, 8, 2, 256, 128, None, None, None) == 1
     assert lib.nvfp4_grouped_gemm_combine_noalloc(*([None] * 5), 4, 8, 2, 128, 128,
                                                   None, None, None, None, None) == 1
+    assert lib.nvfp4_grouped_gemm_sparse(*([None] * 5), 8, 4, 2, 128, 128, None, None, None,
+                                         None, None, 0, None) == 1
+    assert lib.nvfp4_prune_2of4(None, 4, 16, 16, None, 16, None) == 1
+    assert lib.nvfp4_prune_2of4(None, 4, 16, 8, None, 16, None) == 1           # ld < cols
+    assert lib.nvfp4_prepack_sparse_weight_tiles(None, None, 4, 64, None, None) == 1
     # unsupported shapes are refused before any CUDA call too
     p = ctypes.c_void_p(256)
     assert lib.nvfp4_gemm(p, p, p, p, p, p, p, 16, 16, 48, 16, None) == 2
     assert lib.nvfp4_quantize(p, 4, 24, 24, p, p, p, 0, None) == 2
     assert lib.nvfp4_amax_partials(p, 4, 48, 48, 8, 2, p, None) == 2            # K % 64
+    assert lib.nvfp4_prune_2of4(p, 4, 12, 12, p, 12, None) == 2                 # cols % 8
+    assert lib.nvfp4_prepack_sparse_weight_tiles(p, p, 4, 96, p, None) == 2     # K % 64
+    assert lib.nvfp4_grouped_gemm_sparse(p, p, p, p, p, 4, 8, 2, 200, 128, p, p, None, p,
+                                         None, 0, None) == 2                     # N % 128
     # fused MLP: N must split into gate and up halves of whole 128-row tiles
     assert lib.nvfp4_moe_gate_up_silu(p, p, p, p, p, 4, 8, 2, 384, 128, p, p, None) == 2
     # conflicting quantiser flags: a given global and amax maxima already present

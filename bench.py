@@ -77,6 +77,16 @@ def gemm_bytes(K, N, n_active, R, out_rows):
     return w + a + o
 
 
+def sparse_gemm_bytes(K, N, n_active, R, out_rows):
+    """gemm_bytes with 2:4-sparse weights: per weight element 0.25 B of kept
+    codes, 0.0625 B of combination indices (4 bits per 8 elements) and the
+    0.0625 B of scales."""
+    w = n_active * N * K * (0.25 + 0.0625 + 0.0625)
+    a = R * K * (0.5 + 1.0 / 16)
+    o = out_rows * N * 2.0
+    return w + a + o
+
+
 def step_bytes(n_active):
     """Algorithmic HBM bytes of a step: weights of the active experts, BF16
     activations in (x, h) and BF16 outputs (gate_up, down) once each."""
@@ -545,6 +555,8 @@ def run_configs(args):
         for e in range(cfg.E):
             w[e] = inputs.device_normal_bf16((cfg.N, cfg.K), 0.02, cfg.seed * 100003 + e, dev)
         W = moe.quantize_experts(w)
+        # the same weights pruned to 2:4 over element pairs (decode shapes)
+        W_sp = moe.quantize_experts_sparse(w) if name != "prefill_skewed" else None
         del w
         if cfg.kind == "down":
             ids = inputs.uniform_topk(g, cfg.T, cfg.E, cfg.topk)
@@ -577,7 +589,22 @@ def run_configs(args):
                       "frac_of_fp4_peak": round(fl / t_gemm / 1e9 / fp4_peak, 4),
                       "pass_ms_route_quantize_gemm": round(t_all, 4),
                       "peak_source": f"{peak_kind} hbm_gbs; fp4 = bf16_tflops x 6"})
-        del W, plan
+        if W_sp is not None:
+            sp_plan = moe.GroupedPlan(W_sp, cfg.T, cfg.topk, plan.mode, dev, routing_from=plan)
+            sp_plan.a_tiles.copy_(plan.a_tiles)
+            sp_plan.a_g.copy_(plan.a_g)
+            t_sp = _timed(lambda: sp_plan.gemm(wts), iters, flush)
+            byt_sp = sparse_gemm_bytes(cfg.K, cfg.N, n_act, R, cfg.T if cfg.kind == "down" else R)
+            lines.append({"workload": name + "_sparse24", "gemm_ms": round(t_sp, 4),
+                          "dense_equiv_tflops": round(fl / t_sp / 1e9, 1),
+                          "gbs": round(byt_sp / t_sp / 1e6, 1),
+                          "frac_of_hbm_roofline": round(byt_sp / t_sp / 1e6 / peak, 4),
+                          "speedup_vs_dense": round(t_gemm / t_sp, 3),
+                          "note": "weights pruned to 2:4 over element pairs, streamed as sparse "
+                                  "tiles (2/3 of the dense bytes), expanded in shared memory; "
+                                  "dense_equiv_tflops counts the dense GEMM's FLOPs"})
+            del sp_plan
+        del W, W_sp, plan
         torch.cuda.empty_cache()
 
     # decode expert MLP: the fused path (gate_up + SiLU * up + NVFP4 h in one

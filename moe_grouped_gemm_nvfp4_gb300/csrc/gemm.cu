@@ -56,7 +56,8 @@ struct Cfg {
   static_assert(MT == 1 || (MT == 2 && (BN == 32 || BN == 64)), "unit height");
   // SP: X (the weights) arrives as 2:4-sparse tiles and is expanded in shared
   // memory by the decompression warps before the MMAs read it
-  static_assert(!SP || (MT == 1 && BN <= 128), "sparse weights: one X tile, token tiles <= 128");
+  static_assert(!SP || (BN <= 128 && (MT == 1 || BN == 32)),
+                "sparse weights: token tiles <= 128, two X tiles only for 32-route tiles");
   static constexpr int kYTileBytes = BN * kRowBytes;
   static constexpr int kSfyAtomsPerStep = BN == 256 ? 2 : 1;   // 128-row scale atoms of Y
   // rows of one grouped operand tile / layout chunk: a 256-row token tile
@@ -73,12 +74,16 @@ struct Cfg {
   static constexpr int kYOffset = MT * kXPartBytes;
   static constexpr int kStageBytes = kYOffset + kYTileBytes + kSfyStageBytes;
   static_assert(kYOffset % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle alignment");
-  static constexpr int kStages = SP ? (BN == 32 ? 7 : (BN == 64 ? 6 : 5))
+  static constexpr int kStages = SP ? (MT == 2 ? 4 : (BN == 32 ? 7 : (BN == 64 ? 6 : 5)))
                                     : MT == 2 ? (BN == 32 ? 5 : 4)
                                               : (BN == 32 ? 9 : (BN == 256 ? 4 : 6));
   // sparse: ring of expanded (dense) X code tiles, written by the
-  // decompression warps, read by the MMAs
-  static constexpr int kDStages = SP ? (BN == 32 ? 4 : 3) : 0;
+  // decompression warps, read by the MMAs.  A slot stays taken from its
+  // expansion until the MMAs reading it complete (~4000 cycles at decode
+  // rates, half of it the commit latency).  (Six slots for the one-tile
+  // units of 64 and 128 routes, at the cost of compressed stages, measured
+  // slightly slower than three.)
+  static constexpr int kDStages = SP ? (BN == 32 && MT == 1 ? 4 : 3) : 0;   // slots of MT tiles
   static constexpr int kDecWarps = SP ? 8 : 0;
   // Stages are released to the producer in groups with one tcgen05.commit
   // per group.  One stage per group: a commit completes ~1000 cycles after it
@@ -96,7 +101,12 @@ struct Cfg {
   // signals the MMA warp, so the two warps issue tcgen05 instructions in
   // parallel (each warp's issue rate, not the tensor pipe, bounds a stage).
   static constexpr bool kSplit = kIssuers == 1;
-  static constexpr bool kXsfOnScaleWarp = kSplit && (BN == 128 || MT == 2);
+  // Sparse two-tile units: the two MMA warps issue only MMAs and commits; a
+  // scale warp of its own (after the decompression warps) copies all of the
+  // stage's scale atoms.
+  static constexpr bool kSpScaleWarp = SP && MT == 2;
+  static constexpr bool kScaleWarp = kSplit || kSpScaleWarp;
+  static constexpr bool kXsfOnScaleWarp = kScaleWarp && (BN == 128 || MT == 2);
   // accumulator buffers: two (the epilogue of one tile overlaps the next
   // tile's MMAs), except for 256-wide tiles, whose one accumulator already
   // takes half of tensor memory
@@ -108,7 +118,8 @@ struct Cfg {
   static constexpr int kEpiGroups = BN == 256 ? 2 : 1;
   // decompression warps (sparse) follow the epilogue warps: warps 7-14
   static constexpr int kDecWarp0 = 7 + 4 * (kEpiGroups - 1);
-  static constexpr int kThreads = (kDecWarp0 + kDecWarps) * 32;
+  static constexpr int kScaleWarpId = kSplit ? 6 : kDecWarp0 + kDecWarps;
+  static constexpr int kThreads = (kDecWarp0 + kDecWarps + (kSpScaleWarp ? 1 : 0)) * 32;
   // accumulator (buffer b, X tile x, issuer j) at column ((b * MT + x) *
   // kIssuers + j) * BN; scale columns follow the accumulators: per stage 16
   // for each X tile, 16 or 32 for Y
@@ -120,9 +131,9 @@ struct Cfg {
   // barriers: full[S], empty[S / G], acc_full[2], acc_empty[2], drain,
   // scales_ready[S] (split issue only), dense_ready[D] and dense_free[D]
   // (sparse only)
-  static constexpr int kBarOffset = kDenseOffset + kDStages * kXTileBytes;
+  static constexpr int kBarOffset = kDenseOffset + kDStages * MT * kXTileBytes;
   static constexpr int kBarBytes =
-      8 * (kStages + kGroups + 5 + (kSplit ? kStages : 0) + 2 * kDStages);
+      8 * (kStages + kGroups + 5 + (kScaleWarp ? kStages : 0) + 2 * kDStages);
   static constexpr int kTableInts = 3 * (kGroupedMaxExperts + 1);
   static constexpr int kCtlOffset = kBarOffset + kBarBytes;
   // ring of per-unit token-row counts published by the producer (see below)
@@ -316,7 +327,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
   const uint32_t drain_bar = bar0 + 8u * (C::kStages + C::kGroups + 4);
   auto sfr_bar = [&](int s) { return bar0 + 8u * (C::kStages + C::kGroups + 5 + s); };
   // sparse: an expanded X tile is ready for the MMAs / free for the next expansion
-  constexpr int kDBar0 = C::kStages + C::kGroups + 5 + (C::kSplit ? C::kStages : 0);
+  constexpr int kDBar0 = C::kStages + C::kGroups + 5 + (C::kScaleWarp ? C::kStages : 0);
   auto dready_bar = [&](int d) { return bar0 + 8u * (kDBar0 + d); };
   auto dfree_bar = [&](int d) { return bar0 + 8u * (kDBar0 + C::kDStages + d); };
   CtaCtl* ctl = reinterpret_cast<CtaCtl*>(smem + C::kCtlOffset);
@@ -346,13 +357,14 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
       mbar_init(accf_bar(b), C::kIssuers);
       mbar_init(acce_bar(b), 128 * C::kEpiGroups);
     }
-    mbar_init(drain_bar, C::kSplit ? 2 : C::kIssuers);
-    if (C::kSplit)
+    mbar_init(drain_bar, C::kIssuers + (C::kScaleWarp ? 1 : 0));
+    if (C::kScaleWarp)
       for (int s = 0; s < C::kStages; ++s) mbar_init(sfr_bar(s), 1);
     for (int d = 0; d < C::kDStages; ++d) {
       mbar_init(dready_bar(d), C::kDecWarps);
       mbar_init(dfree_bar(d), C::kIssuers);
     }
+
     ctl->abort = 0;
     ctl->timeout_ns = a.timeout_ns;
     fence_mbar_init();
@@ -478,7 +490,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
           if (MT == 2)                   // the unit's second weight tile
             bulk_load_elect(sx + C::kXPartBytes,
                             xt + static_cast<int64_t>(un.x_pair) * ((a.K + kBK - 1) / kBK) *
-                                     kOperandTileBytes,
+                                     (SP ? kSparseTileBytes : kOperandTileBytes),
                             xbytes, full_bar(stage), pol_x);
           bulk_load_elect(sy, yt, ybox_lo * 16 * kRowBytes, full_bar(stage), pol_y);
           bulk_load_elect(ssfy, yt + kXTileBytes, ksteps * 512, full_bar(stage), pol_y);
@@ -515,7 +527,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
                         static_cast<uint32_t>((n / C::kStages) & 1), ctl->timeout_ns);
     }
     __syncwarp();
-  } else if (C::kSplit && warp == 6) {
+  } else if (C::kScaleWarp && warp == C::kScaleWarpId) {
     // ---------------------------------------------------------- scale warp
     // Copies each stage's Y scale atoms (and X's for 128-wide tiles) into the
     // stage's tensor-memory columns once the stage has landed, then arrives
@@ -594,7 +606,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
         // split issue: the scales-ready barrier completes after the stage
         // landed (the scale warp waited for it) and its scale copies were
         // issued; the fence orders these MMAs after those copies
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(C::kSplit ? sfr_bar(stage) : full_bar(stage),
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(C::kScaleWarp ? sfr_bar(stage) : full_bar(stage),
                                                phase, ctl, a.status))) {
           alive = false;
           break;
@@ -606,7 +618,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
           alive = false;
           break;
         }
-        if (C::kSplit) tc_fence_after();
+        if (C::kScaleWarp) tc_fence_after();
         if (kb == 0) {
           y_rows = unit_rows[uidx & (C::kUnitRing - 1)];
           idesc = idesc_nvf4(static_cast<uint32_t>((y_rows + 15) & ~15));
@@ -618,8 +630,10 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
         const uint32_t ssfy = sy + C::kYTileBytes;
         const uint32_t tsfx = tmem + C::kSfColBase + stage * C::kSfColsPerStage;
         const uint32_t tsfy = tsfx + 16 * MT;
-        const uint64_t dx =
-            sdesc_sw128(SP ? sbase + C::kDenseOffset + dstage * kXTileBytes : sx);
+        // X tile x: the stage's dense X part, or slot x of the expanded ring
+        const uint32_t sx_tile0 = SP ? sbase + C::kDenseOffset + dstage * MT * kXTileBytes : sx;
+        const uint32_t x_tile_step = SP ? kXTileBytes : C::kXPartBytes;
+        const uint64_t dx = sdesc_sw128(sx_tile0);
         const uint64_t dy = sdesc_sw128(sy);
         // Every token tile starts at row 0 of its operand tile, so every
         // scale address handed to the MMA is a multiple of 4 columns (an
@@ -628,7 +642,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
           const uint32_t tsfy_ks = tsfy + C::kSfyColsPerStep * ks;
           if (!C::kXsfOnScaleWarp)
             tc_cp_sf_atom_elect(tsfx + 4 * ks, sdesc_sf_atom(ssfx + 512 * ks));
-          if (!C::kSplit) {
+          if (!C::kScaleWarp) {
             tc_cp_sf_atom_elect(tsfy_ks, sdesc_sf_atom(ssfy + 512 * ks));
             // rows 128-255 of a 256-wide Y tile: the next 4 columns (the MMA
             // reads the scales of row n from column base + n / 32)
@@ -642,7 +656,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
               tc_cp_sf_atom_elect(tsfx + 16 + 4 * ks,
                                   sdesc_sf_atom(ssfx + C::kXPartBytes + 512 * ks));
             tc_mma_nvf4_elect(d_tmem + C::kIssuers * C::kAccCols,
-                              sdesc_sw128(sx + C::kXPartBytes) + 2 * ks, dy + 2 * ks, idesc,
+                              sdesc_sw128(sx_tile0 + x_tile_step) + 2 * ks, dy + 2 * ks, idesc,
                               tsfx + 16 + 4 * ks, tsfy_ks,
                               (kb > 0 || ks >= C::kIssuers) ? 1u : 0u);
           }
@@ -665,8 +679,11 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
   } else if (SP && warp >= C::kDecWarp0) {
     // ------------------------------------------------------- decompression
     // Eight warps; thread (row r, half h) expands K elements 128h .. 128h +
-    // 127 of row r of every stage's sparse X tile into the next free tile of
-    // the expanded ring, then the warp hands the tile to the MMA warps.
+    // 127 of row r of each of the stage's MT sparse X tiles into the next
+    // free slot of the expanded ring, then the warp hands the slot to the MMA
+    // warps.  (Spreading the stage's scale copies over these warps instead
+    // was measured slower: tcgen05 work issued from ten warps backed up the
+    // tensor pipe.)
     static_assert(!SP || C::kDecWarps == 8, "one thread per row half");
     const int dt = threadIdx.x - C::kDecWarp0 * 32;
     const int r = dt & 127, h = dt >> 7;
@@ -681,8 +698,10 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
           alive = false;
           break;
         }
-        sp_expand_row_half(smem + stage * C::kStageBytes,
-                           smem + C::kDenseOffset + dstage * kXTileBytes, r, h);
+#pragma unroll
+        for (int x = 0; x < MT; ++x)
+          sp_expand_row_half(smem + stage * C::kStageBytes + x * C::kXPartBytes,
+                             smem + C::kDenseOffset + (dstage * MT + x) * kXTileBytes, r, h);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(dready_bar(dstage));
@@ -730,7 +749,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
       tc_fence_after();
       const float alpha = __fmul_rn(grouped ? a.gx[un.e] : a.gx[0], gy);
       const int n_valid = un.y_rows;
-      if (MT == 2 && mode == kGroupedSiluMul) {
+      if (!SP && MT == 2 && mode == kGroupedSiluMul) {   // (sparse weights: not fused)
         // Gate (X tile 0) and up (X tile 1) accumulators of the same 128
         // features: h = SiLU(alpha * gate) * (alpha * up) in FP32, quantised
         // per 16 features with the given global of h and written as NVFP4
@@ -993,6 +1012,7 @@ cudaError_t init_gemm_attributes() {
   if (e == cudaSuccess) e = set_smem_attr<128>();
   if (e == cudaSuccess) e = set_smem_attr<256>();
   if (e == cudaSuccess) e = set_smem_attr<32, 1, true>();
+  if (e == cudaSuccess) e = set_smem_attr<32, 2, true>();
   if (e == cudaSuccess) e = set_smem_attr<64, 1, true>();
   if (e == cudaSuccess) e = set_smem_attr<128, 1, true>();
   return e;
@@ -1021,11 +1041,13 @@ cudaError_t launch_gemm(const CUtensorMap& tmx, const CUtensorMap& tmy, const Ge
   }
   // gate and up tiles pair up in one unit of 32 or 64 routes (<64, 2> serves
   // only this mode: its single accumulator buffer has no other epilogue)
-  // 2:4-sparse weights (gather or combine): one weight tile per unit, token
-  // tiles of the activation layout's chunk width (128 for prefill shapes)
+  // 2:4-sparse weights (gather or combine): token tiles of the activation
+  // layout's chunk width (128 for prefill shapes)
   if (a.sparse_w) {
     switch (grouped_chunk_rows(a.rows_y, a.E)) {
-      case 32: return launch_bn<32, 1, true>(tmx, tmy, a, mode, grid, s);
+      case 32:   // two weight tiles per unit when the expert's rows pair up
+        return (a.n_out / 128) % 2 == 0 ? launch_bn<32, 2, true>(tmx, tmy, a, mode, grid, s)
+                                         : launch_bn<32, 1, true>(tmx, tmy, a, mode, grid, s);
       case 64: return launch_bn<64, 1, true>(tmx, tmy, a, mode, grid, s);
       default: return launch_bn<128, 1, true>(tmx, tmy, a, mode, grid, s);
     }

@@ -87,11 +87,11 @@ def sparse_gemm_bytes(K, N, n_active, R, out_rows):
     return w + a + o
 
 
-def step_bytes(n_active):
+def step_bytes(n_active, sparse=False):
     """Algorithmic HBM bytes of a step: weights of the active experts, BF16
     activations in (x, h) and BF16 outputs (gate_up, down) once each."""
     R = T * TOPK
-    w = n_active * (N1 * K1 + N2 * K2) * (0.5 + 1.0 / 16)
+    w = n_active * (N1 * K1 + N2 * K2) * ((0.375 if sparse else 0.5 + 1.0 / 16))
     io = 2.0 * (T * K1 + R * K2 + R * N1 + T * N2)
     return w + io
 
@@ -189,8 +189,9 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
 
 
-def build_problem(device, seed_base=2, tokens=None):
-    """Resident NVFP4 weights and one batch of per-step inputs (seeded)."""
+def build_problem(device, seed_base=2, tokens=None, sparse=False):
+    """Resident NVFP4 weights and one batch of per-step inputs (seeded);
+    sparse: the same weights pruned to 2:4 and held as sparse tiles."""
     T = globals()["T"] if tokens is None else tokens
     t0 = time.time()
     w1 = torch.empty((E, N1, K1), dtype=torch.bfloat16, device=device)
@@ -198,8 +199,9 @@ def build_problem(device, seed_base=2, tokens=None):
     for e in range(E):
         w1[e] = inputs.device_normal_bf16((N1, K1), 0.02, seed_base * 100003 + e, device)
         w2[e] = inputs.device_normal_bf16((N2, K2), 0.02, (seed_base + 1) * 100003 + e, device)
-    W1 = moe.quantize_experts(w1)
-    W2 = moe.quantize_experts(w2)
+    prep = moe.quantize_experts_sparse if sparse else moe.quantize_experts
+    W1 = prep(w1)
+    W2 = prep(w2)
     g = inputs.rng(seed_base)
     x = inputs.normal_bf16(g, (T, K1))
     ids = inputs.uniform_topk(g, T, E, TOPK)
@@ -214,7 +216,7 @@ def build_problem(device, seed_base=2, tokens=None):
 def run_ours(args, rank, world, local_rank):
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
-    W1, W2, w1, w2, host, setup_s = build_problem(device)
+    W1, W2, w1, w2, host, setup_s = build_problem(device, sparse=args.sparse)
     ids_np = host["ids"].numpy()
     n_active = int(np.count_nonzero(np.bincount(ids_np.reshape(-1), minlength=E)))
     del w1, w2
@@ -360,17 +362,20 @@ def run_ours(args, rank, world, local_rank):
     e2e_value = aggregate_tflops(fl, args.steps, e2e_ms, world)
     peak, peak_kind = measured_peaks()
     R = T * TOPK
-    gu_bytes = gemm_bytes(K1, N1, n_active, R, R)
-    dn_bytes = gemm_bytes(K2, N2, n_active, R, T)
+    launch_bytes = sparse_gemm_bytes if args.sparse else gemm_bytes
+    gu_bytes = launch_bytes(K1, N1, n_active, R, R)
+    dn_bytes = launch_bytes(K2, N2, n_active, R, T)
     achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
-    traffic = recorded_traffic()
+    # the recorded DRAM counters belong to the dense gate_up launch
+    traffic = None if args.sparse else recorded_traffic()
+    sbytes = step_bytes(n_active, sparse=args.sparse)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4",
         "data": "synthetic", "config": workload_config(),
-        "hbm_gbs": round(world * step_bytes(n_active) / (ms_step * 1e-3) / 1e9, 1),
-        "frac_of_hbm_roofline": round(step_bytes(n_active) / (ms_step * 1e-3) / 1e9 / peak, 4),
+        "hbm_gbs": round(world * sbytes / (ms_step * 1e-3) / 1e9, 1),
+        "frac_of_hbm_roofline": round(sbytes / (ms_step * 1e-3) / 1e9 / peak, 4),
         "roofline": {
             "kernel": "nvfp4_gemm_kernel (gate_up grouped launch)", "bound": "hbm",
             "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -394,7 +399,13 @@ def run_ours(args, rank, world, local_rank):
         "clocks_eager": clocks,
         "setup_s": round(setup_s, 1),
     }
-    if world == 1 and not args.no_cpu_baseline:
+    if args.sparse:
+        line["config"]["workload"] += " (2:4-sparse weights)"
+        line["config"]["weights"] = ("the same weights pruned to 2:4 over element pairs, NVFP4, "
+                                     "streamed as sparse tiles (2/3 of the dense bytes)")
+        line["note"] = ("TFLOPS count the dense GEMMs' FLOPs; not the headline (different "
+                        "weights); cpu_baseline is reported on the dense line")
+    elif world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(W_host_seed=2, budget_s=args.cpu_budget)
     return line
 
@@ -646,6 +657,9 @@ def main():
     ap.add_argument("--workload", default="decode_layer", choices=["decode_layer", "configs"],
                     help="configs: one line per workload configuration (not the headline)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sparse", action="store_true",
+                    help="the decode step with the weights pruned to 2:4 and streamed as "
+                         "sparse tiles (not the headline)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--experts", type=int, default=E,
                     help="experts (tokens scale as 2 per expert); smaller values give the "

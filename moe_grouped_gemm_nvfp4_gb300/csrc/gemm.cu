@@ -56,8 +56,8 @@ struct Cfg {
   static_assert(MT == 1 || (MT == 2 && (BN == 32 || BN == 64)), "unit height");
   // SP: X (the weights) arrives as 2:4-sparse tiles and is expanded in shared
   // memory by the decompression warps before the MMAs read it
-  static_assert(!SP || (BN <= 128 && (MT == 1 || BN == 32)),
-                "sparse weights: token tiles <= 128, two X tiles only for 32-route tiles");
+  static_assert(!SP || (BN <= 128 && (MT == 1 || BN <= 64)),
+                "sparse weights: token tiles <= 128, two X tiles only for 32/64-route tiles");
   static constexpr int kYTileBytes = BN * kRowBytes;
   static constexpr int kSfyAtomsPerStep = BN == 256 ? 2 : 1;   // 128-row scale atoms of Y
   // rows of one grouped operand tile / layout chunk: a 256-row token tile
@@ -74,7 +74,7 @@ struct Cfg {
   static constexpr int kYOffset = MT * kXPartBytes;
   static constexpr int kStageBytes = kYOffset + kYTileBytes + kSfyStageBytes;
   static_assert(kYOffset % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle alignment");
-  static constexpr int kStages = SP ? (MT == 2 ? 4 : (BN == 32 ? 7 : (BN == 64 ? 6 : 5)))
+  static constexpr int kStages = SP ? (MT == 2 ? (BN == 32 ? 4 : 3) : (BN == 32 ? 7 : (BN == 64 ? 6 : 5)))
                                     : MT == 2 ? (BN == 32 ? 5 : 4)
                                               : (BN == 32 ? 9 : (BN == 256 ? 4 : 6));
   // sparse: ring of expanded (dense) X code tiles, written by the
@@ -104,7 +104,8 @@ struct Cfg {
   // Sparse two-tile units: the two MMA warps issue only MMAs and commits; a
   // scale warp of its own (after the decompression warps) copies all of the
   // stage's scale atoms.
-  static constexpr bool kSpScaleWarp = SP && MT == 2;
+  // (64-route two-tile units have one MMA warp, so warp 6 is the scale warp)
+  static constexpr bool kSpScaleWarp = SP && MT == 2 && !kSplit;
   static constexpr bool kScaleWarp = kSplit || kSpScaleWarp;
   static constexpr bool kXsfOnScaleWarp = kScaleWarp && (BN == 128 || MT == 2);
   // accumulator buffers: two (the epilogue of one tile overlaps the next
@@ -1013,6 +1014,7 @@ cudaError_t init_gemm_attributes() {
   if (e == cudaSuccess) e = set_smem_attr<256>();
   if (e == cudaSuccess) e = set_smem_attr<32, 1, true>();
   if (e == cudaSuccess) e = set_smem_attr<32, 2, true>();
+  if (e == cudaSuccess) e = set_smem_attr<64, 2, true>();
   if (e == cudaSuccess) e = set_smem_attr<64, 1, true>();
   if (e == cudaSuccess) e = set_smem_attr<128, 1, true>();
   return e;
@@ -1048,7 +1050,9 @@ cudaError_t launch_gemm(const CUtensorMap& tmx, const CUtensorMap& tmy, const Ge
       case 32:   // two weight tiles per unit when the expert's rows pair up
         return (a.n_out / 128) % 2 == 0 ? launch_bn<32, 2, true>(tmx, tmy, a, mode, grid, s)
                                          : launch_bn<32, 1, true>(tmx, tmy, a, mode, grid, s);
-      case 64: return launch_bn<64, 1, true>(tmx, tmy, a, mode, grid, s);
+      case 64:
+        return (a.n_out / 128) % 2 == 0 ? launch_bn<64, 2, true>(tmx, tmy, a, mode, grid, s)
+                                         : launch_bn<64, 1, true>(tmx, tmy, a, mode, grid, s);
       default: return launch_bn<128, 1, true>(tmx, tmy, a, mode, grid, s);
     }
   }

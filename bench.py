@@ -121,10 +121,16 @@ def measured_peaks():
 
 
 def kernel_source_hash():
+    """Hash of the GEMM kernel's sources with comments and blank space taken
+    out, so that edits to comments keep the recorded counters valid."""
+    import re
     h = hashlib.sha256()
     for f in ("gemm.cu", "common.cuh", "kernels.h"):
-        with open(os.path.join(ROOT, "moe_grouped_gemm_nvfp4_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "moe_grouped_gemm_nvfp4_gb300", "csrc", f)) as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -17,7 +17,13 @@
 //               thread for ~60-110 cycles, so one thread cannot issue the
 //               12 instructions of a decode stage as fast as HBM delivers it;
 //   warps 2-5   epilogue: tcgen05.ld, global-scale multiply, BF16 store or
-//               weighted FP32 scatter-add (MoE combine).
+//               weighted FP32 scatter-add (MoE combine);
+//   warps 7-14  (2:4-sparse weights only) expansion of each stage's sparse
+//               weight tiles into dense tiles in shared memory, with byte
+//               permutes ("The FP4 Frontier", Finding 6: 2:4 sparsity halves
+//               the weight bits; decode is bound by the weight bytes);
+//   warp 15     (sparse 32-route units) scale warp.
+// Wider tiles add a second epilogue group and a scale warp (see Cfg).
 // A work unit is one 128-row tile of operand X (the MMA's M side) against up
 // to BN rows of operand Y (the MMA's N side).  For the grouped GEMM, X is an
 // expert's weights and Y its routed tokens, so a decode step streams every

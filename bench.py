@@ -33,7 +33,7 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from moe_grouped_gemm_nvfp4_gb300 import inputs, moe  # noqa: E402
+from moe_grouped_gemm_nvfp4_gb300 import attention, inputs, moe  # noqa: E402
 from moe_grouped_gemm_nvfp4_gb300 import nvfp4 as F  # noqa: E402
 
 METRIC = "NVFP4 grouped-GEMM TFLOPS & HBM GB/s (frac. of roofline) at 16-64 tok/expert"
@@ -546,26 +546,32 @@ def run_configs(args):
     iters = max(3, min(args.steps, 20))
     lines = []
 
+    def want(group):
+        return not args.only or args.only == group
+
     # dense 8192^3: A quantised every call, B prepared offline
-    M = Nn = Kk = 8192
-    a = inputs.device_normal_bf16((M, Kk), 1.0, 1, dev)
-    b = inputs.device_normal_bf16((Nn, Kk), 0.02, 1001, dev)
-    pb, sb, gb = F.quantize(b, atoms=True)
-    pa, sa, ga = F.quantize(a, atoms=True)
-    C = torch.empty((M, Nn), dtype=torch.bfloat16, device=dev)
-    t_gemm = _timed(lambda: F.nvfp4_gemm(pa, sa, ga, pb, sb, gb, C, Kk), iters, flush)
-    t_q = _timed(lambda: F.nvfp4_quantize(a, pa, sa, ga, F.NVFP4_SF_ATOMS), iters, flush)
-    fl = 2.0 * M * Nn * Kk
-    lines.append({"workload": "dense_gemm_8192^3", "gemm_ms": round(t_gemm, 4),
-                  "tflops": round(fl / t_gemm / 1e9, 1),
-                  "frac_of_fp4_peak": round(fl / t_gemm / 1e9 / fp4_peak, 4),
-                  "fp4_peak_tflops": fp4_peak, "quantize_A_ms": round(t_q, 4),
-                  "quantize_A_gbs": round(M * Kk * 2.5625 / t_q / 1e6, 1)})
-    del a, b, pa, sa, pb, sb, C
+    if want("dense_8192"):
+        M = Nn = Kk = 8192
+        a = inputs.device_normal_bf16((M, Kk), 1.0, 1, dev)
+        b = inputs.device_normal_bf16((Nn, Kk), 0.02, 1001, dev)
+        pb, sb, gb = F.quantize(b, atoms=True)
+        pa, sa, ga = F.quantize(a, atoms=True)
+        C = torch.empty((M, Nn), dtype=torch.bfloat16, device=dev)
+        t_gemm = _timed(lambda: F.nvfp4_gemm(pa, sa, ga, pb, sb, gb, C, Kk), iters, flush)
+        t_q = _timed(lambda: F.nvfp4_quantize(a, pa, sa, ga, F.NVFP4_SF_ATOMS), iters, flush)
+        fl = 2.0 * M * Nn * Kk
+        lines.append({"workload": "dense_gemm_8192^3", "gemm_ms": round(t_gemm, 4),
+                      "tflops": round(fl / t_gemm / 1e9, 1),
+                      "frac_of_fp4_peak": round(fl / t_gemm / 1e9 / fp4_peak, 4),
+                      "fp4_peak_tflops": fp4_peak, "quantize_A_ms": round(t_q, 4),
+                      "quantize_A_gbs": round(M * Kk * 2.5625 / t_q / 1e6, 1)})
+        del a, b, pa, sa, pb, sb, C
 
     # decode down-projection sweep and skewed prefill gate_up
     for name in ("decode_gate_up", "decode_down_256", "decode_down_512", "decode_down_1024",
                  "prefill_skewed"):
+        if not want("decode"):
+            break
         cfg = inputs.CONFIGS[name]
         g = inputs.rng(cfg.seed)
         w = torch.empty((cfg.E, cfg.N, cfg.K), dtype=torch.bfloat16, device=dev)
@@ -628,6 +634,8 @@ def run_configs(args):
     # launch) against the same pass with h quantised by its own kernels, at
     # 16 and 32 routes per expert (32- and 64-route token tiles)
     for tokens in (T, 2 * T):
+        if not want("fused_mlp"):
+            break
         W1, W2, w1, w2, host, _ = build_problem(dev, tokens=tokens)
         del w1, w2
         torch.cuda.empty_cache()
@@ -650,6 +658,31 @@ def run_configs(args):
                               "quantised by its own kernels (h drawn at random there)"})
         del layer, mlp, W1, W2, d, gu_out, gate, up
         torch.cuda.empty_cache()
+    # decode attention over an NVFP4 KV cache: bound by the cache bytes (every
+    # byte read once); 128-wide heads in groups of 4, and 512-wide heads
+    for (B_, Hq_, Hkv_, L_, D_) in ((16, 32, 8, 16384, 128), (8, 8, 2, 32768, 512)):
+        if not want("decode_attention"):
+            break
+        kc = inputs.device_normal_bf16((B_, Hkv_, L_, D_), 1.0, 71, dev)
+        kq = attention.quantize_kv(kc)
+        del kc
+        vc = inputs.device_normal_bf16((B_, Hkv_, L_, D_), 1.0, 72, dev)
+        vq = attention.quantize_kv(vc)
+        del vc
+        q = inputs.device_normal_bf16((B_, Hq_, D_), 1.0, 73, dev)
+        seq = torch.full((B_,), L_, dtype=torch.int32, device=dev)
+        plan = attention.DecodeAttention(B_, Hq_, Hkv_, L_, D_, dev)
+        t_att = _timed(lambda: plan.run(q, kq, vq, seq, 1.0 / D_ ** 0.5), iters, flush)
+        byt = 2.0 * B_ * Hkv_ * L_ * D_ * (0.5 + 1.0 / 16) + 2.0 * 2 * B_ * Hq_ * D_
+        lines.append({"workload": f"decode_attention_B{B_}_Hq{Hq_}_Hkv{Hkv_}_L{L_}_D{D_}",
+                      "ms": round(t_att, 4), "gbs": round(byt / t_att / 1e6, 1),
+                      "frac_of_hbm_roofline": round(byt / t_att / 1e6 / peak, 4),
+                      "cache_bytes": int(byt),
+                      "note": "one query token per sequence; K and V in NVFP4 (codes + E4M3 "
+                              "scales along D + one global each), dequantised in registers; "
+                              "split-KV partials merged by a second kernel (both timed)"})
+        del kq, vq, plan
+        torch.cuda.empty_cache()
     for ln in lines:
         print(json.dumps(ln), flush=True)
 
@@ -663,6 +696,9 @@ def main():
     ap.add_argument("--workload", default="decode_layer", choices=["decode_layer", "configs"],
                     help="configs: one line per workload configuration (not the headline)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default=None,
+                    help="configs: run only this group (dense_8192, decode, fused_mlp, "
+                         "decode_attention)")
     ap.add_argument("--sparse", action="store_true",
                     help="the decode step with the weights pruned to 2:4 and streamed as "
                          "sparse tiles (not the headline)")

@@ -408,6 +408,42 @@ nvfp4_status nvfp4_grouped_gemm_sparse(const uint8_t* A_tiles, const float* gA,
                                        void* out, float* workspace, size_t workspace_bytes,
                                        void* stream);
 
+/*
+ * Decode attention over an NVFP4 KV cache ("The Blackwell architectural
+ * split", The Breakthrough -- The A4Q Kernel, and Preserving precision --
+ * dual-tier scale handling): the cache stays packed and is dequantised in
+ * registers inside the attention loop.  One query token per sequence.
+ *   q          BF16 [B, Hq, D].
+ *   k_packed   NVFP4 codes [B, Hkv, L_max, D/2] (token rows of sequence b and
+ *              KV head j contiguous), k_scales E4M3 [B, Hkv, L_max, D/16]
+ *              (row-major, 16-element blocks along D), gk device float: the
+ *              K cache's global.  nvfp4_quantize of the BF16 cache viewed as
+ *              [B * Hkv * L_max, D] rows, with NVFP4_GLOBAL_GIVEN, writes
+ *              exactly this layout.  v_packed, v_scales, gv likewise for V.
+ *   seq_lens   int32 [B] (device): tokens of each sequence, 0 <= n <= L_max
+ *              (others set NVFP4_ERR_DEVICE_CHECK and count as 0).
+ *   scale      softmax scale (e.g. 1 / sqrt(D)).
+ *   out        BF16 [B, Hq, D]: query head h reads KV head h / (Hq / Hkv);
+ *              out = sum_t p_t v_hat_t, p = softmax over t < n of
+ *              scale * q . k_hat_t, with k_hat = e2m1 * e4m3 * gk (likewise
+ *              v_hat); FP32 arithmetic, BF16 round to nearest even; an empty
+ *              sequence gives zeros.
+ *   workspace  FP32, nvfp4_decode_attention_workspace_bytes(B, Hq, Hkv, L_max,
+ *              D) bytes, caller-owned (per-split partials, overwritten).
+ * D in {64, 128, 256, 512}; Hq / Hkv in {1, 2, 4, 8} (at most 4 for D = 512);
+ * q, out, workspace and the code arrays 16-byte aligned, k_scales 2-byte.
+ */
+size_t nvfp4_decode_attention_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int64_t L_max,
+                                              int32_t D);
+
+nvfp4_status nvfp4_decode_attention(const void* q, const uint8_t* k_packed,
+                                    const uint8_t* k_scales, const float* gk,
+                                    const uint8_t* v_packed, const uint8_t* v_scales,
+                                    const float* gv, const int32_t* seq_lens, int32_t B,
+                                    int32_t Hq, int32_t Hkv, int64_t L_max, int32_t D, float scale,
+                                    void* out, float* workspace, size_t workspace_bytes,
+                                    void* stream);
+
 #ifdef __cplusplus
 }  /* extern "C" */
 #endif

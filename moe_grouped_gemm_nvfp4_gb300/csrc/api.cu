@@ -518,6 +518,70 @@ nvfp4_status nvfp4_prepack_sparse_weight_tiles(const uint8_t* packed,
   return NVFP4_OK;
 }
 
+size_t nvfp4_decode_attention_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int64_t L_max,
+                                              int32_t D) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || L_max < 0 || D <= 0) return 0;
+  const int ch = nvfp4::attention_chunk(L_max, B, Hkv);
+  const int64_t splits = (L_max + ch - 1) / ch;
+  return static_cast<size_t>(B) * static_cast<size_t>(Hq) * static_cast<size_t>(splits) *
+         static_cast<size_t>(D + 2) * sizeof(float);
+}
+
+nvfp4_status nvfp4_decode_attention(const void* q, const uint8_t* k_packed,
+                                    const uint8_t* k_scales, const float* gk,
+                                    const uint8_t* v_packed, const uint8_t* v_scales,
+                                    const float* gv, const int32_t* seq_lens, int32_t B,
+                                    int32_t Hq, int32_t Hkv, int64_t L_max, int32_t D, float scale,
+                                    void* out, float* workspace, size_t workspace_bytes,
+                                    void* stream) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || L_max < 0 || D <= 0) return NVFP4_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return NVFP4_ERR_INVALID_ARG;
+  if (B == 0) return NVFP4_OK;
+  if (!q || !gk || !gv || !seq_lens || !out || !workspace) return NVFP4_ERR_INVALID_ARG;
+  if (L_max > 0 && (!k_packed || !k_scales || !v_packed || !v_scales)) return NVFP4_ERR_INVALID_ARG;
+  const int G = Hq / Hkv;
+  if (D != 64 && D != 128 && D != 256 && D != 512) return NVFP4_ERR_UNSUPPORTED;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return NVFP4_ERR_UNSUPPORTED;
+  if (D == 512 && G == 8) return NVFP4_ERR_UNSUPPORTED;
+  if (B > 65535 || Hkv > 65535 || static_cast<int64_t>(B) * Hq > (1LL << 31) - 1)
+    return NVFP4_ERR_UNSUPPORTED;
+  if (L_max > (1LL << 31) - 1) return NVFP4_ERR_UNSUPPORTED;
+  if (workspace_bytes < nvfp4_decode_attention_workspace_bytes(B, Hq, Hkv, L_max, D))
+    return NVFP4_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(workspace) ||
+      (k_packed && !aligned16(k_packed)) || (v_packed && !aligned16(v_packed)) ||
+      (k_scales && (reinterpret_cast<uintptr_t>(k_scales) & 1u)) ||
+      (reinterpret_cast<uintptr_t>(gk) & 3u) || (reinterpret_cast<uintptr_t>(gv) & 3u) ||
+      (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return NVFP4_ERR_UNSUPPORTED;
+  DeviceState* d = nullptr;
+  nvfp4_status st = device_state(&d);
+  if (st != NVFP4_OK) return st;
+  nvfp4::AttnArgs a{};
+  a.q = static_cast<const uint16_t*>(q);
+  a.k_packed = k_packed;
+  a.k_scales = k_scales;
+  a.v_packed = v_packed;
+  a.v_scales = v_scales;
+  a.gk = gk;
+  a.gv = gv;
+  a.seq_lens = seq_lens;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.L_max = L_max;
+  a.chunk = nvfp4::attention_chunk(L_max, B, Hkv);
+  a.splits = static_cast<int32_t>((L_max + a.chunk - 1) / a.chunk);
+  a.scale = scale;
+  a.out = static_cast<uint16_t*>(out);
+  a.ws_o = workspace;
+  a.ws_ml = workspace + static_cast<int64_t>(B) * Hq * a.splits * D;
+  a.status = d->status;
+  if (nvfp4::launch_decode_attention(a, D, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return cuda_fail();
+  return NVFP4_OK;
+}
+
 nvfp4_status nvfp4_moe_gate_up_silu(const uint8_t* A_tiles, const float* gA,
                                     const uint8_t* W_tiles, const float* gW,
                                     const int32_t* expert_offsets, int32_t E, int64_t T,

@@ -1,0 +1,287 @@
+// Decode attention over an NVFP4 KV cache.
+//
+// "The Blackwell architectural split", The Breakthrough -- The A4Q Kernel:
+// keys and values stay packed in NVFP4 (E2M1 values, an E4M3 scale per 16
+// numbers along the head dimension, one FP32 global for K and one for V,
+// "Preserving precision -- dual-tier scale handling") and are dequantised in
+// registers inside the attention loop, never staged as wider copies.  One
+// query token per sequence: every cache byte is read once and each element
+// feeds G = Hq / Hkv multiply-adds, so for the grouped-query ratios of
+// decode the work is bound by HBM and runs on the CUDA cores.
+//
+// Split-KV: CTA (split, kv head j, sequence b) covers the `chunk` tokens
+// [split * chunk, ...) of that sequence for the G query heads of KV head j
+// and leaves an unnormalised partial (running max, sum, weighted values) in
+// the workspace; a second kernel merges the splits and writes BF16.
+//
+// Per warp, blocks of 32 tokens: scores lane-per-token (each lane reads its
+// token's key row, 16 bytes at a time, coalesced across the warp), an online
+// softmax update per block (base-2 exponentials with log2(e) folded into q),
+// then values lane-per-dimension (lane owns D / 32 consecutive dimensions of
+// every token's value row).
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace nvfp4 {
+
+namespace {
+
+constexpr int kAttnWarps = 4;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Two E2M1 codes (low nibble first) -> two floats, exactly.
+__device__ __forceinline__ float2 e2m1x2_to_float2(uint32_t byte) {
+  uint32_t h;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+      : "=r"(h) : "r"(byte & 0xFFu));
+  const __half2 v = *reinterpret_cast<const __half2*>(&h);
+  return __half22float2(v);
+}
+
+// One E4M3 scale byte -> float, exactly.
+__device__ __forceinline__ float e4m3_to_float(uint32_t byte) {
+  uint32_t h;
+  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
+      : "=r"(h) : "r"(byte & 0xFFu));
+  const __half2 v = *reinterpret_cast<const __half2*>(&h);
+  return __low2float(v);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kAttnWarps * 32) decode_attention_kernel(const AttnArgs a) {
+  constexpr int DL = D / 32;          // value dimensions per lane
+  constexpr int KB = D / 2;           // code bytes per token row
+  constexpr int SB = D / 16;          // scale bytes per token row
+  __shared__ __align__(16) float q_s[G][D];
+  __shared__ float m_s[kAttnWarps][G], l_s[kAttnWarps][G];
+  __shared__ __align__(16) float o_s[kAttnWarps][G][D];
+
+  const int split = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int n = a.seq_lens[b];
+  if (n < 0 || n > a.L_max) {
+    if (threadIdx.x == 0) raise_status(a.status, NVFP4_ERR_DEVICE_CHECK);
+    n = 0;
+  }
+  const int64_t t0 = static_cast<int64_t>(split) * a.chunk;
+  const int64_t t1 = min(static_cast<int64_t>(n), t0 + a.chunk);
+  const int64_t row0 = (static_cast<int64_t>(b) * a.Hkv + j) * a.L_max;   // cache row of token 0
+
+  // q of the group's heads, times scale * gk * log2(e)
+  const float qmul = a.scale * (*a.gk) * kLog2e;
+  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+    const int g = i / D, d = i - g * D;
+    const int64_t qi = (static_cast<int64_t>(b) * a.Hq + j * G + g) * D + d;
+    q_s[g][d] = bf16_bits_to_f32(a.q[qi]) * qmul;
+  }
+  __syncthreads();
+
+  float m[G], l[G], o[G][DL];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    m[g] = -INFINITY;
+    l[g] = 0.0f;
+#pragma unroll
+    for (int i = 0; i < DL; ++i) o[g][i] = 0.0f;
+  }
+
+  for (int64_t blk = t0 + 32 * warp; blk < t1; blk += 32 * kAttnWarps) {
+    // ---- scores, lane-per-token
+    const int64_t t = blk + lane;
+    const bool valid = t < t1;
+    float s[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) s[g] = valid ? 0.0f : -INFINITY;
+    if (valid) {
+      const uint8_t* krow = a.k_packed + (row0 + t) * KB;
+      const uint8_t* srow = a.k_scales + (row0 + t) * SB;
+#pragma unroll 1
+      for (int c = 0; c < KB / 16; ++c) {           // 32 elements = two scale blocks
+        const uint4 code = *reinterpret_cast<const uint4*>(krow + 16 * c);
+        const uint32_t sc2 = *reinterpret_cast<const uint16_t*>(srow + 2 * c);
+        const uint32_t w[4] = {code.x, code.y, code.z, code.w};
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {      // one scale block: words 2 half, 2 half + 1
+          float part[G];
+#pragma unroll
+          for (int g = 0; g < G; ++g) part[g] = 0.0f;
+#pragma unroll
+          for (int wi = 0; wi < 2; ++wi) {
+            const uint32_t word = w[2 * half + wi];
+#pragma unroll
+            for (int by = 0; by < 4; ++by) {
+              const float2 e = e2m1x2_to_float2(word >> (8 * by));
+              const int d = 32 * c + 16 * half + 8 * wi + 2 * by;
+#pragma unroll
+              for (int g = 0; g < G; ++g) {
+                const float2 qq = *reinterpret_cast<const float2*>(&q_s[g][d]);
+                part[g] = fmaf(qq.x, e.x, part[g]);
+                part[g] = fmaf(qq.y, e.y, part[g]);
+              }
+            }
+          }
+          const float sf = e4m3_to_float(sc2 >> (8 * half));
+#pragma unroll
+          for (int g = 0; g < G; ++g) s[g] = fmaf(part[g], sf, s[g]);
+        }
+      }
+    }
+    // ---- online softmax over the block (base 2)
+    float p[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float mn = fmaxf(m[g], warp_max(s[g]));    // finite: lane 0 is valid
+      const float corr = (m[g] == -INFINITY) ? 0.0f : exp2f(m[g] - mn);
+      p[g] = valid ? exp2f(s[g] - mn) : 0.0f;
+      l[g] = fmaf(l[g], corr, warp_sum(p[g]));
+#pragma unroll
+      for (int i = 0; i < DL; ++i) o[g][i] *= corr;
+      m[g] = mn;
+    }
+    // ---- values, lane-per-dimension
+    const int nt = static_cast<int>(min(static_cast<int64_t>(32), t1 - blk));
+    for (int tt = 0; tt < nt; ++tt) {
+      const int64_t row = row0 + blk + tt;
+      const uint8_t* vrow = a.v_packed + row * KB + lane * (DL / 2);
+      const float sf = e4m3_to_float(a.v_scales[row * SB + (lane * DL) / 16]);
+      uint32_t codes[(DL / 2 + 3) / 4];
+      if constexpr (DL / 2 == 1) codes[0] = *vrow;
+      else if constexpr (DL / 2 == 2) codes[0] = *reinterpret_cast<const uint16_t*>(vrow);
+      else if constexpr (DL / 2 == 4) codes[0] = *reinterpret_cast<const uint32_t*>(vrow);
+      else {
+        const uint2 c2 = *reinterpret_cast<const uint2*>(vrow);
+        codes[0] = c2.x;
+        codes[1] = c2.y;
+      }
+      float wgt[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) wgt[g] = __shfl_sync(0xFFFFFFFFu, p[g], tt) * sf;
+#pragma unroll
+      for (int i = 0; i < DL / 2; ++i) {
+        const float2 e = e2m1x2_to_float2(codes[i / 4] >> (8 * (i % 4)));
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          o[g][2 * i] = fmaf(wgt[g], e.x, o[g][2 * i]);
+          o[g][2 * i + 1] = fmaf(wgt[g], e.y, o[g][2 * i + 1]);
+        }
+      }
+    }
+  }
+
+  // ---- merge the warps, write this split's partial
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    if (lane == 0) {
+      m_s[warp][g] = m[g];
+      l_s[warp][g] = l[g];
+    }
+#pragma unroll
+    for (int i = 0; i < DL; ++i) o_s[warp][g][lane * DL + i] = o[g][i];
+  }
+  __syncthreads();
+  const int64_t nsplit = a.splits;
+  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+    const int g = i / D, d = i - g * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kAttnWarps; ++w)
+      if (l_s[w][g] > 0.0f) M = fmaxf(M, m_s[w][g]);
+    float L = 0.0f, O = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kAttnWarps; ++w) {
+      if (l_s[w][g] > 0.0f) {
+        const float f = exp2f(m_s[w][g] - M);
+        L = fmaf(l_s[w][g], f, L);
+        O = fmaf(o_s[w][g][d], f, O);
+      }
+    }
+    const int64_t part = (static_cast<int64_t>(b) * a.Hq + j * G + g) * nsplit + split;
+    a.ws_o[part * D + d] = O;
+    if (d == 0) {
+      a.ws_ml[2 * part] = M;
+      a.ws_ml[2 * part + 1] = L;
+    }
+  }
+}
+
+// Merges the splits of (sequence b, query head h): out = gv * sum_s O_s 2^(m_s - M)
+// / sum_s l_s 2^(m_s - M) in BF16; zeros for an empty sequence.
+__global__ void __launch_bounds__(128) decode_attention_combine_kernel(const AttnArgs a, int D) {
+  const int bh = blockIdx.x;
+  const int64_t nsplit = a.splits;
+  const int64_t base = static_cast<int64_t>(bh) * nsplit;
+  float M = -INFINITY;
+  for (int64_t s = 0; s < nsplit; ++s)
+    if (a.ws_ml[2 * (base + s) + 1] > 0.0f) M = fmaxf(M, a.ws_ml[2 * (base + s)]);
+  float L = 0.0f;
+  for (int64_t s = 0; s < nsplit; ++s) {
+    const float l = a.ws_ml[2 * (base + s) + 1];
+    if (l > 0.0f) L = fmaf(l, exp2f(a.ws_ml[2 * (base + s)] - M), L);
+  }
+  const float gv = *a.gv;
+  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    float O = 0.0f;
+    for (int64_t s = 0; s < nsplit; ++s) {
+      const float l = a.ws_ml[2 * (base + s) + 1];
+      if (l > 0.0f) O = fmaf(a.ws_o[(base + s) * D + d], exp2f(a.ws_ml[2 * (base + s)] - M), O);
+    }
+    const float v = L > 0.0f ? __fmul_rn(gv, __fdiv_rn(O, L)) : 0.0f;
+    a.out[static_cast<int64_t>(bh) * D + d] = f32_to_bf16_rn(v);
+  }
+}
+
+template <int D, int G>
+cudaError_t launch_d_g(const AttnArgs& a, cudaStream_t s) {
+  const dim3 grid(static_cast<unsigned>(a.splits), static_cast<unsigned>(a.Hkv),
+                  static_cast<unsigned>(a.B));
+  decode_attention_kernel<D, G><<<grid, kAttnWarps * 32, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(const AttnArgs& a, int G, cudaStream_t s) {
+  switch (G) {
+    case 1: return launch_d_g<D, 1>(a, s);
+    case 2: return launch_d_g<D, 2>(a, s);
+    case 4: return launch_d_g<D, 4>(a, s);
+    default:
+      if constexpr (D <= 256) return launch_d_g<D, 8>(a, s);
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_decode_attention(const AttnArgs& a, int D, cudaStream_t s) {
+  const int G = a.Hq / a.Hkv;
+  cudaError_t e = cudaSuccess;
+  if (a.splits == 0) {             // empty cache: the merge writes zeros
+    decode_attention_combine_kernel<<<static_cast<unsigned>(a.B * a.Hq), 128, 0, s>>>(a, D);
+    return cudaGetLastError();
+  }
+  switch (D) {
+    case 64: e = launch_d<64>(a, G, s); break;
+    case 128: e = launch_d<128>(a, G, s); break;
+    case 256: e = launch_d<256>(a, G, s); break;
+    default: e = launch_d<512>(a, G, s); break;
+  }
+  if (e != cudaSuccess) return e;
+  decode_attention_combine_kernel<<<static_cast<unsigned>(a.B * a.Hq), 128, 0, s>>>(a, D);
+  return cudaGetLastError();
+}
+
+}  // namespace nvfp4

@@ -61,6 +61,9 @@ _SIGS = {
     "nvfp4_moe_gate_up_silu": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I64, _I32, _I64, _I64,
                                               _P, _P, _P]),
     "nvfp4_noalloc_workspace_floats": (_SZ, []),
+    "nvfp4_decode_attention_workspace_bytes": (_SZ, [_I32, _I32, _I32, _I64, _I32]),
+    "nvfp4_decode_attention": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32,
+                                              _I64, _I32, ctypes.c_float, _P, _P, _SZ, _P]),
     "nvfp4_prune_2of4": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I64, _P]),
     "nvfp4_sparse_tiles_bytes": (_SZ, [_I64, _I64]),
     "nvfp4_prepack_sparse_weight_tiles": (ctypes.c_int, [_P, _P, _I64, _I64, _P, _P]),
@@ -272,6 +275,22 @@ def nvfp4_grouped_gemm_sparse(A_tiles, gA, W_sparse_tiles, gW, expert_offsets, E
         _ptr(A_tiles), _ptr(gA), _ptr(W_sparse_tiles), _ptr(gW), _ptr(expert_offsets), E, T,
         topk, N, K, _ptr(route_token), _ptr(route_slot), _ptr(topk_weights), _ptr(out),
         _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def nvfp4_decode_attention_workspace_bytes(B: int, Hq: int, Hkv: int, L_max: int, D: int) -> int:
+    return load().nvfp4_decode_attention_workspace_bytes(B, Hq, Hkv, L_max, D)
+
+
+def nvfp4_decode_attention(q, k_packed, k_scales, gk, v_packed, v_scales, gv, seq_lens,
+                           scale: float, out, workspace, stream=None) -> None:
+    """q BF16 [B, Hq, D]; caches [B, Hkv, L_max, D/2] codes and [.., D/16] scales."""
+    B, Hq, D = q.shape
+    _, Hkv, L_max, _ = k_packed.shape
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("nvfp4_decode_attention", load().nvfp4_decode_attention(
+        _ptr(q), _ptr(k_packed), _ptr(k_scales), _ptr(gk), _ptr(v_packed), _ptr(v_scales),
+        _ptr(gv), _ptr(seq_lens), B, Hq, Hkv, L_max, D, float(scale), _ptr(out), _ptr(workspace),
+        ws_bytes, _stream(stream)))
 
 
 def nvfp4_noalloc_workspace_floats() -> int:

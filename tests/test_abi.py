@@ -65,6 +65,11 @@ def test_pure_host_helpers():
     assert F.nvfp4_sparse_tiles_bytes(128 * 4096, 6144) * 3 == \
         F.nvfp4_operand_tiles_bytes(128 * 4096, 6144) * 2
     assert F.nvfp4_sparse_tiles_bytes(-1, 64) == 0
+    # decode attention: per (sequence, query head, split) D partial values + max + sum
+    assert F.nvfp4_decode_attention_workspace_bytes(2, 8, 2, 1000, 128) == 2 * 8 * 8 * 130 * 4
+    assert F.nvfp4_decode_attention_workspace_bytes(16, 32, 8, 16384, 128) == \
+        16 * 32 * (16384 // 2048) * 130 * 4     # 2048-token splits: ~1024 CTAs
+    assert F.nvfp4_decode_attention_workspace_bytes(0, 8, 2, 1000, 128) == 0
 
 
 def test_host_validation_without_device():
@@ -88,6 +93,10 @@ def test_host_validation_without_device():
     assert lib.nvfp4_prune_2of4(None, 4, 16, 16, None, 16, None) == 1
     assert lib.nvfp4_prune_2of4(None, 4, 16, 8, None, 16, None) == 1           # ld < cols
     assert lib.nvfp4_prepack_sparse_weight_tiles(None, None, 4, 64, None, None) == 1
+    assert lib.nvfp4_decode_attention(*([None] * 8), 1, 4, 1, 16, 64, 0.1, None, None, 0,
+                                      None) == 1
+    assert lib.nvfp4_decode_attention(*([None] * 8), 1, 6, 4, 16, 64, 0.1, None, None, 0,
+                                      None) == 1                                # Hq % Hkv
     # unsupported shapes are refused before any CUDA call too
     p = ctypes.c_void_p(256)
     assert lib.nvfp4_gemm(p, p, p, p, p, p, p, 16, 16, 48, 16, None) == 2
@@ -97,6 +106,13 @@ def test_host_validation_without_device():
     assert lib.nvfp4_prepack_sparse_weight_tiles(p, p, 4, 96, p, None) == 2     # K % 64
     assert lib.nvfp4_grouped_gemm_sparse(p, p, p, p, p, 4, 8, 2, 200, 128, p, p, None, p,
                                          None, 0, None) == 2                     # N % 128
+    q = ctypes.c_void_p(4096)
+    assert lib.nvfp4_decode_attention(*([q] * 8), 1, 4, 1, 16, 96, 0.1, q, q, 1 << 20,
+                                      None) == 2                                # head width
+    assert lib.nvfp4_decode_attention(*([q] * 8), 1, 16, 1, 16, 128, 0.1, q, q, 1 << 20,
+                                      None) == 2                                # group of 16
+    assert lib.nvfp4_decode_attention(*([q] * 8), 1, 4, 1, 16, 128, 0.1, q, q, 16,
+                                      None) == 2                                # workspace
     # fused MLP: N must split into gate and up halves of whole 128-row tiles
     assert lib.nvfp4_moe_gate_up_silu(p, p, p, p, p, 4, 8, 2, 384, 128, p, p, None) == 2
     # conflicting quantiser flags: a given global and amax maxima already present

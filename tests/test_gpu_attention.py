@@ -1,0 +1,97 @@
+"""Decode attention over an NVFP4 KV cache ("The Blackwell architectural
+split", The A4Q Kernel) against the FP64 oracle.
+
+Tolerance: the kernel computes scores, exponentials and weighted sums in
+binary32 (relative error ~1e-6 of the largest output) and rounds the output
+to BF16 (half an ulp), so per element |gpu - ref| <= 0.5 ulp_bf16(ref) +
+1e-4 * max|ref|, and normwise <= 4e-3."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_grouped_gemm_nvfp4_gb300 import attention, inputs
+from moe_grouped_gemm_nvfp4_gb300 import nvfp4 as F
+from parity import ulp_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(seed, B, Hq, Hkv, L, D):
+    g = inputs.rng(seed)
+    q = inputs.normal_bf16(g, (B, Hq, D))
+    k = inputs.normal_bf16(g, (B, Hkv, L, D))
+    v = inputs.normal_bf16(g, (B, Hkv, L, D))
+    return q, k, v
+
+
+def _check(got, ref, name):
+    assert np.isfinite(got).all(), f"{name}: non-finite output"
+    err = np.abs(got - ref)
+    allow = 0.5 * ulp_bf16(ref) + 1e-4 * np.abs(ref).max()
+    worst = float((err / allow).max())
+    nref = np.linalg.norm(ref)
+    normwise = float(np.linalg.norm(got - ref) / nref) if nref > 0 else float(np.linalg.norm(got))
+    assert worst <= 1.0, f"{name}: element error {worst:.3f} x allowance"
+    assert normwise <= 4e-3, f"{name}: normwise {normwise:.2e}"
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,L,D,lens", [
+    (2, 4, 4, 100, 128, [100, 37]),          # one query head per KV head
+    (3, 8, 2, 300, 64, [300, 1, 0]),         # groups of 4, a one-token and an empty sequence
+    (1, 16, 2, 1000, 128, [1000]),           # groups of 8, several splits
+    (2, 4, 1, 2500, 256, [2500, 1333]),      # ragged split tails
+    (1, 4, 1, 700, 512, [700]),              # 512-wide heads
+    (4, 2, 1, 64, 512, [64, 3, 33, 17]),
+    (2, 8, 8, 4097, 64, [4097, 4096]),       # chunk boundary +- 1
+])
+def test_decode_attention_matches_oracle(B, Hq, Hkv, L, D, lens):
+    q, k, v = _case(B * 1000 + Hq * 10 + D + L, B, Hq, Hkv, L, D)
+    kd, vd = k.cuda(), v.cuda()
+    kq = attention.quantize_kv(kd)
+    vq = attention.quantize_kv(vd)
+    # the oracle quantises the same BF16 cache with its own global
+    kf, vf = k.float().numpy(), v.float().numpy()
+    gk, gv = oracle.global_scale(kf), oracle.global_scale(vf)
+    pk, sk = oracle.quantize_kv(kf, gk)
+    pv, sv = oracle.quantize_kv(vf, gv)
+    assert np.array_equal(kq[0].cpu().numpy(), pk) and np.array_equal(kq[1].cpu().numpy(), sk)
+    assert np.array_equal(vq[0].cpu().numpy(), pv) and np.array_equal(vq[1].cpu().numpy(), sv)
+    scale = 1.0 / np.sqrt(D)
+    plan = attention.DecodeAttention(B, Hq, Hkv, L, D)
+    plan.out.view(torch.int16).fill_(0x7FC0)
+    seq = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    out = plan.run(q.cuda(), kq, vq, seq, scale)
+    torch.cuda.synchronize()
+    assert F.nvfp4_device_status() == F.NVFP4_OK
+    ref = oracle.decode_attention(q.float().numpy(), oracle.dequantize_kv(pk, sk, gk),
+                                  oracle.dequantize_kv(pv, sv, gv), lens, scale)
+    _check(out.float().cpu().numpy().astype(np.float64), ref, f"attention B{B} Hq{Hq} D{D}")
+    for b, n in enumerate(lens):
+        if n == 0:
+            assert not out[b].float().abs().sum().item()
+
+
+def test_sequence_length_out_of_range_is_reported():
+    B, Hq, Hkv, L, D = 2, 2, 1, 64, 64
+    q, k, v = _case(5, B, Hq, Hkv, L, D)
+    kq, vq = attention.quantize_kv(k.cuda()), attention.quantize_kv(v.cuda())
+    plan = attention.DecodeAttention(B, Hq, Hkv, L, D)
+    F.nvfp4_device_status(reset=True)
+    out = plan.run(q.cuda(), kq, vq, torch.tensor([65, 10], dtype=torch.int32, device="cuda"), 0.125)
+    torch.cuda.synchronize()
+    assert F.nvfp4_device_status(reset=True) == F.NVFP4_ERR_DEVICE_CHECK
+    assert not out[0].float().abs().sum().item()          # counted as empty
+    assert out[1].float().abs().sum().item() > 0
+
+
+def test_unsupported_shapes_are_refused():
+    q = torch.zeros((1, 8, 512), dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros((1, 1, 4, 256), dtype=torch.uint8, device="cuda")
+    s = torch.zeros((1, 1, 4, 32), dtype=torch.uint8, device="cuda")
+    g = torch.ones(1, dtype=torch.float32, device="cuda")
+    ws = torch.zeros(1 << 16, dtype=torch.float32, device="cuda")
+    out = torch.empty_like(q)
+    with pytest.raises(RuntimeError):            # 512-wide heads take groups of at most 4
+        F.nvfp4_decode_attention(q, k, s, g, k, s, g, torch.ones(1, dtype=torch.int32,
+                                 device="cuda"), 0.1, out, ws)

@@ -658,9 +658,10 @@ def run_configs(args):
                               "quantised by its own kernels (h drawn at random there)"})
         del layer, mlp, W1, W2, d, gu_out, gate, up
         torch.cuda.empty_cache()
-    # decode attention over an NVFP4 KV cache: bound by the cache bytes (every
-    # byte read once); 128-wide heads in groups of 4, and 512-wide heads
-    for (B_, Hq_, Hkv_, L_, D_) in ((16, 32, 8, 16384, 128), (8, 8, 2, 32768, 512)):
+    # decode attention over an NVFP4 KV cache (every cache byte read once):
+    # 128-wide heads in groups of 4 and of 1, and 512-wide heads
+    for (B_, Hq_, Hkv_, L_, D_) in ((16, 32, 8, 16384, 128), (16, 8, 8, 16384, 128),
+                                    (8, 8, 2, 32768, 512)):
         if not want("decode_attention"):
             break
         kc = inputs.device_normal_bf16((B_, Hkv_, L_, D_), 1.0, 71, dev)

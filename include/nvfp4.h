@@ -431,7 +431,8 @@ nvfp4_status nvfp4_grouped_gemm_sparse(const uint8_t* A_tiles, const float* gA,
  *   workspace  FP32, nvfp4_decode_attention_workspace_bytes(B, Hq, Hkv, L_max,
  *              D) bytes, caller-owned (per-split partials, overwritten).
  * D in {64, 128, 256, 512}; Hq / Hkv in {1, 2, 4, 8} (at most 4 for D = 512);
- * q, out, workspace and the code arrays 16-byte aligned, k_scales 2-byte.
+ * q, out, workspace and the code arrays 16-byte aligned, the scale arrays
+ * 4-byte aligned.
  */
 size_t nvfp4_decode_attention_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int64_t L_max,
                                               int32_t D);

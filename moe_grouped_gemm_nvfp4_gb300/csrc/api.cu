@@ -550,7 +550,8 @@ nvfp4_status nvfp4_decode_attention(const void* q, const uint8_t* k_packed,
     return NVFP4_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(out) || !aligned16(workspace) ||
       (k_packed && !aligned16(k_packed)) || (v_packed && !aligned16(v_packed)) ||
-      (k_scales && (reinterpret_cast<uintptr_t>(k_scales) & 1u)) ||
+      (k_scales && (reinterpret_cast<uintptr_t>(k_scales) & 3u)) ||
+      (v_scales && (reinterpret_cast<uintptr_t>(v_scales) & 3u)) ||
       (reinterpret_cast<uintptr_t>(gk) & 3u) || (reinterpret_cast<uintptr_t>(gv) & 3u) ||
       (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
     return NVFP4_ERR_UNSUPPORTED;

@@ -14,11 +14,13 @@
 // and leaves an unnormalised partial (running max, sum, weighted values) in
 // the workspace; a second kernel merges the splits and writes BF16.
 //
-// Per warp, blocks of 32 tokens: scores lane-per-token (each lane reads its
-// token's key row, 16 bytes at a time, coalesced across the warp), an online
-// softmax update per block (base-2 exponentials with log2(e) folded into q),
-// then values lane-per-dimension (lane owns D / 32 consecutive dimensions of
-// every token's value row).
+// Per warp, blocks of 32 tokens: every load of the block is issued first
+// (lane l reads token l's key and value rows, 16 bytes at a time, coalesced
+// across the warp: one memory round trip per block); scores lane-per-token;
+// an online softmax update per block (base-2 exponentials with log2(e)
+// folded into q); the value rows go through a per-warp shared-memory stage
+// and are accumulated lane-per-dimension (lane owns D / 32 consecutive
+// dimensions of every token's value row).
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -66,9 +68,17 @@ __global__ void __launch_bounds__(kAttnWarps * 32) decode_attention_kernel(const
   constexpr int DL = D / 32;          // value dimensions per lane
   constexpr int KB = D / 2;           // code bytes per token row
   constexpr int SB = D / 16;          // scale bytes per token row
+  constexpr int KC = KB / 16;         // 16-byte chunks per row
+  // staged value row: codes, then scales, padded to 16 bytes so that the
+  // 16-byte stores of every lane's row stay aligned
+  constexpr int kVRow = (KB + SB + 15) / 16 * 16;
+  constexpr int kStageBytes = 32 * kVRow;                       // one warp's block
+  constexpr int kOBytes = kAttnWarps * G * D * 4;               // merge buffer
+  constexpr int kUnion = kAttnWarps * kStageBytes > kOBytes ? kAttnWarps * kStageBytes : kOBytes;
   __shared__ __align__(16) float q_s[G][D];
   __shared__ float m_s[kAttnWarps][G], l_s[kAttnWarps][G];
-  __shared__ __align__(16) float o_s[kAttnWarps][G][D];
+  // value blocks staged per warp during the loop; the warps' partials after it
+  __shared__ __align__(16) uint8_t u_s[kUnion];
 
   const int split = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -98,24 +108,43 @@ __global__ void __launch_bounds__(kAttnWarps * 32) decode_attention_kernel(const
 #pragma unroll
     for (int i = 0; i < DL; ++i) o[g][i] = 0.0f;
   }
+  uint8_t* vstage = u_s + warp * kStageBytes;
 
   for (int64_t blk = t0 + 32 * warp; blk < t1; blk += 32 * kAttnWarps) {
-    // ---- scores, lane-per-token
     const int64_t t = blk + lane;
     const bool valid = t < t1;
+    // every load of the block first (one memory round trip): this lane's
+    // token's key row and scales, and its value row and scales (staged below)
+    uint4 kr[KC], vr[KC];
+    uint32_t ks[(SB + 3) / 4], vs[(SB + 3) / 4];
+    if (valid) {
+      const uint8_t* krow = a.k_packed + (row0 + t) * KB;
+      const uint8_t* vrow = a.v_packed + (row0 + t) * KB;
+#pragma unroll
+      for (int c = 0; c < KC; ++c) {
+        kr[c] = *reinterpret_cast<const uint4*>(krow + 16 * c);
+        vr[c] = *reinterpret_cast<const uint4*>(vrow + 16 * c);
+      }
+      const uint8_t* ksrow = a.k_scales + (row0 + t) * SB;
+      const uint8_t* vsrow = a.v_scales + (row0 + t) * SB;
+#pragma unroll
+      for (int i = 0; i < (SB + 3) / 4; ++i) {
+        if constexpr (SB >= 4) {
+          ks[i] = *reinterpret_cast<const uint32_t*>(ksrow + 4 * i);
+          vs[i] = *reinterpret_cast<const uint32_t*>(vsrow + 4 * i);
+        }
+      }
+    }
+    // ---- scores, lane-per-token
     float s[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) s[g] = valid ? 0.0f : -INFINITY;
     if (valid) {
-      const uint8_t* krow = a.k_packed + (row0 + t) * KB;
-      const uint8_t* srow = a.k_scales + (row0 + t) * SB;
-#pragma unroll 1
-      for (int c = 0; c < KB / 16; ++c) {           // 32 elements = two scale blocks
-        const uint4 code = *reinterpret_cast<const uint4*>(krow + 16 * c);
-        const uint32_t sc2 = *reinterpret_cast<const uint16_t*>(srow + 2 * c);
-        const uint32_t w[4] = {code.x, code.y, code.z, code.w};
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {      // one scale block: words 2 half, 2 half + 1
+      for (int c = 0; c < KC; ++c) {                 // 32 elements = two scale blocks
+        const uint32_t w[4] = {kr[c].x, kr[c].y, kr[c].z, kr[c].w};
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
           float part[G];
 #pragma unroll
           for (int g = 0; g < G; ++g) part[g] = 0.0f;
@@ -134,11 +163,21 @@ __global__ void __launch_bounds__(kAttnWarps * 32) decode_attention_kernel(const
               }
             }
           }
-          const float sf = e4m3_to_float(sc2 >> (8 * half));
+          const int blk16 = 2 * c + half;            // scale block of these 16 elements
+          const float sf = e4m3_to_float(ks[blk16 / 4] >> (8 * (blk16 % 4)));
 #pragma unroll
           for (int g = 0; g < G; ++g) s[g] = fmaf(part[g], sf, s[g]);
         }
       }
+    }
+    // ---- stage the value rows: row `lane` of the block at lane * kVRow
+    __syncwarp();                                    // the previous block's reads are done
+    if (valid) {
+#pragma unroll
+      for (int c = 0; c < KC; ++c) *reinterpret_cast<uint4*>(vstage + lane * kVRow + 16 * c) = vr[c];
+#pragma unroll
+      for (int i = 0; i < SB / 4; ++i)
+        *reinterpret_cast<uint32_t*>(vstage + lane * kVRow + KB + 4 * i) = vs[i];
     }
     // ---- online softmax over the block (base 2)
     float p[G];
@@ -152,18 +191,19 @@ __global__ void __launch_bounds__(kAttnWarps * 32) decode_attention_kernel(const
       for (int i = 0; i < DL; ++i) o[g][i] *= corr;
       m[g] = mn;
     }
-    // ---- values, lane-per-dimension
+    __syncwarp();                                    // the staged rows are visible
+    // ---- values, lane-per-dimension, from the staged rows
     const int nt = static_cast<int>(min(static_cast<int64_t>(32), t1 - blk));
     for (int tt = 0; tt < nt; ++tt) {
-      const int64_t row = row0 + blk + tt;
-      const uint8_t* vrow = a.v_packed + row * KB + lane * (DL / 2);
-      const float sf = e4m3_to_float(a.v_scales[row * SB + (lane * DL) / 16]);
+      const uint8_t* vrow = vstage + tt * kVRow;
+      const float sf = e4m3_to_float(vrow[KB + (lane * DL) / 16]);
+      const uint8_t* vc = vrow + lane * (DL / 2);
       uint32_t codes[(DL / 2 + 3) / 4];
-      if constexpr (DL / 2 == 1) codes[0] = *vrow;
-      else if constexpr (DL / 2 == 2) codes[0] = *reinterpret_cast<const uint16_t*>(vrow);
-      else if constexpr (DL / 2 == 4) codes[0] = *reinterpret_cast<const uint32_t*>(vrow);
+      if constexpr (DL / 2 == 1) codes[0] = *vc;
+      else if constexpr (DL / 2 == 2) codes[0] = *reinterpret_cast<const uint16_t*>(vc);
+      else if constexpr (DL / 2 == 4) codes[0] = *reinterpret_cast<const uint32_t*>(vc);
       else {
-        const uint2 c2 = *reinterpret_cast<const uint2*>(vrow);
+        const uint2 c2 = *reinterpret_cast<const uint2*>(vc);
         codes[0] = c2.x;
         codes[1] = c2.y;
       }
@@ -183,6 +223,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32) decode_attention_kernel(const
   }
 
   // ---- merge the warps, write this split's partial
+  __syncthreads();                                   // staging space becomes the merge buffer
+  float (*o_s)[G][D] = reinterpret_cast<float (*)[G][D]>(u_s);
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     if (lane == 0) {

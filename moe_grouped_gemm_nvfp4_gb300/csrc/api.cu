@@ -11,6 +11,7 @@
 
 #include "../../include/nvfp4.h"
 #include "kernels.h"
+#include "attention.h"
 
 namespace {
 

@@ -25,6 +25,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "attention.h"
 
 namespace nvfp4 {
 

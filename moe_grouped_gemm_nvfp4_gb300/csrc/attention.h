@@ -1,0 +1,41 @@
+// Launch arguments of the decode-attention kernels, shared between
+// attention.cu and the C ABI layer.  Not part of the public interface.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace nvfp4 {
+
+struct AttnArgs {
+  const uint16_t* q;               // BF16 [B, Hq, D]
+  const uint8_t* k_packed;         // [B, Hkv, L_max, D/2]
+  const uint8_t* k_scales;         // [B, Hkv, L_max, D/16] E4M3
+  const uint8_t* v_packed;
+  const uint8_t* v_scales;
+  const float* gk;                 // device globals of the K and V caches
+  const float* gv;
+  const int32_t* seq_lens;         // [B]
+  int32_t B, Hq, Hkv;
+  int64_t L_max;
+  int32_t chunk;                   // tokens per split
+  int32_t splits;                  // ceil(L_max / chunk)
+  float scale;                     // softmax scale
+  uint16_t* out;                   // BF16 [B, Hq, D]
+  float* ws_o;                     // [B, Hq, splits, D] partial weighted values
+  float* ws_ml;                    // [B, Hq, splits, 2] partial max (base 2) and sum
+  int* status;
+};
+
+// Tokens per split of the decode attention: the smallest power of two from
+// 128 up to 4096 that leaves about a thousand (sequence, KV head, split)
+// CTAs at most.  A function of the shape only, so that the workspace size is.
+inline int attention_chunk(int64_t L_max, int64_t B, int64_t Hkv) {
+  const int64_t want = (L_max * B * Hkv + 1023) / 1024;
+  int ch = 128;
+  while (ch < want && ch < 4096) ch <<= 1;
+  return ch;
+}
+cudaError_t launch_decode_attention(const AttnArgs& a, int D, cudaStream_t s);
+
+}  // namespace nvfp4

@@ -21,9 +21,12 @@ def _device_weights(E, N, K, seed):
     return w
 
 
-def _oracle_weight_rows(w_dev, e, cols):
-    """Oracle-quantised rows `cols` of expert e (global scale over all of W_e)."""
+def _oracle_weight_rows(w_dev, e, cols, sparse=False):
+    """Oracle-quantised rows `cols` of expert e (global scale over all of W_e;
+    sparse: W_e pruned to 2:4 over element pairs first)."""
     we = w_dev[e].float().cpu().numpy()
+    if sparse:
+        we = oracle.prune_pairs_2of4(we)
     ge = oracle.global_scale(we)
     p, s, _ = oracle.quantize(we[cols], g=ge)
     return oracle.dequantize(p, s, ge)
@@ -35,7 +38,7 @@ def _routing_for(cfg, g):
     return inputs.uniform_topk(g, cfg.T, cfg.E, cfg.topk)
 
 
-def _gate_up_case(cfg, n_route_samples, n_col_samples, experts_pick):
+def _gate_up_case(cfg, n_route_samples, n_col_samples, experts_pick, sparse=False):
     g = inputs.rng(cfg.seed)
     xf = g.standard_normal((cfg.T, cfg.K), dtype=np.float32)
     if cfg.outliers:
@@ -43,7 +46,7 @@ def _gate_up_case(cfg, n_route_samples, n_col_samples, experts_pick):
     x = inputs.to_bf16(xf)
     ids = _routing_for(cfg, g)
     w = _device_weights(cfg.E, cfg.N, cfg.K, cfg.seed)
-    W = moe.quantize_experts(w)
+    W = moe.quantize_experts_sparse(w) if sparse else moe.quantize_experts(w)
     plan = moe.GroupedPlan(W, cfg.T, cfg.topk, "gather")
     plan.out.view(torch.int16).fill_(0x7FC0)
     out = plan.run(x.cuda(), torch.from_numpy(ids).cuda())
@@ -68,7 +71,7 @@ def _gate_up_case(cfg, n_route_samples, n_col_samples, experts_pick):
             rest = sel.choice(p.size, n_route_samples, replace=False)
             p = p[np.unique(np.concatenate([edges, rest]))]
         px, sx, _ = oracle.quantize(x_np[tok[p]], g=gx)
-        ref = oracle.dequantize(px, sx, gx) @ _oracle_weight_rows(w, e, cols).T
+        ref = oracle.dequantize(px, sx, gx) @ _oracle_weight_rows(w, e, cols, sparse).T
         got = bf16_to_np(out[torch.from_numpy(p).cuda()][:, torch.from_numpy(cols).cuda()])
         check_gemm(got, ref, f"{cfg.name} expert {e} ({hi - lo} routes)")
     # nothing left unwritten anywhere in the route-ordered output
@@ -78,6 +81,14 @@ def _gate_up_case(cfg, n_route_samples, n_col_samples, experts_pick):
 def test_decode_gate_up_full():
     cfg = inputs.CONFIGS["decode_gate_up"]
     _gate_up_case(cfg, 64, 256, lambda c: [int(np.argmax(c)), int(np.argmin(c)), 0, 77])
+
+
+def test_decode_gate_up_sparse_full():
+    """The same workload with the weights pruned to 2:4 and streamed as sparse
+    tiles (32-route token tiles, two weight tiles per unit)."""
+    cfg = inputs.CONFIGS["decode_gate_up"]
+    _gate_up_case(cfg, 64, 256, lambda c: [int(np.argmax(c)), int(np.argmin(c)), 0, 77],
+                  sparse=True)
 
 
 def test_prefill_skewed_full():
@@ -91,8 +102,9 @@ def test_prefill_skewed_full():
                              int(np.argmin(np.where(c > 0, c, 1 << 30)))])
 
 
-@pytest.mark.parametrize("name", ["decode_down_256", "decode_down_512", "decode_down_1024"])
-def test_decode_down_full(name):
+@pytest.mark.parametrize("name,sparse", [("decode_down_256", False), ("decode_down_512", False),
+                                         ("decode_down_1024", False), ("decode_down_512", True)])
+def test_decode_down_full(name, sparse):
     cfg = inputs.CONFIGS[name]
     g = inputs.rng(cfg.seed)
     ids = inputs.uniform_topk(g, cfg.T, cfg.E, cfg.topk)
@@ -100,7 +112,7 @@ def test_decode_down_full(name):
     R = cfg.T * cfg.topk
     h = inputs.normal_bf16(g, (R, cfg.K))
     w = _device_weights(cfg.E, cfg.N, cfg.K, cfg.seed)
-    W = moe.quantize_experts(w)
+    W = moe.quantize_experts_sparse(w) if sparse else moe.quantize_experts(w)
     plan = moe.GroupedPlan(W, cfg.T, cfg.topk, "combine")
     plan.out.view(torch.int16).fill_(0x7FC0)
     out = plan.run(h.cuda(), torch.from_numpy(ids).cuda(), torch.from_numpy(wts).cuda())
@@ -118,7 +130,7 @@ def test_decode_down_full(name):
         for p in np.nonzero(tok == t)[0]:
             e = int(np.searchsorted(off, p, side="right") - 1)
             ph, sh, _ = oracle.quantize(h_np[p:p + 1], g=gh)
-            y = oracle.dequantize(ph, sh, gh) @ _oracle_weight_rows(w, e, cols).T
+            y = oracle.dequantize(ph, sh, gh) @ _oracle_weight_rows(w, e, cols, sparse).T
             ref[i] += np.float64(wts[t, slot[p]]) * y[0]
     got = bf16_to_np(out[torch.from_numpy(tokens).cuda()][:, torch.from_numpy(cols).cuda()])
-    check_gemm(got, ref, name)
+    check_gemm(got, ref, name + (" sparse" if sparse else ""))

@@ -52,6 +52,17 @@ __device__ __forceinline__ float e4m3_to_float(uint32_t byte) {
   return __low2float(v);
 }
 
+// Two FP32 fused multiply-adds in one instruction: (a.x b.x + c.x, a.y b.y + c.y).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 r;
+  asm("{\n\t.reg .b64 pa, pb, pc, pd;\n\t"
+      "mov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\tmov.b64 pc, {%6, %7};\n\t"
+      "fma.rn.f32x2 pd, pa, pb, pc;\n\tmov.b64 {%0, %1}, pd;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return r;
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
@@ -146,9 +157,9 @@ __global__ void __launch_bounds__(kAttnWarps * 32) decode_attention_kernel(const
         const uint32_t w[4] = {kr[c].x, kr[c].y, kr[c].z, kr[c].w};
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-          float part[G];
+          float2 part[G];                            // even / odd elements' partial sums
 #pragma unroll
-          for (int g = 0; g < G; ++g) part[g] = 0.0f;
+          for (int g = 0; g < G; ++g) part[g] = make_float2(0.0f, 0.0f);
 #pragma unroll
           for (int wi = 0; wi < 2; ++wi) {
             const uint32_t word = w[2 * half + wi];
@@ -157,17 +168,14 @@ __global__ void __launch_bounds__(kAttnWarps * 32) decode_attention_kernel(const
               const float2 e = e2m1x2_to_float2(word >> (8 * by));
               const int d = 32 * c + 16 * half + 8 * wi + 2 * by;
 #pragma unroll
-              for (int g = 0; g < G; ++g) {
-                const float2 qq = *reinterpret_cast<const float2*>(&q_s[g][d]);
-                part[g] = fmaf(qq.x, e.x, part[g]);
-                part[g] = fmaf(qq.y, e.y, part[g]);
-              }
+              for (int g = 0; g < G; ++g)
+                part[g] = ffma2(*reinterpret_cast<const float2*>(&q_s[g][d]), e, part[g]);
             }
           }
           const int blk16 = 2 * c + half;            // scale block of these 16 elements
           const float sf = e4m3_to_float(ks[blk16 / 4] >> (8 * (blk16 % 4)));
 #pragma unroll
-          for (int g = 0; g < G; ++g) s[g] = fmaf(part[g], sf, s[g]);
+          for (int g = 0; g < G; ++g) s[g] = fmaf(part[g].x + part[g].y, sf, s[g]);
         }
       }
     }
@@ -208,16 +216,20 @@ __global__ void __launch_bounds__(kAttnWarps * 32) decode_attention_kernel(const
         codes[0] = c2.x;
         codes[1] = c2.y;
       }
-      float wgt[G];
+      float2 wgt[G];
 #pragma unroll
-      for (int g = 0; g < G; ++g) wgt[g] = __shfl_sync(0xFFFFFFFFu, p[g], tt) * sf;
+      for (int g = 0; g < G; ++g) {
+        const float w1 = __shfl_sync(0xFFFFFFFFu, p[g], tt) * sf;
+        wgt[g] = make_float2(w1, w1);
+      }
 #pragma unroll
       for (int i = 0; i < DL / 2; ++i) {
         const float2 e = e2m1x2_to_float2(codes[i / 4] >> (8 * (i % 4)));
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          o[g][2 * i] = fmaf(wgt[g], e.x, o[g][2 * i]);
-          o[g][2 * i + 1] = fmaf(wgt[g], e.y, o[g][2 * i + 1]);
+          const float2 r = ffma2(wgt[g], e, make_float2(o[g][2 * i], o[g][2 * i + 1]));
+          o[g][2 * i] = r.x;
+          o[g][2 * i + 1] = r.y;
         }
       }
     }

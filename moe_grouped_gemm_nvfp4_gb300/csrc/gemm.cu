@@ -58,7 +58,8 @@ struct Cfg {
   // MT 128-row X tiles per unit (2 only for 32-row token tiles: two MMAs per
   // K step share the token operand, halving the units, the token re-reads
   // and the scale copies of Y per weight byte)
-  // (64-row tiles with two X tiles serve only the fused SiLU-mul epilogue)
+  // (64-row tiles with two X tiles serve the fused SiLU-mul epilogue and
+  // sparse weights)
   static_assert(MT == 1 || (MT == 2 && (BN == 32 || BN == 64)), "unit height");
   // SP: X (the weights) arrives as 2:4-sparse tiles and is expanded in shared
   // memory by the decompression warps before the MMAs read it
@@ -1047,8 +1048,6 @@ cudaError_t launch_gemm(const CUtensorMap& tmx, const CUtensorMap& tmy, const Ge
     return bn == 256 ? launch_bn<256>(tmx, tmy, a, mode, grid, s)
                      : launch_bn<128>(tmx, tmy, a, mode, grid, s);
   }
-  // gate and up tiles pair up in one unit of 32 or 64 routes (<64, 2> serves
-  // only this mode: its single accumulator buffer has no other epilogue)
   // 2:4-sparse weights (gather or combine): token tiles of the activation
   // layout's chunk width (128 for prefill shapes)
   if (a.sparse_w) {
@@ -1062,6 +1061,8 @@ cudaError_t launch_gemm(const CUtensorMap& tmx, const CUtensorMap& tmy, const Ge
       default: return launch_bn<128, 1, true>(tmx, tmy, a, mode, grid, s);
     }
   }
+  // gate and up tiles pair up in one unit of 32 or 64 routes (with dense
+  // weights, <64, 2> serves only this mode)
   if (mode == kGroupedSiluMul)
     return grouped_tile_width(a.rows_y, a.E) == 32 ? launch_bn<32, 2>(tmx, tmy, a, mode, grid, s)
                                                    : launch_bn<64, 2>(tmx, tmy, a, mode, grid, s);

@@ -120,17 +120,21 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def normalised_source(src):
+    """C++ source without comments, runs of blank space as one space."""
+    import re
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
+
+
 def kernel_source_hash():
     """Hash of the GEMM kernel's sources with comments and blank space taken
     out, so that edits to comments keep the recorded counters valid."""
-    import re
     h = hashlib.sha256()
     for f in ("gemm.cu", "common.cuh", "kernels.h"):
         with open(os.path.join(ROOT, "moe_grouped_gemm_nvfp4_gb300", "csrc", f)) as fh:
-            src = fh.read()
-        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
-        src = re.sub(r"//[^\n]*", " ", src)
-        h.update(" ".join(src.split()).encode())
+            h.update(normalised_source(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

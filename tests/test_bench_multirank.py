@@ -1,5 +1,6 @@
-"""The benchmark's multi-rank bookkeeping (replicas, max over ranks) on two
-gloo ranks on the CPU."""
+"""The benchmark's bookkeeping on the CPU: multi-rank replicas (max over
+ranks, two gloo ranks), byte accounting, and the source hash that keeps
+recorded counters tied to the kernel they were taken on."""
 import os
 import socket
 
@@ -49,3 +50,28 @@ def test_aggregate_is_all_ranks_work_over_slowest_time():
     # 2 ranks x 100 steps x 1e12 FLOP in 200 ms (the slower rank) -> 1000 TFLOPS
     assert bench.aggregate_tflops(1e12, 100, 200.0, 2) == pytest.approx(1000.0)
     assert bench.aggregate_tflops(1e12, 100, 200.0, 1) == pytest.approx(500.0)
+
+
+def test_sparse_byte_accounting():
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    K, N, E, R = 6144, 4096, 128, 2048
+    dense, sparse = bench.gemm_bytes(K, N, E, R, R), bench.sparse_gemm_bytes(K, N, E, R, R)
+    io = bench.gemm_bytes(K, N, 0, R, R)
+    assert io == bench.sparse_gemm_bytes(K, N, 0, R, R)
+    # weights: 0.375 B per element sparse (kept codes, indices, scales), 0.5625 dense
+    assert (sparse - io) * 0.5625 == pytest.approx((dense - io) * 0.375)
+    assert bench.step_bytes(E, sparse=True) < bench.step_bytes(E)
+
+
+def test_source_hash_ignores_comments_only():
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    a = "int f(int x) {\n  return x + 1;  // one\n}\n"
+    b = "/* doc */ int f(int x) {\n\n  return x + 1;\n}  // trailing\n"
+    c = "int f(int x) {\n  return x + 2;\n}\n"
+    assert bench.normalised_source(a) == bench.normalised_source(b)
+    assert bench.normalised_source(a) != bench.normalised_source(c)
+    assert bench.kernel_source_hash() == bench.kernel_source_hash()

@@ -6,7 +6,8 @@
 // Investigation", The Comprehensive Synthesis: A/B FP4 tiles plus their
 // scale-factor tiles staged through shared memory over several stages).
 //
-// Roles of the 224 threads of a CTA (one CTA per SM):
+// Roles of the warps of a CTA (one CTA per SM; 224 threads for dense weights
+// and token tiles up to 128 wide):
 //   warp 0      TMA producer: operand tiles (128-byte swizzle) and scale
 //               atoms into a ring of shared-memory stages;
 //   warp 1      tensor-memory allocation; lane 0 issues tcgen05.cp (scales

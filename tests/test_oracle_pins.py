@@ -516,3 +516,87 @@ def test_silu_mul_uses_the_first_half_as_gate():
     h2 = oracle.silu_mul(np.concatenate([up, gate], axis=1))
     assert not np.allclose(h2, h)
     assert np.allclose(h2, oracle.silu(1.0) * gate)
+
+
+# ------------------------------------------- grouped GEMM across experts ----
+
+def _expert_of_route(off, p):
+    """The expert whose route range [off[e], off[e+1]) holds p, by a linear scan."""
+    for e in range(len(off) - 1):
+        if int(off[e]) <= p < int(off[e + 1]):
+            return e
+    raise AssertionError(f"route {p} outside every expert range")
+
+
+def test_grouped_gemm_many_experts_matches_per_route_exact_rationals():
+    """Several experts with uneven counts and an empty one: every route's row
+    is the exact rational dot product of its decoded activation with the rows
+    of its own expert's decoded weight ("The FP4 Frontier", Finding 5: one
+    grouped GEMM over all experts).  A wrong expert index or an off-by-one in
+    the offset slices changes rows of distinct random weights, so it fails."""
+    g = inputs.rng(47)
+    E, N, K = 4, 3, 32
+    # uneven routing: expert 0 gets 4 routes, expert 1 none, expert 2 one,
+    # expert 3 five (tokens 0..4, top-2)
+    ids = np.array([[0, 3], [3, 0], [0, 3], [3, 2], [0, 3]], np.int32)
+    T = ids.shape[0]
+    x = inputs.normal_bf16(g, (T, K)).float().numpy()
+    w = inputs.normal_bf16(g, (E, N, K), 0.5).float().numpy()
+    off, tok, slot = oracle.route(ids, E)
+    assert [int(off[e + 1] - off[e]) for e in range(E)] == [4, 0, 1, 5]
+    xh = oracle.dequantize(*oracle.quantize(x))[tok]
+    wh = np.stack([oracle.dequantize(*oracle.quantize(w[e])) for e in range(E)])
+    y = oracle.grouped_gemm(xh, wh, off)
+    gamma = (K + 1) * 2.0 ** -53 / (1 - (K + 1) * 2.0 ** -53)
+    for p in range(T * 2):
+        e = _expert_of_route(off, p)
+        assert ids[tok[p], slot[p]] == e            # the route really belongs to e
+        for n in range(N):
+            terms = [Fraction(float(xh[p, k])) * Fraction(float(wh[e, n, k])) for k in range(K)]
+            exact = sum(terms)
+            bound = Fraction(gamma) * sum(abs(t) for t in terms)
+            assert abs(Fraction(float(y[p, n])) - exact) <= bound, (p, n)
+    # and a neighbouring expert's weights would give a different row
+    for p in range(T * 2):
+        e = _expert_of_route(off, p)
+        for e2 in range(E):
+            if e2 != e:
+                assert not np.allclose(y[p], xh[p] @ wh[e2].T)
+
+
+# ------------------------------------------------- global scale rounding ----
+
+def _rne_binary32(q: Fraction) -> float:
+    """The binary32 value nearest to the positive rational q (ties to even),
+    by integer arithmetic on the exact quotient."""
+    assert q > 0
+    e = q.numerator.bit_length() - q.denominator.bit_length()
+    if Fraction(2) ** e > q:
+        e -= 1                                       # 2^e <= q < 2^(e+1)
+    e = max(e, -126)                                 # subnormals share 2^-149 steps
+    ulp = Fraction(2) ** (e - 23)
+    m = q / ulp                                      # significand in units of ulp
+    lo = m.numerator // m.denominator
+    rem = m - lo
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and lo % 2 == 1):
+        lo += 1
+    return float(lo * ulp)
+
+
+def test_global_scale_is_one_rounding_of_amax_over_2688():
+    """g = tensor_amax / (6 * 448) as ONE binary32 division (reading of the
+    recipe "global = tensor_amax / (6 * 448)"; 2688 is exact).  The test
+    searches amax values where one rounding of the exact quotient and the
+    two-step (amax / 6) / 448 disagree, and checks the oracle against the
+    exact quotient rounded by integer arithmetic."""
+    g = inputs.rng(53)
+    cands = g.uniform(1.0, 1000.0, 4000).astype(np.float32)
+    found = 0
+    for a in cands:
+        exact = _rne_binary32(Fraction(float(a)) / 2688)
+        two_step = float(np.float32(np.float32(a) / np.float32(6.0)) / np.float32(448.0))
+        got = float(oracle.global_scale(np.array([[a, -a / 2]], np.float32)))
+        assert got == exact, (float(a), got, exact)
+        if two_step != exact:
+            found += 1
+    assert found >= 10          # the pin separates the two readings on these inputs

@@ -422,32 +422,42 @@ def run_ours(args, rank, world, local_rank):
 
 # --------------------------------------------------------------- CPU oracle
 
-def _oracle_sample(experts, seed_base=2, device=None):
-    """One bounded sample of the workload run by the CPU oracle: route, the
-    activation quantisation of the whole batch, and for the given experts
-    the weight quantisation plus their routes' gate_up and down GEMMs and
-    the combine.  Returns the FLOPs of the GEMMs it computed."""
+def _oracle_batch(seed_base=2):
+    """The per-batch part of the decode pass run by the CPU oracle: routing
+    and the activation quantisation of x and h.  Returns its results and its
+    wall time."""
     import oracle
     g = inputs.rng(seed_base)
     x = inputs.normal_bf16(g, (T, K1)).float().numpy()
     ids = inputs.uniform_topk(g, T, E, TOPK)
     h = inputs.normal_bf16(inputs.rng(seed_base + 1), (T * TOPK, K2)).float().numpy()
     wts = inputs.dirichlet_weights(inputs.rng(seed_base + 1), T, TOPK)
-    flops = 0.0
     t0 = time.perf_counter()
     off, tok, slot = oracle.route(ids, E)
     xh = oracle.dequantize(*oracle.quantize(x))
     hh = oracle.dequantize(*oracle.quantize(h))
-    for e in experts:
-        w1 = _host_weight(seed_base * 100003 + e, (N1, K1))
-        w2 = _host_weight((seed_base + 1) * 100003 + e, (N2, K2))
-        lo, hi = int(off[e]), int(off[e + 1])
-        y1 = xh[tok[lo:hi]] @ oracle.dequantize(*oracle.quantize(w1)).T
-        y2 = hh[lo:hi] @ oracle.dequantize(*oracle.quantize(w2)).T
-        oracle.combine(y2, tok[lo:hi], slot[lo:hi], wts, T)
-        flops += 2.0 * (hi - lo) * (N1 * K1 + N2 * K2)
-        del y1
-    return flops, time.perf_counter() - t0
+    return dict(off=off, tok=tok, slot=slot, xh=xh, hh=hh, wts=wts), time.perf_counter() - t0
+
+
+def _oracle_expert(batch, e, seed_base=2):
+    """One expert of the pass in the CPU oracle: its weight quantisation
+    (offline on the GPU side, timed apart), then its routes' gate_up and down
+    GEMMs and their combine.  Returns (GEMM FLOPs, weight-quantise s, GEMM s)."""
+    import oracle
+    w1 = _host_weight(seed_base * 100003 + e, (N1, K1))
+    w2 = _host_weight((seed_base + 1) * 100003 + e, (N2, K2))
+    t0 = time.perf_counter()
+    w1h = oracle.dequantize(*oracle.quantize(w1))
+    w2h = oracle.dequantize(*oracle.quantize(w2))
+    t1 = time.perf_counter()
+    off, tok = batch["off"], batch["tok"]
+    lo, hi = int(off[e]), int(off[e + 1])
+    y1 = batch["xh"][tok[lo:hi]] @ w1h.T
+    y2 = batch["hh"][lo:hi] @ w2h.T
+    oracle.combine(y2, tok[lo:hi], batch["slot"][lo:hi], batch["wts"], T)
+    t2 = time.perf_counter()
+    del y1
+    return 2.0 * (hi - lo) * (N1 * K1 + N2 * K2), t1 - t0, t2 - t1
 
 
 def _host_weight(seed, shape):
@@ -460,21 +470,34 @@ def _host_weight(seed, shape):
 
 
 def cpu_baseline(W_host_seed=2, budget_s=20.0):
+    """The oracle on the host cores over a bounded sample of the decode pass:
+    the whole batch's routing and activation quantisation, then whole experts
+    until about budget_s seconds have gone.  The value is the sampled GEMM
+    FLOPs over the GEMM time plus the sampled experts' share of the batch
+    quantisation; the weight quantisation (offline on the GPU side) is timed
+    but left out of it."""
+    batch, t_batch = _oracle_batch(W_host_seed)
     experts = []
-    flops, secs = 0.0, 0.0
+    flops, t_wq, t_gemm = 0.0, 0.0, 0.0
     e = 0
-    while secs < budget_s and e < E:
-        f, s = _oracle_sample([e], W_host_seed)
+    while t_batch + t_wq + t_gemm < budget_s and e < E:
+        f, wq, gm = _oracle_expert(batch, e, W_host_seed)
         flops += f
-        secs += s
+        t_wq += wq
+        t_gemm += gm
         experts.append(e)
         e += 1
+    share = t_batch * len(experts) / E
     cores = _blas_threads()
-    return {"value": round(flops / secs / 1e12, 6), "unit": UNIT, "cores": cores,
+    return {"value": round(flops / (t_gemm + share) / 1e12, 6), "unit": UNIT, "cores": cores,
             "kind": "oracle",
+            "activation_quantize_s": round(t_batch, 3), "gemm_s": round(t_gemm, 3),
+            "weight_quantize_s": round(t_wq, 3),
             "sample": f"experts {experts[0]}..{experts[-1]} of the gate_up+down pass "
-                      f"({len(experts)} of {E}); each sample also routes and quantises the "
-                      f"whole batch; {secs:.1f} s of CPU time"}
+                      f"({len(experts)} of {E}): their GEMMs and combine ({t_gemm:.1f} s) plus "
+                      f"{len(experts)}/{E} of the batch's routing and activation quantisation "
+                      f"({t_batch:.1f} s for the batch); their weight quantisation "
+                      f"({t_wq:.1f} s) is offline on the GPU side and left out"}
 
 
 def _blas_threads():
@@ -489,15 +512,19 @@ def _blas_threads():
 
 
 def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step one expert's GEMMs and
+    combine plus 1/E of the batch's routing and activation quantisation."""
     if rank != 0:
         return None
+    batch, t_batch = _oracle_batch()
     for i in range(args.warmup):
-        _oracle_sample([i % E])
-    times, flops = [], 0.0
+        _oracle_expert(batch, i % E)
+    times, flops, t_wq = [], 0.0, 0.0
     for i in range(args.steps):
-        f, s = _oracle_sample([(args.warmup + i) % E])
-        times.append(s)
+        f, wq, gm = _oracle_expert(batch, (args.warmup + i) % E)
+        times.append(gm + t_batch / E)
         flops += f
+        t_wq += wq
     total = sum(times)
     value = flops / total / 1e12
     return {
@@ -507,10 +534,12 @@ def run_reference(args, rank, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(),
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": _blas_threads(),
-                         "kind": "oracle",
-                         "sample": "each step: one expert's gate_up + down GEMMs, its weight "
-                                   "quantisation, and the route + activation quantisation of "
-                                   "the whole batch"},
+                         "kind": "oracle", "activation_quantize_s": round(t_batch, 3),
+                         "weight_quantize_s": round(t_wq, 3),
+                         "sample": "each step: one expert's gate_up + down GEMMs and combine, "
+                                   "plus 1/E of the batch's routing and activation "
+                                   "quantisation; the expert's weight quantisation is timed "
+                                   "apart and left out (offline on the GPU side)"},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -534,24 +563,57 @@ def _timed(fn, iters, flush):
     return total / iters
 
 
-def run_configs(args):
-    """One JSON line per workload configuration: kernel time with CUDA events,
-    L2 flushed (256 MB write) before every timed call."""
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)
-    peak, peak_kind = measured_peaks()
-    bf16_tflops = None
+def _peaks():
+    """(HBM GB/s, dense FP4 TFLOPS, source): the measured HBM copy rate, and
+    the FP4 peak as 6 x the measured BF16 burst (the nominal dense ratio
+    13.5 / 2.25 PFLOPS)."""
+    hbm, kind = measured_peaks()
+    bf16 = None
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
-            bf16_tflops = json.load(f).get("bf16_tflops")
-    fp4_peak = (bf16_tflops or 1900.0) * 6.0      # nominal dense FP4 / BF16 ratio 13.5 / 2.25
+            bf16 = json.load(f).get("bf16_tflops")
+    return hbm, (bf16 or 1900.0) * 6.0, f"{kind} hbm_gbs; fp4 = 6 x {kind} bf16_tflops"
+
+
+def _entry(ms, flops, byts, hbm, fp4, **extra):
+    """One configuration's figures: time, TFLOPS, GB/s and the achieved
+    fraction of the slower of its two rooflines (max(t_hbm, t_fp4) / t)."""
+    t_mem = byts / (hbm * 1e9)
+    t_cmp = flops / (fp4 * 1e12)
+    d = {"us": round(ms * 1e3, 2), "tflops": round(flops / ms / 1e9, 1),
+         "gbs": round(byts / ms / 1e6, 1), "bound": "hbm" if t_mem >= t_cmp else "fp4",
+         "frac_of_roofline": round(max(t_mem, t_cmp) / (ms * 1e-3), 4),
+         "algorithmic_flops": int(flops), "algorithmic_bytes": int(byts)}
+    d.update(extra)
+    return d
+
+
+def measure_configs(args, dev, groups=None):
+    """Every workload configuration, kernel by kernel: name -> figures.  CUDA
+    events, L2 flushed (256 MB write) before every timed call."""
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    hbm, fp4, peak_src = _peaks()
     iters = max(3, min(args.steps, 20))
-    lines = []
+    out = {}
 
     def want(group):
-        return not args.only or args.only == group
+        return groups is None or group in groups
+
+    # tiny single GEMM (16 x 256 x 512, seed 0): launch-latency bound
+    if want("tiny_gemm"):
+        g = inputs.rng(0)
+        a = inputs.normal_bf16(g, (16, 512)).to(dev)
+        b = inputs.normal_bf16(g, (256, 512), 0.02).to(dev)
+        pa, sa, ga = F.quantize(a, atoms=True)
+        pb, sb, gb = F.quantize(b, atoms=True)
+        C = torch.empty((16, 256), dtype=torch.bfloat16, device=dev)
+        t_g = _timed(lambda: F.nvfp4_gemm(pa, sa, ga, pb, sb, gb, C, 512), iters, flush)
+        t_q = _timed(lambda: F.nvfp4_quantize(a, pa, sa, ga, F.NVFP4_SF_ATOMS), iters, flush)
+        byt = (16 + 256) * 512 * (0.5 + 1 / 16) + 16 * 256 * 2
+        out["tiny_gemm_16x256x512"] = _entry(
+            t_g, 2.0 * 16 * 256 * 512, byt, hbm, fp4, quantize_A_us=round(t_q * 1e3, 2),
+            note="launch-latency bound; the roofline fraction is not meaningful here")
 
     # dense 8192^3: A quantised every call, B prepared offline
     if want("dense_8192"):
@@ -564,14 +626,17 @@ def run_configs(args):
         t_gemm = _timed(lambda: F.nvfp4_gemm(pa, sa, ga, pb, sb, gb, C, Kk), iters, flush)
         t_q = _timed(lambda: F.nvfp4_quantize(a, pa, sa, ga, F.NVFP4_SF_ATOMS), iters, flush)
         fl = 2.0 * M * Nn * Kk
-        lines.append({"workload": "dense_gemm_8192^3", "gemm_ms": round(t_gemm, 4),
-                      "tflops": round(fl / t_gemm / 1e9, 1),
-                      "frac_of_fp4_peak": round(fl / t_gemm / 1e9 / fp4_peak, 4),
-                      "fp4_peak_tflops": fp4_peak, "quantize_A_ms": round(t_q, 4),
-                      "quantize_A_gbs": round(M * Kk * 2.5625 / t_q / 1e6, 1)})
+        gemm_b = (M + Nn) * Kk * (0.5 + 1 / 16) + M * Nn * 2
+        out["dense_gemm_8192^3"] = _entry(t_gemm, fl, gemm_b, hbm, fp4)
+        out["dense_gemm_8192^3_with_quantize_A"] = _entry(
+            t_gemm + t_q, fl, gemm_b + M * Kk * 2, hbm, fp4,
+            note="the GEMM plus the BF16 -> NVFP4 quantisation of A (two launches)")
+        # the activation quantiser alone: 2 B read + 0.5625 B written per element
+        out["quantize_8192x8192"] = _entry(t_q, 0.0, M * Kk * 2.5625, hbm, fp4,
+                                           note="tensor amax + block quantiser, atom scales")
         del a, b, pa, sa, pb, sb, C
 
-    # decode down-projection sweep and skewed prefill gate_up
+    # decode gate_up, down sweep and skewed prefill (and the 2:4-sparse decode shapes)
     for name in ("decode_gate_up", "decode_down_256", "decode_down_512", "decode_down_1024",
                  "prefill_skewed"):
         if not want("decode"):
@@ -582,8 +647,8 @@ def run_configs(args):
         for e in range(cfg.E):
             w[e] = inputs.device_normal_bf16((cfg.N, cfg.K), 0.02, cfg.seed * 100003 + e, dev)
         W = moe.quantize_experts(w)
-        # the same weights pruned to 2:4 over element pairs (decode shapes)
-        W_sp = moe.quantize_experts_sparse(w) if name != "prefill_skewed" else None
+        sparse = want("sparse") and name != "prefill_skewed"
+        W_sp = moe.quantize_experts_sparse(w) if sparse else None
         del w
         if cfg.kind == "down":
             ids = inputs.uniform_topk(g, cfg.T, cfg.E, cfg.topk)
@@ -608,28 +673,22 @@ def run_configs(args):
         n_act = int(np.count_nonzero(counts))
         R = cfg.T * cfg.topk
         fl = 2.0 * R * cfg.N * cfg.K
-        byt = gemm_bytes(cfg.K, cfg.N, n_act, R, cfg.T if cfg.kind == "down" else R)
-        lines.append({"workload": name, "tokens_per_expert": [int(counts.min()), int(counts.max())],
-                      "active_experts": n_act, "gemm_ms": round(t_gemm, 4),
-                      "tflops": round(fl / t_gemm / 1e9, 1), "gbs": round(byt / t_gemm / 1e6, 1),
-                      "frac_of_hbm_roofline": round(byt / t_gemm / 1e6 / peak, 4),
-                      "frac_of_fp4_peak": round(fl / t_gemm / 1e9 / fp4_peak, 4),
-                      "pass_ms_route_quantize_gemm": round(t_all, 4),
-                      "peak_source": f"{peak_kind} hbm_gbs; fp4 = bf16_tflops x 6"})
+        out_rows = cfg.T if cfg.kind == "down" else R
+        byt = gemm_bytes(cfg.K, cfg.N, n_act, R, out_rows)
+        out[name] = _entry(t_gemm, fl, byt, hbm, fp4,
+                           tokens_per_expert=[int(counts.min()), int(counts.max())],
+                           active_experts=n_act,
+                           pass_us_route_quantize_gemm=round(t_all * 1e3, 2))
         if W_sp is not None:
             sp_plan = moe.GroupedPlan(W_sp, cfg.T, cfg.topk, plan.mode, dev, routing_from=plan)
             sp_plan.a_tiles.copy_(plan.a_tiles)
             sp_plan.a_g.copy_(plan.a_g)
             t_sp = _timed(lambda: sp_plan.gemm(wts), iters, flush)
-            byt_sp = sparse_gemm_bytes(cfg.K, cfg.N, n_act, R, cfg.T if cfg.kind == "down" else R)
-            lines.append({"workload": name + "_sparse24", "gemm_ms": round(t_sp, 4),
-                          "dense_equiv_tflops": round(fl / t_sp / 1e9, 1),
-                          "gbs": round(byt_sp / t_sp / 1e6, 1),
-                          "frac_of_hbm_roofline": round(byt_sp / t_sp / 1e6 / peak, 4),
-                          "speedup_vs_dense": round(t_gemm / t_sp, 3),
-                          "note": "weights pruned to 2:4 over element pairs, streamed as sparse "
-                                  "tiles (2/3 of the dense bytes), expanded in shared memory; "
-                                  "dense_equiv_tflops counts the dense GEMM's FLOPs"})
+            byt_sp = sparse_gemm_bytes(cfg.K, cfg.N, n_act, R, out_rows)
+            out[name + "_sparse24"] = _entry(
+                t_sp, fl, byt_sp, hbm, fp4, speedup_vs_dense=round(t_gemm / t_sp, 3),
+                note="weights pruned to 2:4 over element pairs, streamed as sparse tiles (2/3 "
+                     "of the dense bytes); TFLOPS count the dense GEMM's FLOPs")
             del sp_plan
         del W, W_sp, plan
         torch.cuda.empty_cache()
@@ -654,12 +713,13 @@ def run_configs(args):
         t_fused = _timed(lambda: mlp.step(d["x"], d["ids"], d["wts"]), iters, flush)
         t_split = _timed(lambda: layer.step(d["x"], d["ids"], d["h"], d["wts"]), iters, flush)
         fl = 2.0 * tokens * TOPK * (N1 * K1 + N2 * K2)
-        lines.append({"workload": f"decode_mlp_fused_T{tokens}", "pass_ms": round(t_fused, 4),
-                      "tflops": round(fl / t_fused / 1e9, 1),
-                      "unfused_pass_ms": round(t_split, 4),
-                      "note": "route + quantise x + fused gate_up/SiLU/quantise-h + down with "
-                              "combine; unfused = the same pass with a BF16 gate_up output and h "
-                              "quantised by its own kernels (h drawn at random there)"})
+        n_act = int(np.count_nonzero(np.bincount(host["ids"].numpy().reshape(-1), minlength=E)))
+        byt = n_act * (N1 * K1 + N2 * K2) * 0.5625 + 2.0 * (tokens * K1 + tokens * N2)
+        out[f"decode_mlp_fused_T{tokens}"] = _entry(
+            t_fused, fl, byt, hbm, fp4, unfused_pass_us=round(t_split * 1e3, 2),
+            note="route + quantise x + fused gate_up/SiLU/quantise-h + down with combine; "
+                 "unfused = the same pass with a BF16 gate_up output and h quantised by its "
+                 "own kernels")
         del layer, mlp, W1, W2, d, gu_out, gate, up
         torch.cuda.empty_cache()
     # decode attention over an NVFP4 KV cache (every cache byte read once):
@@ -679,17 +739,26 @@ def run_configs(args):
         plan = attention.DecodeAttention(B_, Hq_, Hkv_, L_, D_, dev)
         t_att = _timed(lambda: plan.run(q, kq, vq, seq, 1.0 / D_ ** 0.5), iters, flush)
         byt = 2.0 * B_ * Hkv_ * L_ * D_ * (0.5 + 1.0 / 16) + 2.0 * 2 * B_ * Hq_ * D_
-        lines.append({"workload": f"decode_attention_B{B_}_Hq{Hq_}_Hkv{Hkv_}_L{L_}_D{D_}",
-                      "ms": round(t_att, 4), "gbs": round(byt / t_att / 1e6, 1),
-                      "frac_of_hbm_roofline": round(byt / t_att / 1e6 / peak, 4),
-                      "cache_bytes": int(byt),
-                      "note": "one query token per sequence; K and V in NVFP4 (codes + E4M3 "
-                              "scales along D + one global each), dequantised in registers; "
-                              "split-KV partials merged by a second kernel (both timed)"})
+        fl = 4.0 * B_ * Hq_ * L_ * D_
+        out[f"decode_attention_B{B_}_Hq{Hq_}_Hkv{Hkv_}_L{L_}_D{D_}"] = _entry(
+            t_att, fl, byt, hbm, fp4,
+            note="one query token per sequence; K and V in NVFP4 (codes + E4M3 scales along "
+                 "D + one global each); split-KV partials merged by a second kernel (both "
+                 "timed)")
         del kq, vq, plan
         torch.cuda.empty_cache()
-    for ln in lines:
-        print(json.dumps(ln), flush=True)
+    for v in out.values():
+        v.setdefault("peak_source", peak_src)
+    return out
+
+
+def run_configs(args):
+    """One JSON line per workload configuration (not the headline)."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    groups = None if not args.only else set(args.only.split(","))
+    for name, v in measure_configs(args, dev, groups).items():
+        print(json.dumps({"workload": name, **v}), flush=True)
 
 
 def main():
@@ -702,8 +771,10 @@ def main():
                     help="configs: one line per workload configuration (not the headline)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default=None,
-                    help="configs: run only this group (dense_8192, decode, fused_mlp, "
-                         "decode_attention)")
+                    help="configs: run only these comma-separated groups (tiny_gemm, "
+                         "dense_8192, decode, sparse, fused_mlp, decode_attention)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="leave the per-configuration table out of the headline line")
     ap.add_argument("--sparse", action="store_true",
                     help="the decode step with the weights pruned to 2:4 and streamed as "
                          "sparse tiles (not the headline)")
@@ -728,6 +799,19 @@ def main():
         line = run_reference(args, rank, world)
     else:
         line = run_ours(args, rank, world, local_rank)
+        if line is not None and world == 1 and not args.no_configs and not args.sparse:
+            # every workload configuration, kernel by kernel, beside the headline
+            dev = torch.device("cuda", local_rank)
+            torch.cuda.empty_cache()
+            sampler = ClockSampler(local_rank)
+            sampler.start()
+            t0 = time.time()
+            cfgs = measure_configs(args, dev)
+            cfgs["wall_s"] = round(time.time() - t0, 1)
+            cfgs["clocks"] = sampler.stop()
+            cfgs["timing"] = ("CUDA events around each call, L2 flushed (256 MB write) before "
+                              "every timed call; mean of min(steps, 20) calls")
+            line["configs"] = cfgs
     if line is not None:
         print(json.dumps(line), flush=True)
     if world > 1 and args.impl == "ours":

@@ -105,7 +105,10 @@ size_t nvfp4_prepacked_scales_bytes(int64_t rows, int64_t kblk);
 
 /*
  * BF16 -> NVFP4 quantiser (per-16 amax, E4M3 block scale, E2M1 round to
- * nearest even, pack).
+ * nearest even, pack): the dual-tier scaling of "The Blackwell architectural
+ * split", Preserving precision -- one FP32 global scale per tensor and one
+ * block scale per 16 values -- applied to activations as they arrive in BF16
+ * ("The SM120 FP4 GEMM Kernel Investigation", The Context).
  *   x        BF16 [rows, cols], row stride `ld` elements (ld >= cols);
  *            cols % 16 == 0 (cols % 64 == 0 with NVFP4_SF_ATOMS).
  *   packed   uint8 [rows, cols/2] out, row-major, dense.
@@ -125,7 +128,11 @@ nvfp4_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t l
 /*
  * Rewrites row-major E4M3 scales [rows, kblk] (kblk = K/16, kblk % 4 == 0)
  * into the atom layout (nvfp4_atom_scales_bytes(rows, 16 * kblk) bytes);
- * padding rows are written as zero.  Offline step for weights.
+ * padding rows are written as zero.  Offline step for weights: the block
+ * scales of "The Blackwell architectural split", Preserving precision, staged
+ * as the scale-factor tiles the block-scaled MMA reads ("The SM120 FP4 GEMM
+ * Kernel Investigation", The Comprehensive Synthesis: scale-factor tiles
+ * beside the A/B FP4 tiles).
  */
 nvfp4_status nvfp4_prepack_weights(const uint8_t* scales_rowmajor, int64_t rows,
                                    int64_t kblk, uint8_t* scales_atoms, void* stream);
@@ -133,7 +140,10 @@ nvfp4_status nvfp4_prepack_weights(const uint8_t* scales_rowmajor, int64_t rows,
 /*
  * Single NVFP4 GEMM: C[M, N] (BF16, row stride ldc elements) =
  * (*gA) * (*gB) * A_hat . B_hat^T, FP32 accumulation in tensor memory,
- * BF16 round-to-nearest-even output.
+ * BF16 round-to-nearest-even output.  A_hat = e2m1 * e4m3 * global, the
+ * dual-tier dequantisation of "The Blackwell architectural split",
+ * Preserving precision; the large-GEMM case is the one "The Tile That Didn't
+ * Fit", The Core Finding, measures against the FP4 tensor peak.
  *   A  packed [M, K/2], sfA atom layout for [M, K];
  *   B  packed [N, K/2], sfB atom layout for [N, K];
  *   K % 64 == 0, M, N >= 1, ldc >= N; A, B, sfA, sfB 16-byte aligned, C
@@ -157,7 +167,10 @@ nvfp4_status nvfp4_gemm(const uint8_t* A, const uint8_t* sfA, const float* gA,
  *   route_pos       int32 [T*topk] out (may be NULL): sorted position of the
  *                   route t*topk + slot
  * E <= 1024.  An id out of range sets NVFP4_ERR_DEVICE_CHECK on the device
- * and the route is dropped (expert_offsets[E] < T*topk then).
+ * and the route is dropped: expert_offsets[E] < T*topk then, route_token and
+ * route_slot past expert_offsets[E] are left unwritten (undefined), and
+ * route_pos of the dropped route is -1.  Every consumer in this library
+ * reads only positions below expert_offsets[E].
  */
 nvfp4_status nvfp4_moe_route(const int32_t* topk_ids, int64_t T, int32_t topk, int32_t E,
                              int32_t* expert_offsets, int32_t* route_token,
@@ -244,14 +257,58 @@ nvfp4_status nvfp4_amax_partials(const void* x, int64_t rows, int64_t K, int64_t
 /* Bytes of the FP32 combine workspace for T tokens and N outputs. */
 size_t nvfp4_combine_workspace_bytes(int64_t T, int64_t N);
 
-/* The same as nvfp4_combine_workspace_bytes(T, N): FP32 [T, N]. */
-size_t nvfp4_grouped_gemm_workspace_bytes(int64_t T, int64_t N);
+/*
+ * Workspace bytes of nvfp4_grouped_gemm for T tokens, top-k, E experts, N
+ * outputs and depth K: the activation operand tiles of the R = T * topk
+ * routes (nvfp4_grouped_tiles_bytes without its scratch), plus, when combine
+ * != 0 (topk_weights given), the FP32 sums [T, N].
+ */
+size_t nvfp4_grouped_gemm_workspace_bytes(int64_t T, int32_t topk, int32_t E, int64_t N,
+                                          int64_t K, int32_t combine);
 
 /*
- * MoE expert grouped GEMM ("The FP4 Frontier", Finding 5 and Finding 7:
- * small-batch decode is bound by streaming the expert weights).  One
- * persistent launch covers every (expert, 128-row weight tile, token tile)
- * unit; experts without routes are skipped and their weights never read.
+ * MoE expert grouped GEMM ("The FP4 Frontier", Finding 5: one persistent
+ * grouped GEMM over all experts, token counts padded for TMA; Finding 7:
+ * small-batch decode is bound by streaming the expert weights), on
+ * already-quantised operands in their plain layouts.
+ *   A, sfA, gA   NVFP4 activations: packed codes uint8 [rows, K/2] and
+ *                row-major E4M3 scales uint8 [rows, K/16] (nvfp4_quantize with
+ *                NVFP4_SF_ROWMAJOR), device float global.  Without
+ *                topk_weights: rows = T token rows gathered by route_token
+ *                (route p reads row route_token[p]), or, with route_token
+ *                NULL, rows = R = T * topk already in route order.  With
+ *                topk_weights (the combine): rows = R in route order (the
+ *                experts' intermediate), route_token then places outputs.
+ *   W, sfW_tc, gW  expert weights: packed codes [E * N, K/2] (expert e's
+ *                rows e * N .. e * N + N - 1), their scales in the
+ *                tensor-core atom layout (nvfp4_prepack_weights over E * N
+ *                rows), device float [E], one global per expert.
+ *   expert_offsets, route_token, route_slot  int32, from nvfp4_moe_route.
+ *   topk_weights NULL: out = BF16 [R, N] in route order, out[p, n] = gA *
+ *                gW[e] * sum_k A_hat[src(p), k] W_hat[e, n, k].  FP32 [T, topk]:
+ *                out = BF16 [T, N], out[t] = sum over the routes p of t of
+ *                w[t, slot(p)] * y[p].
+ *   workspace    caller-owned, >= nvfp4_grouped_gemm_workspace_bytes(T, topk, E,
+ *                N, K, topk_weights != NULL) bytes, 16-byte aligned: the call
+ *                first copies the activation rows into grouped operand tiles
+ *                there (one pass over R rows), then runs the persistent GEMM.
+ * N % 128 == 0, K % 64 == 0, E <= 256; A, W, sfW_tc, out 16-byte aligned.  A
+ * gathered row index outside [0, rows), a token outside [0, T) or a slot
+ * outside [0, topk) sets NVFP4_ERR_DEVICE_CHECK and the route is skipped.
+ */
+nvfp4_status nvfp4_grouped_gemm(const uint8_t* A, const uint8_t* sfA, const float* gA,
+                                const uint8_t* W, const uint8_t* sfW_tc, const float* gW,
+                                const int32_t* expert_offsets, int32_t E,
+                                const int32_t* route_token, const float* topk_weights,
+                                const int32_t* route_slot, int64_t T, int32_t topk, int64_t N,
+                                int64_t K, void* out, void* workspace, size_t workspace_bytes,
+                                void* stream);
+
+/*
+ * The same grouped GEMM on operand tiles: the form the decode step uses,
+ * with the activations quantised straight into route order by
+ * nvfp4_quantize_dispatch (no separate copy pass) and the weights in one
+ * contiguous tile per pipeline stage.
  *   A_tiles, gA  route-ordered activation tiles from nvfp4_quantize_dispatch
  *                and their device float global scale.
  *   W_tiles      expert weights as operand tiles over [E * N, K]
@@ -264,17 +321,19 @@ size_t nvfp4_grouped_gemm_workspace_bytes(int64_t T, int64_t N);
  *       out[t] = sum over the routes p of t of w[t, slot(p)] * y[p], with
  *       route_token / route_slot from nvfp4_moe_route and an FP32 workspace
  *       of nvfp4_combine_workspace_bytes(T, N) bytes (zeroed here).  The FP32
- *       additions run in no fixed order.
+ *       additions run in no fixed order.  A token outside [0, T) or a slot
+ *       outside [0, topk) sets NVFP4_ERR_DEVICE_CHECK and that route adds
+ *       nothing.
  * N % 128 == 0, K % 64 == 0, E <= 256; all buffers 16-byte aligned.
  */
-nvfp4_status nvfp4_grouped_gemm(const uint8_t* A_tiles, const float* gA,
-                                const uint8_t* W_tiles, const float* gW,
-                                const int32_t* expert_offsets, int32_t E,
-                                int64_t T, int32_t topk, int64_t N, int64_t K,
-                                const int32_t* route_token, const int32_t* route_slot,
-                                const float* topk_weights,
-                                void* out, float* workspace, size_t workspace_bytes,
-                                void* stream);
+nvfp4_status nvfp4_grouped_gemm_tiles(const uint8_t* A_tiles, const float* gA,
+                                      const uint8_t* W_tiles, const float* gW,
+                                      const int32_t* expert_offsets, int32_t E,
+                                      int64_t T, int32_t topk, int64_t N, int64_t K,
+                                      const int32_t* route_token, const int32_t* route_slot,
+                                      const float* topk_weights,
+                                      void* out, float* workspace, size_t workspace_bytes,
+                                      void* stream);
 
 /*
  * Fused expert MLP front half: the gate_up grouped GEMM, SiLU(gate) * up,
@@ -282,7 +341,7 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* A_tiles, const float* gA,
  * Frontier", Finding 5: persistent grouped GEMM; the activation between the
  * two projections never goes to memory in BF16).
  *   A_tiles, gA, W_tiles, gW, expert_offsets, E, T, topk, K  as in
- *       nvfp4_grouped_gemm (gather orientation: A in route order).
+ *       nvfp4_grouped_gemm_tiles (gather orientation: A in route order).
  *   N         rows of each expert's W: rows [0, N/2) are the gate projection,
  *             rows [N/2, N) the up projection of the same N/2 features.
  *   g_h       device float: the global scale of h (given, for instance
@@ -293,7 +352,7 @@ nvfp4_status nvfp4_grouped_gemm(const uint8_t* A_tiles, const float* gA,
  *             per 16 features with g_h exactly as nvfp4_quantize does, into the
  *             grouped tile layout nvfp4_quantize_dispatch writes for R routes,
  *             E experts and K = N/2 (nvfp4_grouped_tiles_bytes(R, E, N/2)
- *             bytes).  Feed it to nvfp4_grouped_gemm as A_tiles with gA = g_h.
+ *             bytes).  Feed it to nvfp4_grouped_gemm_tiles as A_tiles with gA = g_h.
  * N % 256 == 0, K % 64 == 0, E <= 256, and the decode regime: the token-tile
  * width nvfp4_grouped_chunk_rows(R, E) must be 32 or 64 (NVFP4_ERR_UNSUPPORTED
  * otherwise).
@@ -308,7 +367,7 @@ nvfp4_status nvfp4_moe_gate_up_silu(const uint8_t* A_tiles, const float* gA,
  * Allocation-free weighted-combine grouped GEMM.  (This entry point is a
  * library convenience; the pages have no counterpart.)
  *
- * Same operation and arguments as nvfp4_grouped_gemm with topk_weights given
+ * Same operation and arguments as nvfp4_grouped_gemm_tiles with topk_weights given
  * (out = BF16 [T, N], out[t] = sum over the routes p of token t of
  * w[t, slot(p)] * y[p]), except that there is no workspace argument: the FP32
  * sums go to a fixed workspace inside the library, a device array of
@@ -391,10 +450,10 @@ nvfp4_status nvfp4_prepack_sparse_weight_tiles(const uint8_t* packed,
                                                int64_t K, uint8_t* tiles, void* stream);
 
 /*
- * nvfp4_grouped_gemm over 2:4-sparse expert weights: the same operation,
+ * nvfp4_grouped_gemm_tiles over 2:4-sparse expert weights: the same operation,
  * arguments, orientations (route-ordered out or weighted combine), limits
  * and errors, with W_sparse_tiles = nvfp4_prepack_sparse_weight_tiles over
- * [E * N, K].  The result equals that of nvfp4_grouped_gemm on the dense
+ * [E * N, K].  The result equals that of nvfp4_grouped_gemm_tiles on the dense
  * tiles of the same pruned weights: the kernel streams the sparse tiles (two
  * thirds of the dense bytes) and expands them in shared memory before the
  * block-scaled MMAs.

@@ -169,8 +169,11 @@ size_t nvfp4_prepacked_scales_bytes(int64_t rows, int64_t kblk) {
   return nvfp4_atom_scales_bytes(rows, 16 * ((kblk + 3) / 4 * 4));
 }
 
-size_t nvfp4_grouped_gemm_workspace_bytes(int64_t T, int64_t N) {
-  return nvfp4_combine_workspace_bytes(T, N);
+size_t nvfp4_grouped_gemm_workspace_bytes(int64_t T, int32_t topk, int32_t E, int64_t N,
+                                          int64_t K, int32_t combine) {
+  if (T < 0 || topk <= 0 || E <= 0 || N < 0 || K < 0) return 0;
+  return grouped_tiles_body_bytes(T * topk, E, K) +
+         (combine ? nvfp4_combine_workspace_bytes(T, N) : 0);
 }
 
 size_t nvfp4_atom_scales_bytes(int64_t rows, int64_t cols) {
@@ -397,7 +400,7 @@ static nvfp4_status grouped_gemm_impl(const uint8_t* A_tiles, const float* gA,
                                       const int32_t* route_token, const int32_t* route_slot,
                                       const float* topk_weights,
                                       void* out, float* workspace, size_t workspace_bytes,
-                                      bool sparse_w, void* stream) {
+                                      bool sparse_w, const CUtensorMap* w_map, void* stream) {
   if (!A_tiles || !gA || !W_tiles || !gW || !expert_offsets || !out) return NVFP4_ERR_INVALID_ARG;
   if (E <= 0 || T < 0 || topk <= 0 || N <= 0 || K <= 0) return NVFP4_ERR_INVALID_ARG;
   const bool combine = topk_weights != nullptr;
@@ -417,10 +420,12 @@ static nvfp4_status grouped_gemm_impl(const uint8_t* A_tiles, const float* gA,
     if (combine && T > 0 && cudaMemsetAsync(out, 0, T * N * 2, s) != cudaSuccess) return cuda_fail();
     return NVFP4_OK;
   }
-  CUtensorMap unused;                  // the grouped path copies operand tiles, no tensor map
+  // operand tiles need no tensor map; row-major weights come through w_map
+  CUtensorMap unused;
   std::memset(&unused, 0, sizeof(unused));
   nvfp4::GemmArgs a{};
   a.sfx = W_tiles;
+  a.x_map = w_map ? 1 : 0;
   a.sfy = A_tiles;
   a.gx = gW;
   a.gy = gA;
@@ -438,6 +443,7 @@ static nvfp4_status grouped_gemm_impl(const uint8_t* A_tiles, const float* gA,
   a.route_slot = route_slot;
   a.topk_w = topk_weights;
   a.topk = topk;
+  a.n_tokens = static_cast<int32_t>(T);
   a.ws = workspace;
   a.status = d->status;
   a.timeout_ns = g_timeout_ns.load();
@@ -445,25 +451,26 @@ static nvfp4_status grouped_gemm_impl(const uint8_t* A_tiles, const float* gA,
   a.sparse_w = sparse_w ? 1 : 0;
   if (combine && cudaMemsetAsync(workspace, 0, nvfp4_combine_workspace_bytes(T, N), s) != cudaSuccess)
     return cuda_fail();
-  if (nvfp4::launch_gemm(unused, unused, a, combine ? nvfp4::kGroupedCombine : nvfp4::kGrouped,
-                         d->sms, s) != cudaSuccess)
+  if (nvfp4::launch_gemm(w_map ? *w_map : unused, unused, a,
+                         combine ? nvfp4::kGroupedCombine : nvfp4::kGrouped, d->sms, s) !=
+      cudaSuccess)
     return cuda_fail();
   if (combine && nvfp4::launch_combine_finalize(workspace, T, N, out, d->sms, s) != cudaSuccess)
     return cuda_fail();
   return NVFP4_OK;
 }
 
-nvfp4_status nvfp4_grouped_gemm(const uint8_t* A_tiles, const float* gA,
-                                const uint8_t* W_tiles, const float* gW,
-                                const int32_t* expert_offsets, int32_t E,
-                                int64_t T, int32_t topk, int64_t N, int64_t K,
-                                const int32_t* route_token, const int32_t* route_slot,
-                                const float* topk_weights,
-                                void* out, float* workspace, size_t workspace_bytes,
-                                void* stream) {
+nvfp4_status nvfp4_grouped_gemm_tiles(const uint8_t* A_tiles, const float* gA,
+                                      const uint8_t* W_tiles, const float* gW,
+                                      const int32_t* expert_offsets, int32_t E,
+                                      int64_t T, int32_t topk, int64_t N, int64_t K,
+                                      const int32_t* route_token, const int32_t* route_slot,
+                                      const float* topk_weights,
+                                      void* out, float* workspace, size_t workspace_bytes,
+                                      void* stream) {
   return grouped_gemm_impl(A_tiles, gA, W_tiles, gW, expert_offsets, E, T, topk, N, K,
                            route_token, route_slot, topk_weights, out, workspace,
-                           workspace_bytes, false, stream);
+                           workspace_bytes, false, nullptr, stream);
 }
 
 nvfp4_status nvfp4_grouped_gemm_sparse(const uint8_t* A_tiles, const float* gA,
@@ -476,7 +483,56 @@ nvfp4_status nvfp4_grouped_gemm_sparse(const uint8_t* A_tiles, const float* gA,
                                        void* stream) {
   return grouped_gemm_impl(A_tiles, gA, W_sparse_tiles, gW, expert_offsets, E, T, topk, N, K,
                            route_token, route_slot, topk_weights, out, workspace,
-                           workspace_bytes, true, stream);
+                           workspace_bytes, true, nullptr, stream);
+}
+
+nvfp4_status nvfp4_grouped_gemm(const uint8_t* A, const uint8_t* sfA, const float* gA,
+                                const uint8_t* W, const uint8_t* sfW_tc, const float* gW,
+                                const int32_t* expert_offsets, int32_t E,
+                                const int32_t* route_token, const float* topk_weights,
+                                const int32_t* route_slot, int64_t T, int32_t topk, int64_t N,
+                                int64_t K, void* out, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  if (!A || !sfA || !gA || !W || !sfW_tc || !gW || !expert_offsets || !out || !workspace)
+    return NVFP4_ERR_INVALID_ARG;
+  if (E <= 0 || T < 0 || topk <= 0 || N <= 0 || K <= 0) return NVFP4_ERR_INVALID_ARG;
+  const bool combine = topk_weights != nullptr;
+  if (combine && (!route_token || !route_slot)) return NVFP4_ERR_INVALID_ARG;
+  if (N % 128 != 0 || K % 64 != 0 || E > nvfp4::kGroupedMaxExperts) return NVFP4_ERR_UNSUPPORTED;
+  const int64_t R = T * topk;
+  if (R > (1LL << 30) || static_cast<int64_t>(E) * N > (1LL << 30)) return NVFP4_ERR_UNSUPPORTED;
+  if (workspace_bytes < nvfp4_grouped_gemm_workspace_bytes(T, topk, E, N, K, combine ? 1 : 0))
+    return NVFP4_ERR_UNSUPPORTED;
+  if (!aligned16(A) || !aligned16(W) || !aligned16(sfW_tc) || !aligned16(out) ||
+      !aligned16(workspace))
+    return NVFP4_ERR_UNSUPPORTED;
+  DeviceState* d = nullptr;
+  nvfp4_status st = device_state(&d);
+  if (st != NVFP4_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (R == 0) {
+    if (combine && T > 0 && cudaMemsetAsync(out, 0, T * N * 2, s) != cudaSuccess) return cuda_fail();
+    return NVFP4_OK;
+  }
+  // the activation rows into route order, as grouped operand tiles at the
+  // start of the workspace; the FP32 combine sums follow them
+  uint8_t* a_tiles = static_cast<uint8_t*>(workspace);
+  const size_t tiles_bytes = grouped_tiles_body_bytes(R, E, K);
+  // gather by route_token only when the output stays in route order; the
+  // combine's input (the experts' intermediate) is already route-ordered
+  const bool gather = route_token != nullptr && !combine;
+  if (nvfp4::launch_gather_dispatch(A, sfA, gather ? T : R, K, gather ? route_token : nullptr,
+                                    expert_offsets, E, R, nvfp4::grouped_chunk_rows(R, E), a_tiles,
+                                    d->status, d->sms, s) != cudaSuccess)
+    return cuda_fail();
+  CUtensorMap w_map;
+  if (make_operand_map(&w_map, W, static_cast<uint64_t>(E) * N, K / 2, 128) != NVFP4_OK)
+    return NVFP4_ERR_UNSUPPORTED;
+  float* ws = combine ? reinterpret_cast<float*>(a_tiles + tiles_bytes) : nullptr;
+  return grouped_gemm_impl(a_tiles, gA, sfW_tc, gW, expert_offsets, E, T, topk, N, K,
+                           route_token, route_slot, topk_weights, out, ws,
+                           combine ? nvfp4_combine_workspace_bytes(T, N) : 0, false, &w_map,
+                           stream);
 }
 
 size_t nvfp4_sparse_tiles_bytes(int64_t rows, int64_t K) {
@@ -725,9 +781,11 @@ nvfp4_status nvfp4_grouped_gemm_combine_noalloc(const uint8_t* A_tiles, const fl
   a.route_slot = route_slot;
   a.topk_w = topk_weights;
   a.topk = topk;
+  a.n_tokens = static_cast<int32_t>(T);
   a.ws = ws;
   a.status = d->status;
   a.timeout_ns = g_timeout_ns.load();
+  a.debug_flags = g_debug_flags.load();
   // the workspace keeps the previous call's sums: clear the part this call uses
   if (cudaMemsetAsync(ws, 0, static_cast<size_t>(T) * N * sizeof(float), s) != cudaSuccess)
     return cuda_fail();

@@ -200,8 +200,11 @@ __device__ __forceinline__ Unit get_unit(int u, int mode, const GemmArgs& a, con
     un.y_row0 = t.off[e] + nt * BN;
     un.y_rows = min(BN, cnt - nt * BN);
     const int64_t n_kb = (a.K + kBK - 1) / kBK;
-    un.sfx_off = static_cast<int64_t>(e * mtiles + mt) * n_kb *
-                 (SP ? kSparseTileBytes : kOperandTileBytes);
+    // X from operand tiles: the unit's first tile; X from the tensor map: its
+    // row tile's scale atoms (the codes come by TMA at row x_row0)
+    un.sfx_off = a.x_map ? static_cast<int64_t>(e * mtiles + mt) * atoms_per_rowtile * 512
+                         : static_cast<int64_t>(e * mtiles + mt) * n_kb *
+                               (SP ? kSparseTileBytes : kOperandTileBytes);
     un.y_tile = t.tb[e] + nt * (BN / Cfg<BN, MT>::kLayoutRows);
     un.sfy_off = static_cast<int64_t>(un.y_tile) * n_kb * kOperandTileBytes;
     un.x_reused = cnt > BN;
@@ -493,14 +496,29 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
         if (grouped) {
           // operand tiles: X codes + scales in one contiguous copy, Y codes
           // (only the unit's rows) and Y scales in two more
-          const uint8_t* xt = a.sfx + un.sfx_off + kb * (SP ? kSparseTileBytes : kOperandTileBytes);
           const uint8_t* yt = a.sfy + un.sfy_off + kb * kOperandTileBytes;
-          bulk_load_elect(sx, xt, xbytes, full_bar(stage), pol_x);
-          if (MT == 2)                   // the unit's second weight tile
-            bulk_load_elect(sx + C::kXPartBytes,
-                            xt + static_cast<int64_t>(un.x_pair) * ((a.K + kBK - 1) / kBK) *
-                                     (SP ? kSparseTileBytes : kOperandTileBytes),
-                            xbytes, full_bar(stage), pol_x);
+          if (!SP && a.x_map) {
+            // X as row-major codes (TMA, 128-byte swizzle: the layout the
+            // operand tiles store) and atom-layout scales (one bulk copy)
+            for (int x = 0; x < MT; ++x) {
+              const int xo = x * un.x_pair;            // row tiles to the unit's tile x
+              tma_load_2d_elect(sx + x * C::kXPartBytes, &tmx, full_bar(stage), kb * kRowBytes,
+                                un.x_row0 + 128 * xo, pol_x);
+              bulk_load_elect(sx + x * C::kXPartBytes + kXTileBytes,
+                              a.sfx + un.sfx_off + xo * atoms_per_rowtile * 512 +
+                                  kb * kSFStageBytes,
+                              ksteps * 512, full_bar(stage), pol_x);
+            }
+          } else {
+            const uint8_t* xt =
+                a.sfx + un.sfx_off + kb * (SP ? kSparseTileBytes : kOperandTileBytes);
+            bulk_load_elect(sx, xt, xbytes, full_bar(stage), pol_x);
+            if (MT == 2)                 // the unit's second weight tile
+              bulk_load_elect(sx + C::kXPartBytes,
+                              xt + static_cast<int64_t>(un.x_pair) * ((a.K + kBK - 1) / kBK) *
+                                       (SP ? kSparseTileBytes : kOperandTileBytes),
+                              xbytes, full_bar(stage), pol_x);
+          }
           bulk_load_elect(sy, yt, ybox_lo * 16 * kRowBytes, full_bar(stage), pol_y);
           bulk_load_elect(ssfy, yt + kXTileBytes, ksteps * 512, full_bar(stage), pol_y);
           if (ybox_hi > 0) {               // second operand tile of a 256-row token tile
@@ -735,19 +753,27 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
       const Unit un = get_unit<BN, MT, SP>(u, mode, a, t, tiles_x, atoms_per_rowtile);
       // Combine: fetch this lane's tokens and routing weights (one token per
       // lane per 32-column chunk) before waiting, so the dependent L2 round
-      // trips overlap the MMAs instead of following them.
+      // trips overlap the MMAs instead of following them.  A token outside
+      // [0, T) or a slot outside [0, topk) is a device-side input error: the
+      // route is skipped (c_tok = -1) and the status word records it.
       int c_tok[BN / 32];
       float c_w[BN / 32];
       if (mode == kGroupedCombine) {
 #pragma unroll
         for (int ci = 0; ci < BN / 32; ++ci) {
           const int col = ci * 32 + lane;
-          c_tok[ci] = 0;
+          c_tok[ci] = -1;
           c_w[ci] = 0.0f;
           if (col < un.y_rows) {
             const int p = un.y_row0 + col;
-            c_tok[ci] = a.route_token[p];
-            c_w[ci] = a.topk_w[static_cast<int64_t>(c_tok[ci]) * a.topk + a.route_slot[p]];
+            const int tok = a.route_token[p];
+            const int slot = a.route_slot[p];
+            if (tok >= 0 && tok < a.n_tokens && slot >= 0 && slot < a.topk) {
+              c_tok[ci] = tok;
+              c_w[ci] = a.topk_w[static_cast<int64_t>(tok) * a.topk + slot];
+            } else {
+              raise_status(a.status, NVFP4_ERR_DEVICE_CHECK);
+            }
           }
         }
       }
@@ -942,6 +968,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
               float* dst = a.ws + static_cast<int64_t>(tok) * a.n_out + f0;
 #pragma unroll
               for (int v = 0; v < 8; ++v) {
+                if (tok < 0) break;                  // rejected route (see above)
                 float4 acc4;
                 acc4.x = __fmul_rn(w, __fmul_rn(__uint_as_float(r[4 * v + 0]), alpha));
                 acc4.y = __fmul_rn(w, __fmul_rn(__uint_as_float(r[4 * v + 1]), alpha));

@@ -27,6 +27,12 @@ cudaError_t launch_quantize_dispatch(const uint16_t* x, int64_t rows, int64_t K,
                                      int chunk_rows, uint8_t* tiles, float* g,
                                      const uint32_t* partials, int n_partials, int* status,
                                      int sms, cudaStream_t s);
+// Copies already-quantised rows (packed + row-major scales) into the grouped
+// operand tiles of route order; route p reads row route_token[p] (or p).
+cudaError_t launch_gather_dispatch(const uint8_t* packed, const uint8_t* sf, int64_t rows,
+                                   int64_t K, const int32_t* route_token,
+                                   const int32_t* expert_offsets, int E, int64_t R, int chunk_rows,
+                                   uint8_t* tiles, int* status, int sms, cudaStream_t s);
 cudaError_t launch_prepack_tiles(const uint8_t* packed, const uint8_t* sf, int64_t rows,
                                  int64_t K, uint8_t* tiles, int sms, cudaStream_t s);
 cudaError_t launch_prepack(const uint8_t* src, int64_t rows, int64_t kblk, uint8_t* dst,
@@ -73,6 +79,7 @@ struct GemmArgs {
   const int32_t* route_slot;
   const float* topk_w;
   int32_t topk;
+  int32_t n_tokens;                // combine: T, the rows of ws (route_token must be < T)
   float* ws;                       // combine: FP32 [T, n_out]
   int* status;
   uint64_t timeout_ns;
@@ -81,6 +88,9 @@ struct GemmArgs {
   const float* g_h;                // SiLU-mul: global scale of h (given)
   int32_t h_nkb;                   // SiLU-mul: 256-element K blocks of h
   int32_t sparse_w;                // grouped: X operand tiles are 2:4-sparse tiles
+  int32_t x_map;                   // grouped: X codes through the tensor map tmx (row-major
+                                   // [E * n_out, K/2]) and X scales in the atom layout at sfx,
+                                   // instead of operand tiles
 };
 
 // Test hook: the producer of every CTA leaves its first pipeline stage

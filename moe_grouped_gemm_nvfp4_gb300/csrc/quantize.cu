@@ -273,6 +273,88 @@ __global__ void __launch_bounds__(256) quantize_dispatch_kernel(
   }
 }
 
+// Already-quantised rows into route order: route p copies row src(p) of the
+// packed codes [rows, K/2] and row-major scales [rows, K/16], src(p) =
+// route_token[p] (or p itself without a gather list), into the grouped
+// operand-tile layout the dispatch quantiser writes (same chunking, same
+// positions).  Work item: one 16-byte chunk of codes or one 4-byte word of
+// scales of one route; the expert of a route comes from a binary search of
+// the offsets.  A source row outside [0, rows) is a device-side input error:
+// the route is skipped and the status word records it.
+__global__ void __launch_bounds__(256) gather_dispatch_kernel(
+    const uint8_t* __restrict__ packed, const uint8_t* __restrict__ sf, int64_t rows, int64_t K,
+    const int32_t* __restrict__ route_token, const int32_t* __restrict__ expert_offsets, int E,
+    int64_t R, int chunk, uint8_t* __restrict__ tiles, int* status) {
+  extern __shared__ int32_t sh[];
+  int32_t* off = sh;              // [E + 1]
+  int32_t* tb = sh + (E + 1);     // [E]
+  __shared__ int32_t s_bad;
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) off[e] = expert_offsets[e];
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int per = (E + 31) / 32;
+    const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+    int32_t sum = 0;
+    bool ok = true;
+    for (int e = e0; e < e1; ++e) {
+      const int32_t c = off[e + 1] - off[e];
+      ok = ok && c >= 0;
+      sum += (c + chunk - 1) / chunk;
+    }
+    int32_t incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int32_t acc = incl - sum;
+    for (int e = e0; e < e1; ++e) {
+      tb[e] = acc;
+      acc += (off[e + 1] - off[e] + chunk - 1) / chunk;
+    }
+    const bool all_ok = __all_sync(0xFFFFFFFFu, ok) && off[0] == 0 && off[E] <= R;
+    if (lane == 0) {
+      s_bad = all_ok ? 0 : 1;
+      if (!all_ok) raise_status(status, NVFP4_ERR_DEVICE_CHECK);
+    }
+  }
+  __syncthreads();
+  if (s_bad) return;
+  const int64_t half = K >> 1, kblk = K >> 4;
+  const int64_t n_kb = (K + 255) >> 8;
+  const int64_t per_route = (half >> 4) + (kblk >> 2);   // 16-byte code chunks + scale words
+  const int64_t total = static_cast<int64_t>(off[E]) * per_route;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += stride) {
+    const int32_t p = static_cast<int32_t>(i / per_route);
+    const int64_t w = i - static_cast<int64_t>(p) * per_route;
+    const int64_t src = route_token ? static_cast<int64_t>(route_token[p]) : p;
+    if (src < 0 || src >= rows) {
+      if (w == 0) raise_status(status, NVFP4_ERR_DEVICE_CHECK);
+      continue;
+    }
+    const int e = find_expert(off, E, p);
+    const int32_t local = p - off[e];
+    const int64_t rt = tb[e] + local / chunk;
+    const int row = local % chunk;
+    if (w < (half >> 4)) {
+      const int64_t byte = w << 4;
+      *reinterpret_cast<uint4*>(tiles + tile_code_offset(rt, row, byte >> 7,
+                                                         static_cast<int>(byte & 127), n_kb)) =
+          *reinterpret_cast<const uint4*>(packed + src * half + byte);
+    } else {
+      const int64_t col = (w - (half >> 4)) << 2;        // first of four scale columns
+      const uint8_t* q = sf + src * kblk + col;
+      const uint32_t v = static_cast<uint32_t>(q[0]) | (static_cast<uint32_t>(q[1]) << 8) |
+                         (static_cast<uint32_t>(q[2]) << 16) | (static_cast<uint32_t>(q[3]) << 24);
+      *reinterpret_cast<uint32_t*>(tiles + tile_scale_offset(rt, row, col >> 4,
+                                                             static_cast<int>(col & 15), n_kb)) = v;
+    }
+  }
+}
+
 // Packed rows [rows, K/2] + row-major scales [rows, K/16] -> operand tiles,
 // rows padded to 128 and K to 256 with zeros.  One thread per 16-byte chunk
 // of codes (and per 4 scale bytes).
@@ -415,6 +497,18 @@ cudaError_t launch_quantize_dispatch(const uint16_t* x, int64_t rows, int64_t K,
                              256, shmem, s>>>(
       x, rows, K, ld, route_pos, fanout, expert_offsets, E, R, chunk_rows, tiles, g, partials,
       n_partials, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_dispatch(const uint8_t* packed, const uint8_t* sf, int64_t rows,
+                                   int64_t K, const int32_t* route_token,
+                                   const int32_t* expert_offsets, int E, int64_t R, int chunk_rows,
+                                   uint8_t* tiles, int* status, int sms, cudaStream_t s) {
+  if (R == 0) return cudaSuccess;
+  const size_t shmem = sizeof(int32_t) * (2 * static_cast<size_t>(E) + 1);
+  const int64_t work = R * ((K >> 5) + (K >> 6));
+  gather_dispatch_kernel<<<grid_for(work, sms), 256, shmem, s>>>(
+      packed, sf, rows, K, route_token, expert_offsets, E, R, chunk_rows, tiles, status);
   return cudaGetLastError();
 }
 

@@ -46,6 +46,36 @@ def quantize_experts(w: torch.Tensor, stream=None) -> ExpertWeights:
     return ExpertWeights(tiles, g, E, N, K)
 
 
+@dataclass
+class PlainExpertWeights:
+    """NVFP4 expert weights in the plain layouts nvfp4_grouped_gemm takes:
+    packed codes [E*N, K/2] and their scales in the tensor-core atom layout."""
+    packed: torch.Tensor
+    sf_atoms: torch.Tensor
+    g: torch.Tensor
+    E: int
+    N: int
+    K: int
+
+
+def quantize_experts_plain(w: torch.Tensor, stream=None) -> PlainExpertWeights:
+    """BF16 [E, N, K] on the device -> packed codes + atom-layout scales, one
+    global per expert (nvfp4_quantize per expert, then nvfp4_prepack_weights
+    over all E*N rows)."""
+    E, N, K = w.shape
+    dev = w.device
+    packed = torch.empty((E * N, K // 2), dtype=torch.uint8, device=dev)
+    sf_rm = torch.empty((E * N, K // 16), dtype=torch.uint8, device=dev)
+    g = torch.empty(E, dtype=torch.float32, device=dev)
+    for e in range(E):
+        F.nvfp4_quantize(w[e], packed[e * N:(e + 1) * N], sf_rm[e * N:(e + 1) * N], g[e:e + 1],
+                         0, stream)
+    atoms = torch.empty(F.nvfp4_prepacked_scales_bytes(E * N, K // 16), dtype=torch.uint8,
+                        device=dev)
+    F.nvfp4_prepack_weights(sf_rm, atoms, stream)
+    return PlainExpertWeights(packed, atoms, g, E, N, K)
+
+
 def quantize_experts_sparse(w: torch.Tensor, stream=None, pruned: bool = False) -> ExpertWeights:
     """BF16 [E, N, K] on the device -> 2:4-sparse NVFP4 tiles ("The FP4
     Frontier", Finding 6): each expert pruned to 2:4 over element pairs (unless
@@ -129,7 +159,7 @@ class GroupedPlan:
 
     def gemm(self, topk_weights=None, stream=None):
         w = self.w
-        fn = F.nvfp4_grouped_gemm_sparse if w.sparse else F.nvfp4_grouped_gemm
+        fn = F.nvfp4_grouped_gemm_sparse if w.sparse else F.nvfp4_grouped_gemm_tiles
         fn(self.a_tiles, self.a_g, w.tiles, w.g,
                              self.expert_offsets, w.E, self.T, self.topk, w.N, w.K,
                              self.route_token, self.route_slot,
@@ -218,7 +248,7 @@ class FusedMLP:
         gu.quantize(x, stream, amax_done=True)
         F.nvfp4_moe_gate_up_silu(gu.a_tiles, gu.a_g, w1.tiles, w1.g, gu.expert_offsets, w1.E,
                                  self.T, self.topk, w1.N, w1.K, self.g_h, dn.a_tiles, stream)
-        F.nvfp4_grouped_gemm(dn.a_tiles, self.g_h, w2.tiles, w2.g, dn.expert_offsets, w2.E,
+        F.nvfp4_grouped_gemm_tiles(dn.a_tiles, self.g_h, w2.tiles, w2.g, dn.expert_offsets, w2.E,
                              self.T, self.topk, w2.N, w2.K, dn.route_token, dn.route_slot,
                              topk_weights, dn.out, dn.workspace, stream)
         return dn.out

@@ -43,7 +43,7 @@ _SIGS = {
     "nvfp4_atom_scales_bytes": (_SZ, [_I64, _I64]),
     "nvfp4_last_device_status": (ctypes.c_int, [_P]),
     "nvfp4_prepacked_scales_bytes": (_SZ, [_I64, _I64]),
-    "nvfp4_grouped_gemm_workspace_bytes": (_SZ, [_I64, _I64]),
+    "nvfp4_grouped_gemm_workspace_bytes": (_SZ, [_I64, _I32, _I32, _I64, _I64, _I32]),
     "nvfp4_quantize": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _P, _U32, _P]),
     "nvfp4_prepack_weights": (ctypes.c_int, [_P, _I64, _I64, _P, _P]),
     "nvfp4_gemm": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P]),
@@ -56,8 +56,10 @@ _SIGS = {
                                                _P, _P, _U32, _P]),
     "nvfp4_amax_partials": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, _I32, _P, _P]),
     "nvfp4_combine_workspace_bytes": (_SZ, [_I64, _I64]),
-    "nvfp4_grouped_gemm": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I64, _I32, _I64, _I64,
-                                          _P, _P, _P, _P, _P, _SZ, _P]),
+    "nvfp4_grouped_gemm": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I32, _P, _P, _P, _I64,
+                                          _I32, _I64, _I64, _P, _P, _SZ, _P]),
+    "nvfp4_grouped_gemm_tiles": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I64, _I32, _I64,
+                                                _I64, _P, _P, _P, _P, _P, _SZ, _P]),
     "nvfp4_moe_gate_up_silu": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I64, _I32, _I64, _I64,
                                               _P, _P, _P]),
     "nvfp4_noalloc_workspace_floats": (_SZ, []),
@@ -161,8 +163,9 @@ def nvfp4_prepacked_scales_bytes(rows: int, kblk: int) -> int:
     return load().nvfp4_prepacked_scales_bytes(rows, kblk)
 
 
-def nvfp4_grouped_gemm_workspace_bytes(T: int, N: int) -> int:
-    return load().nvfp4_grouped_gemm_workspace_bytes(T, N)
+def nvfp4_grouped_gemm_workspace_bytes(T: int, topk: int, E: int, N: int, K: int,
+                                       combine: bool) -> int:
+    return load().nvfp4_grouped_gemm_workspace_bytes(T, topk, E, N, K, int(bool(combine)))
 
 
 def nvfp4_atom_scales_bytes(rows: int, cols: int) -> int:
@@ -240,11 +243,23 @@ def nvfp4_amax_partials(x, R: int, E: int, tiles, stream=None) -> None:
         _ptr(x), rows, K, _row_stride(x), R, E, _ptr(tiles), _stream(stream)))
 
 
-def nvfp4_grouped_gemm(A_tiles, gA, W_tiles, gW, expert_offsets, E: int, T: int, topk: int,
-                       N: int, K: int, route_token, route_slot, topk_weights, out, workspace,
-                       stream=None) -> None:
-    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+def nvfp4_grouped_gemm(A, sfA, gA, W, sfW_tc, gW, expert_offsets, E: int, route_token,
+                       topk_weights, route_slot, T: int, topk: int, N: int, K: int, out,
+                       workspace, stream=None) -> None:
+    """Grouped GEMM on plain NVFP4 operands (packed rows + row-major scales for
+    A, packed rows + atom-layout scales for W); see include/nvfp4.h."""
+    ws_bytes = workspace.numel() * workspace.element_size()
     _check("nvfp4_grouped_gemm", load().nvfp4_grouped_gemm(
+        _ptr(A), _ptr(sfA), _ptr(gA), _ptr(W), _ptr(sfW_tc), _ptr(gW), _ptr(expert_offsets), E,
+        _ptr(route_token), _ptr(topk_weights), _ptr(route_slot), T, topk, N, K, _ptr(out),
+        _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def nvfp4_grouped_gemm_tiles(A_tiles, gA, W_tiles, gW, expert_offsets, E: int, T: int,
+                             topk: int, N: int, K: int, route_token, route_slot, topk_weights,
+                             out, workspace, stream=None) -> None:
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("nvfp4_grouped_gemm_tiles", load().nvfp4_grouped_gemm_tiles(
         _ptr(A_tiles), _ptr(gA), _ptr(W_tiles), _ptr(gW), _ptr(expert_offsets), E, T, topk, N,
         K, _ptr(route_token), _ptr(route_slot), _ptr(topk_weights), _ptr(out),
         _ptr(workspace), ws_bytes, _stream(stream)))

@@ -21,7 +21,9 @@ def _declared():
 def test_header_declares_the_boundary():
     names = _declared()
     for want in ("nvfp4_quantize", "nvfp4_prepack_weights", "nvfp4_gemm", "nvfp4_grouped_gemm",
-                 "nvfp4_moe_route", "nvfp4_quantize_dispatch"):
+                 "nvfp4_grouped_gemm_tiles", "nvfp4_moe_route", "nvfp4_quantize_dispatch",
+                 "nvfp4_prepacked_scales_bytes", "nvfp4_grouped_gemm_workspace_bytes",
+                 "nvfp4_last_device_status"):
         assert want in names
 
 
@@ -42,7 +44,11 @@ def test_pure_host_helpers():
     assert F.nvfp4_atom_scales_bytes(300, 512) == 384 * 32
     assert F.nvfp4_atom_scales_bytes(0, 512) == 0
     assert F.nvfp4_combine_workspace_bytes(256, 6144) == 256 * 6144 * 4
-    assert F.nvfp4_grouped_gemm_workspace_bytes(256, 6144) == 256 * 6144 * 4
+    # grouped GEMM on plain operands: activation tiles (+ FP32 sums with the combine)
+    tiles_2048 = (2048 + 31 * 128) // 32 * 24 * 18432
+    assert F.nvfp4_grouped_gemm_workspace_bytes(256, 8, 128, 4096, 6144, False) == tiles_2048
+    assert F.nvfp4_grouped_gemm_workspace_bytes(256, 8, 128, 6144, 2048, True) == \
+        (2048 + 31 * 128) // 32 * 8 * 18432 + 256 * 6144 * 4
     assert F.nvfp4_prepacked_scales_bytes(300, 32) == F.nvfp4_atom_scales_bytes(300, 512)
     assert F.nvfp4_prepacked_scales_bytes(1, 3) == 128 * 4      # kblk padded to 4
     # operand tiles: 18432 bytes per 128 rows x 256 K
@@ -79,7 +85,9 @@ def test_host_validation_without_device():
     assert lib.nvfp4_quantize(None, -1, 16, 16, None, None, None, 0, None) == 1
     assert lib.nvfp4_quantize(None, 4, 16, 16, None, None, None, 0, None) == 1
     assert lib.nvfp4_moe_route(None, 4, 0, 8, None, None, None, None, None) == 1
-    assert lib.nvfp4_grouped_gemm(*([None] * 5), 8, 4, 2, 128, 128, None, None, None, None,
+    assert lib.nvfp4_grouped_gemm_tiles(*([None] * 5), 8, 4, 2, 128, 128, None, None, None,
+                                        None, None, 0, None) == 1
+    assert lib.nvfp4_grouped_gemm(*([None] * 7), 8, None, None, None, 4, 2, 128, 128, None,
                                   None, 0, None) == 1
     assert lib.nvfp4_prepack_weight_tiles(None, None, 4, 64, None, None) == 1
     assert lib.nvfp4_set_timeout_ns(0) == 1
@@ -106,6 +114,11 @@ def test_host_validation_without_device():
     assert lib.nvfp4_prepack_sparse_weight_tiles(p, p, 4, 96, p, None) == 2     # K % 64
     assert lib.nvfp4_grouped_gemm_sparse(p, p, p, p, p, 4, 8, 2, 200, 128, p, p, None, p,
                                          None, 0, None) == 2                     # N % 128
+    # the plain-operand grouped GEMM: N % 128, then a workspace that is too small
+    assert lib.nvfp4_grouped_gemm(*([p] * 7), 8, p, None, p, 4, 2, 200, 128, p, p, 1 << 30,
+                                  None) == 2
+    assert lib.nvfp4_grouped_gemm(*([p] * 7), 8, p, None, p, 4, 2, 256, 128, p, p, 1024,
+                                  None) == 2
     q = ctypes.c_void_p(4096)
     assert lib.nvfp4_decode_attention(*([q] * 8), 1, 4, 1, 16, 96, 0.1, q, q, 1 << 20,
                                       None) == 2                                # head width

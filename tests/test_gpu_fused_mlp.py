@@ -86,13 +86,16 @@ def test_fused_gate_up_silu_down_matches_oracle(T, E, k, K1, N1, N2, hot):
     firm_blocks = ~amb.reshape(R, -1, 16).any(axis=2)
     assert np.array_equal(hs[firm_blocks], sh[firm_blocks])
     assert amb.mean() < 0.02                         # the exemption stays a small minority
-    # the layer output: the usual GEMM tolerance when no code sits on a tie
-    got = bf16_to_np(out[:T])
+    # the layer output against the oracle's down projection and combine of
+    # the h codes and scales the fused epilogue wrote (a code on a rounding
+    # tie is legitimately either neighbour; the GEMM that follows must be
+    # exact whichever was taken), at the usual GEMM tolerance in every case
+    y2_gpu_h = oracle.grouped_gemm(oracle.dequantize(hp, hs, g_h), _oracle_weights(w2), off)
+    check_gemm(bf16_to_np(out[:T]), oracle.combine(y2_gpu_h, tok, slot, wts, T), "fused mlp")
+    # and the pass as a whole stays within the GEMM tolerance of the oracle's
+    # own h wherever no code of h sits on a tie
     if not amb.any():
-        check_gemm(got, ref, "fused mlp")
-    else:
-        err = np.linalg.norm(got - ref) / np.linalg.norm(ref)
-        assert err <= 5e-3, err
+        check_gemm(bf16_to_np(out[:T]), ref, "fused mlp, oracle h")
 
 
 def test_fused_rejects_wide_token_tiles():

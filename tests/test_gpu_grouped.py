@@ -171,33 +171,84 @@ def test_bounded_wait_expires_reports_timeout_and_context_survives():
     check_gemm(bf16_to_np(plan.out[: T * k]), ref, "after timeout")
 
 
-def test_layer_step_overlapping_route_and_amax_matches_sequential_calls():
+def test_layer_step_overlapping_route_and_amax_matches_oracle_eager_and_replayed():
     """DecodeLayer.step runs the amax of x on a side stream beside the routing
-    (NVFP4_AMAX_DONE for the dispatch); eagerly and replayed from a CUDA graph
-    it must give the bytes the plain sequence route -> quantize -> GEMM gives."""
+    (NVFP4_AMAX_DONE for the dispatch).  Eagerly and replayed from a CUDA
+    graph, both of its outputs (gate_up in route order, down with the
+    weighted combine) must match the FP64 oracle, and gate_up must be the
+    bytes the plain sequence route -> quantize -> GEMM gives."""
     T, E, k, K1, N1, K2, N2 = 48, 8, 2, 256, 256, 128, 256
     g = inputs.rng(4242)
-    x = inputs.normal_bf16(g, (T, K1)).cuda()
-    h = inputs.normal_bf16(g, (T * k, K2)).cuda()
-    ids = torch.from_numpy(inputs.uniform_topk(g, T, E, k)).cuda()
-    wts = torch.from_numpy(inputs.dirichlet_weights(g, T, k)).cuda()
-    W1 = moe.quantize_experts(_weights_host(g, E, N1, K1).cuda())
-    W2 = moe.quantize_experts(_weights_host(g, E, N2, K2).cuda())
-    ref = moe.GroupedPlan(W1, T, k, "gather")
-    ref_out = ref.run(x, ids).clone()
-    ref_dn = moe.GroupedPlan(W2, T, k, "combine", routing_from=ref)
-    ref_dn_out = ref_dn.run(h, None, wts, route=False).clone()
+    x_h = inputs.normal_bf16(g, (T, K1))
+    h_h = inputs.normal_bf16(g, (T * k, K2))
+    ids_h = inputs.uniform_topk(g, T, E, k)
+    wts_h = inputs.dirichlet_weights(g, T, k)
+    w1 = _weights_host(g, E, N1, K1)
+    w2 = _weights_host(g, E, N2, K2)
+    x, h = x_h.cuda(), h_h.cuda()
+    ids, wts = torch.from_numpy(ids_h).cuda(), torch.from_numpy(wts_h).cuda()
+    W1 = moe.quantize_experts(w1.cuda())
+    W2 = moe.quantize_experts(w2.cuda())
+    # oracle: gate_up in route order; down over the route-ordered h, combined
+    off, tok, slot = oracle.route(ids_h, E)
+    px, sx, gx = oracle.quantize(x_h.float().numpy())
+    ref_gu = oracle.grouped_gemm(oracle.dequantize(px, sx, gx)[tok], _oracle_weights(w1), off)
+    ph, sh, gh = oracle.quantize(h_h.float().numpy())
+    ref_dn = oracle.combine(oracle.grouped_gemm(oracle.dequantize(ph, sh, gh),
+                                                _oracle_weights(w2), off), tok, slot, wts_h, T)
+    seq = moe.GroupedPlan(W1, T, k, "gather")
+    seq_out = seq.run(x, ids).clone()
     layer = moe.DecodeLayer(W1, W2, T, k)
     gu_out, dn_out = layer.step(x, ids, h, wts)
     torch.cuda.synchronize()
     assert F.nvfp4_device_status() == F.NVFP4_OK
-    assert torch.equal(layer.gate_up.a_g, ref.a_g)
-    assert torch.equal(gu_out[:T * k], ref_out[:T * k])
-    assert torch.equal(dn_out[:T].float(), ref_dn_out[:T].float()) or \
-        torch.allclose(dn_out[:T].float(), ref_dn_out[:T].float(), rtol=1e-2, atol=1e-3)
+    assert torch.equal(layer.gate_up.a_g, seq.a_g)
+    assert torch.equal(gu_out[:T * k], seq_out[:T * k])
+    check_gemm(bf16_to_np(gu_out[:T * k]), ref_gu, "eager gate_up")
+    check_gemm(bf16_to_np(dn_out[:T]), ref_dn, "eager down + combine")
     cap = moe.CapturedStep(layer, x, ids, h, wts)
-    gu_out.zero_()
-    cap.replay()
+    for _ in range(2):                           # two replays, outputs poisoned before each
+        gu_out.view(torch.int16).fill_(0x7FC0)
+        dn_out.view(torch.int16).fill_(0x7FC0)
+        cap.replay()
+        torch.cuda.synchronize()
+        assert F.nvfp4_device_status() == F.NVFP4_OK
+        assert torch.equal(gu_out[:T * k], seq_out[:T * k])
+        check_gemm(bf16_to_np(gu_out[:T * k]), ref_gu, "replayed gate_up")
+        check_gemm(bf16_to_np(dn_out[:T]), ref_dn, "replayed down + combine")
+
+
+def test_combine_rejects_a_token_outside_the_batch():
+    """A route whose token is T (one past the batch) is a device-side input
+    error: the kernel records NVFP4_ERR_DEVICE_CHECK, adds nothing for that
+    route and writes no FP32 row past T (the workspace handed in is twice as
+    large, its upper half a sentinel); every other route is combined."""
+    T, E, k, N, K = 16, 4, 2, 128, 256
+    g = inputs.rng(77)
+    ids_h = inputs.uniform_topk(g, T, E, k)
+    wts_h = inputs.dirichlet_weights(g, T, k)
+    h_h = inputs.normal_bf16(g, (T * k, K))
+    w = _weights_host(g, E, N, K)
+    W = moe.quantize_experts(w.cuda())
+    plan = moe.GroupedPlan(W, T, k, "combine")
+    plan.route(torch.from_numpy(ids_h).cuda())
+    plan.quantize(h_h.cuda())
     torch.cuda.synchronize()
-    assert F.nvfp4_device_status() == F.NVFP4_OK
-    assert torch.equal(gu_out[:T * k], ref_out[:T * k])
+    off, tok, slot = oracle.route(ids_h, E)
+    bad = 5                                      # route position whose token goes bad
+    t_bad, s_bad = int(tok[bad]), int(slot[bad])
+    plan.route_token[bad] = T
+    ws = torch.full((2 * T, N), 7.0, dtype=torch.float32, device="cuda")
+    out = nan_filled((T, N))
+    F.nvfp4_device_status(reset=True)
+    F.nvfp4_grouped_gemm_tiles(plan.a_tiles, plan.a_g, W.tiles, W.g, plan.expert_offsets, E, T, k, N,
+                         K, plan.route_token, plan.route_slot,
+                         torch.from_numpy(wts_h).cuda(), out, ws)
+    torch.cuda.synchronize()
+    assert F.nvfp4_device_status(reset=True) == F.NVFP4_ERR_DEVICE_CHECK
+    assert torch.all(ws[T:] == 7.0)
+    ph, sh, gh = oracle.quantize(h_h.float().numpy())
+    y = oracle.grouped_gemm(oracle.dequantize(ph, sh, gh), _oracle_weights(w), off)
+    wts_ref = wts_h.astype(np.float64).copy()
+    wts_ref[t_bad, s_bad] = 0.0                  # the rejected route adds nothing
+    check_gemm(bf16_to_np(out), oracle.combine(y, tok, slot, wts_ref, T), "bad token dropped")

@@ -60,6 +60,7 @@ nvfp4_status device_state(DeviceState** out) {
       if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return cuda_fail();
       d.status = static_cast<int*>(p);
       if (nvfp4::init_gemm_attributes() != cudaSuccess) return cuda_fail();
+      if (nvfp4::init_gemm_pair_attributes() != cudaSuccess) return cuda_fail();
       if (nvfp4::init_route_attributes() != cudaSuccess) return cuda_fail();
     }
     if (!g_encode) {
@@ -106,6 +107,21 @@ nvfp4_status make_operand_map(CUtensorMap* m, const void* base, uint64_t rows, u
   const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
                               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NVFP4_OK : NVFP4_ERR_UNSUPPORTED;
+}
+
+// 2-D map over atom-layout scales of a [rows, K] operand viewed as rows of
+// one 512-byte atom (128 32-bit words), box of four atoms (one 256-K block
+// of a 128-row tile).  Rows past the last atom read zeros.
+nvfp4_status make_scale_map(CUtensorMap* m, const void* base, uint64_t rows, int64_t K) {
+  const cuuint64_t dims[2] = {128u, ((rows + 127) / 128) * static_cast<uint64_t>(K / 64)};
+  const cuuint64_t strides[1] = {512u};
+  const cuuint32_t box[2] = {128u, 4u};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? NVFP4_OK : NVFP4_ERR_UNSUPPORTED;
 }
@@ -262,6 +278,29 @@ nvfp4_status nvfp4_gemm(const uint8_t* A, const uint8_t* sfA, const float* gA,
   DeviceState* d = nullptr;
   nvfp4_status st = device_state(&d);
   if (st != NVFP4_OK) return st;
+  // Large M and N: CTA pairs, 256 x 256 tiles with one MMA across two SMs.
+  if (M >= 256 && N >= 256) {
+    CUtensorMap tmx, tmy, tsx, tsy;
+    if (make_operand_map(&tmx, A, M, K / 2, 128) != NVFP4_OK ||
+        make_operand_map(&tmy, B, N, K / 2, 128) != NVFP4_OK ||
+        make_scale_map(&tsx, sfA, M, K) != NVFP4_OK || make_scale_map(&tsy, sfB, N, K) != NVFP4_OK)
+      return NVFP4_ERR_UNSUPPORTED;
+    nvfp4::GemmArgs a{};
+    a.gx = gA;
+    a.gy = gB;
+    a.K = K;
+    a.rows_x = static_cast<int32_t>(M);
+    a.rows_y = static_cast<int32_t>(N);
+    a.out = C;
+    a.ldc = ldc;
+    a.vec_store = (ldc % 8 == 0 && aligned16(C)) ? 1 : 0;
+    a.status = d->status;
+    a.timeout_ns = g_timeout_ns.load();
+    if (nvfp4::launch_gemm_pair(tmx, tmy, tsx, tsy, a, static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+      return cuda_fail();
+    return NVFP4_OK;
+  }
   // Small M (decode-like): weights on the MMA's M side, tokens on its N side.
   const bool swap = M <= 64;
   const uint8_t* X = swap ? B : A;

@@ -325,6 +325,108 @@ __device__ __forceinline__ uint32_t idesc_nvf4(uint32_t n) {
 }
 
 // ---------------------------------------------------------------------------
+// CTA pairs (a cluster of two CTAs on neighbouring SMs sharing one MMA with
+// cta_group::2: M = 256 split 128 + 128 over the pair, each CTA holding half
+// of B; every tcgen05 instruction of such a kernel carries cta_group::2)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Address of the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// Arrive on an mbarrier of any CTA of the cluster (release at cluster scope).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
+               :: "r"(cluster_bar) : "memory");
+}
+
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" :: "r"(cluster_addr), "r"(v) : "memory");
+}
+
+// Every thread of both CTAs arrives; returns once all have (release/acquire).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+               :: "r"(dst_smem), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;"
+               :: "r"(taddr), "r"(ncols) : "memory");
+}
+
+// 2-D tiled TMA load into this CTA's shared memory whose completion counts
+// on an mbarrier of either CTA of the pair (cluster address `bar`).
+__device__ __forceinline__ void tma_load_2d_pair_elect(uint32_t dst, const void* tmap, uint32_t bar,
+                                                       int32_t x, int32_t y, uint64_t policy) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 l;\n\t"
+      "elect.sync l|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;\n\t}"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+
+// Arrive on the mbarrier at offset `bar` of both CTAs of the pair once every
+// tcgen05 operation issued so far by this thread has completed.
+__device__ __forceinline__ void tc_commit_pair_elect(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 l;\n\t"
+      "elect.sync l|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;\n\t}"
+      :: "r"(bar), "h"(static_cast<uint16_t>(3)) : "memory");
+}
+
+// Scale atom -> tensor memory in both CTAs of the pair (each from its own
+// shared memory at the same offset).
+__device__ __forceinline__ void tc_cp_sf_atom_pair_elect(uint32_t taddr, uint64_t sdesc) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 l;\n\t"
+      "elect.sync l|e, 0xffffffff;\n\t"
+      "@e tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;\n\t}"
+      :: "r"(taddr), "l"(sdesc) : "memory");
+}
+
+// D (+)= A . B^T over the pair: M = 256 (128 rows of A and of D in each CTA),
+// B's N rows split N/2 + N/2 over the two CTAs' shared memory.
+__device__ __forceinline__ void tc_mma_nvf4_pair_elect(uint32_t d_tmem, uint64_t adesc,
+                                                       uint64_t bdesc, uint32_t idesc,
+                                                       uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .pred e;\n\t.reg .b32 l;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "elect.sync l|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X"
+      " [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+      :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
+         "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor of kind::mxf4nvf4 for M = m (128 or 256) and N = n.
+__device__ __forceinline__ uint32_t idesc_nvf4_m(uint32_t m, uint32_t n) {
+  return (1u << 7) | (1u << 10) | ((n >> 3) << 17) | (0u << 23) | ((m >> 4) << 24);
+}
+
+// ---------------------------------------------------------------------------
 // BF16 helpers
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {

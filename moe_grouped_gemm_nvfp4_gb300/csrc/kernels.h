@@ -130,6 +130,13 @@ constexpr int kSparseScaleOffset = 10240;
 cudaError_t init_gemm_attributes();
 cudaError_t launch_gemm(const CUtensorMap& tmx, const CUtensorMap& tmy, const GemmArgs& a,
                         int mode, int sms, cudaStream_t s);
+// gemm_pair.cu: the single GEMM on CTA pairs (cta_group::2, 256 x 256 tiles);
+// tmx / tmy: A and B codes (128-row boxes, 128-byte swizzle), tsx / tsy: their
+// atom-layout scales as rows of 512 bytes (boxes of four atoms).
+cudaError_t init_gemm_pair_attributes();
+cudaError_t launch_gemm_pair(const CUtensorMap& tmx, const CUtensorMap& tmy,
+                             const CUtensorMap& tsx, const CUtensorMap& tsy, const GemmArgs& a,
+                             cudaStream_t s);
 cudaError_t launch_combine_finalize(const float* ws, int64_t T, int64_t N, void* out, int sms,
                                     cudaStream_t s);
 

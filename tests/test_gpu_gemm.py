@@ -27,7 +27,8 @@ def _run(pa, sa, ga, pb, sb, gb, M, N, K):
     return bf16_to_np(C)
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (16, 128, 64), (16, 256, 512)])
+@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (16, 128, 64), (16, 256, 512),
+                                   (256, 256, 256)])       # CTA-pair tiles
 def test_gemm_unit_scales_code_space(M, N, K):
     """All scales 1.0 and g = 1: checks operand staging and descriptors alone."""
     g = inputs.rng(M + N + K)
@@ -42,7 +43,8 @@ def test_gemm_unit_scales_code_space(M, N, K):
     check_gemm(got, ref, "unit-scale")
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (16, 256, 512)])
+@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (16, 256, 512),
+                                   (256, 256, 512), (512, 256, 256)])   # CTA-pair tiles
 def test_gemm_scale_layout_code_space(M, N, K):
     """Distinct power-of-two scales per (row, block): checks the scale-factor path."""
     g = inputs.rng(3 * M + N + K)
@@ -74,6 +76,9 @@ def _quantized_case(M, N, K, seed):
     (1, 128, 64), (15, 128, 128), (64, 384, 192), (65, 128, 256),
     (127, 130, 320), (128, 128, 512), (129, 256, 256), (300, 200, 1024), (512, 384, 2048),
     (256, 448, 512), (200, 700, 320),     # 256-wide tiles with ragged last tiles
+    # CTA-pair tiles (M, N >= 256): full, ragged in M / N / K block, many tiles per pair
+    (256, 256, 64), (512, 768, 320), (300, 600, 1024), (257, 513, 256), (1024, 1024, 2048),
+    (2560, 2304, 256),
 ])
 def test_gemm_matches_oracle(M, N, K):
     ops, ref = _quantized_case(M, N, K, seed=M * 31 + N * 7 + K)

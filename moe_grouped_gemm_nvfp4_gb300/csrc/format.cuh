@@ -76,37 +76,99 @@ __device__ __forceinline__ uint32_t e2m1x8_rn_satfinite(const float* q) {
   return r;
 }
 
-// One block from its magnitude maximum and an accessor for its 16 finite
-// binary32 values: s = (amax_b / 6) / g (0 when g == 0), sf = E4M3(s),
-// d = e4m3(sf) * g, code = E2M1(v / d), or the signed zero code when d == 0.
-// The sign bit of every code is set from v itself, so values that round to
-// zero keep their sign whatever the conversion does with negative zeros.
+// Per-tensor constants of the block quantiser: the global scale g and, for
+// the fast path of the block scale, c = RN(1 / RN(6 g)) (fast only while g is
+// a normal number well inside the binary32 range).
+struct ScaleK {
+  float g;
+  float c;
+  bool fast;
+};
+
+__device__ __forceinline__ ScaleK scale_consts(float g) {
+  ScaleK k;
+  k.g = g;
+  k.fast = g >= 7.52316384526264e-37f && g <= 1.0e35f;   // [2^-120, 1e35]
+  k.c = k.fast ? __frcp_rn(__fmul_rn(6.0f, g)) : 0.0f;
+  return k;
+}
+
+// E4M3 code of the block scale: sf = E4M3(RN(RN(amax_b / 6) / g)), 0 when
+// g == 0.  s1 = RN(amax_b * c) is within 5 * 2^-24 (relative) of that exact
+// two-rounding chain s, i.e. within 10 units in the last place of s; E4M3
+// rounding tells two nearby values apart only across a midpoint between E4M3
+// values, which in the normal range (s >= 2^-6) has binary32 mantissa bits
+// 19..0 equal to 0x80000.  So when s1 is normal for E4M3, below 448 and more
+// than 16 units in the last place from such a midpoint, E4M3(s1) = E4M3(s);
+// at or above 448 both saturate.  Everything else takes the exact chain.
+__device__ __forceinline__ uint32_t block_scale_code(float amax_b, const ScaleK& k) {
+  if (!(k.g > 0.0f)) return 0u;
+  if (k.fast) {
+    const float s1 = __fmul_rn(amax_b, k.c);
+    if (s1 >= 448.0f) return 0x7Eu;
+    const uint32_t low = __float_as_uint(s1) & 0xFFFFFu;
+    if (s1 >= 0.015625f && low - 0x7FFF0u > 32u) return e4m3_from_f32(s1);
+  }
+  return e4m3_from_f32(__fdiv_rn(__fdiv_rn(amax_b, 6.0f), k.g));
+}
+
+// Exact element codes of a block with decode scale d > 0 (or d == 0): code =
+// E2M1(RN(v / d)), the signed zero code when d == 0; the sign bit of every
+// code is set from v itself.
 template <typename Get>
-__device__ __forceinline__ Block16 quantize16_with(float amax_b, float g, Get get) {
-  const float s = (g > 0.0f) ? __fdiv_rn(__fdiv_rn(amax_b, 6.0f), g) : 0.0f;
-  const uint32_t sf = e4m3_from_f32(s);
-  const float d = __fmul_rn(f32_from_e4m3(sf), g);
+__device__ __forceinline__ uint2 codes_exact(float d, Get get) {
   uint32_t sgn[2] = {0u, 0u};
 #pragma unroll
   for (int e = 0; e < 16; ++e) sgn[e >> 3] |= (__float_as_uint(get(e)) >> 31) << (4 * (e & 7) + 3);
-  Block16 b;
-  b.sf = sf;
-  // Fast path: q1 = v * RN(1/d) is within 2^-23 (relative) of v / d, and the
-  // correctly rounded quotient within 2^-24 of that, so both lie between
-  // q1 (1 - 2^-20) and q1 (1 + 2^-20).  The E2M1 conversion is monotone, so
-  // when the two bounds give the same codes those are the codes of the
-  // rounded quotient.  Otherwise (a quotient within ~2^-20 of a rounding
-  // boundary, or 1/d out of range) every code comes from the exact division.
-  const float inv = __frcp_rn(d);
-  if (d != 0.0f && inv < 3.0e38f) {
-    float lo[16], hi[16];
-    const float2 inv2 = make_float2(inv, inv);
-    const float2 dn = make_float2(0.99999904632568359375f, 0.99999904632568359375f);  // 1 - 2^-20
-    const float2 up = make_float2(1.00000095367431640625f, 1.00000095367431640625f);  // 1 + 2^-20
+  float q[16];
 #pragma unroll
-    for (int e = 0; e < 16; e += 2) {        // the same roundings, two per instruction
-      const float2 q1 = fmul2_rn(make_float2(get(e), get(e + 1)), inv2);
-      const float2 l = fmul2_rn(q1, dn), h = fmul2_rn(q1, up);
+  for (int e = 0; e < 16; ++e) {
+    const float v = get(e);
+    q[e] = (d != 0.0f) ? __fdiv_rn(v, d) : __fmul_rn(v, 0.0f);
+  }
+  return make_uint2(e2m1x8_rn_satfinite(q) | sgn[0], e2m1x8_rn_satfinite(q + 8) | sgn[1]);
+}
+
+// Bracketing multipliers of 1/d: with inv = RN(1/d), ilo = RN(inv (1 - 2^-20))
+// and ihi = RN(inv (1 + 2^-20)) satisfy, for every v, |v ilo| < |RN(v/d)| <
+// |v ihi| after rounding (the combined relative error of the roundings is
+// below 4 * 2^-24, far inside the 2^-20 margin; products that underflow are
+// below every E2M1 rounding boundary).  E2M1 rounding is monotone, so when
+// RN(v ilo) and RN(v ihi) give the same code, so does RN(v/d).
+struct Bracket {
+  float lo, hi;
+  bool ok;
+};
+
+__device__ __forceinline__ Bracket bracket_of(float d) {
+  Bracket b;
+  const float inv = __frcp_rn(d);
+  b.ok = d != 0.0f && inv < 3.0e38f && inv > 2.4e-38f;   // 1/d normal: relative bounds hold
+  b.lo = __fmul_rn(inv, 0.99999904632568359375f);   // 1 - 2^-20
+  b.hi = __fmul_rn(inv, 1.00000095367431640625f);   // 1 + 2^-20
+  return b;
+}
+
+// One block from its magnitude maximum and an accessor for its 16 finite
+// binary32 values: s = (amax_b / 6) / g (0 when g == 0), sf = E4M3(s),
+// d = e4m3(sf) * g, code = E2M1(v / d), or the signed zero code when d == 0.
+template <typename Get>
+__device__ __forceinline__ Block16 quantize16_with(float amax_b, const ScaleK& k, Get get) {
+  Block16 b;
+  b.sf = block_scale_code(amax_b, k);
+  const float d = __fmul_rn(f32_from_e4m3(b.sf), k.g);
+  const Bracket br = bracket_of(d);
+  if (br.ok) {
+    uint32_t sgn[2] = {0u, 0u};
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      sgn[e >> 3] |= (__float_as_uint(get(e)) >> 31) << (4 * (e & 7) + 3);
+    float lo[16], hi[16];
+    const float2 l2 = make_float2(br.lo, br.lo), h2 = make_float2(br.hi, br.hi);
+#pragma unroll
+    for (int e = 0; e < 16; e += 2) {        // two roundings per instruction
+      const float2 v = make_float2(get(e), get(e + 1));
+      const float2 l = fmul2_rn(v, l2), h = fmul2_rn(v, h2);
       lo[e] = l.x;
       lo[e + 1] = l.y;
       hi[e] = h.x;
@@ -118,22 +180,56 @@ __device__ __forceinline__ Block16 quantize16_with(float amax_b, float g, Get ge
       return b;
     }
   }
-  float q[16];
+  b.packed = codes_exact(d, get);
+  return b;
+}
+
+// Sixteen BF16 values as eight words (value 2i in the low half of word i).
+// The block maximum compares BF16 magnitudes as unsigned 16-bit integers
+// (two per instruction); the element codes take their sign from the
+// conversion of the bracketing products, which carry the sign of v (E2M1
+// rounding is symmetric, and a product that rounds to zero keeps its sign).
+__device__ __forceinline__ Block16 quantize_bf16x16(const uint32_t (&w)[8], const ScaleK& k) {
+  uint32_t m = __vmaxu2(w[0] & 0x7FFF7FFFu, w[1] & 0x7FFF7FFFu);
+  m = __vmaxu2(m, __vmaxu2(w[2] & 0x7FFF7FFFu, w[3] & 0x7FFF7FFFu));
+  m = __vmaxu2(m, __vmaxu2(w[4] & 0x7FFF7FFFu, w[5] & 0x7FFF7FFFu));
+  m = __vmaxu2(m, __vmaxu2(w[6] & 0x7FFF7FFFu, w[7] & 0x7FFF7FFFu));
+  const uint32_t amax_bits = max(m & 0xFFFFu, m >> 16);
+  auto get = [&](int e) {
+    return __uint_as_float((e & 1) ? (w[e >> 1] & 0xFFFF0000u) : (w[e >> 1] << 16));
+  };
+  Block16 b;
+  b.sf = block_scale_code(__uint_as_float(amax_bits << 16), k);
+  const float d = __fmul_rn(f32_from_e4m3(b.sf), k.g);
+  const Bracket br = bracket_of(d);
+  if (br.ok) {
+    float lo[16], hi[16];
+    const float2 l2 = make_float2(br.lo, br.lo), h2 = make_float2(br.hi, br.hi);
 #pragma unroll
-  for (int e = 0; e < 16; ++e) {
-    const float v = get(e);
-    q[e] = (d != 0.0f) ? __fdiv_rn(v, d) : __fmul_rn(v, 0.0f);
+    for (int i = 0; i < 8; ++i) {
+      const float2 v = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
+      const float2 l = fmul2_rn(v, l2), h = fmul2_rn(v, h2);
+      lo[2 * i] = l.x;
+      lo[2 * i + 1] = l.y;
+      hi[2 * i] = h.x;
+      hi[2 * i + 1] = h.y;
+    }
+    const uint32_t c0 = e2m1x8_rn_satfinite(lo), c1 = e2m1x8_rn_satfinite(lo + 8);
+    if (c0 == e2m1x8_rn_satfinite(hi) && c1 == e2m1x8_rn_satfinite(hi + 8)) {
+      b.packed = make_uint2(c0, c1);
+      return b;
+    }
   }
-  b.packed = make_uint2(e2m1x8_rn_satfinite(q) | sgn[0], e2m1x8_rn_satfinite(q + 8) | sgn[1]);
+  b.packed = codes_exact(d, get);
   return b;
 }
 
 // Sixteen finite binary32 values (amax_b = max |v|).
-__device__ __forceinline__ Block16 quantize16(const float* v, float g) {
+__device__ __forceinline__ Block16 quantize16(const float* v, const ScaleK& k) {
   float amax_b = 0.0f;
 #pragma unroll
   for (int e = 0; e < 16; ++e) amax_b = fmaxf(amax_b, fabsf(v[e]));
-  return quantize16_with(amax_b, g, [&](int e) { return v[e]; });
+  return quantize16_with(amax_b, k, [&](int e) { return v[e]; });
 }
 
 }  // namespace nvfp4

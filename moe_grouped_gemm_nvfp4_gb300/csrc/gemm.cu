@@ -816,7 +816,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
         warp_transpose32(rg, lane);                // lane = token, 32 features of quarter q
         warp_transpose32(ru, lane);
         if (ci * 32 + lane < n_valid) {
-          const float gh = *a.g_h;
+          const ScaleK gh = scale_consts(*a.g_h);
           float h[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {

@@ -44,14 +44,12 @@ __global__ void __launch_bounds__(256) amax_kernel(const uint16_t* __restrict__ 
       q[k] = (v0 + 32u * k < vpr) ? __ldg(row + v0 + 32u * k) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const uint32_t w[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        m = max(m, w[j] & 0x7FFFu);
-        m = max(m, (w[j] >> 16) & 0x7FFFu);
-      }
+      // BF16 magnitudes compare as unsigned 16-bit integers, two per instruction
+      m = __vmaxu2(m, __vmaxu2(__vmaxu2(q[k].x & 0x7FFF7FFFu, q[k].y & 0x7FFF7FFFu),
+                                __vmaxu2(q[k].z & 0x7FFF7FFFu, q[k].w & 0x7FFF7FFFu)));
     }
   }
+  m = max(m & 0xFFFFu, m >> 16);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
   __shared__ uint32_t wm[8];
@@ -77,19 +75,10 @@ __device__ __forceinline__ uint32_t gather4_bytes(uint32_t byte) {
   return (byte & 0xFFu) | ((b1 & 0xFFu) << 8) | ((b2 & 0xFFu) << 16) | ((b3 & 0xFFu) << 24);
 }
 
-// One 16-element block of BF16 (two 16-byte vectors) -> codes + scale.  BF16
-// magnitudes compare as integers, so the block maximum needs no conversion.
-__device__ __forceinline__ Block16 quantize_block(const uint4 lo, const uint4 hi, float g) {
+// One 16-element block of BF16 (two 16-byte vectors) -> codes + scale.
+__device__ __forceinline__ Block16 quantize_block(const uint4 lo, const uint4 hi, const ScaleK& k) {
   const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-  uint32_t amax_bits = 0;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    amax_bits = max(amax_bits, w[j] & 0x7FFFu);
-    amax_bits = max(amax_bits, (w[j] >> 16) & 0x7FFFu);
-  }
-  return quantize16_with(bf16_bits_to_f32(amax_bits), g, [&](int e) {
-    return bf16_bits_to_f32((w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu);
-  });
+  return quantize_bf16x16(w, k);
 }
 
 __device__ __forceinline__ int64_t atom_offset(int64_t r, int64_t c, int64_t n_cgroups) {
@@ -105,15 +94,19 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint16_t* __restric
                                                        uint8_t* __restrict__ packed,
                                                        uint8_t* __restrict__ scales,
                                                        int sf_atoms, const float* g_ptr) {
-  const float g = *g_ptr;
+  const ScaleK k = scale_consts(*g_ptr);
   const int lane = threadIdx.x & 31;
   const uint32_t bpr = static_cast<uint32_t>(cols >> 4);
   const uint32_t segs = (bpr + 31u) / 32u;
   const uint64_t items = static_cast<uint64_t>(rows) * segs;
   const uint64_t wstride = static_cast<uint64_t>(gridDim.x) * (blockDim.x >> 5);
   const int64_t ncg = (cols + 63) >> 6;                 // 4-block scale groups per row
-  for (uint64_t it = static_cast<uint64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-       it < items; it += wstride) {
+  // Items run from the end of the tensor backwards: the tensor amax pass
+  // that precedes this kernel swept it front to back, so its tail is what
+  // L2 still holds.
+  for (uint64_t j = static_cast<uint64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       j < items; j += wstride) {
+    const uint64_t it = items - 1 - j;
     const int64_t r = static_cast<int64_t>(it / segs);
     const uint32_t b = static_cast<uint32_t>(it - static_cast<uint64_t>(r) * segs) * 32u + lane;
     const bool valid = b < bpr;
@@ -122,7 +115,7 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint16_t* __restric
     q.sf = 0u;
     if (valid) {
       const uint4* src = reinterpret_cast<const uint4*>(x + r * ld + b * 16);
-      q = quantize_block(__ldg(src), __ldg(src + 1), g);
+      q = quantize_block(__ldg(src), __ldg(src + 1), k);
       *reinterpret_cast<uint2*>(packed + r * (cols >> 1) + b * 8) = q.packed;
     }
     if (sf_atoms) {
@@ -230,6 +223,7 @@ __global__ void __launch_bounds__(256) quantize_dispatch_kernel(
   } else {
     g = *g_ptr;
   }
+  const ScaleK k = scale_consts(g);
   if (s_bad) return;
   // Work item: a warp quantises 32 consecutive 16-element blocks of one
   // source row (K % 64 == 0, so every group of four blocks is whole) and
@@ -252,7 +246,7 @@ __global__ void __launch_bounds__(256) quantize_dispatch_kernel(
     q.sf = 0u;
     if (valid) {
       const uint4* src = reinterpret_cast<const uint4*>(x + r * ld + static_cast<int64_t>(b) * 16);
-      q = quantize_block(__ldg(src), __ldg(src + 1), g);
+      q = quantize_block(__ldg(src), __ldg(src + 1), k);
     }
     const uint32_t word = gather4_bytes(q.sf);
     const int64_t kb = b >> 4;

@@ -88,6 +88,33 @@ def test_quantize_e2m1_rounding_at_exact_ties(dstep, amax, scode):
     assert np.array_equal(packed.cpu().numpy(), p_ref)
 
 
+@pytest.mark.parametrize("gval", [2.0 ** -8, 0.0123, 3.0e-38, 1.0e-39, 5.0e35])
+def test_quantize_block_scales_at_e4m3_midpoints(gval):
+    """Block maxima b = 3 (2j + 1) 2^k make s = (b / 6) / g an exact midpoint
+    between two E4M3 values when g is a power of two (ties go to the even
+    code); their BF16 neighbours fall just either side.  Other globals put s
+    anywhere, including a global so small (or subnormal, or huge) that every
+    block takes the exact division chain."""
+    vals = []
+    for j in range(8, 16):
+        for k in range(-12, 4):
+            b = np.float32(3 * (2 * j + 1) * 2.0 ** k)
+            bits = inputs.to_bf16(np.array([b], np.float32)).view(torch.int16).numpy()[0]
+            for db in (-2, -1, 0, 1, 2):
+                vals.append(np.array([bits + db], np.int32).astype(np.int16)[0])
+    amaxes = torch.from_numpy(np.array(vals, np.int16)).view(torch.bfloat16).float().numpy()
+    g = inputs.rng(1234)
+    x = g.standard_normal((len(amaxes), 16)).astype(np.float32) * 0.3 * amaxes[:, None]
+    x[:, 5] = amaxes                                 # the block maximum
+    x[::2, 5] *= -1.0                                # half of them negative
+    xb = inputs.to_bf16(x.reshape(-1, 64)) if x.size % 64 == 0 else inputs.to_bf16(x)
+    gg = torch.tensor([gval], dtype=torch.float32, device="cuda")
+    packed, scales, _ = F.quantize(xb.cuda(), global_scale=gg)
+    p_ref, s_ref, _ = oracle.quantize(xb.float().numpy(), g=np.float32(gval))
+    assert np.array_equal(scales.cpu().numpy(), s_ref)
+    assert np.array_equal(packed.cpu().numpy(), p_ref)
+
+
 def test_quantize_strided_rows_and_given_global():
     g = inputs.rng(99)
     base = inputs.normal_bf16(g, (20, 200)).cuda()

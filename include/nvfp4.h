@@ -353,15 +353,31 @@ nvfp4_status nvfp4_grouped_gemm_tiles(const uint8_t* A_tiles, const float* gA,
  *             grouped tile layout nvfp4_quantize_dispatch writes for R routes,
  *             E experts and K = N/2 (nvfp4_grouped_tiles_bytes(R, E, N/2)
  *             bytes).  Feed it to nvfp4_grouped_gemm_tiles as A_tiles with gA = g_h.
- * N % 256 == 0, K % 64 == 0, E <= 256, and the decode regime: the token-tile
- * width nvfp4_grouped_chunk_rows(R, E) must be 32 or 64 (NVFP4_ERR_UNSUPPORTED
- * otherwise).
+ * N % 256 == 0, K % 64 == 0, E <= 256.  A unit holds a gate tile and its up
+ * tile against one token tile of nvfp4_grouped_chunk_rows(R, E) routes (32,
+ * 64 or 128).
  */
 nvfp4_status nvfp4_moe_gate_up_silu(const uint8_t* A_tiles, const float* gA,
                                     const uint8_t* W_tiles, const float* gW,
                                     const int32_t* expert_offsets, int32_t E, int64_t T,
                                     int32_t topk, int64_t N, int64_t K, const float* g_h,
                                     uint8_t* h_tiles, void* stream);
+
+/*
+ * Two-phase form of the fused gate_up epilogue, for callers that do not have
+ * the global scale of h in advance: the same grouped GEMM and h = SiLU(g) * u
+ * (binary32), written as BF16 (round to nearest even) in route order,
+ * h_out[p, f] for route p and feature f < N/2 (row stride N/2 elements,
+ * 16-byte aligned).  Then nvfp4_quantize_dispatch over h_out (rows = R,
+ * route_pos NULL, fanout 1) finds the global of h from its amax and writes
+ * the operand tiles of the down projection.  Same arguments and limits as
+ * nvfp4_moe_gate_up_silu otherwise.
+ */
+nvfp4_status nvfp4_moe_gate_up_silu_bf16(const uint8_t* A_tiles, const float* gA,
+                                         const uint8_t* W_tiles, const float* gW,
+                                         const int32_t* expert_offsets, int32_t E, int64_t T,
+                                         int32_t topk, int64_t N, int64_t K, void* h_out,
+                                         void* stream);
 
 /*
  * Allocation-free weighted-combine grouped GEMM.  (This entry point is a

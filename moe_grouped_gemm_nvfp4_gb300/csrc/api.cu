@@ -690,10 +690,6 @@ nvfp4_status nvfp4_moe_gate_up_silu(const uint8_t* A_tiles, const float* gA,
   if (N % 256 != 0 || K % 64 != 0 || E > nvfp4::kGroupedMaxExperts) return NVFP4_ERR_UNSUPPORTED;
   const int64_t R = T * topk;
   if (R > (1LL << 30) || static_cast<int64_t>(E) * N > (1LL << 30)) return NVFP4_ERR_UNSUPPORTED;
-  // the fused epilogue pairs each gate tile with its up tile in one unit,
-  // which the 32- and 64-route token tiles of the decode regime provide
-  const int tw = nvfp4::grouped_tile_width(R, E);
-  if (tw != 32 && tw != 64) return NVFP4_ERR_UNSUPPORTED;
   if (!aligned16(A_tiles) || !aligned16(W_tiles) || !aligned16(h_tiles) ||
       (reinterpret_cast<uintptr_t>(g_h) & 3u))
     return NVFP4_ERR_UNSUPPORTED;
@@ -725,6 +721,50 @@ nvfp4_status nvfp4_moe_gate_up_silu(const uint8_t* A_tiles, const float* gA,
   a.g_h = g_h;
   a.h_nkb = static_cast<int32_t>((N / 2 + 255) / 256);
   if (nvfp4::launch_gemm(unused, unused, a, nvfp4::kGroupedSiluMul, d->sms,
+                         static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return cuda_fail();
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_moe_gate_up_silu_bf16(const uint8_t* A_tiles, const float* gA,
+                                         const uint8_t* W_tiles, const float* gW,
+                                         const int32_t* expert_offsets, int32_t E, int64_t T,
+                                         int32_t topk, int64_t N, int64_t K, void* h_out,
+                                         void* stream) {
+  if (!A_tiles || !gA || !W_tiles || !gW || !expert_offsets || !h_out)
+    return NVFP4_ERR_INVALID_ARG;
+  if (E <= 0 || T < 0 || topk <= 0 || N <= 0 || K <= 0) return NVFP4_ERR_INVALID_ARG;
+  if (N % 256 != 0 || K % 64 != 0 || E > nvfp4::kGroupedMaxExperts) return NVFP4_ERR_UNSUPPORTED;
+  const int64_t R = T * topk;
+  if (R > (1LL << 30) || static_cast<int64_t>(E) * N > (1LL << 30)) return NVFP4_ERR_UNSUPPORTED;
+  if (!aligned16(A_tiles) || !aligned16(W_tiles) || !aligned16(h_out))
+    return NVFP4_ERR_UNSUPPORTED;
+  DeviceState* d = nullptr;
+  nvfp4_status st = device_state(&d);
+  if (st != NVFP4_OK) return st;
+  if (R == 0) return NVFP4_OK;
+  CUtensorMap unused;
+  std::memset(&unused, 0, sizeof(unused));
+  nvfp4::GemmArgs a{};
+  a.sfx = W_tiles;
+  a.sfy = A_tiles;
+  a.gx = gW;
+  a.gy = gA;
+  a.K = K;
+  a.rows_x = static_cast<int32_t>(E * N);
+  a.rows_y = static_cast<int32_t>(R);
+  a.expert_offsets = expert_offsets;
+  a.E = E;
+  a.n_out = static_cast<int32_t>(N);
+  a.out = h_out;
+  a.ldc = N / 2;
+  a.vec_store = 1;
+  a.ybox_rows = 16;
+  a.topk = topk;
+  a.status = d->status;
+  a.timeout_ns = g_timeout_ns.load();
+  a.debug_flags = g_debug_flags.load();
+  if (nvfp4::launch_gemm(unused, unused, a, nvfp4::kGroupedSiluBf16, d->sms,
                          static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return cuda_fail();
   return NVFP4_OK;

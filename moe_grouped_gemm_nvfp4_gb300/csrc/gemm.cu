@@ -61,7 +61,10 @@ struct Cfg {
   // and the scale copies of Y per weight byte)
   // (64-row tiles with two X tiles serve the fused SiLU-mul epilogue and
   // sparse weights)
-  static_assert(MT == 1 || (MT == 2 && (BN == 32 || BN == 64)), "unit height");
+  // (128-row token tiles with two X tiles: the fused SiLU-mul epilogue of the
+  // gate_up projection at wide token tiles)
+  static_assert(MT == 1 || (MT == 2 && (BN == 32 || BN == 64 || (BN == 128 && !SP))),
+                "unit height");
   // SP: X (the weights) arrives as 2:4-sparse tiles and is expanded in shared
   // memory by the decompression warps before the MMAs read it
   static_assert(!SP || (BN <= 128 && (MT == 1 || BN <= 64)),
@@ -119,7 +122,8 @@ struct Cfg {
   // accumulator buffers: two (the epilogue of one tile overlaps the next
   // tile's MMAs), except for 256-wide tiles, whose one accumulator already
   // takes half of tensor memory
-  static constexpr int kAccBufs = BN == 256 ? 1 : 2;
+  // (and for the two 128-column accumulators of a 128-row two-tile unit)
+  static constexpr int kAccBufs = (BN == 256 || (MT == 2 && BN == 128)) ? 1 : 2;
   static constexpr int kAccCols = BN;                  // one accumulator
   // Epilogue warp groups: 256-wide tiles hold their single accumulator until
   // the epilogue has read it, so a second group of four warps (warps 7-10)
@@ -178,7 +182,8 @@ template <int BN, int MT, bool SP = false>
 __device__ __forceinline__ Unit get_unit(int u, int mode, const GemmArgs& a, const Tables& t,
                                          int tiles_x, int64_t atoms_per_rowtile) {
   Unit un;
-  if (mode == kGrouped || mode == kGroupedCombine || mode == kGroupedSiluMul) {
+  if (mode == kGrouped || mode == kGroupedCombine || mode == kGroupedSiluMul ||
+      mode == kGroupedSiluBf16) {
     int lo = 0, hi = a.E;
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -190,7 +195,7 @@ __device__ __forceinline__ Unit get_unit(int u, int mode, const GemmArgs& a, con
     const int local = u - t.up[e];
     // SiLU-mul: X tile m (gate rows) pairs with X tile m + mtiles / 2 (the
     // up rows of the same features); otherwise a unit's X tiles are adjacent
-    const bool glu = mode == kGroupedSiluMul;
+    const bool glu = mode == kGroupedSiluMul || mode == kGroupedSiluBf16;
     const int mt = glu ? (local % munits) : (local % munits) * MT;   // first X tile
     const int nt = local / munits;
     const int cnt = t.off[e + 1] - t.off[e];
@@ -357,7 +362,8 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const bool grouped = (mode == kGrouped || mode == kGroupedCombine || mode == kGroupedSiluMul);
+  const bool grouped = (mode == kGrouped || mode == kGroupedCombine || mode == kGroupedSiluMul ||
+                        mode == kGroupedSiluBf16);
   const int64_t atoms_per_rowtile = a.K >> 6;
   const int nkb = static_cast<int>((a.K + kBK - 1) / kBK);
   const int tiles_x = (a.rows_x + 127) >> 7;
@@ -784,7 +790,8 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
       tc_fence_after();
       const float alpha = __fmul_rn(grouped ? a.gx[un.e] : a.gx[0], gy);
       const int n_valid = un.y_rows;
-      if (!SP && MT == 2 && mode == kGroupedSiluMul) {   // (sparse weights: not fused)
+      if (!SP && MT == 2 && (mode == kGroupedSiluMul || mode == kGroupedSiluBf16)) {
+        // (sparse weights: not fused)
         // Gate (X tile 0) and up (X tile 1) accumulators of the same 128
         // features: h = SiLU(alpha * gate) * (alpha * up) in FP32, quantised
         // per 16 features with the given global of h and written as NVFP4
@@ -806,7 +813,8 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
         };
         // one 32-token chunk at a time; the accumulator buffer goes back to
         // the MMA warps after the last chunk (the other buffer keeps them busy)
-        static_assert(MT != 2 || C::kAccBufs == 2, "fused epilogue: double-buffered accumulator");
+        // (one accumulator buffer for 128-row units: the next unit's MMAs
+        // wait for this epilogue)
 #pragma unroll 1
         for (int ci = 0; ci < BN / 32; ++ci) {
         if (ci * 32 >= n_valid) break;
@@ -816,7 +824,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
         warp_transpose32(rg, lane);                // lane = token, 32 features of quarter q
         warp_transpose32(ru, lane);
         if (ci * 32 + lane < n_valid) {
-          const ScaleK gh = scale_consts(*a.g_h);
+          const ScaleK gh = scale_consts(mode == kGroupedSiluMul ? *a.g_h : 0.0f);
           float h[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
@@ -824,10 +832,25 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
             const float uz = __fmul_rn(__uint_as_float(ru[i]), alpha);
             h[i] = __fmul_rn(__fdiv_rn(gz, __fadd_rn(1.0f, expf(-gz))), uz);
           }
+          const int f0 = un.x_local0 + q * 32;     // first feature of h in this lane
+          if (mode == kGroupedSiluBf16) {
+            // two-phase form: h in BF16, route order, 32 consecutive features
+            uint16_t* dst = reinterpret_cast<uint16_t*>(a.out) +
+                            static_cast<int64_t>(un.y_row0 + ci * 32 + lane) * a.ldc + f0;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint32_t w4[4];
+#pragma unroll
+              for (int hh = 0; hh < 4; ++hh)
+                w4[hh] = static_cast<uint32_t>(f32_to_bf16_rn(h[8 * v + 2 * hh])) |
+                         (static_cast<uint32_t>(f32_to_bf16_rn(h[8 * v + 2 * hh + 1])) << 16);
+              reinterpret_cast<uint4*>(dst)[v] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+            continue;
+          }
           const Block16 b0 = quantize16(h, gh);
           const Block16 b1 = quantize16(h + 16, gh);
-          const int f0 = un.x_local0 + q * 32;     // first feature of h in this lane
-          const int row = ci * 32 + lane;          // token tile = one layout chunk (BN <= 64)
+          const int row = ci * 32 + lane;          // token tile = one layout chunk (BN <= 128)
           const int64_t tile = (static_cast<int64_t>(un.y_tile) * a.h_nkb + (f0 >> 8)) *
                                kOperandTileBytes;
           const int chunk = (f0 & 255) >> 5;       // 16-byte chunk of the 128-byte row
@@ -844,7 +867,8 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
         if (++abuf == C::kAccBufs) { abuf = 0; aphase ^= 1u; }
         continue;
       }
-      if (C::kAccBufs == 1 && mode != kGroupedCombine && mode != kGroupedSiluMul) {
+      if (C::kAccBufs == 1 && mode != kGroupedCombine && mode != kGroupedSiluMul &&
+          mode != kGroupedSiluBf16) {
         // One accumulator: the next unit's MMAs wait for it.  Read all of it
         // into registers as BF16 first, hand it back, then store, so the
         // stores overlap the next unit's MMAs.
@@ -1044,6 +1068,7 @@ cudaError_t init_gemm_attributes() {
   cudaError_t e = set_smem_attr<32>();
   if (e == cudaSuccess) e = set_smem_attr<32, 2>();
   if (e == cudaSuccess) e = set_smem_attr<64, 2>();
+  if (e == cudaSuccess) e = set_smem_attr<128, 2>();
   if (e == cudaSuccess) e = set_smem_attr<64>();
   if (e == cudaSuccess) e = set_smem_attr<128>();
   if (e == cudaSuccess) e = set_smem_attr<256>();
@@ -1089,11 +1114,16 @@ cudaError_t launch_gemm(const CUtensorMap& tmx, const CUtensorMap& tmy, const Ge
       default: return launch_bn<128, 1, true>(tmx, tmy, a, mode, grid, s);
     }
   }
-  // gate and up tiles pair up in one unit of 32 or 64 routes (with dense
-  // weights, <64, 2> serves only this mode)
-  if (mode == kGroupedSiluMul)
-    return grouped_tile_width(a.rows_y, a.E) == 32 ? launch_bn<32, 2>(tmx, tmy, a, mode, grid, s)
-                                                   : launch_bn<64, 2>(tmx, tmy, a, mode, grid, s);
+  // gate and up tiles pair up in one unit of 32, 64 or 128 routes, the
+  // activation layout's chunk width (with dense weights, <64, 2> and <128, 2>
+  // serve only these modes)
+  if (mode == kGroupedSiluMul || mode == kGroupedSiluBf16) {
+    switch (grouped_chunk_rows(a.rows_y, a.E)) {
+      case 32: return launch_bn<32, 2>(tmx, tmy, a, mode, grid, s);
+      case 64: return launch_bn<64, 2>(tmx, tmy, a, mode, grid, s);
+      default: return launch_bn<128, 2>(tmx, tmy, a, mode, grid, s);
+    }
+  }
   switch (grouped_tile_width(a.rows_y, a.E)) {
     case 32:   // two weight tiles per unit when the expert's rows pair up
       return (a.n_out / 128) % 2 == 0 ? launch_bn<32, 2>(tmx, tmy, a, mode, grid, s)

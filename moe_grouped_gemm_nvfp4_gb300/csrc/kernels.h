@@ -58,6 +58,7 @@ enum GemmMode : int {
   kGrouped = 2,         // out[route][n]
   kGroupedCombine = 3,  // ws[token][n] += w * y
   kGroupedSiluMul = 4,  // h[route][f] = SiLU(gate) * up, quantised into h_tiles
+  kGroupedSiluBf16 = 5, // h[route][f] = SiLU(gate) * up, BF16 into out (two-phase form)
 };
 
 struct GemmArgs {

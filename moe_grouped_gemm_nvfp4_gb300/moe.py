@@ -225,19 +225,25 @@ class DecodeLayer:
 
 
 class FusedMLP:
-    """One expert MLP pass, decode regime: route, quantise + dispatch x, then
-    gate_up, SiLU(gate) * up and the NVFP4 quantisation of h in one grouped
-    GEMM launch (nvfp4_moe_gate_up_silu), then the down projection with the
-    weighted combine.  h never exists in BF16; its global scale g_h is given
-    (a device float, calibrated by the caller).
+    """One expert MLP pass: route, quantise + dispatch x, then gate_up,
+    SiLU(gate) * up and the NVFP4 quantisation of h in one grouped GEMM launch
+    (nvfp4_moe_gate_up_silu), then the down projection with the weighted
+    combine.  h never exists in BF16; its global scale g_h is given (a device
+    float, calibrated by the caller).
+
+    g_h=None selects the two-phase form: the gate_up launch writes h in BF16
+    (nvfp4_moe_gate_up_silu_bf16), the dispatch quantiser finds its global from
+    its amax and writes the down projection's tiles.
     """
 
     def __init__(self, w_gate_up: ExpertWeights, w_down: ExpertWeights, T: int, topk: int,
-                 g_h: torch.Tensor, device="cuda"):
+                 g_h: torch.Tensor = None, device="cuda"):
         assert w_gate_up.E == w_down.E and w_gate_up.N == 2 * w_down.K
         self.w1, self.w2, self.T, self.topk, self.g_h = w_gate_up, w_down, T, topk, g_h
         self.gate_up = GroupedPlan(w_gate_up, T, topk, "gather", device, out=False)
         self.down = GroupedPlan(w_down, T, topk, "combine", device, routing_from=self.gate_up)
+        self.h = (torch.empty((max(T * topk, 1), w_down.K), dtype=torch.bfloat16,
+                              device=torch.device(device)) if g_h is None else None)
         self._side = torch.cuda.Stream(device=torch.device(device))
 
     def step(self, x, topk_ids, topk_weights, stream=None):
@@ -246,11 +252,18 @@ class FusedMLP:
         gu, dn, w1, w2 = self.gate_up, self.down, self.w1, self.w2
         _route_and_amax(gu, x, topk_ids, self._side, stream)
         gu.quantize(x, stream, amax_done=True)
-        F.nvfp4_moe_gate_up_silu(gu.a_tiles, gu.a_g, w1.tiles, w1.g, gu.expert_offsets, w1.E,
-                                 self.T, self.topk, w1.N, w1.K, self.g_h, dn.a_tiles, stream)
-        F.nvfp4_grouped_gemm_tiles(dn.a_tiles, self.g_h, w2.tiles, w2.g, dn.expert_offsets, w2.E,
-                             self.T, self.topk, w2.N, w2.K, dn.route_token, dn.route_slot,
-                             topk_weights, dn.out, dn.workspace, stream)
+        if self.g_h is not None:
+            F.nvfp4_moe_gate_up_silu(gu.a_tiles, gu.a_g, w1.tiles, w1.g, gu.expert_offsets, w1.E,
+                                     self.T, self.topk, w1.N, w1.K, self.g_h, dn.a_tiles, stream)
+            g_h = self.g_h
+        else:
+            F.nvfp4_moe_gate_up_silu_bf16(gu.a_tiles, gu.a_g, w1.tiles, w1.g, gu.expert_offsets,
+                                          w1.E, self.T, self.topk, w1.N, w1.K, self.h, stream)
+            dn.quantize(self.h, stream)
+            g_h = dn.a_g
+        F.nvfp4_grouped_gemm_tiles(dn.a_tiles, g_h, w2.tiles, w2.g, dn.expert_offsets, w2.E,
+                                   self.T, self.topk, w2.N, w2.K, dn.route_token, dn.route_slot,
+                                   topk_weights, dn.out, dn.workspace, stream)
         return dn.out
 
 

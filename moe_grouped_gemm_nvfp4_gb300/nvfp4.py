@@ -62,6 +62,8 @@ _SIGS = {
                                                 _I64, _P, _P, _P, _P, _P, _SZ, _P]),
     "nvfp4_moe_gate_up_silu": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I64, _I32, _I64, _I64,
                                               _P, _P, _P]),
+    "nvfp4_moe_gate_up_silu_bf16": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I64, _I32, _I64,
+                                                   _I64, _P, _P]),
     "nvfp4_noalloc_workspace_floats": (_SZ, []),
     "nvfp4_decode_attention_workspace_bytes": (_SZ, [_I32, _I32, _I32, _I64, _I32]),
     "nvfp4_decode_attention": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32,
@@ -235,6 +237,13 @@ def nvfp4_moe_gate_up_silu(A_tiles, gA, W_tiles, gW, expert_offsets, E: int, T: 
     _check("nvfp4_moe_gate_up_silu", load().nvfp4_moe_gate_up_silu(
         _ptr(A_tiles), _ptr(gA), _ptr(W_tiles), _ptr(gW), _ptr(expert_offsets), E, T, topk, N, K,
         _ptr(g_h), _ptr(h_tiles), _stream(stream)))
+
+
+def nvfp4_moe_gate_up_silu_bf16(A_tiles, gA, W_tiles, gW, expert_offsets, E: int, T: int,
+                                topk: int, N: int, K: int, h_out, stream=None) -> None:
+    _check("nvfp4_moe_gate_up_silu_bf16", load().nvfp4_moe_gate_up_silu_bf16(
+        _ptr(A_tiles), _ptr(gA), _ptr(W_tiles), _ptr(gW), _ptr(expert_offsets), E, T, topk, N, K,
+        _ptr(h_out), _stream(stream)))
 
 
 def nvfp4_amax_partials(x, R: int, E: int, tiles, stream=None) -> None:

@@ -710,17 +710,26 @@ def measure_configs(args, dev, groups=None):
         gate, up = gu_out.float().split(N1 // 2, dim=1)
         g_h = (torch.nn.functional.silu(gate) * up).abs().amax().reshape(1) / 2688.0
         mlp = moe.FusedMLP(W1, W2, tokens, TOPK, g_h.to(torch.float32), dev)
+        mlp1 = moe.FusedMLP(W1, W2, tokens, TOPK, g_h.to(torch.float32), dev, single_launch=True)
+        mlp2 = moe.FusedMLP(W1, W2, tokens, TOPK, None, dev)          # two-phase global of h
         t_fused = _timed(lambda: mlp.step(d["x"], d["ids"], d["wts"]), iters, flush)
+        t_one = _timed(lambda: mlp1.step(d["x"], d["ids"], d["wts"]), iters, flush)
+        t_two = _timed(lambda: mlp2.step(d["x"], d["ids"], d["wts"]), iters, flush)
         t_split = _timed(lambda: layer.step(d["x"], d["ids"], d["h"], d["wts"]), iters, flush)
         fl = 2.0 * tokens * TOPK * (N1 * K1 + N2 * K2)
         n_act = int(np.count_nonzero(np.bincount(host["ids"].numpy().reshape(-1), minlength=E)))
         byt = n_act * (N1 * K1 + N2 * K2) * 0.5625 + 2.0 * (tokens * K1 + tokens * N2)
         out[f"decode_mlp_fused_T{tokens}"] = _entry(
             t_fused, fl, byt, hbm, fp4, unfused_pass_us=round(t_split * 1e3, 2),
+            one_launch_pass_us=round(t_one * 1e3, 2), two_phase_pass_us=round(t_two * 1e3, 2),
             note="route + quantise x + fused gate_up/SiLU/quantise-h + down with combine; "
-                 "unfused = the same pass with a BF16 gate_up output and h quantised by its "
-                 "own kernels")
-        del layer, mlp, W1, W2, d, gu_out, gate, up
+                 "one_launch = gate_up and down in one persistent launch; two_phase = h "
+                 "written in BF16 and quantised with the global of its own amax; unfused = "
+                 "the same pass with a BF16 gate_up output and h quantised by its own kernels")
+        out[f"decode_mlp_one_launch_T{tokens}"] = _entry(
+            t_one, fl, byt, hbm, fp4,
+            note="the fused expert MLP with gate_up and down in one persistent launch")
+        del layer, mlp, mlp1, mlp2, W1, W2, d, gu_out, gate, up
         torch.cuda.empty_cache()
     # decode attention over an NVFP4 KV cache (every cache byte read once):
     # 128-wide heads in groups of 4 and of 1, and 512-wide heads

@@ -364,6 +364,38 @@ nvfp4_status nvfp4_moe_gate_up_silu(const uint8_t* A_tiles, const float* gA,
                                     uint8_t* h_tiles, void* stream);
 
 /*
+ * The whole expert MLP in one persistent launch ("The FP4 Frontier",
+ * Finding 5: a persistent kernel over all experts; the MLP's intermediate
+ * stays NVFP4 between the projections): the gate_up units of
+ * nvfp4_moe_gate_up_silu (h = SiLU(g) * u quantised with the given g_h into
+ * h_tiles), then in the same launch the down projection's units over h with
+ * the weighted combine of nvfp4_grouped_gemm_tiles, then the BF16 rounding of
+ * the sums.  A down unit starts once every gate_up unit of its token tile has
+ * written its features of h (a count per token tile in the workspace, waited
+ * on with the bounded wait: NVFP4_ERR_TIMEOUT on expiry).  The launch is
+ * cooperative (all CTAs resident at once), so those waits always end.
+ *   A_tiles, gA, W1_tiles, gW1, expert_offsets, E, T, topk, N1, K1, g_h,
+ *       h_tiles  as in nvfp4_moe_gate_up_silu (N = N1).
+ *   W2_tiles, gW2  down weights as operand tiles over [E * N2, N1 / 2], one
+ *       global per expert.
+ *   route_token, route_slot, topk_weights, out  as in nvfp4_grouped_gemm_tiles
+ *       with the combine: out = BF16 [T, N2].
+ *   workspace  nvfp4_moe_mlp_workspace_bytes(T, topk, E, N2) bytes, 16-byte
+ *       aligned, caller-owned: the FP32 sums [T, N2] and the ready counts,
+ *       cleared by the call.
+ * N1 % 256 == 0, N2 % 256 == 0, K1 % 64 == 0, E <= 256.
+ */
+size_t nvfp4_moe_mlp_workspace_bytes(int64_t T, int32_t topk, int32_t E, int64_t N2);
+
+nvfp4_status nvfp4_moe_mlp(const uint8_t* A_tiles, const float* gA, const uint8_t* W1_tiles,
+                           const float* gW1, const uint8_t* W2_tiles, const float* gW2,
+                           const int32_t* expert_offsets, int32_t E, int64_t T, int32_t topk,
+                           int64_t N1, int64_t K1, int64_t N2, const float* g_h, uint8_t* h_tiles,
+                           const int32_t* route_token, const int32_t* route_slot,
+                           const float* topk_weights, void* out, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/*
  * Two-phase form of the fused gate_up epilogue, for callers that do not have
  * the global scale of h in advance: the same grouped GEMM and h = SiLU(g) * u
  * (binary32), written as BF16 (round to nearest even) in route order,

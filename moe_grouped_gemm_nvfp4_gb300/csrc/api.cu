@@ -87,11 +87,15 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // The grouped activation tiles proper, and the scratch after them that holds
 // the tensor amax's per-block maxima between the amax and dispatch kernels.
-size_t grouped_tiles_body_bytes(int64_t R, int32_t E, int64_t K) {
+// Upper bound on the token tiles (layout chunks) of R routes over E experts.
+int64_t grouped_token_tiles(int64_t R, int32_t E) {
   const int64_t chunk = nvfp4::grouped_chunk_rows(R, E);
   const int64_t nonempty = R < E ? R : E;
-  const int64_t tiles = (R + (chunk - 1) * nonempty) / chunk;
-  return static_cast<size_t>(tiles) * static_cast<size_t>((K + 255) / 256) *
+  return (R + (chunk - 1) * nonempty) / chunk;
+}
+
+size_t grouped_tiles_body_bytes(int64_t R, int32_t E, int64_t K) {
+  return static_cast<size_t>(grouped_token_tiles(R, E)) * static_cast<size_t>((K + 255) / 256) *
          static_cast<size_t>(nvfp4::kOperandTileBytes);
 }
 constexpr size_t kAmaxScratchBytes = 16384;
@@ -767,6 +771,84 @@ nvfp4_status nvfp4_moe_gate_up_silu_bf16(const uint8_t* A_tiles, const float* gA
   if (nvfp4::launch_gemm(unused, unused, a, nvfp4::kGroupedSiluBf16, d->sms,
                          static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return cuda_fail();
+  return NVFP4_OK;
+}
+
+size_t nvfp4_moe_mlp_workspace_bytes(int64_t T, int32_t topk, int32_t E, int64_t N2) {
+  if (T < 0 || topk <= 0 || E <= 0 || N2 < 0) return 0;
+  const size_t sums = nvfp4_combine_workspace_bytes(T, N2);
+  return sums + static_cast<size_t>(grouped_token_tiles(T * topk, E)) * sizeof(uint32_t);
+}
+
+nvfp4_status nvfp4_moe_mlp(const uint8_t* A_tiles, const float* gA, const uint8_t* W1_tiles,
+                           const float* gW1, const uint8_t* W2_tiles, const float* gW2,
+                           const int32_t* expert_offsets, int32_t E, int64_t T, int32_t topk,
+                           int64_t N1, int64_t K1, int64_t N2, const float* g_h, uint8_t* h_tiles,
+                           const int32_t* route_token, const int32_t* route_slot,
+                           const float* topk_weights, void* out, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  if (!A_tiles || !gA || !W1_tiles || !gW1 || !W2_tiles || !gW2 || !expert_offsets || !g_h ||
+      !h_tiles || !route_token || !route_slot || !topk_weights || !out || !workspace)
+    return NVFP4_ERR_INVALID_ARG;
+  if (E <= 0 || T < 0 || topk <= 0 || N1 <= 0 || K1 <= 0 || N2 <= 0) return NVFP4_ERR_INVALID_ARG;
+  if (N1 % 256 != 0 || N2 % 256 != 0 || K1 % 64 != 0 || E > nvfp4::kGroupedMaxExperts)
+    return NVFP4_ERR_UNSUPPORTED;
+  const int64_t R = T * topk;
+  if (R > (1LL << 30) || static_cast<int64_t>(E) * N1 > (1LL << 30) ||
+      static_cast<int64_t>(E) * N2 > (1LL << 30))
+    return NVFP4_ERR_UNSUPPORTED;
+  if (workspace_bytes < nvfp4_moe_mlp_workspace_bytes(T, topk, E, N2)) return NVFP4_ERR_UNSUPPORTED;
+  if (!aligned16(A_tiles) || !aligned16(W1_tiles) || !aligned16(W2_tiles) || !aligned16(h_tiles) ||
+      !aligned16(out) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(g_h) & 3u))
+    return NVFP4_ERR_UNSUPPORTED;
+  DeviceState* d = nullptr;
+  nvfp4_status st = device_state(&d);
+  if (st != NVFP4_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (R == 0) {
+    if (T > 0 && cudaMemsetAsync(out, 0, T * N2 * 2, s) != cudaSuccess) return cuda_fail();
+    return NVFP4_OK;
+  }
+  // FP32 sums of the combine, then one ready count per token tile; both start at zero
+  float* ws = static_cast<float*>(workspace);
+  uint32_t* ready = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) +
+                                                nvfp4_combine_workspace_bytes(T, N2));
+  if (cudaMemsetAsync(workspace, 0, nvfp4_moe_mlp_workspace_bytes(T, topk, E, N2), s) !=
+      cudaSuccess)
+    return cuda_fail();
+  nvfp4::GemmArgs a{};
+  a.sfx = W1_tiles;
+  a.sfy = A_tiles;
+  a.gx = gW1;
+  a.gy = gA;
+  a.K = K1;
+  a.rows_x = static_cast<int32_t>(E * N1);
+  a.rows_y = static_cast<int32_t>(R);
+  a.expert_offsets = expert_offsets;
+  a.E = E;
+  a.n_out = static_cast<int32_t>(N1);
+  a.ldc = N2;
+  a.vec_store = 1;
+  a.ybox_rows = 16;
+  a.route_token = route_token;
+  a.route_slot = route_slot;
+  a.topk_w = topk_weights;
+  a.topk = topk;
+  a.n_tokens = static_cast<int32_t>(T);
+  a.ws = ws;
+  a.status = d->status;
+  a.timeout_ns = g_timeout_ns.load();
+  a.debug_flags = g_debug_flags.load();
+  a.h_tiles = h_tiles;
+  a.g_h = g_h;
+  a.h_nkb = static_cast<int32_t>((N1 / 2 + 255) / 256);
+  a.sfx2 = W2_tiles;
+  a.gx2 = gW2;
+  a.K2 = N1 / 2;
+  a.n_out2 = static_cast<int32_t>(N2);
+  a.ready = ready;
+  if (nvfp4::launch_mlp_fused(a, d->sms, s) != cudaSuccess) return cuda_fail();
+  if (nvfp4::launch_combine_finalize(ws, T, N2, out, d->sms, s) != cudaSuccess) return cuda_fail();
   return NVFP4_OK;
 }
 

@@ -170,6 +170,14 @@ struct Unit {
                       // weight tiles are read again by other units
   int32_t x_pair;     // grouped, MT == 2: row tiles from the first X tile to the second
   int32_t y_tile;     // grouped: first operand tile of the unit's token tile
+  // per-unit phase of the fused MLP (the other modes: one phase, these are
+  // the launch's own values)
+  int32_t emode;      // epilogue mode of the unit
+  int32_t k64;        // K / 64 of the unit's GEMM
+  int32_t n_out;      // rows of each expert's X (output features)
+  const uint8_t* xsrc;  // X operand tiles (or X scales)
+  const uint8_t* ysrc;  // Y operand tiles (or Y scales)
+  const float* gxp;     // X globals
 };
 
 struct Tables {
@@ -182,8 +190,51 @@ template <int BN, int MT, bool SP = false>
 __device__ __forceinline__ Unit get_unit(int u, int mode, const GemmArgs& a, const Tables& t,
                                          int tiles_x, int64_t atoms_per_rowtile) {
   Unit un;
+  un.emode = mode;
+  un.k64 = static_cast<int32_t>(a.K >> 6);
+  un.n_out = a.n_out;
+  un.xsrc = a.sfx;
+  un.ysrc = a.sfy;
+  un.gxp = a.gx;
+  if (mode == kMlpFused && u >= t.up[a.E]) {
+    // down projection unit: token tile tt (every expert's token tiles in
+    // order), X tiles m and m + 1 of the expert's down weight, Y = h tiles
+    const int munits1 = (a.n_out >> 7) / 2;       // gate_up units per token tile
+    const int mtiles2 = a.n_out2 >> 7;
+    const int munits2 = mtiles2 / MT;
+    const int u2 = u - t.up[a.E];
+    const int tt = u2 / munits2;
+    const int mt = (u2 % munits2) * MT;
+    int lo = 0, hi = a.E;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (t.up[mid] <= tt * munits1) lo = mid; else hi = mid;
+    }
+    const int e = lo;
+    const int nt = tt - t.up[e] / munits1;
+    const int cnt = t.off[e + 1] - t.off[e];
+    const int64_t n_kb2 = (a.K2 + kBK - 1) / kBK;
+    un.emode = kGroupedCombine;
+    un.k64 = static_cast<int32_t>(a.K2 >> 6);
+    un.n_out = a.n_out2;
+    un.xsrc = a.sfx2;
+    un.ysrc = a.h_tiles;
+    un.gxp = a.gx2;
+    un.e = e;
+    un.x_row0 = e * a.n_out2 + mt * 128;
+    un.x_local0 = mt * 128;
+    un.y_row0 = t.off[e] + nt * BN;
+    un.y_rows = min(BN, cnt - nt * BN);
+    un.sfx_off = static_cast<int64_t>(e * mtiles2 + mt) * n_kb2 * kOperandTileBytes;
+    un.y_tile = tt;
+    un.sfy_off = static_cast<int64_t>(tt) * n_kb2 * kOperandTileBytes;
+    un.x_reused = cnt > BN;
+    un.x_pair = 1;
+    return un;
+  }
   if (mode == kGrouped || mode == kGroupedCombine || mode == kGroupedSiluMul ||
-      mode == kGroupedSiluBf16) {
+      mode == kGroupedSiluBf16 || mode == kMlpFused) {
+    if (mode == kMlpFused) un.emode = kGroupedSiluMul;
     int lo = 0, hi = a.E;
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -195,7 +246,7 @@ __device__ __forceinline__ Unit get_unit(int u, int mode, const GemmArgs& a, con
     const int local = u - t.up[e];
     // SiLU-mul: X tile m (gate rows) pairs with X tile m + mtiles / 2 (the
     // up rows of the same features); otherwise a unit's X tiles are adjacent
-    const bool glu = mode == kGroupedSiluMul || mode == kGroupedSiluBf16;
+    const bool glu = mode == kGroupedSiluMul || mode == kGroupedSiluBf16 || mode == kMlpFused;
     const int mt = glu ? (local % munits) : (local % munits) * MT;   // first X tile
     const int nt = local / munits;
     const int cnt = t.off[e + 1] - t.off[e];
@@ -315,6 +366,39 @@ __device__ __forceinline__ void red_add_v4(float* dst, float4 v) {
                :: "l"(dst), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w) : "memory");
 }
 
+// Generic-proxy global accesses of this thread ordered with its async-proxy
+// (bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Adds 1 to a counter in global memory with release semantics at GPU scope.
+__device__ __forceinline__ void red_release_add1(uint32_t* p) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], 1;" :: "l"(p) : "memory");
+}
+
+// Waits (acquire at GPU scope) until *p >= target.  Gives up when the CTA
+// has aborted or after the time limit, recording NVFP4_ERR_TIMEOUT.
+__device__ __forceinline__ bool wait_count(const uint32_t* p, uint32_t target, CtaCtl* ctl,
+                                           int* status) {
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 0; i < 0x7FFFFFFFu; ++i) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    if (v >= target) return true;
+    if (*reinterpret_cast<volatile uint32_t*>(&ctl->abort)) return false;
+    if (globaltimer() - t0 > ctl->timeout_ns) {
+      *reinterpret_cast<volatile uint32_t*>(&ctl->abort) = 1u;
+      raise_status(status, NVFP4_ERR_TIMEOUT);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  *reinterpret_cast<volatile uint32_t*>(&ctl->abort) = 1u;
+  raise_status(status, NVFP4_ERR_TIMEOUT);
+  return false;
+}
+
 // Waits for a phase regardless of the abort flag (used only to drain copies
 // and MMAs already in flight); bounded by the timeout.
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t timeout) {
@@ -363,9 +447,13 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const bool grouped = (mode == kGrouped || mode == kGroupedCombine || mode == kGroupedSiluMul ||
-                        mode == kGroupedSiluBf16);
+                        mode == kGroupedSiluBf16 || mode == kMlpFused);
   const int64_t atoms_per_rowtile = a.K >> 6;
-  const int nkb = static_cast<int>((a.K + kBK - 1) / kBK);
+  // K / 64 of unit u: the fused MLP's down units (u at or past the gate_up
+  // units) have the down projection's depth
+  auto unit_k64 = [&](int u) {
+    return static_cast<int>(((mode == kMlpFused && u >= t.up[a.E]) ? a.K2 : a.K) >> 6);
+  };
   const int tiles_x = (a.rows_x + 127) >> 7;
 
   if (threadIdx.x == 0) {
@@ -429,7 +517,11 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
         t.tb[E] = it;
         const bool good = all_ok && t.off[0] == 0 && oE <= a.rows_y;
         if (!good) raise_status(a.status, NVFP4_ERR_DEVICE_CHECK);
-        s_units = good ? iu : 0;
+        // fused MLP: the down units follow, munits2 per token tile
+        const int32_t all = mode == kMlpFused
+                                ? iu + iu / ((a.n_out >> 7) / 2) * ((a.n_out2 >> 7) / MT)
+                                : iu;
+        s_units = good ? all : 0;
       }
     }
   } else if (threadIdx.x == 0) {
@@ -466,6 +558,22 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
       const uint64_t pol_x = un.x_reused ? pol_again : pol_once;
       const int ybox = (un.y_rows + 15) >> 4;                  // 16-row groups
       const int ny_loads = (un.y_rows + a.ybox_rows - 1) / a.ybox_rows;
+      const int k64 = unit_k64(u);
+      const int nkb = (k64 + 3) >> 2;
+      if (mode == kMlpFused && un.emode == kGroupedCombine) {
+        // a down unit reads h of its token tile: wait until every gate_up
+        // unit of that token tile has written its features (bounded), then
+        // order those generic-proxy stores before this warp's bulk copies
+        bool ok = true;
+        if (lane == 0)
+          ok = wait_count(a.ready + un.y_tile, static_cast<uint32_t>((a.n_out >> 7) / 2) * 4u,
+                          ctl, a.status);
+        if (!__shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0)) {
+          alive = false;
+          break;
+        }
+        fence_proxy_async_global();
+      }
       for (int kb = 0; kb < nkb; ++kb) {
         // a group of stages is refilled once the MMAs of its previous round completed
         if (stage % C::kGroup == 0 &&
@@ -474,7 +582,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
           alive = false;
           break;
         }
-        const int ksteps = min(4, static_cast<int>((a.K >> 6) - 4 * kb));
+        const int ksteps = min(4, k64 - 4 * kb);
         const uint32_t sx = sbase + stage * C::kStageBytes;
         const uint32_t ssfx = sx + kXTileBytes;
         const uint32_t sy = sx + C::kYOffset;
@@ -502,7 +610,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
         if (grouped) {
           // operand tiles: X codes + scales in one contiguous copy, Y codes
           // (only the unit's rows) and Y scales in two more
-          const uint8_t* yt = a.sfy + un.sfy_off + kb * kOperandTileBytes;
+          const uint8_t* yt = un.ysrc + un.sfy_off + kb * kOperandTileBytes;
           if (!SP && a.x_map) {
             // X as row-major codes (TMA, 128-byte swizzle: the layout the
             // operand tiles store) and atom-layout scales (one bulk copy)
@@ -517,18 +625,18 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
             }
           } else {
             const uint8_t* xt =
-                a.sfx + un.sfx_off + kb * (SP ? kSparseTileBytes : kOperandTileBytes);
+                un.xsrc + un.sfx_off + kb * (SP ? kSparseTileBytes : kOperandTileBytes);
             bulk_load_elect(sx, xt, xbytes, full_bar(stage), pol_x);
             if (MT == 2)                 // the unit's second weight tile
               bulk_load_elect(sx + C::kXPartBytes,
-                              xt + static_cast<int64_t>(un.x_pair) * ((a.K + kBK - 1) / kBK) *
+                              xt + static_cast<int64_t>(un.x_pair) * nkb *
                                        (SP ? kSparseTileBytes : kOperandTileBytes),
                               xbytes, full_bar(stage), pol_x);
           }
           bulk_load_elect(sy, yt, ybox_lo * 16 * kRowBytes, full_bar(stage), pol_y);
           bulk_load_elect(ssfy, yt + kXTileBytes, ksteps * 512, full_bar(stage), pol_y);
           if (ybox_hi > 0) {               // second operand tile of a 256-row token tile
-            const uint8_t* yt2 = yt + static_cast<int64_t>((a.K + kBK - 1) / kBK) * kOperandTileBytes;
+            const uint8_t* yt2 = yt + static_cast<int64_t>(nkb) * kOperandTileBytes;
             bulk_load_elect(sy + 128 * kRowBytes, yt2, ybox_hi * 16 * kRowBytes, full_bar(stage),
                             pol_y);
             bulk_load_elect(ssfy + kSFStageBytes, yt2 + kXTileBytes, ksteps * 512, full_bar(stage),
@@ -573,13 +681,15 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
     int uidx = 0;
     for (int u = blockIdx.x; u < units && alive; u += gridDim.x, ++uidx) {
       int y_rows = 0;
+      const int k64 = unit_k64(u);
+      const int nkb = (k64 + 3) >> 2;
       for (int kb = 0; kb < nkb; ++kb) {
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(full_bar(stage), phase, ctl, a.status))) {
           alive = false;
           break;
         }
         if (kb == 0) y_rows = unit_rows[uidx & (C::kUnitRing - 1)];
-        const int ksteps = min(4, static_cast<int>((a.K >> 6) - 4 * kb));
+        const int ksteps = min(4, k64 - 4 * kb);
         const uint32_t sx = sbase + stage * C::kStageBytes;
         const uint32_t ssfx = sx + C::kXsfOffset;
         const uint32_t ssfy = sx + C::kYOffset + C::kYTileBytes;
@@ -627,6 +737,8 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
     for (int u = blockIdx.x; u < units && alive; u += gridDim.x, ++uidx) {
       int y_rows = 0;
       uint32_t idesc = 0;
+      const int k64 = unit_k64(u);
+      const int nkb = (k64 + 3) >> 2;
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(acce_bar(abuf), aphase ^ 1u, ctl, a.status))) break;
       tc_fence_after();
       // accumulator of X tile x: column ((abuf * MT + x) * kIssuers + j) * BN
@@ -656,7 +768,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
           y_rows = unit_rows[uidx & (C::kUnitRing - 1)];
           idesc = idesc_nvf4(static_cast<uint32_t>((y_rows + 15) & ~15));
         }
-        const int ksteps = min(4, static_cast<int>((a.K >> 6) - 4 * kb));
+        const int ksteps = min(4, k64 - 4 * kb);
         const uint32_t sx = sbase + stage * C::kStageBytes;
         const uint32_t ssfx = sx + C::kXsfOffset;
         const uint32_t sy = sx + C::kYOffset;
@@ -724,6 +836,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
     uint32_t phase = 0, dphase = 0;
     bool alive = true;
     for (int u = blockIdx.x; u < units && alive; u += gridDim.x) {
+      const int nkb = (unit_k64(u) + 3) >> 2;
       for (int kb = 0; kb < nkb; ++kb) {
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(full_bar(stage), phase, ctl, a.status)) ||
             !__all_sync(0xFFFFFFFFu,
@@ -753,10 +866,13 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
     int abuf = 0;
     uint32_t aphase = 0;
     const float gy = *a.gy;
-    // accumulators that received at least one K step (issuer j's first is ks = j)
-    const int n_acc = (a.K >> 6) < C::kIssuers ? static_cast<int>(a.K >> 6) : C::kIssuers;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const Unit un = get_unit<BN, MT, SP>(u, mode, a, t, tiles_x, atoms_per_rowtile);
+      const int emode = un.emode;
+      // accumulators that received at least one K step (issuer j's first is ks = j)
+      const int n_acc = un.k64 < C::kIssuers ? un.k64 : C::kIssuers;
+      // the fused MLP's down units scale by the global of h
+      const float gy_u = (mode == kMlpFused && emode == kGroupedCombine) ? *a.g_h : gy;
       // Combine: fetch this lane's tokens and routing weights (one token per
       // lane per 32-column chunk) before waiting, so the dependent L2 round
       // trips overlap the MMAs instead of following them.  A token outside
@@ -764,7 +880,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
       // route is skipped (c_tok = -1) and the status word records it.
       int c_tok[BN / 32];
       float c_w[BN / 32];
-      if (mode == kGroupedCombine) {
+      if (emode == kGroupedCombine) {
 #pragma unroll
         for (int ci = 0; ci < BN / 32; ++ci) {
           const int col = ci * 32 + lane;
@@ -788,9 +904,9 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
       if (!__all_sync(0xFFFFFFFFu, mbar_wait_sleepy(accf_bar(abuf), aphase, ctl, a.status)))
         break;
       tc_fence_after();
-      const float alpha = __fmul_rn(grouped ? a.gx[un.e] : a.gx[0], gy);
+      const float alpha = __fmul_rn(grouped ? un.gxp[un.e] : a.gx[0], gy_u);
       const int n_valid = un.y_rows;
-      if (!SP && MT == 2 && (mode == kGroupedSiluMul || mode == kGroupedSiluBf16)) {
+      if (!SP && MT == 2 && (emode == kGroupedSiluMul || emode == kGroupedSiluBf16)) {
         // (sparse weights: not fused)
         // Gate (X tile 0) and up (X tile 1) accumulators of the same 128
         // features: h = SiLU(alpha * gate) * (alpha * up) in FP32, quantised
@@ -824,7 +940,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
         warp_transpose32(rg, lane);                // lane = token, 32 features of quarter q
         warp_transpose32(ru, lane);
         if (ci * 32 + lane < n_valid) {
-          const ScaleK gh = scale_consts(mode == kGroupedSiluMul ? *a.g_h : 0.0f);
+          const ScaleK gh = scale_consts(emode == kGroupedSiluMul ? *a.g_h : 0.0f);
           float h[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
@@ -833,7 +949,7 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
             h[i] = __fmul_rn(__fdiv_rn(gz, __fadd_rn(1.0f, expf(-gz))), uz);
           }
           const int f0 = un.x_local0 + q * 32;     // first feature of h in this lane
-          if (mode == kGroupedSiluBf16) {
+          if (emode == kGroupedSiluBf16) {
             // two-phase form: h in BF16, route order, 32 consecutive features
             uint16_t* dst = reinterpret_cast<uint16_t*>(a.out) +
                             static_cast<int64_t>(un.y_row0 + ci * 32 + lane) * a.ldc + f0;
@@ -865,10 +981,21 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
         tc_fence_before();
         mbar_arrive(acce_bar(abuf));               // both accumulators have been read
         if (++abuf == C::kAccBufs) { abuf = 0; aphase ^= 1u; }
+        if (mode == kMlpFused) {
+          // this warp's 32 features of h for the unit's tokens are written:
+          // count them for the token tile (each lane orders its stores, the
+          // warp meets, one lane releases); a token tile is complete at 4
+          // counts per gate_up unit.  No wait here: a warp that gave up
+          // above never blocks the others.
+          fence_proxy_async_global();
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) red_release_add1(a.ready + un.y_tile);
+        }
         continue;
       }
-      if (C::kAccBufs == 1 && mode != kGroupedCombine && mode != kGroupedSiluMul &&
-          mode != kGroupedSiluBf16) {
+      if (C::kAccBufs == 1 && emode != kGroupedCombine && emode != kGroupedSiluMul &&
+          emode != kGroupedSiluBf16) {
         // One accumulator: the next unit's MMAs wait for it.  Read all of it
         // into registers as BF16 first, hand it back, then store, so the
         // stores overlap the next unit's MMAs.
@@ -983,13 +1110,13 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
           const int f0 = un.x_local0 + xt * 128 + q * 32;  // first feature of this warp
           if (col < n_valid) {
             const int64_t y = un.y_row0 + col;
-            if (mode == kGroupedCombine) {
+            if (emode == kGroupedCombine) {
               int tok = c_tok[0];
               float w = c_w[0];
 #pragma unroll
               for (int ci = 1; ci < BN / 32; ++ci)
                 if (c0 == ci * 32) { tok = c_tok[ci]; w = c_w[ci]; }
-              float* dst = a.ws + static_cast<int64_t>(tok) * a.n_out + f0;
+              float* dst = a.ws + static_cast<int64_t>(tok) * un.n_out + f0;
 #pragma unroll
               for (int v = 0; v < 8; ++v) {
                 if (tok < 0) break;                  // rejected route (see above)
@@ -1131,6 +1258,32 @@ cudaError_t launch_gemm(const CUtensorMap& tmx, const CUtensorMap& tmy, const Ge
     case 64: return launch_bn<64>(tmx, tmy, a, mode, grid, s);
     case 128: return launch_bn<128>(tmx, tmy, a, mode, grid, s);
     default: return launch_bn<256>(tmx, tmy, a, mode, grid, s);
+  }
+}
+
+template <int BN>
+static cudaError_t launch_mlp_bn(const GemmArgs& a, int grid, cudaStream_t s) {
+  static_assert(Cfg<BN, 2>::kEpiGroups == 1, "the ready counts assume four epilogue warps");
+  CUtensorMap unused{};                          // the grouped path needs no tensor map
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;   // the down units wait on other CTAs' work
+  attr[0].val.cooperative = 1;
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(Cfg<BN, 2>::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Cfg<BN, 2>::kSmemBytes;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, nvfp4_gemm_kernel<BN, 2, false>, unused, unused, a,
+                            static_cast<int>(kMlpFused));
+}
+
+cudaError_t launch_mlp_fused(const GemmArgs& a, int sms, cudaStream_t s) {
+  switch (grouped_chunk_rows(a.rows_y, a.E)) {
+    case 32: return launch_mlp_bn<32>(a, sms, s);
+    case 64: return launch_mlp_bn<64>(a, sms, s);
+    default: return launch_mlp_bn<128>(a, sms, s);
   }
 }
 

@@ -59,6 +59,9 @@ enum GemmMode : int {
   kGroupedCombine = 3,  // ws[token][n] += w * y
   kGroupedSiluMul = 4,  // h[route][f] = SiLU(gate) * up, quantised into h_tiles
   kGroupedSiluBf16 = 5, // h[route][f] = SiLU(gate) * up, BF16 into out (two-phase form)
+  kMlpFused = 6,        // the SiLU-mul units, then the down projection's combine units over
+                        // h in the same launch (each token tile's down units wait on a
+                        // ready count its gate_up units raise)
 };
 
 struct GemmArgs {
@@ -89,6 +92,11 @@ struct GemmArgs {
   const float* g_h;                // SiLU-mul: global scale of h (given)
   int32_t h_nkb;                   // SiLU-mul: 256-element K blocks of h
   int32_t sparse_w;                // grouped: X operand tiles are 2:4-sparse tiles
+  const uint8_t* sfx2;             // fused MLP: operand tiles of the down projection [E * n_out2, K2]
+  const float* gx2;                // fused MLP: down projection globals [E]
+  int64_t K2;                      // fused MLP: depth of the down projection (= n_out / 2)
+  int32_t n_out2;                  // fused MLP: rows of each expert's down weight
+  uint32_t* ready;                 // fused MLP: per token tile, gate_up units done
   int32_t x_map;                   // grouped: X codes through the tensor map tmx (row-major
                                    // [E * n_out, K/2]) and X scales in the atom layout at sfx,
                                    // instead of operand tiles
@@ -138,6 +146,8 @@ cudaError_t init_gemm_pair_attributes();
 cudaError_t launch_gemm_pair(const CUtensorMap& tmx, const CUtensorMap& tmy,
                              const CUtensorMap& tsx, const CUtensorMap& tsy, const GemmArgs& a,
                              cudaStream_t s);
+// Fused expert MLP in one cooperative persistent launch (mode kMlpFused).
+cudaError_t launch_mlp_fused(const GemmArgs& a, int sms, cudaStream_t s);
 cudaError_t launch_combine_finalize(const float* ws, int64_t T, int64_t N, void* out, int sms,
                                     cudaStream_t s);
 

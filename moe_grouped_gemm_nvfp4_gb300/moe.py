@@ -234,17 +234,27 @@ class FusedMLP:
     g_h=None selects the two-phase form: the gate_up launch writes h in BF16
     (nvfp4_moe_gate_up_silu_bf16), the dispatch quantiser finds its global from
     its amax and writes the down projection's tiles.
+
+    single_launch=True (with a given g_h) runs gate_up, SiLU * up, the NVFP4
+    quantisation of h, the down projection and the combine in one persistent
+    launch (nvfp4_moe_mlp).
     """
 
     def __init__(self, w_gate_up: ExpertWeights, w_down: ExpertWeights, T: int, topk: int,
-                 g_h: torch.Tensor = None, device="cuda"):
+                 g_h: torch.Tensor = None, device="cuda", single_launch: bool = False):
         assert w_gate_up.E == w_down.E and w_gate_up.N == 2 * w_down.K
+        assert not (single_launch and g_h is None), "one launch needs the global of h"
         self.w1, self.w2, self.T, self.topk, self.g_h = w_gate_up, w_down, T, topk, g_h
+        self.single_launch = single_launch
+        dev = torch.device(device)
         self.gate_up = GroupedPlan(w_gate_up, T, topk, "gather", device, out=False)
         self.down = GroupedPlan(w_down, T, topk, "combine", device, routing_from=self.gate_up)
-        self.h = (torch.empty((max(T * topk, 1), w_down.K), dtype=torch.bfloat16,
-                              device=torch.device(device)) if g_h is None else None)
-        self._side = torch.cuda.Stream(device=torch.device(device))
+        self.h = (torch.empty((max(T * topk, 1), w_down.K), dtype=torch.bfloat16, device=dev)
+                  if g_h is None else None)
+        self.mlp_ws = (torch.empty(max(F.nvfp4_moe_mlp_workspace_bytes(T, topk, w_down.E,
+                                                                      w_down.N), 16),
+                                   dtype=torch.uint8, device=dev) if single_launch else None)
+        self._side = torch.cuda.Stream(device=dev)
 
     def step(self, x, topk_ids, topk_weights, stream=None):
         """x [T, K1] BF16, topk_ids [T, k] int32, topk_weights [T, k] FP32 ->
@@ -252,6 +262,12 @@ class FusedMLP:
         gu, dn, w1, w2 = self.gate_up, self.down, self.w1, self.w2
         _route_and_amax(gu, x, topk_ids, self._side, stream)
         gu.quantize(x, stream, amax_done=True)
+        if self.single_launch:
+            F.nvfp4_moe_mlp(gu.a_tiles, gu.a_g, w1.tiles, w1.g, w2.tiles, w2.g, gu.expert_offsets,
+                            w1.E, self.T, self.topk, w1.N, w1.K, w2.N, self.g_h, dn.a_tiles,
+                            dn.route_token, dn.route_slot, topk_weights, dn.out, self.mlp_ws,
+                            stream)
+            return dn.out
         if self.g_h is not None:
             F.nvfp4_moe_gate_up_silu(gu.a_tiles, gu.a_g, w1.tiles, w1.g, gu.expert_offsets, w1.E,
                                      self.T, self.topk, w1.N, w1.K, self.g_h, dn.a_tiles, stream)

@@ -64,6 +64,9 @@ _SIGS = {
                                               _P, _P, _P]),
     "nvfp4_moe_gate_up_silu_bf16": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I64, _I32, _I64,
                                                    _I64, _P, _P]),
+    "nvfp4_moe_mlp_workspace_bytes": (_SZ, [_I64, _I32, _I32, _I64]),
+    "nvfp4_moe_mlp": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I32, _I64, _I32, _I64, _I64,
+                                     _I64, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "nvfp4_noalloc_workspace_floats": (_SZ, []),
     "nvfp4_decode_attention_workspace_bytes": (_SZ, [_I32, _I32, _I32, _I64, _I32]),
     "nvfp4_decode_attention": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32,
@@ -244,6 +247,23 @@ def nvfp4_moe_gate_up_silu_bf16(A_tiles, gA, W_tiles, gW, expert_offsets, E: int
     _check("nvfp4_moe_gate_up_silu_bf16", load().nvfp4_moe_gate_up_silu_bf16(
         _ptr(A_tiles), _ptr(gA), _ptr(W_tiles), _ptr(gW), _ptr(expert_offsets), E, T, topk, N, K,
         _ptr(h_out), _stream(stream)))
+
+
+def nvfp4_moe_mlp_workspace_bytes(T: int, topk: int, E: int, N2: int) -> int:
+    return load().nvfp4_moe_mlp_workspace_bytes(T, topk, E, N2)
+
+
+def nvfp4_moe_mlp(A_tiles, gA, W1_tiles, gW1, W2_tiles, gW2, expert_offsets, E: int, T: int,
+                  topk: int, N1: int, K1: int, N2: int, g_h, h_tiles, route_token, route_slot,
+                  topk_weights, out, workspace, stream=None) -> None:
+    """The expert MLP (gate_up, SiLU * up, NVFP4 h, down, combine) in one
+    persistent launch; see include/nvfp4.h."""
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("nvfp4_moe_mlp", load().nvfp4_moe_mlp(
+        _ptr(A_tiles), _ptr(gA), _ptr(W1_tiles), _ptr(gW1), _ptr(W2_tiles), _ptr(gW2),
+        _ptr(expert_offsets), E, T, topk, N1, K1, N2, _ptr(g_h), _ptr(h_tiles), _ptr(route_token),
+        _ptr(route_slot), _ptr(topk_weights), _ptr(out), _ptr(workspace), ws_bytes,
+        _stream(stream)))
 
 
 def nvfp4_amax_partials(x, R: int, E: int, tiles, stream=None) -> None:

@@ -1,5 +1,6 @@
 """Fused expert MLP (gate_up, SiLU(gate) * up and the NVFP4 quantisation of h
-in one grouped-GEMM launch, then the down projection with the combine)
+in one grouped-GEMM launch, then the down projection with the combine, in a
+second launch or in the same persistent launch) and its two-phase form
 against the FP64 oracle."""
 import numpy as np
 import pytest
@@ -43,6 +44,7 @@ def _ambiguous(h, g_h):
     return (near_q | near_zero | near_s[..., None]).reshape(R, K)
 
 
+@pytest.mark.parametrize("single", [False, True], ids=["two_launches", "one_launch"])
 @pytest.mark.parametrize("T,E,k,K1,N1,N2,hot", [
     (64, 16, 2, 256, 512, 256, False),     # 8 routes per expert on average
     (40, 8, 2, 512, 768, 384, False),      # gate/up halves of 384 features (3 tiles each)
@@ -52,7 +54,9 @@ def _ambiguous(h, g_h):
     (1024, 16, 2, 256, 512, 256, False),   # 128 routes per expert: 128-route token tiles
     (700, 8, 2, 128, 768, 384, True),      # 128-route tiles, a hot expert with 700 routes
 ])
-def test_fused_gate_up_silu_down_matches_oracle(T, E, k, K1, N1, N2, hot):
+def test_fused_gate_up_silu_down_matches_oracle(T, E, k, K1, N1, N2, hot, single):
+    if single and N2 % 256:
+        pytest.skip("one launch pairs the down projection's 128-row tiles: N2 % 256 == 0")
     g = inputs.rng(T * 31 + E + K1 + N1)
     x = inputs.normal_bf16(g, (T, K1))
     w1 = inputs.normal_bf16(g, (E, N1, K1), 0.1)
@@ -75,7 +79,8 @@ def test_fused_gate_up_silu_down_matches_oracle(T, E, k, K1, N1, N2, hot):
     # CUDA path
     W1 = moe.quantize_experts(w1.cuda())
     W2 = moe.quantize_experts(w2.cuda())
-    mlp = moe.FusedMLP(W1, W2, T, k, torch.tensor([g_h], dtype=torch.float32, device="cuda"))
+    mlp = moe.FusedMLP(W1, W2, T, k, torch.tensor([g_h], dtype=torch.float32, device="cuda"),
+                       single_launch=single)
     mlp.down.out.view(torch.int16).fill_(0x7FC0)
     out = mlp.step(x.cuda(), torch.from_numpy(ids).cuda(), torch.from_numpy(wts).cuda())
     torch.cuda.synchronize()
@@ -102,6 +107,16 @@ def test_fused_gate_up_silu_down_matches_oracle(T, E, k, K1, N1, N2, hot):
     # own h wherever no code of h sits on a tie
     if not amb.any():
         check_gemm(bf16_to_np(out[:T]), ref, "fused mlp, oracle h")
+
+
+def test_one_launch_refuses_unpaired_down_tiles():
+    z = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    gf = torch.ones(4, dtype=torch.float32, device="cuda")
+    i32 = torch.zeros(8, dtype=torch.int32, device="cuda")
+    with pytest.raises(F.NVFP4Error) as ei:
+        F.nvfp4_moe_mlp(z, gf, z, gf, z, gf, i32, 4, 8, 2, 512, 256, 384, gf, z, i32, i32, gf, z,
+                        torch.zeros(1 << 16, dtype=torch.uint8, device="cuda"))
+    assert ei.value.status == F.NVFP4_ERR_UNSUPPORTED
 
 
 @pytest.mark.parametrize("T,E,k,K1,N1,N2", [(64, 16, 2, 256, 512, 256), (1024, 16, 2, 256, 512, 256)])

@@ -732,9 +732,10 @@ def measure_configs(args, dev, groups=None):
         del layer, mlp, mlp1, mlp2, W1, W2, d, gu_out, gate, up
         torch.cuda.empty_cache()
     # decode attention over an NVFP4 KV cache (every cache byte read once):
-    # 128-wide heads in groups of 4 and of 1, and 512-wide heads
-    for (B_, Hq_, Hkv_, L_, D_) in ((16, 32, 8, 16384, 128), (16, 8, 8, 16384, 128),
-                                    (8, 8, 2, 32768, 512)):
+    # 128-wide heads in groups of 4, 8 (tensor-core kernel) and 1 (CUDA-core
+    # kernel), and 512-wide heads
+    for (B_, Hq_, Hkv_, L_, D_) in ((16, 32, 8, 16384, 128), (16, 64, 8, 16384, 128),
+                                    (16, 8, 8, 16384, 128), (8, 8, 2, 32768, 512)):
         if not want("decode_attention"):
             break
         kc = inputs.device_normal_bf16((B_, Hkv_, L_, D_), 1.0, 71, dev)
@@ -753,7 +754,8 @@ def measure_configs(args, dev, groups=None):
             t_att, fl, byt, hbm, fp4,
             note="one query token per sequence; K and V in NVFP4 (codes + E4M3 scales along "
                  "D + one global each); split-KV partials merged by a second kernel (both "
-                 "timed)")
+                 "timed); " + ("tcgen05 pipelined kernel" if D_ <= 128 and Hq_ // Hkv_ >= 4
+                               else "CUDA-core kernel"))
         del kq, vq, plan
         torch.cuda.empty_cache()
     for v in out.values():

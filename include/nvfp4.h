@@ -518,8 +518,12 @@ nvfp4_status nvfp4_grouped_gemm_sparse(const uint8_t* A_tiles, const float* gA,
 /*
  * Decode attention over an NVFP4 KV cache ("The Blackwell architectural
  * split", The Breakthrough -- The A4Q Kernel, and Preserving precision --
- * dual-tier scale handling): the cache stays packed and is dequantised in
- * registers inside the attention loop.  One query token per sequence.
+ * dual-tier scale handling): the cache stays packed in memory and is expanded
+ * on chip inside the attention loop.  One query token per sequence.  Groups of
+ * 4 or 8 query heads over heads of 64 or 128 run both contractions as tcgen05
+ * MMAs on exact FP16 expansions of the cache (when both scale arrays are
+ * 16-byte aligned and L_max * D / 16 is a multiple of 16); other shapes
+ * multiply-add on the CUDA cores.  Both give the result defined below.
  *   q          BF16 [B, Hq, D].
  *   k_packed   NVFP4 codes [B, Hkv, L_max, D/2] (token rows of sequence b and
  *              KV head j contiguous), k_scales E4M3 [B, Hkv, L_max, D/16]
@@ -539,7 +543,8 @@ nvfp4_status nvfp4_grouped_gemm_sparse(const uint8_t* A_tiles, const float* gA,
  *              D) bytes, caller-owned (per-split partials, overwritten).
  * D in {64, 128, 256, 512}; Hq / Hkv in {1, 2, 4, 8} (at most 4 for D = 512);
  * q, out, workspace and the code arrays 16-byte aligned, the scale arrays
- * 4-byte aligned.
+ * 4-byte aligned.  The tensor-core kernel's waits are bounded: a wait that
+ * runs out records NVFP4_ERR_TIMEOUT in the device status word.
  */
 size_t nvfp4_decode_attention_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int64_t L_max,
                                               int32_t D);

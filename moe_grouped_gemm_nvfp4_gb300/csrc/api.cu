@@ -61,6 +61,7 @@ nvfp4_status device_state(DeviceState** out) {
       d.status = static_cast<int*>(p);
       if (nvfp4::init_gemm_attributes() != cudaSuccess) return cuda_fail();
       if (nvfp4::init_gemm_pair_attributes() != cudaSuccess) return cuda_fail();
+      if (nvfp4::init_attention_tc_attributes() != cudaSuccess) return cuda_fail();
       if (nvfp4::init_route_attributes() != cudaSuccess) return cuda_fail();
     }
     if (!g_encode) {
@@ -678,6 +679,7 @@ nvfp4_status nvfp4_decode_attention(const void* q, const uint8_t* k_packed,
   a.ws_o = workspace;
   a.ws_ml = workspace + static_cast<int64_t>(B) * Hq * a.splits * D;
   a.status = d->status;
+  a.timeout_ns = g_timeout_ns.load();
   if (nvfp4::launch_decode_attention(a, D, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return cuda_fail();
   return NVFP4_OK;

@@ -328,11 +328,18 @@ cudaError_t launch_decode_attention(const AttnArgs& a, int D, cudaStream_t s) {
     decode_attention_combine_kernel<<<static_cast<unsigned>(a.B * a.Hq), 128, 0, s>>>(a, D);
     return cudaGetLastError();
   }
-  switch (D) {
-    case 64: e = launch_d<64>(a, G, s); break;
-    case 128: e = launch_d<128>(a, G, s); break;
-    case 256: e = launch_d<256>(a, G, s); break;
-    default: e = launch_d<512>(a, G, s); break;
+  // groups of 4 and 8 query heads over heads of 64 or 128: the tensor-core
+  // kernel (attention_tc.cu); smaller groups, where the per-head multiply-adds
+  // cost less than the FP16 operand traffic, and wider heads: the kernel above
+  if (decode_attention_tc_applies(a, D)) {
+    e = launch_decode_attention_tc(a, D, s);
+  } else {
+    switch (D) {
+      case 64: e = launch_d<64>(a, G, s); break;
+      case 128: e = launch_d<128>(a, G, s); break;
+      case 256: e = launch_d<256>(a, G, s); break;
+      default: e = launch_d<512>(a, G, s); break;
+    }
   }
   if (e != cudaSuccess) return e;
   decode_attention_combine_kernel<<<static_cast<unsigned>(a.B * a.Hq), 128, 0, s>>>(a, D);

@@ -25,11 +25,14 @@ struct AttnArgs {
   float* ws_o;                     // [B, Hq, splits, D] partial weighted values
   float* ws_ml;                    // [B, Hq, splits, 2] partial max (base 2) and sum
   int* status;
+  uint64_t timeout_ns;             // bounded waits of the tensor-core kernel
 };
 
 // Tokens per split of the decode attention: the smallest power of two from
-// 128 up to 4096 that leaves about a thousand (sequence, KV head, split)
-// CTAs at most.  A function of the shape only, so that the workspace size is.
+// 128 up to 4096 that leaves about a thousand (sequence, KV head, split) work
+// items at most.  A function of the shape only, so that the workspace size
+// is.  The CUDA-core kernel launches one CTA per item; the tensor-core kernel
+// (one CTA per SM) walks several items per CTA.
 inline int attention_chunk(int64_t L_max, int64_t B, int64_t Hkv) {
   const int64_t want = (L_max * B * Hkv + 1023) / 1024;
   int ch = 128;
@@ -37,5 +40,11 @@ inline int attention_chunk(int64_t L_max, int64_t B, int64_t Hkv) {
   return ch;
 }
 cudaError_t launch_decode_attention(const AttnArgs& a, int D, cudaStream_t s);
+// The pipelined split kernel with both contractions on the tensor cores
+// (attention_tc.cu): heads of 64 and 128, groups of 4 or 8 query heads, both
+// scale arrays 16-byte aligned and L_max * D / 16 a multiple of 16.
+bool decode_attention_tc_applies(const AttnArgs& a, int D);
+cudaError_t launch_decode_attention_tc(const AttnArgs& a, int D, cudaStream_t s);
+cudaError_t init_attention_tc_attributes();
 
 }  // namespace nvfp4

@@ -325,6 +325,67 @@ __device__ __forceinline__ uint32_t idesc_nvf4(uint32_t n) {
 }
 
 // ---------------------------------------------------------------------------
+// FP16 tensor-core operands (kind::f16)
+// ---------------------------------------------------------------------------
+// Descriptor of an MN-major operand in the 128-byte swizzle: atoms of 64
+// 16-bit elements along M/N (128 bytes) x 8 rows along K, lbo bytes between
+// atoms along M/N and sbo bytes between atoms along K.
+__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo & 0x3FFFFu) >> 4) << 16;
+  d |= static_cast<uint64_t>((sbo & 0x3FFFFu) >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Instruction descriptor of kind::f16: FP16 A and B, FP32 accumulator,
+// A K-major (a_mn = 0) or MN-major (a_mn = 1), B K-major, M = 128, N = n.
+__device__ __forceinline__ uint32_t idesc_f16(uint32_t n, uint32_t a_mn) {
+  return (1u << 4)                 // D format: F32
+       | (a_mn << 15)              // A major
+       | ((n >> 3) << 17)          // N / 8
+       | ((128u >> 4) << 24);      // M / 16
+}
+
+__device__ __forceinline__ void tc_mma_f16_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .pred e;\n\t.reg .b32 l;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync l|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+// 32 lanes x 16 consecutive 32-bit columns -> 16 registers per thread.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+// This thread's 16 registers -> its lane's 16 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+      :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+         "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]),
+         "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // CTA pairs (a cluster of two CTAs on neighbouring SMs sharing one MMA with
 // cta_group::2: M = 256 split 128 + 128 over the pair, each CTA holding half
 // of B; every tcgen05 instruction of such a kernel carries cta_group::2)

@@ -44,6 +44,10 @@ def _check(got, ref, name):
     (1, 4, 1, 700, 512, [700]),              # 512-wide heads
     (4, 2, 1, 64, 512, [64, 3, 33, 17]),
     (2, 8, 8, 4097, 64, [4097, 4096]),       # chunk boundary +- 1
+    (2, 8, 2, 333, 128, [333, 200]),         # scale slabs not in 16-byte units
+    (4, 16, 2, 5000, 128, [5000, 4999, 2048, 129]),  # several work items per CTA, empty splits
+    (2, 8, 1, 1500, 64, [1500, 777]),        # groups of 8 over 64-wide heads, ragged tiles
+    (2, 8, 2, 3000, 128, [3000, 2999]),      # groups of 4, a tile of one token
 ])
 def test_decode_attention_matches_oracle(B, Hq, Hkv, L, D, lens):
     q, k, v = _case(B * 1000 + Hq * 10 + D + L, B, Hq, Hkv, L, D)

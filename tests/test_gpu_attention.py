@@ -99,3 +99,50 @@ def test_unsupported_shapes_are_refused():
     with pytest.raises(RuntimeError):            # 512-wide heads take groups of at most 4
         F.nvfp4_decode_attention(q, k, s, g, k, s, g, torch.ones(1, dtype=torch.int32,
                                  device="cuda"), 0.1, out, ws)
+
+
+def test_rising_and_spiking_scores_move_the_reference_maximum():
+    """Long splits (L_max 262144 with B 2, Hkv 2: 1024-token splits of 8
+    tiles) whose scores rise by about 50 (base 2) along sequence 0 and jump by
+    about 70 at a few tokens of sequence 1: the tensor-core kernel's reference
+    maximum moves inside a split, so O and the sums are rescaled there.  Tokens
+    past the first 3000 are zero and unread."""
+    B, Hq, Hkv, D, n, L_max = 2, 8, 2, 128, 3000, 262144
+    G = Hq // Hkv
+    g = inputs.rng(91)
+    q = inputs.normal_bf16(g, (B, Hq, D))
+    qf = q.float().numpy()
+    k = g.standard_normal((B, Hkv, n, D)) * 0.5
+    v = g.standard_normal((B, Hkv, n, D))
+    for b in range(B):
+        for j in range(Hkv):
+            u = qf[b, j * G:(j + 1) * G].mean(0)
+            u /= np.linalg.norm(u)
+            amp = np.linspace(0.0, 6.0, n) if b == 0 else np.zeros(n)
+            if b == 1:
+                amp[1500:1510] = 8.0
+            k[b, j] += 12.0 * amp[:, None] * u[None, :]
+    kb = torch.from_numpy(k.astype(np.float32)).to(torch.bfloat16)
+    vb = torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16)
+    kd = torch.zeros((B, Hkv, L_max, D), dtype=torch.bfloat16, device="cuda")
+    vd = torch.zeros_like(kd)
+    kd[:, :, :n] = kb.cuda()
+    vd[:, :, :n] = vb.cuda()
+    kq, vq = attention.quantize_kv(kd), attention.quantize_kv(vd)
+    kf, vf = kb.float().numpy(), vb.float().numpy()
+    gk, gv = oracle.global_scale(kf), oracle.global_scale(vf)   # the zero tail leaves amax alone
+    assert kq[2].item() == gk and vq[2].item() == gv
+    pk, sk = oracle.quantize_kv(kf, gk)
+    pv, sv = oracle.quantize_kv(vf, gv)
+    assert np.array_equal(kq[0][:, :, :n].cpu().numpy(), pk)
+    assert np.array_equal(vq[1][:, :, :n].cpu().numpy(), sv)
+    scale = 1.0 / np.sqrt(D)
+    plan = attention.DecodeAttention(B, Hq, Hkv, L_max, D)
+    plan.out.view(torch.int16).fill_(0x7FC0)
+    seq = torch.tensor([n, n], dtype=torch.int32, device="cuda")
+    out = plan.run(q.cuda(), kq, vq, seq, scale)
+    torch.cuda.synchronize()
+    assert F.nvfp4_device_status() == F.NVFP4_OK
+    ref = oracle.decode_attention(qf, oracle.dequantize_kv(pk, sk, gk),
+                                  oracle.dequantize_kv(pv, sv, gv), [n, n], scale)
+    _check(out.float().cpu().numpy().astype(np.float64), ref, "rising / spiking scores")

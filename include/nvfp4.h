@@ -80,12 +80,13 @@ nvfp4_status nvfp4_last_device_status(void* stream);
 nvfp4_status nvfp4_set_timeout_ns(uint64_t ns);
 
 /*
- * Test hook for the failure path of the GEMM kernels (0 = off, the default).
- * Flag 1: the producer of every CTA leaves its first pipeline stage unfilled,
- * so the first MMA wait can only end by its time limit; the kernel then
- * records NVFP4_ERR_TIMEOUT, drains its own copies and MMAs, frees tensor
- * memory and returns, and the output is incomplete.  Meant for tests, with a
- * short nvfp4_set_timeout_ns.  Other bits return NVFP4_ERR_INVALID_ARG.
+ * Test hook for the failure path of the GEMM kernels and of the tensor-core
+ * decode attention (0 = off, the default).  Flag 1: the producer of every CTA
+ * leaves its first pipeline stage unfilled, so the first wait on it can only
+ * end by its time limit; the kernel then records NVFP4_ERR_TIMEOUT, drains its
+ * own copies and MMAs, frees tensor memory and returns, and the output is
+ * incomplete.  Meant for tests, with a short nvfp4_set_timeout_ns.  Other bits
+ * return NVFP4_ERR_INVALID_ARG.
  */
 nvfp4_status nvfp4_debug_set_flags(uint32_t flags);
 

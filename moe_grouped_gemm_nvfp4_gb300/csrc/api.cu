@@ -667,6 +667,7 @@ nvfp4_status nvfp4_decode_attention(const void* q, const uint8_t* k_packed,
   a.v_scales = v_scales;
   a.gk = gk;
   a.gv = gv;
+  a.debug_flags = g_debug_flags.load();
   a.seq_lens = seq_lens;
   a.B = B;
   a.Hq = Hq;

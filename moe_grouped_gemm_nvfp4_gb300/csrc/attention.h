@@ -26,6 +26,7 @@ struct AttnArgs {
   float* ws_ml;                    // [B, Hq, splits, 2] partial max (base 2) and sum
   int* status;
   uint64_t timeout_ns;             // bounded waits of the tensor-core kernel
+  uint32_t debug_flags;            // kDebugSkipFirstStage: test hook, see nvfp4.h
 };
 
 // Tokens per split of the decode attention: the smallest power of two from

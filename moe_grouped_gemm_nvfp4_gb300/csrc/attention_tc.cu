@@ -321,7 +321,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_attention_ws_kernel(cons
     // ---------------------------------------------------------------- producer
     const uint64_t policy = l2_policy_evict_first();
     uint32_t i = 0;
-    bool ok = true;
+    bool ok = true, skipped_first = false;
     int n_nxt = ws_len(a, blockIdx.x, items);
     for (int64_t w = blockIdx.x; w < items && ok; w += gridDim.x) {
       const WsItem it = ws_item(a, w, n_nxt);
@@ -337,6 +337,10 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_attention_ws_kernel(cons
         const uint32_t bytes_s = (rows * SB) & ~15u;     // whole 16-byte units by copy
         const uint32_t dst = sbase + st * C::kStage;
         const int64_t r = it.row0 + tt;
+        if (i == 0 && (a.debug_flags & kDebugSkipFirstStage)) {
+          skipped_first = true;                          // test hook: this stage never fills
+          continue;
+        }
         mbar_arrive_expect_tx_elect(raw_full(st), 2 * bytes_c + 2 * bytes_s);
         bulk_load_elect(dst, a.k_packed + r * KB, bytes_c, raw_full(st), policy);
         bulk_load_elect(dst + C::kRawCodes, a.v_packed + r * KB, bytes_c, raw_full(st), policy);
@@ -351,7 +355,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_attention_ws_kernel(cons
     // every copy this warp issued has landed before the CTA can exit
     const uint32_t issued = i;
     for (uint32_t k = issued > kWsStages ? issued - kWsStages : 0; k < issued; ++k)
-      ws_drain(raw_full(k % kWsStages), (k / kWsStages) & 1u, a.timeout_ns);
+      if (k > 0 || !skipped_first) ws_drain(raw_full(k % kWsStages), (k / kWsStages) & 1u, a.timeout_ns);
   } else if (warp >= kSoftWarps && warp < kProdWarp) {
     // --------------------------------------------------------------- expansion
     constexpr int kRowStep = 256 / NB;                   // rows between a thread's units

@@ -146,3 +146,38 @@ def test_rising_and_spiking_scores_move_the_reference_maximum():
     ref = oracle.decode_attention(qf, oracle.dequantize_kv(pk, sk, gk),
                                   oracle.dequantize_kv(pv, sv, gv), [n, n], scale)
     _check(out.float().cpu().numpy().astype(np.float64), ref, "rising / spiking scores")
+
+
+def test_tensor_core_kernel_wait_expires_reports_timeout_and_context_survives():
+    """Failure path of the tensor-core kernel: with the test hook every CTA's
+    producer leaves its first ring stage unfilled, so the expansion's wait can
+    only end by its time limit; the kernel records NVFP4_ERR_TIMEOUT, every
+    role leaves, the copies in flight are drained, and the next call on the
+    same context is correct."""
+    B, Hq, Hkv, L, D = 2, 8, 2, 1000, 128                # groups of 4: the tensor-core kernel
+    q, k, v = _case(17, B, Hq, Hkv, L, D)
+    kq, vq = attention.quantize_kv(k.cuda()), attention.quantize_kv(v.cuda())
+    plan = attention.DecodeAttention(B, Hq, Hkv, L, D)
+    seq = torch.tensor([L, 611], dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    F.nvfp4_device_status(reset=True)
+    F.nvfp4_set_timeout_ns(20_000_000)                 # 20 ms
+    F.nvfp4_debug_set_flags(1)
+    try:
+        plan.run(q.cuda(), kq, vq, seq, 0.125)
+        torch.cuda.synchronize()
+        assert F.nvfp4_device_status(reset=True) == F.NVFP4_ERR_TIMEOUT
+    finally:
+        F.nvfp4_debug_set_flags(0)
+        F.nvfp4_set_timeout_ns(1_000_000_000)
+    plan.out.view(torch.int16).fill_(0x7FC0)
+    out = plan.run(q.cuda(), kq, vq, seq, 0.125)
+    torch.cuda.synchronize()
+    assert F.nvfp4_device_status() == F.NVFP4_OK
+    kf, vf = k.float().numpy(), v.float().numpy()
+    gk, gv = oracle.global_scale(kf), oracle.global_scale(vf)
+    pk, sk = oracle.quantize_kv(kf, gk)
+    pv, sv = oracle.quantize_kv(vf, gv)
+    ref = oracle.decode_attention(q.float().numpy(), oracle.dequantize_kv(pk, sk, gk),
+                                  oracle.dequantize_kv(pv, sv, gv), [L, 611], 0.125)
+    _check(out.float().cpu().numpy().astype(np.float64), ref, "after timeout")

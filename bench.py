@@ -639,8 +639,8 @@ def measure_configs(args, dev, groups=None):
     # decode gate_up, down sweep and skewed prefill (and the 2:4-sparse decode shapes)
     for name in ("decode_gate_up", "decode_down_256", "decode_down_512", "decode_down_1024",
                  "prefill_skewed"):
-        if not want("decode"):
-            break
+        if not (want("decode") or (name == "prefill_skewed" and want("prefill"))):
+            continue
         cfg = inputs.CONFIGS[name]
         g = inputs.rng(cfg.seed)
         w = torch.empty((cfg.E, cfg.N, cfg.K), dtype=torch.bfloat16, device=dev)
@@ -650,6 +650,7 @@ def measure_configs(args, dev, groups=None):
         sparse = want("sparse") and name != "prefill_skewed"
         W_sp = moe.quantize_experts_sparse(w) if sparse else None
         del w
+        torch.cuda.empty_cache()          # the BF16 weights' memory leaves the process
         if cfg.kind == "down":
             ids = inputs.uniform_topk(g, cfg.T, cfg.E, cfg.topk)
             wts = torch.from_numpy(inputs.dirichlet_weights(g, cfg.T, cfg.topk)).to(dev)
@@ -783,7 +784,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default=None,
                     help="configs: run only these comma-separated groups (tiny_gemm, "
-                         "dense_8192, decode, sparse, fused_mlp, decode_attention)")
+                         "dense_8192, decode (with prefill), prefill, sparse, fused_mlp, "
+                         "decode_attention)")
     ap.add_argument("--no-configs", action="store_true",
                     help="leave the per-configuration table out of the headline line")
     ap.add_argument("--sparse", action="store_true",

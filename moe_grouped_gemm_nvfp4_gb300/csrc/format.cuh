@@ -149,6 +149,29 @@ __device__ __forceinline__ Bracket bracket_of(float d) {
   return b;
 }
 
+// The elements of a block whose bracketing products gave different codes
+// (diff: the XOR of the two code words, kBase: the block index of the word's
+// first value) get the exact code E2M1(RN(v / d)) in place; every other code
+// is already exact.  Typically one element or none: only a quotient within
+// 2^-19 of an E2M1 rounding boundary lands here.
+template <int kBase, typename Get>
+__device__ __forceinline__ uint32_t fix_codes(uint32_t c, uint32_t diff, float d, Get get) {
+#pragma unroll
+  for (int n = 0; n < 8; ++n) {
+    const uint32_t mask = 0xFu << (4 * n);
+    if (diff & mask) {
+      const float q = __fdiv_rn(get(kBase + n), d);
+      uint32_t code;
+      asm("{\n\t.reg .b8 t;\n\t"
+          "cvt.rn.satfinite.e2m1x2.f32 t, %2, %1;\n\t"
+          "cvt.u32.u8 %0, t;\n\t}"
+          : "=r"(code) : "f"(q), "f"(0.0f));
+      c = (c & ~mask) | ((code & 0xFu) << (4 * n));
+    }
+  }
+  return c;
+}
+
 // One block from its magnitude maximum and an accessor for its 16 finite
 // binary32 values: s = (amax_b / 6) / g (0 when g == 0), sf = E4M3(s),
 // d = e4m3(sf) * g, code = E2M1(v / d), or the signed zero code when d == 0.
@@ -174,11 +197,14 @@ __device__ __forceinline__ Block16 quantize16_with(float amax_b, const ScaleK& k
       hi[e] = h.x;
       hi[e + 1] = h.y;
     }
-    const uint32_t c0 = e2m1x8_rn_satfinite(lo), c1 = e2m1x8_rn_satfinite(lo + 8);
-    if (c0 == e2m1x8_rn_satfinite(hi) && c1 == e2m1x8_rn_satfinite(hi + 8)) {
-      b.packed = make_uint2(c0 | sgn[0], c1 | sgn[1]);
-      return b;
+    uint32_t c0 = e2m1x8_rn_satfinite(lo), c1 = e2m1x8_rn_satfinite(lo + 8);
+    const uint32_t x0 = c0 ^ e2m1x8_rn_satfinite(hi), x1 = c1 ^ e2m1x8_rn_satfinite(hi + 8);
+    if ((x0 | x1) != 0u) {
+      c0 = fix_codes<0>(c0, x0, d, get);
+      c1 = fix_codes<8>(c1, x1, d, get);
     }
+    b.packed = make_uint2(c0 | sgn[0], c1 | sgn[1]);
+    return b;
   }
   b.packed = codes_exact(d, get);
   return b;
@@ -214,11 +240,14 @@ __device__ __forceinline__ Block16 quantize_bf16x16(const uint32_t (&w)[8], cons
       hi[2 * i] = h.x;
       hi[2 * i + 1] = h.y;
     }
-    const uint32_t c0 = e2m1x8_rn_satfinite(lo), c1 = e2m1x8_rn_satfinite(lo + 8);
-    if (c0 == e2m1x8_rn_satfinite(hi) && c1 == e2m1x8_rn_satfinite(hi + 8)) {
-      b.packed = make_uint2(c0, c1);
-      return b;
+    uint32_t c0 = e2m1x8_rn_satfinite(lo), c1 = e2m1x8_rn_satfinite(lo + 8);
+    const uint32_t x0 = c0 ^ e2m1x8_rn_satfinite(hi), x1 = c1 ^ e2m1x8_rn_satfinite(hi + 8);
+    if ((x0 | x1) != 0u) {
+      c0 = fix_codes<0>(c0, x0, d, get);
+      c1 = fix_codes<8>(c1, x1, d, get);
     }
+    b.packed = make_uint2(c0, c1);
+    return b;
   }
   b.packed = codes_exact(d, get);
   return b;

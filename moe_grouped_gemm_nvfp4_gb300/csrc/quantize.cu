@@ -85,11 +85,15 @@ __device__ __forceinline__ int64_t atom_offset(int64_t r, int64_t c, int64_t n_c
   return ((r >> 7) * n_cgroups + (c >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (c & 3);
 }
 
-// Work item: a warp quantises 32 consecutive 16-element blocks of one row
-// (lane l takes block 32 * seg + l): one division per item, 1 KB of
-// coalesced loads, 256 contiguous bytes of codes.  Atom-layout scales leave
-// as one word per four blocks.
-__global__ void __launch_bounds__(256) quantize_kernel(const uint16_t* __restrict__ x,
+// Work item: a warp quantises 64 consecutive 16-element blocks of one row,
+// lane l taking blocks l and l + 32 of the item (each half 1 KB of coalesced
+// loads and 256 contiguous bytes of codes); atom-layout scales leave as one
+// word per four blocks.  The item index is split into (row, segment) once and
+// then stepped by the grid stride with a borrow, so no division sits in the
+// loop.
+constexpr uint32_t kQuantItemBlocks = 64;
+
+__global__ void __launch_bounds__(256, 5) quantize_kernel(const uint16_t* __restrict__ x,
                                                        int64_t rows, int64_t cols, int64_t ld,
                                                        uint8_t* __restrict__ packed,
                                                        uint8_t* __restrict__ scales,
@@ -97,36 +101,52 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint16_t* __restric
   const ScaleK k = scale_consts(*g_ptr);
   const int lane = threadIdx.x & 31;
   const uint32_t bpr = static_cast<uint32_t>(cols >> 4);
-  const uint32_t segs = (bpr + 31u) / 32u;
+  const uint32_t segs = (bpr + kQuantItemBlocks - 1) / kQuantItemBlocks;
   const uint64_t items = static_cast<uint64_t>(rows) * segs;
   const uint64_t wstride = static_cast<uint64_t>(gridDim.x) * (blockDim.x >> 5);
   const int64_t ncg = (cols + 63) >> 6;                 // 4-block scale groups per row
+  const uint64_t j0 = static_cast<uint64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (j0 >= items) return;
   // Items run from the end of the tensor backwards: the tensor amax pass
   // that precedes this kernel swept it front to back, so its tail is what
-  // L2 still holds.
-  for (uint64_t j = static_cast<uint64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-       j < items; j += wstride) {
-    const uint64_t it = items - 1 - j;
-    const int64_t r = static_cast<int64_t>(it / segs);
-    const uint32_t b = static_cast<uint32_t>(it - static_cast<uint64_t>(r) * segs) * 32u + lane;
-    const bool valid = b < bpr;
-    Block16 q;
-    q.packed = make_uint2(0u, 0u);
-    q.sf = 0u;
-    if (valid) {
-      const uint4* src = reinterpret_cast<const uint4*>(x + r * ld + b * 16);
-      q = quantize_block(__ldg(src), __ldg(src + 1), k);
-      *reinterpret_cast<uint2*>(packed + r * (cols >> 1) + b * 8) = q.packed;
+  // L2 still holds.  Item it = items - 1 - j is (row r, segment sg).
+  const uint64_t it0 = items - 1 - j0;
+  int64_t r = static_cast<int64_t>(it0 / segs);
+  uint32_t sg = static_cast<uint32_t>(it0 - static_cast<uint64_t>(r) * segs);
+  const int64_t dr = static_cast<int64_t>(wstride / segs);
+  const uint32_t ds = static_cast<uint32_t>(wstride - static_cast<uint64_t>(dr) * segs);
+  const size_t half_row = static_cast<size_t>(cols >> 1);
+  for (uint64_t j = j0; j < items; j += wstride) {
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t b = sg * kQuantItemBlocks + h * 32 + lane;
+      const bool valid = b < bpr;
+      Block16 q;
+      q.packed = make_uint2(0u, 0u);
+      q.sf = 0u;
+      if (valid) {
+        const uint4* src = reinterpret_cast<const uint4*>(x + r * ld + b * 16);
+        q = quantize_block(__ldg(src), __ldg(src + 1), k);
+        *reinterpret_cast<uint2*>(packed + r * half_row + b * 8) = q.packed;
+      }
+      if (sf_atoms) {
+        // blocks 4j..4j+3 share one word of an atom (padding columns past the
+        // row end get zero scales)
+        const uint32_t word = gather4_bytes(q.sf);
+        if ((lane & 3) == 0 && b < static_cast<uint32_t>(ncg * 4))
+          *reinterpret_cast<uint32_t*>(scales + atom_offset(r, b, ncg)) = word;
+      } else if (valid) {
+        scales[r * bpr + b] = static_cast<uint8_t>(q.sf);
+      }
     }
-    if (sf_atoms) {
-      // blocks 4j..4j+3 of the item share one word of an atom (padding
-      // columns past the row end get zero scales)
-      const uint32_t word = gather4_bytes(q.sf);
-      if ((lane & 3) == 0 && b < static_cast<uint32_t>(ncg * 4))
-        *reinterpret_cast<uint32_t*>(scales + atom_offset(r, b, ncg)) = word;
-    } else if (valid) {
-      scales[r * bpr + b] = static_cast<uint8_t>(q.sf);
+    // the next item: it - wstride = (r - dr) * segs + (sg - ds), with a borrow
+    if (sg >= ds) {
+      sg -= ds;
+    } else {
+      sg += segs - ds;
+      r -= 1;
     }
+    r -= dr;
   }
 }
 
@@ -472,7 +492,8 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64
                             uint8_t* packed, uint8_t* scales, int sf_atoms, const float* g,
                             int sms, cudaStream_t s) {
   if (rows == 0 || cols == 0) return cudaSuccess;
-  const int64_t items = rows * (((cols >> 4) + 31) / 32);
+  const int64_t items =
+      rows * (((cols >> 4) + kQuantItemBlocks - 1) / kQuantItemBlocks);
   quantize_kernel<<<grid_for_items(quantize_kernel, 0, items, sms), 256, 0, s>>>(
       x, rows, cols, ld, packed, scales, sf_atoms, g);
   return cudaGetLastError();

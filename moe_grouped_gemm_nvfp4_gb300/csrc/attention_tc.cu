@@ -261,6 +261,7 @@ __device__ __forceinline__ void mbar_arrive_elect(uint32_t bar) {
 template <int D, int G>
 __global__ void __launch_bounds__(kWsThreads, 1) decode_attention_ws_kernel(const AttnArgs a) {
   static_assert(G <= 8, "P's high and low parts share the MMA's 16 columns");
+  static_assert(D == 64 || D == 128, "four or eight 16-element blocks per row");
   using C = WsCfg<D>;
   constexpr int KB = C::KB, SB = C::SB, NB = D / 16;
   extern __shared__ uint8_t smem_raw[];
@@ -360,8 +361,14 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_attention_ws_kernel(cons
     // --------------------------------------------------------------- expansion
     constexpr int kRowStep = 256 / NB;                   // rows between a thread's units
     constexpr int kUnits = kTile / kRowStep;             // units per operand per thread
-    const int x = tid - kSoftWarps * 32;
-    const int blk = x % NB, trow0 = x / NB;              // trow0 % 8 is the same for every unit
+    // Lanes 8m .. 8m + 7 (one pass of a 16-byte shared-memory store) take four
+    // blocks of two adjacent rows: the 128-byte swizzle then spreads them over
+    // all eight 16-byte bank groups.  A warp covers 32 / NB rows of NB blocks.
+    const int e = warp - kSoftWarps;
+    const int blk = NB == 8 ? ((lane >> 3) & 1) * 4 + (lane & 3) : (lane & 3);
+    const int rin = NB == 8 ? ((lane >> 4) * 2 + ((lane >> 2) & 1))
+                            : ((lane >> 3) * 2 + ((lane >> 2) & 1));
+    const int trow0 = e * (32 / NB) + rin;               // trow0 % 8 is the same for every unit
     const uint32_t sw = static_cast<uint32_t>(trow0 & 7);
     const uint32_t c = static_cast<uint32_t>(2 * blk) & 7u;
     const uint32_t off0 = (blk >> 2) * 16384 + (trow0 >> 3) * 1024 + sw * 128;

@@ -116,6 +116,39 @@ nvfp4_status make_operand_map(CUtensorMap* m, const void* base, uint64_t rows, u
   return r == CUDA_SUCCESS ? NVFP4_OK : NVFP4_ERR_UNSUPPORTED;
 }
 
+// 2-D map over a KV-cache code array [rows, D/2] (uint8) for the tensor-core
+// attention: boxes of 128 whole rows with the swizzle of the row width (64
+// bytes for D = 128, 32 for D = 64).  Rows past the array read zeros.
+nvfp4_status make_kv_code_map(CUtensorMap* m, const void* base, uint64_t rows, int D) {
+  const uint64_t row_bytes = static_cast<uint64_t>(D / 2);
+  const cuuint64_t dims[2] = {row_bytes, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(row_bytes), 128u};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              D == 128 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NVFP4_OK : NVFP4_ERR_UNSUPPORTED;
+}
+
+// 2-D map over a KV-cache scale array [rows, D/16] (uint8) viewed as 16-byte
+// rows, boxes of 128 cache rows (rows * D/16 a multiple of 16).  Rows past the
+// array read zeros.
+nvfp4_status make_kv_scale_map(CUtensorMap* m, const void* base, uint64_t rows, int D) {
+  const uint64_t sb = static_cast<uint64_t>(D / 16);
+  const cuuint64_t dims[2] = {16u, rows * sb / 16};
+  const cuuint64_t strides[1] = {16u};
+  const cuuint32_t box[2] = {16u, static_cast<cuuint32_t>(128 * sb / 16)};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NVFP4_OK : NVFP4_ERR_UNSUPPORTED;
+}
+
 // 2-D map over atom-layout scales of a [rows, K] operand viewed as rows of
 // one 512-byte atom (128 32-bit words), box of four atoms (one 256-K block
 // of a 128-row tile).  Rows past the last atom read zeros.
@@ -681,7 +714,18 @@ nvfp4_status nvfp4_decode_attention(const void* q, const uint8_t* k_packed,
   a.ws_ml = workspace + static_cast<int64_t>(B) * Hq * a.splits * D;
   a.status = d->status;
   a.timeout_ns = g_timeout_ns.load();
-  if (nvfp4::launch_decode_attention(a, D, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+  nvfp4::AttnMaps maps;
+  const bool tc = nvfp4::decode_attention_tc_applies(a, D);
+  if (tc) {
+    const uint64_t rows = static_cast<uint64_t>(B) * Hkv * L_max;
+    if (make_kv_code_map(&maps.k_codes, k_packed, rows, D) != NVFP4_OK ||
+        make_kv_code_map(&maps.v_codes, v_packed, rows, D) != NVFP4_OK ||
+        make_kv_scale_map(&maps.k_scales, k_scales, rows, D) != NVFP4_OK ||
+        make_kv_scale_map(&maps.v_scales, v_scales, rows, D) != NVFP4_OK)
+      return NVFP4_ERR_UNSUPPORTED;
+  }
+  if (nvfp4::launch_decode_attention(a, D, tc ? &maps : nullptr,
+                                     static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return cuda_fail();
   return NVFP4_OK;
 }

@@ -321,7 +321,8 @@ cudaError_t launch_d(const AttnArgs& a, int G, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_decode_attention(const AttnArgs& a, int D, cudaStream_t s) {
+cudaError_t launch_decode_attention(const AttnArgs& a, int D, const AttnMaps* maps,
+                                    cudaStream_t s) {
   const int G = a.Hq / a.Hkv;
   cudaError_t e = cudaSuccess;
   if (a.splits == 0) {             // empty cache: the merge writes zeros
@@ -331,8 +332,8 @@ cudaError_t launch_decode_attention(const AttnArgs& a, int D, cudaStream_t s) {
   // groups of 4 and 8 query heads over heads of 64 or 128: the tensor-core
   // kernel (attention_tc.cu); smaller groups, where the per-head multiply-adds
   // cost less than the FP16 operand traffic, and wider heads: the kernel above
-  if (decode_attention_tc_applies(a, D)) {
-    e = launch_decode_attention_tc(a, D, s);
+  if (maps && decode_attention_tc_applies(a, D)) {
+    e = launch_decode_attention_tc(a, D, *maps, s);
   } else {
     switch (D) {
       case 64: e = launch_d<64>(a, G, s); break;

@@ -2,6 +2,8 @@
 // attention.cu and the C ABI layer.  Not part of the public interface.
 #pragma once
 
+#include <cuda.h>
+
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -40,12 +42,23 @@ inline int attention_chunk(int64_t L_max, int64_t B, int64_t Hkv) {
   while (ch < want && ch < 4096) ch <<= 1;
   return ch;
 }
-cudaError_t launch_decode_attention(const AttnArgs& a, int D, cudaStream_t s);
+// The tensor-core kernel's copies: 2-D maps over the K and V code arrays
+// (rows of D/2 bytes, 128-row boxes, the row-width swizzle) and over the
+// scale arrays viewed as 16-byte rows (boxes of 128 cache rows).
+struct AttnMaps {
+  CUtensorMap k_codes, v_codes, k_scales, v_scales;
+};
+
+// maps: null when decode_attention_tc_applies is false.
+cudaError_t launch_decode_attention(const AttnArgs& a, int D, const AttnMaps* maps,
+                                    cudaStream_t s);
 // The pipelined split kernel with both contractions on the tensor cores
 // (attention_tc.cu): heads of 64 and 128, groups of 4 or 8 query heads, both
-// scale arrays 16-byte aligned and L_max * D / 16 a multiple of 16.
+// scale arrays 16-byte aligned, L_max * D / 16 a multiple of 16, and fewer
+// than 2^31 cache rows (the copies' row coordinate).
 bool decode_attention_tc_applies(const AttnArgs& a, int D);
-cudaError_t launch_decode_attention_tc(const AttnArgs& a, int D, cudaStream_t s);
+cudaError_t launch_decode_attention_tc(const AttnArgs& a, int D, const AttnMaps& m,
+                                       cudaStream_t s);
 cudaError_t init_attention_tc_attributes();
 
 }  // namespace nvfp4

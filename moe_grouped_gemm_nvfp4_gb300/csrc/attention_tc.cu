@@ -120,10 +120,12 @@ constexpr int kSoftWarps = 4, kExpWarps = 8;
 constexpr int kProdWarp = kSoftWarps + kExpWarps, kSWarp = kProdWarp + 1, kOWarp = kSWarp + 1;
 constexpr int kWsThreads = (kOWarp + 1) * 32;            // 480
 constexpr float kRescaleLog2 = 8.0f;                     // p <= 2^8 between rescales
-// tensor memory: S of tile parity b at columns 32 b, O of item parity c at
-// 64 + 32 c; each as two 16-column accumulators (even and odd MMA K steps,
-// two independent chains) that the softmax adds
-constexpr uint32_t kOCol = 64, kWsTmemCols = 128;
+constexpr int kNBuf = 3;                                 // tiles in flight between the roles
+// tensor memory (512 columns): K^ of buffer b at columns 64 b (the score
+// MMA's A operand: lane t = token t, two FP16 per column along D); S of
+// buffer b at 192 + 32 b and O of item parity c at 288 + 32 c, each as two
+// 16-column accumulators (even and odd MMA K steps) that the softmax adds
+constexpr uint32_t kKCol = 0, kSCol = 192, kOCol = 288, kWsTmemCols = 512;
 
 template <int D>
 struct WsCfg {
@@ -134,22 +136,23 @@ struct WsCfg {
   static constexpr int kRawScales = 128 * SB;
   // a ring stage: K codes, V codes, K scales, V scales of 128 tokens
   static constexpr int kStage = 2 * kRawCodes + 2 * kRawScales;
-  static constexpr int kKhBuf = kBlk * 16384;            // K^: 128 rows x D FP16, K-major
   static constexpr int kVhBuf = 2 * 16384;               // V^: M padded to 128, MN-major
+  static constexpr int kPhBuf = 4096;                    // P^T: 16 rows x 128 tokens FP16
   static constexpr int kQhBuf = kBlk * 2048;             // q: 16 rows x D FP16, K-major
-  static constexpr int kKh = kWsStages * kStage;
-  static constexpr int kVh = kKh + 2 * kKhBuf;
-  static constexpr int kQh = kVh + 2 * kVhBuf;
+  static constexpr int kVh = kWsStages * kStage;
+  static constexpr int kPh = kVh + kNBuf * kVhBuf;
+  static constexpr int kQh = kPh + kNBuf * kPhBuf;
   static constexpr int kRed = kQh + 2 * kQhBuf;          // [4][16] maxima
   static constexpr int kRedQ = kRed + 256;               // [4][16] q maxima
   static constexpr int kRedL = kRedQ + 256;              // [4][16] sums
   static constexpr int kCtl = kRedL + 256;
   static constexpr int kBar = kCtl + 16;
-  static constexpr int kNumBars = 2 * kWsStages + 14;
+  static constexpr int kNumBars = 2 * kWsStages + 4 * kNBuf + 6;
   static constexpr int kSlot = kBar + kNumBars * 8;
   static constexpr int kBytes = kSlot + 16 + 1024;       // + alignment slack
-  static_assert(kStage % 1024 == 0 && kKhBuf >= 4096, "layout");
+  static_assert(kStage % 1024 == 0, "layout");
   static_assert(sizeof(CtaCtl) == 16, "control block");
+  static_assert(kBytes <= 232448, "shared memory");
 };
 
 // bar.red over the softmax warps (named barrier 1): every one of them
@@ -259,7 +262,11 @@ __device__ __forceinline__ void mbar_arrive_elect(uint32_t bar) {
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(kWsThreads, 1) decode_attention_ws_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(kWsThreads, 1)
+decode_attention_ws_kernel(const __grid_constant__ CUtensorMap tmk,
+                           const __grid_constant__ CUtensorMap tmv,
+                           const __grid_constant__ CUtensorMap tsk,
+                           const __grid_constant__ CUtensorMap tsv, const AttnArgs a) {
   static_assert(G <= 8, "P's high and low parts share the MMA's 16 columns");
   static_assert(D == 64 || D == 128, "four or eight 16-element blocks per row");
   using C = WsCfg<D>;
@@ -270,9 +277,11 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_attention_ws_kernel(cons
   const uint32_t sbase = smem_u32(smem);
   CtaCtl* ctl = reinterpret_cast<CtaCtl*>(smem + C::kCtl);
   const uint32_t bars = sbase + C::kBar;
-  const uint32_t op_full0 = bars + 8u * (2 * kWsStages), o_done0 = op_full0 + 16,
-                 s_full0 = o_done0 + 16, p_full0 = s_full0 + 16, q_full0 = p_full0 + 16,
-                 q_empty0 = q_full0 + 16, fin_s = q_empty0 + 16, fin_o = fin_s + 8;
+  // per-buffer barriers (kNBuf each), then the q buffers' pair and the drains
+  const uint32_t op_full0 = bars + 8u * (2 * kWsStages), o_done0 = op_full0 + 8 * kNBuf,
+                 s_full0 = o_done0 + 8 * kNBuf, p_full0 = s_full0 + 8 * kNBuf,
+                 q_full0 = p_full0 + 8 * kNBuf, q_empty0 = q_full0 + 16, fin_s = q_empty0 + 16,
+                 fin_o = fin_s + 8;
   auto raw_full = [&](uint32_t st) { return bars + 8u * st; };
   auto raw_empty = [&](uint32_t st) { return bars + 8u * (kWsStages + st); };
   uint32_t* slot = reinterpret_cast<uint32_t*>(smem + C::kSlot);
@@ -285,11 +294,13 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_attention_ws_kernel(cons
       mbar_init(raw_full(st), 1);
       mbar_init(raw_empty(st), kExpWarps);
     }
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < kNBuf; ++h) {
       mbar_init(op_full0 + 8 * h, kExpWarps);
       mbar_init(o_done0 + 8 * h, 1);
       mbar_init(s_full0 + 8 * h, 1);
       mbar_init(p_full0 + 8 * h, kSoftWarps);
+    }
+    for (int h = 0; h < 2; ++h) {
       mbar_init(q_full0 + 8 * h, kSoftWarps);
       mbar_init(q_empty0 + 8 * h, 1);
     }
@@ -301,12 +312,14 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_attention_ws_kernel(cons
     tmem_alloc(smem_u32(slot), kWsTmemCols);
     tmem_relinquish();
   }
-  // both q buffers start at zero (rows G..15 stay so); for 64-wide heads the
-  // value operands' second M block is zero padding
+  // the q and P^T buffers start at zero (rows the group does not use stay
+  // so); for 64-wide heads the value operands' second M block is zero padding
   for (int i = tid; i < 2 * C::kQhBuf / 16; i += kWsThreads)
     reinterpret_cast<uint4*>(smem + C::kQh)[i] = make_uint4(0u, 0u, 0u, 0u);
+  for (int i = tid; i < kNBuf * C::kPhBuf / 16; i += kWsThreads)
+    reinterpret_cast<uint4*>(smem + C::kPh)[i] = make_uint4(0u, 0u, 0u, 0u);
   if (D < 128)
-    for (int i = tid; i < 2 * 16384 / 16; i += kWsThreads) {
+    for (int i = tid; i < kNBuf * 16384 / 16; i += kWsThreads) {
       const int h = i / (16384 / 16), r = i % (16384 / 16);
       reinterpret_cast<uint4*>(smem + C::kVh + h * C::kVhBuf + 16384)[r] =
           make_uint4(0u, 0u, 0u, 0u);
@@ -333,24 +346,24 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_attention_ws_kernel(cons
           ok = __all_sync(0xFFFFFFFFu, ws_wait(raw_empty(st), ((i / kWsStages) - 1) & 1u, ctl,
                                                a.status));
         if (!ok) break;
-        const uint32_t rows = static_cast<uint32_t>(min(static_cast<int64_t>(kTile), it.t1 - tt));
-        const uint32_t bytes_c = rows * KB;
-        const uint32_t bytes_s = (rows * SB) & ~15u;     // whole 16-byte units by copy
         const uint32_t dst = sbase + st * C::kStage;
         const int64_t r = it.row0 + tt;
         if (i == 0 && (a.debug_flags & kDebugSkipFirstStage)) {
           skipped_first = true;                          // test hook: this stage never fills
           continue;
         }
-        mbar_arrive_expect_tx_elect(raw_full(st), 2 * bytes_c + 2 * bytes_s);
-        bulk_load_elect(dst, a.k_packed + r * KB, bytes_c, raw_full(st), policy);
-        bulk_load_elect(dst + C::kRawCodes, a.v_packed + r * KB, bytes_c, raw_full(st), policy);
-        if (bytes_s) {
-          bulk_load_elect(dst + 2 * C::kRawCodes, a.k_scales + r * SB, bytes_s, raw_full(st),
+        // 128-row TMA boxes: the codes with the row-width swizzle, the scales
+        // as 16-byte rows (16 / SB cache rows each).  Rows past the split's
+        // end are read too and left unused; past the cache's end they are
+        // zero-filled.
+        mbar_arrive_expect_tx_elect(raw_full(st), 2 * C::kRawCodes + 2 * C::kRawScales);
+        tma_load_2d_elect(dst, &tmk, raw_full(st), 0, static_cast<int32_t>(r), policy);
+        tma_load_2d_elect(dst + C::kRawCodes, &tmv, raw_full(st), 0, static_cast<int32_t>(r),
                           policy);
-          bulk_load_elect(dst + 2 * C::kRawCodes + C::kRawScales, a.v_scales + r * SB, bytes_s,
-                          raw_full(st), policy);
-        }
+        const int32_t rs = static_cast<int32_t>(r * SB / 16);
+        tma_load_2d_elect(dst + 2 * C::kRawCodes, &tsk, raw_full(st), 0, rs, policy);
+        tma_load_2d_elect(dst + 2 * C::kRawCodes + C::kRawScales, &tsv, raw_full(st), 0, rs,
+                          policy);
       }
     }
     // every copy this warp issued has landed before the CTA can exit
@@ -359,12 +372,22 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_attention_ws_kernel(cons
       if (k > 0 || !skipped_first) ws_drain(raw_full(k % kWsStages), (k / kWsStages) & 1u, a.timeout_ns);
   } else if (warp >= kSoftWarps && warp < kProdWarp) {
     // --------------------------------------------------------------- expansion
-    constexpr int kRowStep = 256 / NB;                   // rows between a thread's units
-    constexpr int kUnits = kTile / kRowStep;             // units per operand per thread
-    // Lanes 8m .. 8m + 7 (one pass of a 16-byte shared-memory store) take four
-    // blocks of two adjacent rows: the 128-byte swizzle then spreads them over
-    // all eight 16-byte bank groups.  A warp covers 32 / NB rows of NB blocks.
+    // The raw code rows arrive swizzled by the TMA: 16-byte chunk c of row t
+    // sits at chunk c ^ ((t >> 1) & 3) for 64-byte rows (D 128) and c ^ ((t >> 2)
+    // & 1) for 32-byte rows (D 64).
+    auto swz = [](int t) { return NB == 8 ? ((t >> 1) & 3) : ((t >> 2) & 1); };
     const int e = warp - kSoftWarps;
+    // K: lane = token (the tensor-memory lane the score MMA reads as row t of
+    // A); warp e takes the 32 tokens of its lane quarter and half hh of the
+    // row's blocks, expands them and stores them with one tcgen05.st
+    constexpr int NBH = NB / 2;                          // blocks per half row
+    const int tk = (warp & 3) * 32 + lane, hh = e >> 2;
+    const uint32_t kcol = static_cast<uint32_t>(hh * NBH * 8);
+    // V: lanes 8m .. 8m + 7 (one pass of a 16-byte shared-memory store) take
+    // four blocks of two adjacent rows, so the 128-byte swizzle of the V^
+    // operand spreads each pass over all eight bank groups
+    constexpr int kRowStep = 256 / NB;                   // rows between a thread's V units
+    constexpr int kUnits = kTile / kRowStep;             // V units per thread
     const int blk = NB == 8 ? ((lane >> 3) & 1) * 4 + (lane & 3) : (lane & 3);
     const int rin = NB == 8 ? ((lane >> 4) * 2 + ((lane >> 2) & 1))
                             : ((lane >> 3) * 2 + ((lane >> 2) & 1));
@@ -381,53 +404,77 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_attention_ws_kernel(cons
       const WsItem it = ws_item(a, w, n_nxt);
       n_nxt = ws_len(a, w + gridDim.x, items);
       for (int64_t tt = it.t0; tt < it.t1; tt += kTile, ++i) {
-        const uint32_t st = i % kWsStages, ob = i & 1u;
+        const uint32_t st = i % kWsStages, ob = i % kNBuf;
         ok = __all_sync(0xFFFFFFFFu, ws_wait(raw_full(st), (i / kWsStages) & 1u, ctl, a.status));
         if (!ok) break;
         const int rows = static_cast<int>(min(static_cast<int64_t>(kTile), it.t1 - tt));
-        const int rows_s = static_cast<int>(((rows * SB) & ~15) / SB);
         const uint8_t* raw = smem + st * C::kStage;
-        uint2 kcode[kUnits], vcode[kUnits];
-        uint32_t kscale[kUnits], vscale[kUnits];
+        const uint8_t* ksr = raw + 2 * C::kRawCodes;    // scales, row-major [128][SB]
+        const uint8_t* vsr = ksr + C::kRawScales;
+        // K half row of token tk: NBH blocks = NBH / 2 chunks of 16 bytes
+        uint4 kch[NBH / 2];
+        uint32_t ksw = 0u;                               // the half row's NBH scale bytes
+#pragma unroll
+        for (int j = 0; j < NBH / 2; ++j) {
+          kch[j] = make_uint4(0u, 0u, 0u, 0u);
+          if (tk < rows) {
+            const int ch = (hh * (NBH / 2) + j) ^ swz(tk);
+            kch[j] = *reinterpret_cast<const uint4*>(raw + tk * KB + ch * 16);
+          }
+        }
+        if (tk < rows)
+          ksw = NBH == 4 ? *reinterpret_cast<const uint32_t*>(ksr + tk * SB + hh * 4)
+                         : *reinterpret_cast<const uint16_t*>(ksr + tk * SB + hh * 2);
+        uint2 vcode[kUnits];
+        uint32_t vscale[kUnits];
 #pragma unroll
         for (int k = 0; k < kUnits; ++k) {
           const int t = trow0 + k * kRowStep;
-          kcode[k] = make_uint2(0u, 0u);
           vcode[k] = make_uint2(0u, 0u);
-          kscale[k] = 0u;
           vscale[k] = 0u;
           if (t < rows) {
-            kcode[k] = *reinterpret_cast<const uint2*>(raw + t * KB + blk * 8);
-            vcode[k] = *reinterpret_cast<const uint2*>(raw + C::kRawCodes + t * KB + blk * 8);
-            if (t < rows_s) {
-              kscale[k] = raw[2 * C::kRawCodes + t * SB + blk];
-              vscale[k] = raw[2 * C::kRawCodes + C::kRawScales + t * SB + blk];
-            } else {                                     // rows past the copied scale units
-              const int64_t r = it.row0 + tt + t;
-              kscale[k] = __ldg(a.k_scales + r * SB + blk);
-              vscale[k] = __ldg(a.v_scales + r * SB + blk);
-            }
+            const int ch = (blk >> 1) ^ swz(t);
+            vcode[k] = *reinterpret_cast<const uint2*>(raw + C::kRawCodes + t * KB + ch * 16 +
+                                                      (blk & 1) * 8);
+            vscale[k] = vsr[t * SB + blk];
           }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(raw_empty(st));       // the ring stage may be refilled
-        if (i >= 2)                                      // tile i-2's MMAs are done with the buffers
-          ok = __all_sync(0xFFFFFFFFu, ws_wait(o_done0 + 8 * ob, ((i >> 1) - 1) & 1u, ctl,
+        if (i >= kNBuf)                                  // tile i - 3's MMAs are done with the buffers
+          ok = __all_sync(0xFFFFFFFFu, ws_wait(o_done0 + 8 * ob, ((i / kNBuf) - 1) & 1u, ctl,
                                                a.status));
         if (!ok) break;
-        uint8_t* kh = smem + C::kKh + ob * C::kKhBuf;
+        // K^ -> tensor memory, row tk, columns kcol .. kcol + 8 NBH
+        uint32_t kv[8 * NBH];
+#pragma unroll
+        for (int u = 0; u < NBH; ++u) {
+          const uint4 wq = kch[u >> 1];
+          uint4 lo, hi;
+          expand16((u & 1) ? wq.z : wq.x, (u & 1) ? wq.w : wq.y, (ksw >> (8 * u)) & 0xFFu, lo,
+                   hi);
+          kv[8 * u + 0] = lo.x; kv[8 * u + 1] = lo.y; kv[8 * u + 2] = lo.z; kv[8 * u + 3] = lo.w;
+          kv[8 * u + 4] = hi.x; kv[8 * u + 5] = hi.y; kv[8 * u + 6] = hi.z; kv[8 * u + 7] = hi.w;
+        }
+        const uint32_t kt = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kKCol +
+                            64u * ob + kcol;
+        if constexpr (NBH == 4) {
+          tmem_st32(kt, kv);
+        } else {
+          tmem_st16(kt, kv);
+        }
+        // V^ -> shared memory (MN-major operand)
         uint8_t* vh = smem + C::kVh + ob * C::kVhBuf;
 #pragma unroll
         for (int k = 0; k < kUnits; ++k) {
           uint4 lo, hi;
-          expand16(kcode[k].x, kcode[k].y, kscale[k], lo, hi);
-          *reinterpret_cast<uint4*>(kh + offlo + k * kUnitStride) = lo;
-          *reinterpret_cast<uint4*>(kh + offhi + k * kUnitStride) = hi;
           expand16(vcode[k].x, vcode[k].y, vscale[k], lo, hi);
           *reinterpret_cast<uint4*>(vh + offlo + k * kUnitStride) = lo;
           *reinterpret_cast<uint4*>(vh + offhi + k * kUnitStride) = hi;
         }
+        tmem_st_wait();
         fence_proxy_async_smem();
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(op_full0 + 8 * ob);
       }
@@ -449,18 +496,18 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_attention_ws_kernel(cons
         continue;
       }
       for (int64_t tt = it.t0; tt < it.t1 && ok; tt += kTile, ++i) {
-        const uint32_t ob = i & 1u;
-        ok = __all_sync(0xFFFFFFFFu, ws_wait(op_full0 + 8 * ob, (i >> 1) & 1u, ctl, a.status));
+        const uint32_t ob = i % kNBuf;
+        ok = __all_sync(0xFFFFFFFFu, ws_wait(op_full0 + 8 * ob, (i / kNBuf) & 1u, ctl, a.status));
         if (!ok) break;
         tc_fence_after();
+        // A = K^ in tensor memory: 16 K values (8 columns) per MMA
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          tc_mma_f16_elect(tmem + 32 * ob + 16 * (kk & 1),
-                           sdesc_sw128(sbase + C::kKh + ob * C::kKhBuf + (kk >> 2) * 16384 +
-                                       (kk & 3) * 32),
-                           sdesc_sw128(sbase + C::kQh + qb * C::kQhBuf + (kk >> 2) * 2048 +
-                                       (kk & 3) * 32),
-                           idesc_s, kk > 1 ? 1u : 0u);
+          tc_mma_f16_ts_elect(tmem + kSCol + 32 * ob + 16 * (kk & 1),
+                              tmem + kKCol + 64 * ob + 8 * kk,
+                              sdesc_sw128(sbase + C::kQh + qb * C::kQhBuf + (kk >> 2) * 2048 +
+                                          (kk & 3) * 32),
+                              idesc_s, kk > 1 ? 1u : 0u);
         tc_commit_elect(s_full0 + 8 * ob);
       }
       if (ok) tc_commit_elect(q_empty0 + 8 * qb);        // q's buffer is free once these finish
@@ -478,15 +525,15 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_attention_ws_kernel(cons
       n_nxt = ws_len(a, w + gridDim.x, items);
       const uint32_t otm = tmem + kOCol + 32 * (k & 1u);
       for (int64_t tt = it.t0; tt < it.t1 && ok; tt += kTile, ++i) {
-        const uint32_t pb = i & 1u;
-        ok = __all_sync(0xFFFFFFFFu, ws_wait(p_full0 + 8 * pb, (i >> 1) & 1u, ctl, a.status));
+        const uint32_t pb = i % kNBuf;
+        ok = __all_sync(0xFFFFFFFFu, ws_wait(p_full0 + 8 * pb, (i / kNBuf) & 1u, ctl, a.status));
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
           const uint64_t va =
               sdesc_sw128_mn(sbase + C::kVh + pb * C::kVhBuf + kk * 2048, 16384, 1024);
-          const uint32_t pa = sbase + C::kKh + pb * C::kKhBuf + (kk >> 2) * 2048 + (kk & 3) * 32;
+          const uint32_t pa = sbase + C::kPh + pb * C::kPhBuf + (kk >> 2) * 2048 + (kk & 3) * 32;
           tc_mma_f16_elect(otm + 16 * (kk & 1), va, sdesc_sw128(pa), idesc_o,
                            (tt > it.t0 || kk > 1) ? 1u : 0u);
         }
@@ -613,9 +660,9 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_attention_ws_kernel(cons
           l_part[g] = 0.0f;
         }
         for (int64_t tt = it.t0; tt < it.t1; tt += kTile, ++i) {
-          const uint32_t ob = i & 1u;
+          const uint32_t ob = i % kNBuf;
           const bool first = tt == it.t0;
-          ok = __all_sync(0xFFFFFFFFu, ok && ws_wait(s_full0 + 8 * ob, (i >> 1) & 1u, ctl,
+          ok = __all_sync(0xFFFFFFFFu, ok && ws_wait(s_full0 + 8 * ob, (i / kNBuf) & 1u, ctl,
                                                      a.status));
           const bool valid = tt + s < it.t1;
           float x[G];
@@ -623,8 +670,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_attention_ws_kernel(cons
           if (ok) {
             tc_fence_after();
             uint32_t sr[16], sr2[16];
-            tmem_ld16(tmem + lane_base + 32 * ob, sr);
-            tmem_ld16(tmem + lane_base + 32 * ob + 16, sr2);
+            tmem_ld16(tmem + lane_base + kSCol + 32 * ob, sr);
+            tmem_ld16(tmem + lane_base + kSCol + 32 * ob + 16, sr2);
             tmem_ld_wait();
 #pragma unroll
             for (int g = 0; g < G; ++g) {
@@ -658,7 +705,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_attention_ws_kernel(cons
             }
             if (!first) {
               // O so far (through tile i - 1) times the correction
-              ok = __all_sync(0xFFFFFFFFu, ws_wait(o_done0 + 8 * ((i - 1) & 1u), ((i - 1) >> 1) & 1u,
+              ok = __all_sync(0xFFFFFFFFu, ws_wait(o_done0 + 8 * ((i - 1) % kNBuf), ((i - 1) / kNBuf) & 1u,
                                                    ctl, a.status));
               if (ok) {
                 tc_fence_after();
@@ -684,7 +731,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_attention_ws_kernel(cons
             if (!ok) break;
           }
           // P^T: row g the high part, row 8 + g the low part of p for token s
-          uint8_t* pt = smem + C::kKh + ob * C::kKhBuf;
+          uint8_t* pt = smem + C::kPh + ob * C::kPhBuf;
           const uint32_t pc = (s >> 6) * 2048 + (s & 7) * 2;
 #pragma unroll
           for (int g = 0; g < G; ++g) {
@@ -703,7 +750,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_attention_ws_kernel(cons
         // O of the item: the value MMAs of its last tile have completed
         float o[G];
         if (ok) {
-          ok = __all_sync(0xFFFFFFFFu, ws_wait(o_done0 + 8 * ((i - 1) & 1u), ((i - 1) >> 1) & 1u,
+          ok = __all_sync(0xFFFFFFFFu, ws_wait(o_done0 + 8 * ((i - 1) % kNBuf), ((i - 1) / kNBuf) & 1u,
                                                ctl, a.status));
           if (ok) {
             tc_fence_after();
@@ -778,20 +825,22 @@ cudaError_t set_ws_attrs_d() {
 // One CTA per SM (the pipeline's shared memory), or one per work item when
 // there are fewer items.
 template <int D, int G>
-cudaError_t launch_ws_d_g(const AttnArgs& a, cudaStream_t s) {
+cudaError_t launch_ws_d_g(const AttnArgs& a, const AttnMaps& m, cudaStream_t s) {
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const int64_t items = static_cast<int64_t>(a.splits) * a.Hkv * a.B;
   const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
-  decode_attention_ws_kernel<D, G><<<grid, kWsThreads, WsCfg<D>::kBytes, s>>>(a);
+  decode_attention_ws_kernel<D, G><<<grid, kWsThreads, WsCfg<D>::kBytes, s>>>(m.k_codes, m.v_codes,
+                                                                             m.k_scales,
+                                                                             m.v_scales, a);
   return cudaGetLastError();
 }
 
 template <int D>
-cudaError_t launch_ws_d(const AttnArgs& a, int G, cudaStream_t s) {
-  return G == 4 ? launch_ws_d_g<D, 4>(a, s) : launch_ws_d_g<D, 8>(a, s);
+cudaError_t launch_ws_d(const AttnArgs& a, int G, const AttnMaps& m, cudaStream_t s) {
+  return G == 4 ? launch_ws_d_g<D, 4>(a, m, s) : launch_ws_d_g<D, 8>(a, m, s);
 }
 
 }  // namespace
@@ -811,13 +860,15 @@ bool decode_attention_tc_applies(const AttnArgs& a, int D) {
       ((reinterpret_cast<uintptr_t>(a.k_scales) | reinterpret_cast<uintptr_t>(a.v_scales)) &
        15u) == 0 &&
       (a.L_max * (D / 16)) % 16 == 0;
-  return (D == 64 || D == 128) && (G == 4 || G == 8) && units16;
+  const bool rows31 = static_cast<int64_t>(a.B) * a.Hkv * a.L_max < (int64_t{1} << 31);
+  return (D == 64 || D == 128) && (G == 4 || G == 8) && units16 && rows31;
 }
 
-cudaError_t launch_decode_attention_tc(const AttnArgs& a, int D, cudaStream_t s) {
+cudaError_t launch_decode_attention_tc(const AttnArgs& a, int D, const AttnMaps& m,
+                                       cudaStream_t s) {
   const int G = a.Hq / a.Hkv;
   if (!decode_attention_tc_applies(a, D)) return cudaErrorInvalidValue;
-  return D == 64 ? launch_ws_d<64>(a, G, s) : launch_ws_d<128>(a, G, s);
+  return D == 64 ? launch_ws_d<64>(a, G, m, s) : launch_ws_d<128>(a, G, m, s);
 }
 
 }  // namespace nvfp4

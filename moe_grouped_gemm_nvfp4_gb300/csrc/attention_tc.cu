@@ -378,15 +378,18 @@ decode_attention_ws_kernel(const __grid_constant__ CUtensorMap tmk,
     auto swz = [](int t) { return NB == 8 ? ((t >> 1) & 3) : ((t >> 2) & 1); };
     const int e = warp - kSoftWarps;
     // K: lane = token (the tensor-memory lane the score MMA reads as row t of
-    // A); warp e takes the 32 tokens of its lane quarter and half hh of the
-    // row's blocks, expands them and stores them with one tcgen05.st
-    constexpr int NBH = NB / 2;                          // blocks per half row
-    const int tk = (warp & 3) * 32 + lane, hh = e >> 2;
-    const uint32_t kcol = static_cast<uint32_t>(hh * NBH * 8);
+    // A); warp e takes the 32 tokens of its lane quarter and part pp of the
+    // row's blocks (NBP of them), expands them and stores them with one
+    // tcgen05.st
+    constexpr int kParts = kExpWarps / 4;                // warps per lane quarter
+    constexpr int NBP = NB / kParts;                     // blocks per part
+    static_assert(NBP == 1 || NBP == 2 || NBP == 4, "parts of a K row");
+    const int tk = (warp & 3) * 32 + lane, pp = e >> 2;
+    const uint32_t kcol = static_cast<uint32_t>(pp * NBP * 8);
     // V: lanes 8m .. 8m + 7 (one pass of a 16-byte shared-memory store) take
     // four blocks of two adjacent rows, so the 128-byte swizzle of the V^
     // operand spreads each pass over all eight bank groups
-    constexpr int kRowStep = 256 / NB;                   // rows between a thread's V units
+    constexpr int kRowStep = kExpWarps * 32 / NB;        // rows between a thread's V units
     constexpr int kUnits = kTile / kRowStep;             // V units per thread
     const int blk = NB == 8 ? ((lane >> 3) & 1) * 4 + (lane & 3) : (lane & 3);
     const int rin = NB == 8 ? ((lane >> 4) * 2 + ((lane >> 2) & 1))
@@ -411,20 +414,29 @@ decode_attention_ws_kernel(const __grid_constant__ CUtensorMap tmk,
         const uint8_t* raw = smem + st * C::kStage;
         const uint8_t* ksr = raw + 2 * C::kRawCodes;    // scales, row-major [128][SB]
         const uint8_t* vsr = ksr + C::kRawScales;
-        // K half row of token tk: NBH blocks = NBH / 2 chunks of 16 bytes
-        uint4 kch[NBH / 2];
-        uint32_t ksw = 0u;                               // the half row's NBH scale bytes
+        // part pp of token tk's K row: NBP blocks of 8 code bytes (whole 16-byte
+        // chunks, or half of one when NBP is 1) and their NBP scale bytes
+        uint32_t kw[2 * NBP];
+        uint32_t ksw = 0u;
 #pragma unroll
-        for (int j = 0; j < NBH / 2; ++j) {
-          kch[j] = make_uint4(0u, 0u, 0u, 0u);
-          if (tk < rows) {
-            const int ch = (hh * (NBH / 2) + j) ^ swz(tk);
-            kch[j] = *reinterpret_cast<const uint4*>(raw + tk * KB + ch * 16);
+        for (int j = 0; j < 2 * NBP; ++j) kw[j] = 0u;
+        if (tk < rows) {
+          if constexpr (NBP >= 2) {
+#pragma unroll
+            for (int j = 0; j < NBP / 2; ++j) {
+              const int ch = (pp * (NBP / 2) + j) ^ swz(tk);
+              const uint4 q = *reinterpret_cast<const uint4*>(raw + tk * KB + ch * 16);
+              kw[4 * j] = q.x; kw[4 * j + 1] = q.y; kw[4 * j + 2] = q.z; kw[4 * j + 3] = q.w;
+            }
+          } else {
+            const int ch = (pp >> 1) ^ swz(tk);
+            const uint2 q = *reinterpret_cast<const uint2*>(raw + tk * KB + ch * 16 + (pp & 1) * 8);
+            kw[0] = q.x; kw[1] = q.y;
           }
+          ksw = NBP == 4 ? *reinterpret_cast<const uint32_t*>(ksr + tk * SB + pp * 4)
+                : NBP == 2 ? *reinterpret_cast<const uint16_t*>(ksr + tk * SB + pp * 2)
+                           : ksr[tk * SB + pp];
         }
-        if (tk < rows)
-          ksw = NBH == 4 ? *reinterpret_cast<const uint32_t*>(ksr + tk * SB + hh * 4)
-                         : *reinterpret_cast<const uint16_t*>(ksr + tk * SB + hh * 2);
         uint2 vcode[kUnits];
         uint32_t vscale[kUnits];
 #pragma unroll
@@ -445,23 +457,23 @@ decode_attention_ws_kernel(const __grid_constant__ CUtensorMap tmk,
           ok = __all_sync(0xFFFFFFFFu, ws_wait(o_done0 + 8 * ob, ((i / kNBuf) - 1) & 1u, ctl,
                                                a.status));
         if (!ok) break;
-        // K^ -> tensor memory, row tk, columns kcol .. kcol + 8 NBH
-        uint32_t kv[8 * NBH];
+        // K^ -> tensor memory, row tk, columns kcol .. kcol + 8 NBP
+        uint32_t kv[8 * NBP];
 #pragma unroll
-        for (int u = 0; u < NBH; ++u) {
-          const uint4 wq = kch[u >> 1];
+        for (int u = 0; u < NBP; ++u) {
           uint4 lo, hi;
-          expand16((u & 1) ? wq.z : wq.x, (u & 1) ? wq.w : wq.y, (ksw >> (8 * u)) & 0xFFu, lo,
-                   hi);
+          expand16(kw[2 * u], kw[2 * u + 1], (ksw >> (8 * u)) & 0xFFu, lo, hi);
           kv[8 * u + 0] = lo.x; kv[8 * u + 1] = lo.y; kv[8 * u + 2] = lo.z; kv[8 * u + 3] = lo.w;
           kv[8 * u + 4] = hi.x; kv[8 * u + 5] = hi.y; kv[8 * u + 6] = hi.z; kv[8 * u + 7] = hi.w;
         }
         const uint32_t kt = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kKCol +
                             64u * ob + kcol;
-        if constexpr (NBH == 4) {
+        if constexpr (NBP == 4) {
           tmem_st32(kt, kv);
-        } else {
+        } else if constexpr (NBP == 2) {
           tmem_st16(kt, kv);
+        } else {
+          tmem_st8(kt, kv);
         }
         // V^ -> shared memory (MN-major operand)
         uint8_t* vh = smem + C::kVh + ob * C::kVhBuf;

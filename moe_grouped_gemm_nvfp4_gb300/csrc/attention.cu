@@ -329,9 +329,10 @@ cudaError_t launch_decode_attention(const AttnArgs& a, int D, const AttnMaps* ma
     decode_attention_combine_kernel<<<static_cast<unsigned>(a.B * a.Hq), 128, 0, s>>>(a, D);
     return cudaGetLastError();
   }
-  // groups of 4 and 8 query heads over heads of 64 or 128: the tensor-core
-  // kernel (attention_tc.cu); smaller groups, where the per-head multiply-adds
-  // cost less than the FP16 operand traffic, and wider heads: the kernel above
+  // groups of 2-8 query heads over 128-wide heads and 4-8 over 64-wide heads:
+  // the tensor-core kernel (attention_tc.cu); single heads (and pairs over
+  // 64-wide heads), where the multiply-adds cost less than the FP16
+  // expansion, and wider heads: the kernel above
   if (maps && decode_attention_tc_applies(a, D)) {
     e = launch_decode_attention_tc(a, D, *maps, s);
   } else {

@@ -53,7 +53,8 @@ struct AttnMaps {
 cudaError_t launch_decode_attention(const AttnArgs& a, int D, const AttnMaps* maps,
                                     cudaStream_t s);
 // The pipelined split kernel with both contractions on the tensor cores
-// (attention_tc.cu): heads of 64 and 128, groups of 4 or 8 query heads, both
+// (attention_tc.cu): heads of 128 in groups of 2, 4 or 8 query heads and heads
+// of 64 in groups of 4 or 8, both
 // scale arrays 16-byte aligned, L_max * D / 16 a multiple of 16, and fewer
 // than 2^31 cache rows (the copies' row coordinate).
 bool decode_attention_tc_applies(const AttnArgs& a, int D);

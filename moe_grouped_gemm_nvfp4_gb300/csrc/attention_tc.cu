@@ -1,6 +1,7 @@
 // Decode attention over an NVFP4 KV cache with both contractions on the
 // tensor cores (tcgen05, FP16 operands, FP32 accumulation in tensor memory),
-// for heads of 64 and 128 and groups of 4 or 8 query heads per KV head.
+// for heads of 128 (groups of 2, 4 or 8 query heads per KV head) and of 64
+// (groups of 4 or 8).
 //
 // "The Blackwell architectural split", The Breakthrough -- The A4Q Kernel:
 // the cache stays NVFP4 in memory (E2M1 values, an E4M3 scale per 16 numbers
@@ -831,6 +832,7 @@ template <int D>
 cudaError_t set_ws_attrs_d() {
   cudaError_t e = set_ws_attr<D, 4>();
   if (e == cudaSuccess) e = set_ws_attr<D, 8>();
+  if (D == 128 && e == cudaSuccess) e = set_ws_attr<D, 2>();
   return e;
 }
 
@@ -852,6 +854,8 @@ cudaError_t launch_ws_d_g(const AttnArgs& a, const AttnMaps& m, cudaStream_t s) 
 
 template <int D>
 cudaError_t launch_ws_d(const AttnArgs& a, int G, const AttnMaps& m, cudaStream_t s) {
+  if constexpr (D == 128)
+    if (G == 2) return launch_ws_d_g<D, 2>(a, m, s);
   return G == 4 ? launch_ws_d_g<D, 4>(a, m, s) : launch_ws_d_g<D, 8>(a, m, s);
 }
 
@@ -873,7 +877,10 @@ bool decode_attention_tc_applies(const AttnArgs& a, int D) {
        15u) == 0 &&
       (a.L_max * (D / 16)) % 16 == 0;
   const bool rows31 = static_cast<int64_t>(a.B) * a.Hkv * a.L_max < (int64_t{1} << 31);
-  return (D == 64 || D == 128) && (G == 4 || G == 8) && units16 && rows31;
+  // group sizes where it beats the CUDA-core kernel (measured): 2, 4 and 8
+  // query heads over 128-wide heads, 4 and 8 over 64-wide heads
+  const bool groups = D == 128 ? (G == 2 || G == 4 || G == 8) : (D == 64 && (G == 4 || G == 8));
+  return groups && units16 && rows31;
 }
 
 cudaError_t launch_decode_attention_tc(const AttnArgs& a, int D, const AttnMaps& m,

@@ -48,6 +48,7 @@ def _check(got, ref, name):
     (4, 16, 2, 5000, 128, [5000, 4999, 2048, 129]),  # several work items per CTA, empty splits
     (2, 8, 1, 1500, 64, [1500, 777]),        # groups of 8 over 64-wide heads, ragged tiles
     (2, 8, 2, 3000, 128, [3000, 2999]),      # groups of 4, a tile of one token
+    (2, 8, 4, 1000, 128, [1000, 517]),       # groups of 2 on the tensor cores
 ])
 def test_decode_attention_matches_oracle(B, Hq, Hkv, L, D, lens):
     q, k, v = _case(B * 1000 + Hq * 10 + D + L, B, Hq, Hkv, L, D)

@@ -734,9 +734,11 @@ def measure_configs(args, dev, groups=None):
         torch.cuda.empty_cache()
     # decode attention over an NVFP4 KV cache (every cache byte read once):
     # 128-wide heads in groups of 4, 8 (tensor-core kernel) and 1 (CUDA-core
-    # kernel), and 512-wide heads
+    # kernel), 256-wide heads in groups of 4 and 512-wide heads in groups of 4
+    # (the two-pass tensor-core kernels)
     for (B_, Hq_, Hkv_, L_, D_) in ((16, 32, 8, 16384, 128), (16, 64, 8, 16384, 128),
-                                    (16, 8, 8, 16384, 128), (8, 8, 2, 32768, 512)):
+                                    (16, 8, 8, 16384, 128), (16, 32, 8, 8192, 256),
+                                    (8, 8, 2, 32768, 512)):
         if not want("decode_attention"):
             break
         kc = inputs.device_normal_bf16((B_, Hkv_, L_, D_), 1.0, 71, dev)
@@ -755,13 +757,22 @@ def measure_configs(args, dev, groups=None):
             t_att, fl, byt, hbm, fp4,
             note="one query token per sequence; K and V in NVFP4 (codes + E4M3 scales along "
                  "D + one global each); split-KV partials merged by a second kernel (both "
-                 "timed); " + ("tcgen05 pipelined kernel" if D_ <= 128 and Hq_ // Hkv_ >= 4
-                               else "CUDA-core kernel"))
+                 "timed); " + _attention_kernel_name(D_, Hq_ // Hkv_))
         del kq, vq, plan
         torch.cuda.empty_cache()
     for v in out.values():
         v.setdefault("peak_source", peak_src)
     return out
+
+
+def _attention_kernel_name(D_, G_):
+    """Which decode-attention kernel the library picks for a head width and
+    group size (the dispatch in csrc/attention_tc.cu, aligned scale arrays)."""
+    if D_ >= 256 and G_ in (2, 4, 8) and not (D_ == 512 and G_ == 8):
+        return "tcgen05 two-pass kernels (scores, then values)"
+    if (D_ == 128 and G_ in (2, 4, 8)) or (D_ == 64 and G_ in (4, 8)):
+        return "tcgen05 pipelined kernel"
+    return "CUDA-core kernel"
 
 
 def run_configs(args):

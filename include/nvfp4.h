@@ -542,7 +542,9 @@ nvfp4_status nvfp4_grouped_gemm_sparse(const uint8_t* A_tiles, const float* gA,
  *              v_hat); FP32 arithmetic, BF16 round to nearest even; an empty
  *              sequence gives zeros.
  *   workspace  FP32, nvfp4_decode_attention_workspace_bytes(B, Hq, Hkv, L_max,
- *              D) bytes, caller-owned (per-split partials, overwritten).
+ *              D) bytes, caller-owned (per-split partials and, for heads of
+ *              256 and 512, every cached token's score per query head;
+ *              overwritten).
  * D in {64, 128, 256, 512}; Hq / Hkv in {1, 2, 4, 8} (at most 4 for D = 512);
  * q, out, workspace and the code arrays 16-byte aligned, the scale arrays
  * 4-byte aligned.  The tensor-core kernel's waits are bounded: a wait that

@@ -117,30 +117,35 @@ nvfp4_status make_operand_map(CUtensorMap* m, const void* base, uint64_t rows, u
 }
 
 // 2-D map over a KV-cache code array [rows, D/2] (uint8) for the tensor-core
-// attention: boxes of 128 whole rows with the swizzle of the row width (64
-// bytes for D = 128, 32 for D = 64).  Rows past the array read zeros.
+// attention: boxes of 128 rows, each the whole row with the swizzle of the row
+// width (64 bytes for D = 128, 32 for D = 64) or, for D = 256 and 512, 64
+// bytes of it (128 head dimensions) with the 64-byte swizzle.  Rows past the
+// array read zeros.
 nvfp4_status make_kv_code_map(CUtensorMap* m, const void* base, uint64_t rows, int D) {
   const uint64_t row_bytes = static_cast<uint64_t>(D / 2);
   const cuuint64_t dims[2] = {row_bytes, rows};
   const cuuint64_t strides[1] = {row_bytes};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(row_bytes), 128u};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(row_bytes < 64 ? row_bytes : 64), 128u};
   const cuuint32_t estr[2] = {1u, 1u};
   const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
                               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              D == 128 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B,
+                              D >= 128 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? NVFP4_OK : NVFP4_ERR_UNSUPPORTED;
 }
 
-// 2-D map over a KV-cache scale array [rows, D/16] (uint8) viewed as 16-byte
-// rows, boxes of 128 cache rows (rows * D/16 a multiple of 16).  Rows past the
-// array read zeros.
+// 2-D map over a KV-cache scale array [rows, D/16] (uint8) for the
+// tensor-core attention.  D = 64 and 128: viewed as 16-byte rows, boxes of 128
+// cache rows (rows * D/16 a multiple of 16).  D = 256 and 512: the rows as they
+// are, boxes of 16 bytes (two slices of 128 dimensions) x 128 rows.  Rows past
+// the array read zeros.
 nvfp4_status make_kv_scale_map(CUtensorMap* m, const void* base, uint64_t rows, int D) {
   const uint64_t sb = static_cast<uint64_t>(D / 16);
-  const cuuint64_t dims[2] = {16u, rows * sb / 16};
-  const cuuint64_t strides[1] = {16u};
-  const cuuint32_t box[2] = {16u, static_cast<cuuint32_t>(128 * sb / 16)};
+  const bool wide = sb >= 16;                      // rows of 16 or 32 bytes, 16-byte boxes
+  const cuuint64_t dims[2] = {wide ? sb : 16u, wide ? rows : rows * sb / 16};
+  const cuuint64_t strides[1] = {wide ? sb : 16u};
+  const cuuint32_t box[2] = {16u, static_cast<cuuint32_t>(wide ? 128 : 128 * sb / 16)};
   const cuuint32_t estr[2] = {1u, 1u};
   const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
                               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -657,8 +662,15 @@ size_t nvfp4_decode_attention_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || L_max < 0 || D <= 0) return 0;
   const int ch = nvfp4::attention_chunk(L_max, B, Hkv);
   const int64_t splits = (L_max + ch - 1) / ch;
+  // heads of 256 and 512 also keep every cached token's base-2 score per query
+  // head (the tensor-core path writes them in one pass and reads them in the
+  // next)
+  const size_t scores = D >= 256 ? static_cast<size_t>(B) * static_cast<size_t>(Hq) *
+                                       static_cast<size_t>(L_max) * sizeof(float)
+                                 : 0;
   return static_cast<size_t>(B) * static_cast<size_t>(Hq) * static_cast<size_t>(splits) *
-         static_cast<size_t>(D + 2) * sizeof(float);
+             static_cast<size_t>(D + 2) * sizeof(float) +
+         scores;
 }
 
 nvfp4_status nvfp4_decode_attention(const void* q, const uint8_t* k_packed,
@@ -712,6 +724,7 @@ nvfp4_status nvfp4_decode_attention(const void* q, const uint8_t* k_packed,
   a.out = static_cast<uint16_t*>(out);
   a.ws_o = workspace;
   a.ws_ml = workspace + static_cast<int64_t>(B) * Hq * a.splits * D;
+  a.ws_s = a.ws_ml + static_cast<int64_t>(B) * Hq * a.splits * 2;
   a.status = d->status;
   a.timeout_ns = g_timeout_ns.load();
   nvfp4::AttnMaps maps;

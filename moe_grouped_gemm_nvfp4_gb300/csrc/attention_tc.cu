@@ -702,22 +702,25 @@ cudaError_t launch_ws_d(const AttnArgs& a, int G, const AttnMaps& m, cudaStream_
 cudaError_t init_attention_tc_attributes() {
   cudaError_t e = set_ws_attrs_d<64>();
   if (e == cudaSuccess) e = set_ws_attrs_d<128>();
+  if (e == cudaSuccess) e = init_attention_tc_wide_attributes();
   return e;
 }
 
 bool decode_attention_tc_applies(const AttnArgs& a, int D) {
   const int G = a.Hq / a.Hkv;
-  // the pipelined kernel copies scale rows in 16-byte units: both scale
-  // arrays 16-byte aligned and every (sequence, KV head) slab a whole number
-  // of units (L_max * D / 16 bytes a multiple of 16)
+  // the pipelined kernels copy scale rows in 16-byte units: both scale
+  // arrays 16-byte aligned and, for heads of 64 and 128 (scale rows of 4 and
+  // 8 bytes), every (sequence, KV head) slab a whole number of units (L_max *
+  // D / 16 bytes a multiple of 16)
   const bool units16 =
       ((reinterpret_cast<uintptr_t>(a.k_scales) | reinterpret_cast<uintptr_t>(a.v_scales)) &
        15u) == 0 &&
-      (a.L_max * (D / 16)) % 16 == 0;
+      (D >= 256 || (a.L_max * (D / 16)) % 16 == 0);
   const bool rows31 = static_cast<int64_t>(a.B) * a.Hkv * a.L_max < (int64_t{1} << 31);
   // group sizes where it beats the CUDA-core kernel (measured): 2, 4 and 8
-  // query heads over 128-wide heads, 4 and 8 over 64-wide heads
-  const bool groups = D == 128 ? (G == 2 || G == 4 || G == 8) : (D == 64 && (G == 4 || G == 8));
+  // query heads over heads of 128 and wider, 4 and 8 over 64-wide heads
+  const bool groups = D >= 128 ? (G == 2 || G == 4 || (G == 8 && D != 512))
+                              : (D == 64 && (G == 4 || G == 8));
   return groups && units16 && rows31;
 }
 
@@ -725,6 +728,7 @@ cudaError_t launch_decode_attention_tc(const AttnArgs& a, int D, const AttnMaps&
                                        cudaStream_t s) {
   const int G = a.Hq / a.Hkv;
   if (!decode_attention_tc_applies(a, D)) return cudaErrorInvalidValue;
+  if (D >= 256) return launch_decode_attention_tc_wide(a, D, m, s);
   return D == 64 ? launch_ws_d<64>(a, G, m, s) : launch_ws_d<128>(a, G, m, s);
 }
 

@@ -76,10 +76,11 @@ def test_pure_host_helpers():
     # 2048-token splits: ~1024 (sequence, KV head, split) work items
     assert F.nvfp4_decode_attention_workspace_bytes(16, 32, 8, 16384, 128) == \
         16 * 32 * (16384 // 2048) * 130 * 4
+    # 512-wide heads also hold every token's score per query head
     assert F.nvfp4_decode_attention_workspace_bytes(8, 8, 2, 32768, 512) == \
-        8 * 8 * (32768 // 512) * 514 * 4
+        8 * 8 * (32768 // 512) * 514 * 4 + 8 * 8 * 32768 * 4
     assert F.nvfp4_decode_attention_workspace_bytes(16, 8, 8, 65536, 512) == \
-        16 * 8 * (65536 // 4096) * 514 * 4     # 4096-token splits, the largest
+        16 * 8 * (65536 // 4096) * 514 * 4 + 16 * 8 * 65536 * 4   # 4096-token splits
     assert F.nvfp4_decode_attention_workspace_bytes(0, 8, 2, 1000, 128) == 0
 
 

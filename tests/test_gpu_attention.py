@@ -49,6 +49,11 @@ def _check(got, ref, name):
     (2, 8, 1, 1500, 64, [1500, 777]),        # groups of 8 over 64-wide heads, ragged tiles
     (2, 8, 2, 3000, 128, [3000, 2999]),      # groups of 4, a tile of one token
     (2, 8, 4, 1000, 128, [1000, 517]),       # groups of 2 on the tensor cores
+    (2, 8, 4, 1000, 256, [1000, 517]),       # 256-wide heads: groups of 2, 4 and 8
+    (2, 16, 2, 1500, 256, [1500, 1]),
+    (4, 8, 2, 9000, 256, [9000, 8999, 4100, 130]),   # several work items per CTA
+    (2, 4, 2, 300, 512, [300, 129]),         # 512-wide heads in groups of 2
+    (3, 8, 2, 2000, 512, [2000, 0, 1025]),   # groups of 4, an empty sequence
 ])
 def test_decode_attention_matches_oracle(B, Hq, Hkv, L, D, lens):
     q, k, v = _case(B * 1000 + Hq * 10 + D + L, B, Hq, Hkv, L, D)
@@ -102,13 +107,16 @@ def test_unsupported_shapes_are_refused():
                                  device="cuda"), 0.1, out, ws)
 
 
-def test_rising_and_spiking_scores_move_the_reference_maximum():
+@pytest.mark.parametrize("D", [128, 512])
+def test_rising_and_spiking_scores_move_the_reference_maximum(D):
     """Long splits (L_max 262144 with B 2, Hkv 2: 1024-token splits of 8
     tiles) whose scores rise by about 50 (base 2) along sequence 0 and jump by
-    about 70 at a few tokens of sequence 1: the tensor-core kernel's reference
-    maximum moves inside a split, so O and the sums are rescaled there.  Tokens
-    past the first 3000 are zero and unread."""
-    B, Hq, Hkv, D, n, L_max = 2, 8, 2, 128, 3000, 262144
+    about 70 at a few tokens of sequence 1: for 128-wide heads the tensor-core
+    kernel's reference maximum moves inside a split, so O and the sums are
+    rescaled there; for 512-wide heads the split's maximum comes from the
+    stored scores and every p is at most 1.  Tokens past the first 3000 are
+    zero and unread."""
+    B, Hq, Hkv, n, L_max = 2, 8, 2, 3000, 262144
     G = Hq // Hkv
     g = inputs.rng(91)
     q = inputs.normal_bf16(g, (B, Hq, D))
@@ -149,13 +157,15 @@ def test_rising_and_spiking_scores_move_the_reference_maximum():
     _check(out.float().cpu().numpy().astype(np.float64), ref, "rising / spiking scores")
 
 
-def test_tensor_core_kernel_wait_expires_reports_timeout_and_context_survives():
-    """Failure path of the tensor-core kernel: with the test hook every CTA's
+@pytest.mark.parametrize("D", [128, 512])
+def test_tensor_core_kernel_wait_expires_reports_timeout_and_context_survives(D):
+    """Failure path of the tensor-core kernels: with the test hook every CTA's
     producer leaves its first ring stage unfilled, so the expansion's wait can
     only end by its time limit; the kernel records NVFP4_ERR_TIMEOUT, every
     role leaves, the copies in flight are drained, and the next call on the
-    same context is correct."""
-    B, Hq, Hkv, L, D = 2, 8, 2, 1000, 128                # groups of 4: the tensor-core kernel
+    same context is correct.  (512-wide heads: both the scores and the values
+    kernel take the hook.)"""
+    B, Hq, Hkv, L = 2, 8, 2, 1000                        # groups of 4: the tensor-core kernel
     q, k, v = _case(17, B, Hq, Hkv, L, D)
     kq, vq = attention.quantize_kv(k.cuda()), attention.quantize_kv(v.cuda())
     plan = attention.DecodeAttention(B, Hq, Hkv, L, D)

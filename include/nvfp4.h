@@ -521,11 +521,13 @@ nvfp4_status nvfp4_grouped_gemm_sparse(const uint8_t* A_tiles, const float* gA,
  * split", The Breakthrough -- The A4Q Kernel, and Preserving precision --
  * dual-tier scale handling): the cache stays packed in memory and is expanded
  * on chip inside the attention loop.  One query token per sequence.  Groups of
- * 2, 4 or 8 query heads over 128-wide heads and of 4 or 8 over 64-wide heads
- * run both contractions as tcgen05 MMAs on exact FP16 expansions of the cache
- * (when both scale arrays are 16-byte aligned, L_max * D / 16 is a multiple
- * of 16 and B * Hkv * L_max < 2^31); other shapes multiply-add on the CUDA
- * cores.  Both give the result defined below.
+ * 2, 4 or 8 query heads over heads of 128 and 256, of 2 or 4 over 512-wide
+ * heads and of 4 or 8 over 64-wide heads run both contractions as tcgen05
+ * MMAs on exact FP16 expansions of the cache (when both scale arrays are
+ * 16-byte aligned, for heads of 64 and 128 L_max * D / 16 is a multiple of
+ * 16, and B * Hkv * L_max < 2^31): one pipelined kernel for heads of 64 and
+ * 128, a scores pass and a values pass for the wider heads.  Other shapes
+ * multiply-add on the CUDA cores.  Both give the result defined below.
  *   q          BF16 [B, Hq, D].
  *   k_packed   NVFP4 codes [B, Hkv, L_max, D/2] (token rows of sequence b and
  *              KV head j contiguous), k_scales E4M3 [B, Hkv, L_max, D/16]

@@ -273,30 +273,119 @@ __global__ void __launch_bounds__(kAttnWarps * 32) decode_attention_kernel(const
   }
 }
 
-// Merges the splits of (sequence b, query head h): out = gv * sum_s O_s 2^(m_s - M)
-// / sum_s l_s 2^(m_s - M) in BF16; zeros for an empty sequence.
-__global__ void __launch_bounds__(128) decode_attention_combine_kernel(const AttnArgs a, int D) {
-  const int bh = blockIdx.x;
+// Merges the splits of (sequence b, query head h) for dimensions 128 y ..
+// 128 y + 127 (blockIdx.y = y): out = gv * sum_s O_s 2^(m_s - M) / sum_s l_s
+// 2^(m_s - M) in BF16 over the splits with l_s > 0; zeros for an empty
+// sequence.  The split weights 2^(m_s - M) are computed once per CTA into
+// shared memory (1024 splits at a time); warp c of the eight sums the splits
+// c, c + 8, ... for four dimensions per lane (16-byte loads, four in flight),
+// and the eight partial sums are added in warp order.
+constexpr int kCombineThreads = 256, kCombineChunk = 1024;
+
+__global__ void __launch_bounds__(kCombineThreads) decode_attention_combine_kernel(
+    const AttnArgs a, int D) {
+  __shared__ float wsh[kCombineChunk];
+  __shared__ float4 part[8][32];
+  __shared__ float red[8];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t bh = blockIdx.x;
   const int64_t nsplit = a.splits;
-  const int64_t base = static_cast<int64_t>(bh) * nsplit;
-  float M = -INFINITY;
-  for (int64_t s = 0; s < nsplit; ++s)
-    if (a.ws_ml[2 * (base + s) + 1] > 0.0f) M = fmaxf(M, a.ws_ml[2 * (base + s)]);
+  const int64_t base = bh * nsplit;
+  const float* ml = a.ws_ml + 2 * base;
+  float m = -INFINITY;
+  for (int64_t s = tid; s < nsplit; s += kCombineThreads)
+    if (ml[2 * s + 1] > 0.0f) m = fmaxf(m, ml[2 * s]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  float M = red[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) M = fmaxf(M, red[w]);
+  __syncthreads();
+  float l = 0.0f;
+  for (int64_t s = tid; s < nsplit; s += kCombineThreads) {
+    const float ls = ml[2 * s + 1];
+    if (ls > 0.0f) l = fmaf(ls, exp2f(ml[2 * s] - M), l);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, o);
+  if (lane == 0) red[warp] = l;
+  __syncthreads();
   float L = 0.0f;
-  for (int64_t s = 0; s < nsplit; ++s) {
-    const float l = a.ws_ml[2 * (base + s) + 1];
-    if (l > 0.0f) L = fmaf(l, exp2f(a.ws_ml[2 * (base + s)] - M), L);
-  }
-  const float gv = *a.gv;
-  for (int d = threadIdx.x; d < D; d += blockDim.x) {
-    float O = 0.0f;
-    for (int64_t s = 0; s < nsplit; ++s) {
-      const float l = a.ws_ml[2 * (base + s) + 1];
-      if (l > 0.0f) O = fmaf(a.ws_o[(base + s) * D + d], exp2f(a.ws_ml[2 * (base + s)] - M), O);
+#pragma unroll
+  for (int w = 0; w < 8; ++w) L += red[w];
+  const int d0 = static_cast<int>(blockIdx.y) * 128 + 4 * lane;
+  const bool active = d0 < D;
+  const float* op = a.ws_o + base * D + d0;
+  float ox = 0.0f, oy = 0.0f, oz = 0.0f, ow = 0.0f;
+  for (int64_t s0 = 0; s0 < nsplit; s0 += kCombineChunk) {
+    const int n = static_cast<int>(nsplit - s0 < kCombineChunk ? nsplit - s0 : kCombineChunk);
+    __syncthreads();                                   // the last chunk's weights are used
+    for (int k = tid; k < n; k += kCombineThreads) {
+      const float ls = ml[2 * (s0 + k) + 1];
+      wsh[k] = ls > 0.0f ? exp2f(ml[2 * (s0 + k)] - M) : 0.0f;
     }
-    const float v = L > 0.0f ? __fmul_rn(gv, __fdiv_rn(O, L)) : 0.0f;
-    a.out[static_cast<int64_t>(bh) * D + d] = f32_to_bf16_rn(v);
+    __syncthreads();
+    if (active) {
+      int k = warp;
+      for (; k + 24 < n; k += 32) {
+        float4 v[4];
+        float w[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          w[u] = wsh[k + 8 * u];
+          v[u] = w[u] != 0.0f ? *reinterpret_cast<const float4*>(op + (s0 + k + 8 * u) * D)
+                              : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (w[u] != 0.0f) {
+            ox = fmaf(v[u].x, w[u], ox);
+            oy = fmaf(v[u].y, w[u], oy);
+            oz = fmaf(v[u].z, w[u], oz);
+            ow = fmaf(v[u].w, w[u], ow);
+          }
+      }
+      for (; k < n; k += 8) {
+        const float w = wsh[k];
+        if (w != 0.0f) {
+          const float4 v = *reinterpret_cast<const float4*>(op + (s0 + k) * D);
+          ox = fmaf(v.x, w, ox);
+          oy = fmaf(v.y, w, oy);
+          oz = fmaf(v.z, w, oz);
+          ow = fmaf(v.w, w, ow);
+        }
+      }
+    }
   }
+  part[warp][lane] = make_float4(ox, oy, oz, ow);
+  __syncthreads();
+  if (warp == 0 && active) {
+    float4 t = part[0][lane];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) {
+      const float4 u = part[w][lane];
+      t.x += u.x;
+      t.y += u.y;
+      t.z += u.z;
+      t.w += u.w;
+    }
+    const float gv = *a.gv;
+    uint32_t h[4];
+    const float x[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      h[u] = f32_to_bf16_rn(L > 0.0f ? __fmul_rn(gv, __fdiv_rn(x[u], L)) : 0.0f);
+    *reinterpret_cast<uint2*>(a.out + bh * D + d0) = make_uint2(h[0] | (h[1] << 16),
+                                                                h[2] | (h[3] << 16));
+  }
+}
+
+// the merge: one CTA per (sequence, query head, 128 dimensions)
+dim3 combine_grid(const AttnArgs& a, int D) {
+  return dim3(static_cast<unsigned>(static_cast<int64_t>(a.B) * a.Hq),
+              static_cast<unsigned>((D + 127) / 128));
 }
 
 template <int D, int G>
@@ -326,7 +415,7 @@ cudaError_t launch_decode_attention(const AttnArgs& a, int D, const AttnMaps* ma
   const int G = a.Hq / a.Hkv;
   cudaError_t e = cudaSuccess;
   if (a.splits == 0) {             // empty cache: the merge writes zeros
-    decode_attention_combine_kernel<<<static_cast<unsigned>(a.B * a.Hq), 128, 0, s>>>(a, D);
+    decode_attention_combine_kernel<<<combine_grid(a, D), kCombineThreads, 0, s>>>(a, D);
     return cudaGetLastError();
   }
   // groups of 2-8 query heads over 128-wide heads and 4-8 over 64-wide heads:
@@ -344,7 +433,7 @@ cudaError_t launch_decode_attention(const AttnArgs& a, int D, const AttnMaps* ma
     }
   }
   if (e != cudaSuccess) return e;
-  decode_attention_combine_kernel<<<static_cast<unsigned>(a.B * a.Hq), 128, 0, s>>>(a, D);
+  decode_attention_combine_kernel<<<combine_grid(a, D), kCombineThreads, 0, s>>>(a, D);
   return cudaGetLastError();
 }
 

@@ -35,8 +35,11 @@ struct AttnArgs {
 // Tokens per split of the decode attention: the smallest power of two from
 // 128 up to 4096 that leaves about a thousand (sequence, KV head, split) work
 // items at most.  A function of the shape only, so that the workspace size
-// is.  The CUDA-core kernel launches one CTA per item; the tensor-core kernel
-// (one CTA per SM) walks several items per CTA.
+// is.  The CUDA-core kernel launches one CTA per item; the tensor-core kernels
+// (one CTA per SM for heads of 64 and 128, two for the wider heads' two
+// passes) walk several items per CTA.  (Splits half as long for the wider
+// heads, for an evener share over 304 CTAs, measured slower: each item's q,
+// partials and merge cost more than the balance gained.)
 inline int attention_chunk(int64_t L_max, int64_t B, int64_t Hkv) {
   const int64_t want = (L_max * B * Hkv + 1023) / 1024;
   int ch = 128;

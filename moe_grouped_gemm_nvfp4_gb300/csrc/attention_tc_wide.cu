@@ -31,8 +31,13 @@ namespace nvfp4 {
 
 namespace {
 
-constexpr int kWideStages = 6;                 // raw ring: one slice of a tile each
-constexpr int kWideNBuf = 3;                   // expanded slices in flight
+// raw ring stages (one slice of a tile each) and expanded slices in flight.
+// Both kernels run two CTAs per SM (measured: 512-wide heads in groups of 4,
+// 0.18 ms with one CTA of each per SM, 0.14 ms with two), so that twice the
+// warps hide the latency of the expansion's loads, waits and stores; the
+// values kernel's ring and buffers are sized to fit two CTAs.
+constexpr int kScoreStages = 6, kScoreNBuf = 3;
+constexpr int kValueCtas = 2, kValueStages = 3, kValueNBuf = 2;
 constexpr int kWideFrontWarps = 4, kWideExpWarps = 8;
 constexpr int kWideProdWarp = kWideFrontWarps + kWideExpWarps, kWideMmaWarp = kWideProdWarp + 1;
 constexpr int kWideThreads = (kWideMmaWarp + 1) * 32;   // 448
@@ -47,11 +52,11 @@ struct WideCfg {
   static constexpr int kVhBuf = 2 * 16384;               // V^ slice: 128 tokens x 128 dims
   static constexpr int kPhBuf = 4096;                    // P^T: 16 rows x 128 tokens
   // scores kernel: ring | q x 2 | reductions | control | barriers
-  static constexpr int kSQh = kWideStages * kStage;
+  static constexpr int kSQh = kScoreStages * kStage;
   static constexpr int kSRed = kSQh + 2 * kQhBuf;
-  // values kernel: ring | V^ x 3 | P^T x 2 | reductions | control | barriers
-  static constexpr int kVVh = kWideStages * kStage;
-  static constexpr int kVPh = kVVh + kWideNBuf * kVhBuf;
+  // values kernel: ring | V^ buffers | P^T x 2 | reductions | control | barriers
+  static constexpr int kVVh = kValueStages * kStage;
+  static constexpr int kVPh = kVVh + kValueNBuf * kVhBuf;
   static constexpr int kVRed = kVPh + 2 * kPhBuf;
   static_assert(kStage % 1024 == 0 && kSQh % 1024 == 0 && kVVh % 1024 == 0, "layout");
 };
@@ -64,6 +69,14 @@ template <int D>
 constexpr int wide_scores_bytes() { return WideCfg<D>::kSRed + kWideTail + 1024; }
 template <int D>
 constexpr int wide_values_bytes() { return WideCfg<D>::kVRed + kWideTail + 1024; }
+// two scores CTAs and kValueCtas values CTAs per SM: 228 KB of shared memory
+// per SM, 1 KB of it reserved per CTA
+template <int D>
+constexpr bool wide_fits() {
+  return 2 * (wide_scores_bytes<D>() + 1024) <= 233472 &&
+         kValueCtas * (wide_values_bytes<D>() + 1024) <= 233472;
+}
+static_assert(wide_fits<256>() && wide_fits<512>(), "CTAs per SM");
 
 // 16-byte chunk of a 64-byte code row as the TMA's 64-byte swizzle places it
 __device__ __forceinline__ int swz64(int t) { return (t >> 1) & 3; }
@@ -136,7 +149,7 @@ __device__ __forceinline__ void wide_write_q(const AttnArgs& a, int64_t w, uint8
 // score MMAs.  Tensor memory: K^ slices at 64 b (b < 3), S at 192 + 16 p.
 // ---------------------------------------------------------------------------
 template <int D, int G>
-__global__ void __launch_bounds__(kWideThreads, 1)
+__global__ void __launch_bounds__(kWideThreads, 2)
 decode_scores_wide_kernel(const __grid_constant__ CUtensorMap tmk,
                           const __grid_constant__ CUtensorMap tsk, const AttnArgs a) {
   using C = WideCfg<D>;
@@ -149,9 +162,9 @@ decode_scores_wide_kernel(const __grid_constant__ CUtensorMap tmk,
   CtaCtl* ctl = reinterpret_cast<CtaCtl*>(smem + C::kSRed + 768);
   const uint32_t bars = sbase + C::kSRed + 768 + 16;
   auto raw_full = [&](uint32_t st) { return bars + 8u * st; };
-  auto raw_empty = [&](uint32_t st) { return bars + 8u * (kWideStages + st); };
-  const uint32_t op_full0 = bars + 8u * (2 * kWideStages), k_free0 = op_full0 + 8 * kWideNBuf,
-                 s_full0 = k_free0 + 8 * kWideNBuf, s_empty0 = s_full0 + 16,
+  auto raw_empty = [&](uint32_t st) { return bars + 8u * (kScoreStages + st); };
+  const uint32_t op_full0 = bars + 8u * (2 * kScoreStages), k_free0 = op_full0 + 8 * kScoreNBuf,
+                 s_full0 = k_free0 + 8 * kScoreNBuf, s_empty0 = s_full0 + 16,
                  q_full0 = s_empty0 + 16, q_empty0 = q_full0 + 16, fin = q_empty0 + 16;
   uint32_t* slot = reinterpret_cast<uint32_t*>(smem + C::kSRed + 768 + 16 + 40 * 8);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -159,11 +172,11 @@ decode_scores_wide_kernel(const __grid_constant__ CUtensorMap tmk,
   if (tid == 0) {
     ctl->abort = 0u;
     ctl->timeout_ns = a.timeout_ns;
-    for (int st = 0; st < kWideStages; ++st) {
+    for (int st = 0; st < kScoreStages; ++st) {
       mbar_init(raw_full(st), 1);
       mbar_init(raw_empty(st), kWideExpWarps);
     }
-    for (int h = 0; h < kWideNBuf; ++h) {
+    for (int h = 0; h < kScoreNBuf; ++h) {
       mbar_init(op_full0 + 8 * h, kWideExpWarps);
       mbar_init(k_free0 + 8 * h, 1);
     }
@@ -200,9 +213,9 @@ decode_scores_wide_kernel(const __grid_constant__ CUtensorMap tmk,
       n_nxt = ws_len(a, w + gridDim.x, items);
       for (int64_t tt = it.t0; tt < it.t1 && ok; tt += kTile) {
         for (int s = 0; s < NS && ok; ++s, ++i) {
-          const uint32_t st = i % kWideStages;
-          if (i >= kWideStages)
-            ok = __all_sync(0xFFFFFFFFu, ws_wait(raw_empty(st), ((i / kWideStages) - 1) & 1u,
+          const uint32_t st = i % kScoreStages;
+          if (i >= kScoreStages)
+            ok = __all_sync(0xFFFFFFFFu, ws_wait(raw_empty(st), ((i / kScoreStages) - 1) & 1u,
                                                  ctl, a.status));
           if (!ok) break;
           if (i == 0 && (a.debug_flags & kDebugSkipFirstStage)) {
@@ -218,8 +231,8 @@ decode_scores_wide_kernel(const __grid_constant__ CUtensorMap tmk,
       }
     }
     const uint32_t issued = i;
-    for (uint32_t k = issued > kWideStages ? issued - kWideStages : 0; k < issued; ++k)
-      if (k > 0 || !skipped_first) ws_drain(raw_full(k % kWideStages), (k / kWideStages) & 1u,
+    for (uint32_t k = issued > kScoreStages ? issued - kScoreStages : 0; k < issued; ++k)
+      if (k > 0 || !skipped_first) ws_drain(raw_full(k % kScoreStages), (k / kScoreStages) & 1u,
                                             a.timeout_ns);
   } else if (warp >= kWideFrontWarps && warp < kWideProdWarp) {
     // ------------------------------------------------------- K expansion
@@ -236,8 +249,8 @@ decode_scores_wide_kernel(const __grid_constant__ CUtensorMap tmk,
       for (int64_t tt = it.t0; tt < it.t1 && ok; tt += kTile) {
         const int rows = static_cast<int>(min(static_cast<int64_t>(kTile), it.t1 - tt));
         for (int s = 0; s < NS; ++s, ++i) {
-          const uint32_t st = i % kWideStages, ob = i % kWideNBuf;
-          ok = __all_sync(0xFFFFFFFFu, ws_wait(raw_full(st), (i / kWideStages) & 1u, ctl,
+          const uint32_t st = i % kScoreStages, ob = i % kScoreNBuf;
+          ok = __all_sync(0xFFFFFFFFu, ws_wait(raw_full(st), (i / kScoreStages) & 1u, ctl,
                                                a.status));
           if (!ok) break;
           const uint8_t* raw = smem + st * C::kStage;
@@ -257,8 +270,8 @@ decode_scores_wide_kernel(const __grid_constant__ CUtensorMap tmk,
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(raw_empty(st));
-          if (i >= kWideNBuf)                            // the score MMAs of slice i - 3 are done
-            ok = __all_sync(0xFFFFFFFFu, ws_wait(k_free0 + 8 * ob, ((i / kWideNBuf) - 1) & 1u,
+          if (i >= kScoreNBuf)                   // the score MMAs of the buffer's last slice are done
+            ok = __all_sync(0xFFFFFFFFu, ws_wait(k_free0 + 8 * ob, ((i / kScoreNBuf) - 1) & 1u,
                                                  ctl, a.status));
           if (!ok) break;
           uint32_t kv[32];
@@ -300,8 +313,8 @@ decode_scores_wide_kernel(const __grid_constant__ CUtensorMap tmk,
           ok = __all_sync(0xFFFFFFFFu, ws_wait(s_empty0 + 8 * sb, ((t >> 1) - 1) & 1u, ctl,
                                                a.status));
         for (int s = 0; s < NS && ok; ++s, ++i) {
-          const uint32_t ob = i % kWideNBuf;
-          ok = __all_sync(0xFFFFFFFFu, ws_wait(op_full0 + 8 * ob, (i / kWideNBuf) & 1u, ctl,
+          const uint32_t ob = i % kScoreNBuf;
+          ok = __all_sync(0xFFFFFFFFu, ws_wait(op_full0 + 8 * ob, (i / kScoreNBuf) & 1u, ctl,
                                                a.status));
           if (!ok) break;
           tc_fence_after();
@@ -436,7 +449,7 @@ decode_scores_wide_kernel(const __grid_constant__ CUtensorMap tmk,
 // and are skipped by every role here.
 // ---------------------------------------------------------------------------
 template <int D, int G>
-__global__ void __launch_bounds__(kWideThreads, 1)
+__global__ void __launch_bounds__(kWideThreads, kValueCtas)
 decode_values_wide_kernel(const __grid_constant__ CUtensorMap tmv,
                           const __grid_constant__ CUtensorMap tsv, const AttnArgs a) {
   using C = WideCfg<D>;
@@ -450,9 +463,9 @@ decode_values_wide_kernel(const __grid_constant__ CUtensorMap tmv,
   CtaCtl* ctl = reinterpret_cast<CtaCtl*>(smem + C::kVRed + 768);
   const uint32_t bars = sbase + C::kVRed + 768 + 16;
   auto raw_full = [&](uint32_t st) { return bars + 8u * st; };
-  auto raw_empty = [&](uint32_t st) { return bars + 8u * (kWideStages + st); };
-  const uint32_t v_full0 = bars + 8u * (2 * kWideStages), v_free0 = v_full0 + 8 * kWideNBuf,
-                 p_full0 = v_free0 + 8 * kWideNBuf, p_empty0 = p_full0 + 16,
+  auto raw_empty = [&](uint32_t st) { return bars + 8u * (kValueStages + st); };
+  const uint32_t v_full0 = bars + 8u * (2 * kValueStages), v_free0 = v_full0 + 8 * kValueNBuf,
+                 p_full0 = v_free0 + 8 * kValueNBuf, p_empty0 = p_full0 + 16,
                  o_full0 = p_empty0 + 16, o_empty0 = o_full0 + 16, fin = o_empty0 + 16;
   uint32_t* slot = reinterpret_cast<uint32_t*>(smem + C::kVRed + 768 + 16 + 40 * 8);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -460,11 +473,11 @@ decode_values_wide_kernel(const __grid_constant__ CUtensorMap tmv,
   if (tid == 0) {
     ctl->abort = 0u;
     ctl->timeout_ns = a.timeout_ns;
-    for (int st = 0; st < kWideStages; ++st) {
+    for (int st = 0; st < kValueStages; ++st) {
       mbar_init(raw_full(st), 1);
       mbar_init(raw_empty(st), kWideExpWarps);
     }
-    for (int h = 0; h < kWideNBuf; ++h) {
+    for (int h = 0; h < kValueNBuf; ++h) {
       mbar_init(v_full0 + 8 * h, kWideExpWarps);
       mbar_init(v_free0 + 8 * h, 1);
     }
@@ -501,9 +514,9 @@ decode_values_wide_kernel(const __grid_constant__ CUtensorMap tmv,
       n_nxt = ws_len(a, w + gridDim.x, items);
       for (int64_t tt = it.t0; tt < it.t1 && ok; tt += kTile) {
         for (int s = 0; s < NS && ok; ++s, ++i) {
-          const uint32_t st = i % kWideStages;
-          if (i >= kWideStages)
-            ok = __all_sync(0xFFFFFFFFu, ws_wait(raw_empty(st), ((i / kWideStages) - 1) & 1u,
+          const uint32_t st = i % kValueStages;
+          if (i >= kValueStages)
+            ok = __all_sync(0xFFFFFFFFu, ws_wait(raw_empty(st), ((i / kValueStages) - 1) & 1u,
                                                  ctl, a.status));
           if (!ok) break;
           if (i == 0 && (a.debug_flags & kDebugSkipFirstStage)) {
@@ -519,8 +532,8 @@ decode_values_wide_kernel(const __grid_constant__ CUtensorMap tmv,
       }
     }
     const uint32_t issued = i;
-    for (uint32_t k = issued > kWideStages ? issued - kWideStages : 0; k < issued; ++k)
-      if (k > 0 || !skipped_first) ws_drain(raw_full(k % kWideStages), (k / kWideStages) & 1u,
+    for (uint32_t k = issued > kValueStages ? issued - kValueStages : 0; k < issued; ++k)
+      if (k > 0 || !skipped_first) ws_drain(raw_full(k % kValueStages), (k / kValueStages) & 1u,
                                             a.timeout_ns);
   } else if (warp >= kWideFrontWarps && warp < kWideProdWarp) {
     // ------------------------------------------------------- V expansion
@@ -546,8 +559,8 @@ decode_values_wide_kernel(const __grid_constant__ CUtensorMap tmv,
       for (int64_t tt = it.t0; tt < it.t1 && ok; tt += kTile) {
         const int rows = static_cast<int>(min(static_cast<int64_t>(kTile), it.t1 - tt));
         for (int s = 0; s < NS; ++s, ++i) {
-          const uint32_t st = i % kWideStages, vb = i % kWideNBuf;
-          ok = __all_sync(0xFFFFFFFFu, ws_wait(raw_full(st), (i / kWideStages) & 1u, ctl,
+          const uint32_t st = i % kValueStages, vb = i % kValueNBuf;
+          ok = __all_sync(0xFFFFFFFFu, ws_wait(raw_full(st), (i / kValueStages) & 1u, ctl,
                                                a.status));
           if (!ok) break;
           const uint8_t* raw = smem + st * C::kStage;
@@ -566,8 +579,8 @@ decode_values_wide_kernel(const __grid_constant__ CUtensorMap tmv,
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(raw_empty(st));
-          if (i >= kWideNBuf)                            // the MMAs of slice i - 3 are done
-            ok = __all_sync(0xFFFFFFFFu, ws_wait(v_free0 + 8 * vb, ((i / kWideNBuf) - 1) & 1u,
+          if (i >= kValueNBuf)                   // the MMAs of the buffer's last slice are done
+            ok = __all_sync(0xFFFFFFFFu, ws_wait(v_free0 + 8 * vb, ((i / kValueNBuf) - 1) & 1u,
                                                  ctl, a.status));
           if (!ok) break;
           uint8_t* vh = smem + C::kVVh + vb * C::kVhBuf;
@@ -603,8 +616,8 @@ decode_values_wide_kernel(const __grid_constant__ CUtensorMap tmv,
         const uint32_t pb = t & 1u;
         ok = __all_sync(0xFFFFFFFFu, ws_wait(p_full0 + 8 * pb, (t >> 1) & 1u, ctl, a.status));
         for (int s = 0; s < NS && ok; ++s, ++i) {
-          const uint32_t vb = i % kWideNBuf;
-          ok = __all_sync(0xFFFFFFFFu, ws_wait(v_full0 + 8 * vb, (i / kWideNBuf) & 1u, ctl,
+          const uint32_t vb = i % kValueNBuf;
+          ok = __all_sync(0xFFFFFFFFu, ws_wait(v_full0 + 8 * vb, (i / kValueNBuf) & 1u, ctl,
                                                a.status));
           if (!ok) break;
           tc_fence_after();
@@ -742,8 +755,9 @@ cudaError_t set_wide_attrs_d() {
   return e;
 }
 
-// Both kernels with one CTA per SM (or per work item when there are fewer),
-// on the same stream: the values kernel reads what the scores kernel wrote.
+// Both kernels persistent (two scores CTAs per SM, kValueCtas values CTAs, or
+// one per work item when there are fewer), on the same stream: the values
+// kernel reads what the scores kernel wrote.
 template <int D, int G>
 cudaError_t launch_wide_d_g(const AttnArgs& a, const AttnMaps& m, cudaStream_t s) {
   int dev = 0, sms = 0;
@@ -751,13 +765,13 @@ cudaError_t launch_wide_d_g(const AttnArgs& a, const AttnMaps& m, cudaStream_t s
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const int64_t items = static_cast<int64_t>(a.splits) * a.Hkv * a.B;
-  const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
-  decode_scores_wide_kernel<D, G><<<grid, kWideThreads, wide_scores_bytes<D>(), s>>>(
+  auto grid_of = [&](int64_t ctas) { return static_cast<unsigned>(items < ctas ? items : ctas); };
+  decode_scores_wide_kernel<D, G><<<grid_of(2LL * sms), kWideThreads, wide_scores_bytes<D>(), s>>>(
       m.k_codes, m.k_scales, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  decode_values_wide_kernel<D, G><<<grid, kWideThreads, wide_values_bytes<D>(), s>>>(
-      m.v_codes, m.v_scales, a);
+  decode_values_wide_kernel<D, G><<<grid_of(static_cast<int64_t>(kValueCtas) * sms), kWideThreads,
+                                    wide_values_bytes<D>(), s>>>(m.v_codes, m.v_scales, a);
   return cudaGetLastError();
 }
 

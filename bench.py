@@ -739,8 +739,8 @@ def measure_configs(args, dev, groups=None):
     for (B_, Hq_, Hkv_, L_, D_) in ((16, 32, 8, 16384, 128), (16, 64, 8, 16384, 128),
                                     (16, 8, 8, 16384, 128), (16, 32, 8, 8192, 256),
                                     (8, 8, 2, 32768, 512)):
-        if not want("decode_attention"):
-            break
+        if not (want("decode_attention") or want(f"decode_attention_d{D_}")):
+            continue
         kc = inputs.device_normal_bf16((B_, Hkv_, L_, D_), 1.0, 71, dev)
         kq = attention.quantize_kv(kc)
         del kc
@@ -796,7 +796,8 @@ def main():
     ap.add_argument("--only", default=None,
                     help="configs: run only these comma-separated groups (tiny_gemm, "
                          "dense_8192, decode (with prefill), prefill, sparse, fused_mlp, "
-                         "decode_attention)")
+                         "decode_attention, or one head width of it: decode_attention_d128, "
+                         "_d256, _d512)")
     ap.add_argument("--no-configs", action="store_true",
                     help="leave the per-configuration table out of the headline line")
     ap.add_argument("--sparse", action="store_true",

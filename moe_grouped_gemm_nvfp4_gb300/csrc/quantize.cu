@@ -271,17 +271,34 @@ __global__ void __launch_bounds__(256) quantize_dispatch_kernel(
     const uint32_t word = gather4_bytes(q.sf);
     const int64_t kb = b >> 4;
     const int bb = static_cast<int>(b & 15);        // 16-element block inside the K block
-    for (int j = 0; j < fanout; ++j) {              // the row's routes (warp-uniform)
-      const int32_t p = route_pos ? route_pos[r * fanout + j] : static_cast<int32_t>(r);
-      if (p < 0 || p >= nroutes) continue;          // dropped route
-      const int e = find_expert(off, E, p);
-      const int32_t local = p - off[e];
-      const int64_t rt = tb[e] + local / chunk;
-      const int row = local % chunk;
-      if (valid) {
-        *reinterpret_cast<uint2*>(tiles + tile_code_offset(rt, row, kb, bb * 8, n_kb)) = q.packed;
-        if ((lane & 3) == 0)
-          *reinterpret_cast<uint32_t*>(tiles + tile_scale_offset(rt, row, kb, bb, n_kb)) = word;
+    // The row's routes, 32 at a time: lane j looks up route j (its position,
+    // expert and place in the tile layout) so that the lookups of all routes
+    // overlap, then every route's codes and scales are stored by the warp.
+    for (int j0 = 0; j0 < fanout; j0 += 32) {
+      int32_t p = -1;
+      int32_t rt_l = 0, row_l = 0;
+      if (j0 + lane < fanout) {
+        p = route_pos ? route_pos[r * fanout + j0 + lane] : static_cast<int32_t>(r);
+        if (p >= 0 && p < nroutes) {
+          const int e = find_expert(off, E, p);
+          const int32_t local = p - off[e];
+          rt_l = tb[e] + local / chunk;
+          row_l = local % chunk;
+        } else {
+          p = -1;                                   // dropped route
+        }
+      }
+      const int nj = min(32, fanout - j0);
+      for (int j = 0; j < nj; ++j) {
+        if (__shfl_sync(0xFFFFFFFFu, p, j) < 0) continue;
+        const int64_t rt = __shfl_sync(0xFFFFFFFFu, rt_l, j);
+        const int row = __shfl_sync(0xFFFFFFFFu, row_l, j);
+        if (valid) {
+          *reinterpret_cast<uint2*>(tiles + tile_code_offset(rt, row, kb, bb * 8, n_kb)) =
+              q.packed;
+          if ((lane & 3) == 0)
+            *reinterpret_cast<uint32_t*>(tiles + tile_scale_offset(rt, row, kb, bb, n_kb)) = word;
+        }
       }
     }
   }

@@ -12,7 +12,10 @@ constexpr int ROUTE_WARPS = ROUTE_THREADS / 32;
 // One CTA.  Pass 1 histograms the experts; pass 2 walks the routes in
 // chunks of 1024 consecutive flat indices and gives each route its position
 // base[e] + (same-expert routes of earlier warps in the chunk) + (same-expert
-// lanes before it in its warp), which keeps flat (= token-major) order.
+// lanes before it in its warp), which keeps flat (= token-major) order.  Per
+// chunk, each warp's leader lane of an expert records the warp's count, one
+// thread per expert turns its column of counts into the warps' first
+// positions (advancing base[e]), and each route adds its rank in the warp.
 __global__ void __launch_bounds__(ROUTE_THREADS) route_kernel(
     const int32_t* __restrict__ ids, int64_t R, int topk, int E,
     int32_t* __restrict__ offsets, int32_t* __restrict__ route_token,
@@ -21,6 +24,8 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_kernel(
   int32_t* base = sh;                       // [E]
   int32_t* wcnt = sh + E;                   // [ROUTE_WARPS][E]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int e_nxt = -1;                                 // the first chunk's expert (pass 2)
+  if (tid < R) { e_nxt = ids[tid]; if (e_nxt < 0 || e_nxt >= E) e_nxt = -1; }
   for (int i = tid; i < E * (ROUTE_WARPS + 1); i += ROUTE_THREADS) sh[i] = 0;
   __syncthreads();
   int bad = 0;
@@ -59,29 +64,42 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_kernel(
 
   for (int64_t c0 = 0; c0 < R; c0 += ROUTE_THREADS) {
     const int64_t i = c0 + tid;
-    int e = -1;
-    if (i < R) { e = ids[i]; if (e < 0 || e >= E) e = -1; }
+    const int e = e_nxt;
+    e_nxt = -1;                                     // the next chunk's expert, loaded early
+    if (i + ROUTE_THREADS < R) {
+      e_nxt = ids[i + ROUTE_THREADS];
+      if (e_nxt < 0 || e_nxt >= E) e_nxt = -1;
+    }
     const uint32_t same = __match_any_sync(0xFFFFFFFFu, e);
     const int rank = __popc(same & ((1u << lane) - 1u));
     if (e >= 0 && rank == 0) wcnt[warp * E + e] = __popc(same);
     __syncthreads();
+    // counts -> first positions, only where a warp has routes of the expert:
+    // those entries are the ones their warps' leaders zero after use, so
+    // every entry is zero again when the next chunk's counts arrive
+    for (int ee = tid; ee < E; ee += ROUTE_THREADS) {
+      int32_t run = base[ee];
+      for (int w = 0; w < ROUTE_WARPS; ++w) {
+        const int32_t v = wcnt[w * E + ee];
+        if (v != 0) wcnt[w * E + ee] = run;
+        run += v;
+      }
+      base[ee] = run;
+    }
+    __syncthreads();
     if (e >= 0) {
-      int32_t pre = 0;
-      for (int w = 0; w < warp; ++w) pre += wcnt[w * E + e];
-      const int32_t pos = base[e] + pre + rank;
+      const int32_t pos = wcnt[warp * E + e] + rank;
       route_token[pos] = static_cast<int32_t>(i / topk);
       route_slot[pos] = static_cast<int32_t>(i % topk);
       if (route_pos) route_pos[i] = pos;
     } else if (i < R && route_pos) {
       route_pos[i] = -1;
     }
-    __syncthreads();
-    for (int ee = tid; ee < E; ee += ROUTE_THREADS) {
-      int32_t s = 0;
-      for (int w = 0; w < ROUTE_WARPS; ++w) { s += wcnt[w * E + ee]; wcnt[w * E + ee] = 0; }
-      base[ee] += s;
-    }
-    __syncthreads();
+    // the warp's entries back to zero for the next chunk (its lanes have read
+    // them; the next chunk's first barrier orders this before the scan)
+    __syncwarp();
+    if (e >= 0 && rank == 0) wcnt[warp * E + e] = 0;
+    __syncwarp();                                   // before the next chunk's counts
   }
 }
 

@@ -639,7 +639,7 @@ def measure_configs(args, dev, groups=None):
     # decode gate_up, down sweep and skewed prefill (and the 2:4-sparse decode shapes)
     for name in ("decode_gate_up", "decode_down_256", "decode_down_512", "decode_down_1024",
                  "prefill_skewed"):
-        if not (want("decode") or (name == "prefill_skewed" and want("prefill"))):
+        if not (want("decode") or want(name) or (name == "prefill_skewed" and want("prefill"))):
             continue
         cfg = inputs.CONFIGS[name]
         g = inputs.rng(cfg.seed)
@@ -797,7 +797,8 @@ def main():
                     help="configs: run only these comma-separated groups (tiny_gemm, "
                          "dense_8192, decode (with prefill), prefill, sparse, fused_mlp, "
                          "decode_attention, or one head width of it: decode_attention_d128, "
-                         "_d256, _d512)")
+                         "_d256, _d512; one decode shape: decode_gate_up, decode_down_256, "
+                         "_512, _1024)")
     ap.add_argument("--no-configs", action="store_true",
                     help="leave the per-configuration table out of the headline line")
     ap.add_argument("--sparse", action="store_true",

@@ -16,7 +16,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(OUT_DIR, "libnvfp4_gb300.so")
-SOURCES = ["api.cu", "quantize.cu", "route.cu", "gemm.cu", "gemm_pair.cu", "sparse.cu",
+SOURCES = ["api.cu", "quantize.cu", "route.cu", "gemm.cu", "gemm_pair.cu", "gemm_pair_grouped.cu",
+           "sparse.cu",
            "attention.cu", "attention_tc.cu", "attention_tc_wide.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("common.cuh", "kernels.h", "format.cuh", "attention.h",
                                                 "attention_tc_common.cuh")] + [

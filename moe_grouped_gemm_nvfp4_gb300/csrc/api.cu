@@ -61,6 +61,7 @@ nvfp4_status device_state(DeviceState** out) {
       d.status = static_cast<int*>(p);
       if (nvfp4::init_gemm_attributes() != cudaSuccess) return cuda_fail();
       if (nvfp4::init_gemm_pair_attributes() != cudaSuccess) return cuda_fail();
+      if (nvfp4::init_grouped_pair_attributes() != cudaSuccess) return cuda_fail();
       if (nvfp4::init_attention_tc_attributes() != cudaSuccess) return cuda_fail();
       if (nvfp4::init_route_attributes() != cudaSuccess) return cuda_fail();
     }
@@ -112,6 +113,23 @@ nvfp4_status make_operand_map(CUtensorMap* m, const void* base, uint64_t rows, u
   const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
                               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NVFP4_OK : NVFP4_ERR_UNSUPPORTED;
+}
+
+// 2-D map over a buffer of grouped operand tiles viewed as rows of 128 bytes
+// (a tile is 144 such rows: 128 of codes in the 128-byte swizzle, then 16 of
+// scale atoms), boxes of box_rows rows, no swizzle, so the tiles land in
+// shared memory byte for byte.  Rows past the buffer read zeros.
+nvfp4_status make_tile_rows_map(CUtensorMap* m, const void* base, uint64_t rows,
+                                uint32_t box_rows) {
+  const cuuint64_t dims[2] = {128u, rows};
+  const cuuint64_t strides[1] = {128u};
+  const cuuint32_t box[2] = {128u, box_rows};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? NVFP4_OK : NVFP4_ERR_UNSUPPORTED;
 }
@@ -533,10 +551,24 @@ static nvfp4_status grouped_gemm_impl(const uint8_t* A_tiles, const float* gA,
   a.sparse_w = sparse_w ? 1 : 0;
   if (combine && cudaMemsetAsync(workspace, 0, nvfp4_combine_workspace_bytes(T, N), s) != cudaSuccess)
     return cuda_fail();
-  if (nvfp4::launch_gemm(w_map ? *w_map : unused, unused, a,
-                         combine ? nvfp4::kGroupedCombine : nvfp4::kGrouped, d->sms, s) !=
-      cudaSuccess)
+  const int mode = combine ? nvfp4::kGroupedCombine : nvfp4::kGrouped;
+  const int pair_width = nvfp4::grouped_pair_width(a, mode);
+  if (pair_width > 0) {
+    // 128- and 256-route token tiles of dense operand tiles: the CTA-pair kernel
+    nvfp4::GroupedPairMaps pm;
+    const uint64_t nkb = static_cast<uint64_t>((K + 255) / 256);
+    const uint64_t x_rows = static_cast<uint64_t>(E) * static_cast<uint64_t>(N / 128) * nkb * 144;
+    const uint64_t y_rows = static_cast<uint64_t>(grouped_token_tiles(R, E)) * nkb * 144;
+    if (make_tile_rows_map(&pm.x_tiles, W_tiles, x_rows, 144) != NVFP4_OK ||
+        make_tile_rows_map(&pm.y_codes, A_tiles, y_rows, static_cast<uint32_t>(pair_width / 2)) !=
+            NVFP4_OK ||
+        make_tile_rows_map(&pm.y_scales, A_tiles, y_rows, 16) != NVFP4_OK)
+      return NVFP4_ERR_UNSUPPORTED;
+    if (nvfp4::launch_grouped_pair(pm, a, mode, s) != cudaSuccess) return cuda_fail();
+  } else if (nvfp4::launch_gemm(w_map ? *w_map : unused, unused, a, mode, d->sms, s) !=
+             cudaSuccess) {
     return cuda_fail();
+  }
   if (combine && nvfp4::launch_combine_finalize(workspace, T, N, out, d->sms, s) != cudaSuccess)
     return cuda_fail();
   return NVFP4_OK;

@@ -146,6 +146,20 @@ cudaError_t init_gemm_pair_attributes();
 cudaError_t launch_gemm_pair(const CUtensorMap& tmx, const CUtensorMap& tmy,
                              const CUtensorMap& tsx, const CUtensorMap& tsy, const GemmArgs& a,
                              cudaStream_t s);
+// gemm_pair_grouped.cu: the grouped GEMM on CTA pairs for 256-route token
+// tiles with BF16 output (prefill shapes), dense operand tiles only.  Maps
+// over the tile buffers viewed as rows of 128 bytes (an operand tile is 144
+// such rows: 128 of codes, 16 of scale atoms), no swizzle: the weight tiles
+// with boxes of 144 rows, the token tiles with boxes of 128 rows (codes) and
+// of 16 rows (scales).
+struct GroupedPairMaps {
+  CUtensorMap x_tiles, y_codes, y_scales;
+};
+cudaError_t init_grouped_pair_attributes();
+// 256 when the pair kernel takes this launch, else 0
+int grouped_pair_width(const GemmArgs& a, int mode);
+cudaError_t launch_grouped_pair(const GroupedPairMaps& m, const GemmArgs& a, int mode,
+                                cudaStream_t s);
 // Fused expert MLP in one cooperative persistent launch (mode kMlpFused).
 cudaError_t launch_mlp_fused(const GemmArgs& a, int sms, cudaStream_t s);
 cudaError_t launch_combine_finalize(const float* ws, int64_t T, int64_t N, void* out, int sms,

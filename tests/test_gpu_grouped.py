@@ -40,6 +40,8 @@ def _routing(g, T, E, k, kind):
     (400, 4, 2, 256, 512, "uniform"),     # 256-row token tiles spanning two operand tiles
     (900, 3, 2, 128, 320, "uniform"),     # several 256-row tiles per expert, ragged K block
     (256, 32, 2, 1280, 256, "uniform"),   # more two-tile units than CTAs
+    (900, 3, 2, 256, 320, "uniform"),     # 256-row tiles on CTA pairs, ragged K block
+    (2000, 16, 2, 512, 256, "zipf"),      # CTA pairs, skewed: hot experts, empty ones, odd tiles
 ])
 def test_grouped_gather_matches_oracle(T, E, k, N, K, kind):
     g = inputs.rng(T * 13 + E + N + K)
@@ -138,11 +140,13 @@ def test_grouped_narrow_tiles_hot_expert(T, E, N, K):
     check_gemm(bf16_to_np(out2[:T]), oracle.combine(y, tok, slot, wts, T), "hot expert combine")
 
 
-def test_bounded_wait_expires_reports_timeout_and_context_survives():
+@pytest.mark.parametrize("T,E,k,N,K", [(16, 4, 2, 128, 256),      # one-SM kernel
+                                       (400, 4, 2, 256, 256)])    # 256-route tiles: CTA pairs
+def test_bounded_wait_expires_reports_timeout_and_context_survives(T, E, k, N, K):
     """Failure path: a stage that never fills (test hook) makes the MMA wait run
     out; the kernel records NVFP4_ERR_TIMEOUT and returns, and the next call on
     the same context computes the right result."""
-    T, E, k, N, K = 16, 4, 2, 128, 256
+    assert F.nvfp4_grouped_chunk_rows(T * k, E) in (32, 128)
     g = inputs.rng(9)
     x = inputs.normal_bf16(g, (T, K)).cuda()
     w = _weights_host(g, E, N, K)

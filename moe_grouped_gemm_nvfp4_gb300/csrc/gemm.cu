@@ -1255,7 +1255,12 @@ cudaError_t launch_gemm(const CUtensorMap& tmx, const CUtensorMap& tmy, const Ge
     case 32:   // two weight tiles per unit when the expert's rows pair up
       return (a.n_out / 128) % 2 == 0 ? launch_bn<32, 2>(tmx, tmy, a, mode, grid, s)
                                        : launch_bn<32>(tmx, tmy, a, mode, grid, s);
-    case 64: return launch_bn<64>(tmx, tmy, a, mode, grid, s);
+    case 64:
+      // two weight tiles per unit when the tiles pair up: twice the weight
+      // bytes in flight per stage for the same token bytes (down projection
+      // at 512 tokens: 0.179 -> 0.170 ms)
+      return (a.n_out / 128) % 2 == 0 ? launch_bn<64, 2>(tmx, tmy, a, mode, grid, s)
+                                       : launch_bn<64>(tmx, tmy, a, mode, grid, s);
     case 128: return launch_bn<128>(tmx, tmy, a, mode, grid, s);
     default: return launch_bn<256>(tmx, tmy, a, mode, grid, s);
   }

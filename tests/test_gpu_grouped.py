@@ -40,6 +40,7 @@ def _routing(g, T, E, k, kind):
     (400, 4, 2, 256, 512, "uniform"),     # 256-row token tiles spanning two operand tiles
     (900, 3, 2, 128, 320, "uniform"),     # several 256-row tiles per expert, ragged K block
     (256, 32, 2, 1280, 256, "uniform"),   # more two-tile units than CTAs
+    (160, 8, 2, 256, 256, "uniform"),     # 64-row tiles, two weight tiles per unit
     (900, 3, 2, 256, 320, "uniform"),     # 256-row tiles on CTA pairs, ragged K block
     (2000, 16, 2, 512, 256, "zipf"),      # CTA pairs, skewed: hot experts, empty ones, odd tiles
 ])
@@ -63,7 +64,8 @@ def test_grouped_gather_matches_oracle(T, E, k, N, K, kind):
 
 @pytest.mark.parametrize("T,E,k,N,K", [(32, 8, 2, 256, 512), (64, 16, 8, 384, 256),
                                        (3, 8, 2, 128, 128), (400, 4, 2, 128, 256),
-                                       (256, 32, 2, 1280, 256)])   # units > CTAs
+                                       (256, 32, 2, 1280, 256),    # units > CTAs
+                                       (64, 16, 8, 512, 320)])     # 64-row tiles, weight-tile pairs
 def test_grouped_combine_matches_oracle(T, E, k, N, K):
     g = inputs.rng(T * 17 + E + N + K)
     ids = inputs.uniform_topk(g, T, E, k)

@@ -37,6 +37,9 @@ namespace {
 // warps hide the latency of the expansion's loads, waits and stores; the
 // values kernel's ring and buffers are sized to fit two CTAs.
 constexpr int kScoreStages = 6, kScoreNBuf = 3;
+// score tiles the MMA warp may run ahead of the front warps that read them
+// (their item boundaries, where q of the next item is written, take time)
+constexpr int kScoreSBuf = 4;
 constexpr int kValueCtas = 2, kValueStages = 3, kValueNBuf = 2;
 constexpr int kWideFrontWarps = 4, kWideExpWarps = 8;
 constexpr int kWideProdWarp = kWideFrontWarps + kWideExpWarps, kWideMmaWarp = kWideProdWarp + 1;
@@ -81,32 +84,47 @@ static_assert(wide_fits<256>() && wide_fits<512>(), "CTAs per SM");
 // 16-byte chunk of a 64-byte code row as the TMA's 64-byte swizzle places it
 __device__ __forceinline__ int swz64(int t) { return (t >> 1) & 3; }
 
-// q of work item w -> FP16 operand rows of buffer qb (each head scaled by the
-// power of two that puts its largest magnitude in [2^13, 2^14)); qm[g] gets
-// the factor that turns head g's MMA scores into base-2 scaled scores.
-// Called by the four front warps together (a named-barrier reduction).
+// q of a work item as the front warps hold it: thread tid has elements
+// tid + 128 k (k < G * D / 128) of the item's G heads, two BF16 per word.
+// Loaded one item ahead (the loads are issued where written and land while
+// the current item's tiles go by).
 template <int D, int G>
-__device__ __forceinline__ void wide_write_q(const AttnArgs& a, int64_t w, uint8_t* qh, float* redq,
-                                             float (&qm)[G], bool& ok) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+struct WideQ {
+  static constexpr int kElems = G * D / 128;            // per thread
+  uint32_t w[kElems / 2];
+};
+
+template <int D, int G>
+__device__ __forceinline__ void wide_load_q(const AttnArgs& a, int64_t w, WideQ<D, G>& q) {
+  const int tid = threadIdx.x;
   const int64_t nsplit = a.splits;
   const int j = static_cast<int>((w / nsplit) % a.Hkv);
   const int b = static_cast<int>(w / (nsplit * a.Hkv));
-  const uint16_t* qp = a.q + (static_cast<int64_t>(b) * a.Hq + j * G) * D;
-  constexpr int QE = (G * D + 127) / 128;
+  const uint16_t* qp = a.q + (static_cast<int64_t>(b) * a.Hq + j * G) * D + tid;
+#pragma unroll
+  for (int k = 0; k < WideQ<D, G>::kElems; k += 2)
+    q.w[k / 2] = ld_prefetch_u16(qp + 128 * k) | (ld_prefetch_u16(qp + 128 * (k + 1)) << 16);
+}
+
+// q -> FP16 operand rows of buffer qh (each head scaled by the power of two
+// that puts its largest magnitude in [2^13, 2^14), exact for BF16); qm[g]
+// gets the factor that turns head g's MMA scores into base-2 scaled scores.
+// Element k of a thread is head k / (D / 128), dimension 128 (k % (D / 128))
+// + tid.  Called by the four front warps together (named-barrier reductions,
+// which also make ok the same in all of them).
+template <int D, int G>
+__device__ __forceinline__ void wide_write_q(const AttnArgs& a, const WideQ<D, G>& q, uint8_t* qh,
+                                             float* redq, float (&qm)[G], bool& ok) {
+  constexpr int KE = WideQ<D, G>::kElems, KD = D / 128;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  auto val = [&](int k) {
+    return bf16_bits_to_f32((q.w[k / 2] >> (16 * (k & 1))) & 0xFFFFu);
+  };
   float m[G];
 #pragma unroll
   for (int g = 0; g < G; ++g) m[g] = 0.0f;
 #pragma unroll
-  for (int k = 0; k < QE; ++k) {
-    const int e = tid + 128 * k;
-    if (e < G * D) {
-      const float v = fabsf(bf16_bits_to_f32(__ldg(qp + e)));
-#pragma unroll
-      for (int h = 0; h < G; ++h)
-        if (h == e / D) m[h] = fmaxf(m[h], v);
-    }
-  }
+  for (int k = 0; k < KE; ++k) m[k / KD] = fmaxf(m[k / KD], fabsf(val(k)));
 #pragma unroll
   for (int g = 0; g < G; ++g) {
 #pragma unroll
@@ -115,29 +133,21 @@ __device__ __forceinline__ void wide_write_q(const AttnArgs& a, int64_t w, uint8
   }
   ok = softmax_bar_and(ok);
   const float qmul = a.scale * (*a.gk) * kLog2eTc;
-  int ex[G];
+  float up[G];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     const float mg = fmaxf(fmaxf(redq[g], redq[16 + g]), fmaxf(redq[32 + g], redq[48 + g]));
     int e = 0;
     if (mg > 0.0f) e = 13 - ((__float_as_uint(mg) >> 23) & 0xFF) + 127;
-    ex[g] = max(-100, min(100, e));
-    qm[g] = qmul * __uint_as_float(static_cast<uint32_t>(127 - ex[g]) << 23);
+    e = max(-100, min(100, e));
+    qm[g] = qmul * __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+    up[g] = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
   }
 #pragma unroll
-  for (int k = 0; k < QE; ++k) {
-    const int e = tid + 128 * k;
-    if (e < G * D) {
-      const int g = e / D, d = e - g * D;
-      int eg = 0;
-#pragma unroll
-      for (int h = 0; h < G; ++h)
-        if (h == g) eg = ex[h];
-      const float up = __uint_as_float(static_cast<uint32_t>(127 + eg) << 23);
-      *reinterpret_cast<__half*>(qh + (d >> 6) * 2048 + kmajor_chunk(g, (d & 63) >> 3) +
-                                 (d & 7) * 2) =
-          __float2half_rn(bf16_bits_to_f32(__ldg(qp + e)) * up);
-    }
+  for (int k = 0; k < KE; ++k) {
+    const int g = k / KD, d = (k % KD) * 128 + tid;
+    *reinterpret_cast<__half*>(qh + (d >> 6) * 2048 + kmajor_chunk(g, (d & 63) >> 3) +
+                               (d & 7) * 2) = __float2half_rn(val(k) * up[g]);
   }
   // the next reduction overwrites redq only after every thread read it
   ok = softmax_bar_and(ok);
@@ -146,7 +156,8 @@ __device__ __forceinline__ void wide_write_q(const AttnArgs& a, int64_t w, uint8
 // ---------------------------------------------------------------------------
 // Scores kernel: warps 0-3 write q and store the scores, 4-11 expand K slices
 // into tensor memory (lane = token), 12 copies the raw slices, 13 issues the
-// score MMAs.  Tensor memory: K^ slices at 64 b (b < 3), S at 192 + 16 p.
+// score MMAs.  Tensor memory: K^ slices at 64 b (b < 3), S of tile t at
+// 192 + 16 (t % kScoreSBuf).
 // ---------------------------------------------------------------------------
 template <int D, int G>
 __global__ void __launch_bounds__(kWideThreads, 2)
@@ -164,8 +175,9 @@ decode_scores_wide_kernel(const __grid_constant__ CUtensorMap tmk,
   auto raw_full = [&](uint32_t st) { return bars + 8u * st; };
   auto raw_empty = [&](uint32_t st) { return bars + 8u * (kScoreStages + st); };
   const uint32_t op_full0 = bars + 8u * (2 * kScoreStages), k_free0 = op_full0 + 8 * kScoreNBuf,
-                 s_full0 = k_free0 + 8 * kScoreNBuf, s_empty0 = s_full0 + 16,
-                 q_full0 = s_empty0 + 16, q_empty0 = q_full0 + 16, fin = q_empty0 + 16;
+                 s_full0 = k_free0 + 8 * kScoreNBuf, s_empty0 = s_full0 + 8 * kScoreSBuf,
+                 q_full0 = s_empty0 + 8 * kScoreSBuf, q_empty0 = q_full0 + 16,
+                 fin = q_empty0 + 16;
   uint32_t* slot = reinterpret_cast<uint32_t*>(smem + C::kSRed + 768 + 16 + 40 * 8);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -180,9 +192,11 @@ decode_scores_wide_kernel(const __grid_constant__ CUtensorMap tmk,
       mbar_init(op_full0 + 8 * h, kWideExpWarps);
       mbar_init(k_free0 + 8 * h, 1);
     }
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < kScoreSBuf; ++h) {
       mbar_init(s_full0 + 8 * h, 1);
       mbar_init(s_empty0 + 8 * h, kWideFrontWarps);
+    }
+    for (int h = 0; h < 2; ++h) {
       mbar_init(q_full0 + 8 * h, kWideFrontWarps);
       mbar_init(q_empty0 + 8 * h, 1);
     }
@@ -308,10 +322,10 @@ decode_scores_wide_kernel(const __grid_constant__ CUtensorMap tmk,
         continue;
       }
       for (int64_t tt = it.t0; tt < it.t1 && ok; tt += kTile, ++t) {
-        const uint32_t sb = t & 1u;
-        if (t >= 2)                                      // the front warps read S of tile t - 2
-          ok = __all_sync(0xFFFFFFFFu, ws_wait(s_empty0 + 8 * sb, ((t >> 1) - 1) & 1u, ctl,
-                                               a.status));
+        const uint32_t sb = t % kScoreSBuf;
+        if (t >= kScoreSBuf)                             // the front warps have read this S buffer
+          ok = __all_sync(0xFFFFFFFFu, ws_wait(s_empty0 + 8 * sb, ((t / kScoreSBuf) - 1) & 1u,
+                                               ctl, a.status));
         for (int s = 0; s < NS && ok; ++s, ++i) {
           const uint32_t ob = i % kScoreNBuf;
           ok = __all_sync(0xFFFFFFFFu, ws_wait(op_full0 + 8 * ob, (i / kScoreNBuf) & 1u, ctl,
@@ -338,7 +352,9 @@ decode_scores_wide_kernel(const __grid_constant__ CUtensorMap tmk,
     // score per head; at the end of the item the four warps reduce them (in
     // the buffer of the item's parity, so one barrier per item suffices) and
     // thread 0 writes the split's reference maximum.  A split without tokens
-    // gets its whole partial here (O 0, maximum -inf, sum 0).
+    // gets its whole partial here (O 0, maximum -inf, sum 0).  q of the next
+    // item is written after the item's first tile (from registers loaded an
+    // item earlier), so the scores of a tile never wait for it.
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     float* redm = redq + 64;                             // [2][4][16]
     float qm_cur[G], qm_nxt[G];
@@ -348,62 +364,75 @@ decode_scores_wide_kernel(const __grid_constant__ CUtensorMap tmk,
     const int64_t w0 = blockIdx.x, stride = gridDim.x;
     WsItem it_nxt{};
     int n_nn = 0;
+    WideQ<D, G> qr;
     if (w0 < items) {
-      wide_write_q<D, G>(a, w0, smem + C::kSQh, redq, qm_cur, ok);
+      wide_load_q<D, G>(a, w0, qr);
+      wide_write_q<D, G>(a, qr, smem + C::kSQh, redq, qm_cur, ok);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(q_full0);
       it_nxt = ws_item(a, w0, ws_len(a, w0, items));
       n_nn = ws_len(a, w0 + stride, items);
+      if (w0 + stride < items) wide_load_q<D, G>(a, w0 + stride, qr);
     }
     uint32_t k = 0, t = 0;
     // No warp leaves the item loop on its own: the named-barrier reductions
-    // below need all four (ok is made uniform by each of them).
+    // need all four (ok is made uniform by each of them); after a failed wait
+    // a warp skips its work until the next reduction.
     for (int64_t w = w0; w < items; w += stride, ++k) {
       const WsItem it = it_nxt;
-      if (w + stride < items) {                          // q of the next item, other buffer
+      const bool has_next = w + stride < items;
+      if (it.bad_len && tid == 0) raise_status(a.status, NVFP4_ERR_DEVICE_CHECK);
+      auto part_of = [&](int g) {
+        return (static_cast<int64_t>(it.b) * a.Hq + it.j * G + g) * a.splits + it.split;
+      };
+      float xmax[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) xmax[g] = -INFINITY;
+      // scores of tile tt: from tensor memory, stored, and the maxima kept
+      auto score_tile = [&](int64_t tt) {
+        const uint32_t sb = t % kScoreSBuf;
+        ok = __all_sync(0xFFFFFFFFu, ok && ws_wait(s_full0 + 8 * sb, (t / kScoreSBuf) & 1u, ctl,
+                                                   a.status));
+        ++t;
+        if (!ok) return;
+        tc_fence_after();
+        uint32_t sr[16];
+        tmem_ld16(tmem + lane_base + 192 + 16 * sb, sr);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_empty0 + 8 * sb);
+        const int64_t tok = tt + tid;
+        if (tok < it.t1) {
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const float x = __uint_as_float(sr[g]) * qm_cur[g];
+            xmax[g] = fmaxf(xmax[g], x);
+            a.ws_s[(static_cast<int64_t>(it.b) * a.Hq + it.j * G + g) * a.L_max + tok] = x;
+          }
+        }
+      };
+      int64_t tt = it.t0;
+      if (tt < it.t1) {
+        score_tile(tt);
+        tt += kTile;
+      }
+      if (has_next) {                                    // q of the next item, other buffer
         const uint32_t nb = (k + 1) & 1u;
         if (k >= 1)
           ok = __all_sync(0xFFFFFFFFu, ok && ws_wait(q_empty0 + 8 * nb, ((k - 1) >> 1) & 1u, ctl,
                                                      a.status));
-        wide_write_q<D, G>(a, w + stride, smem + C::kSQh + nb * C::kQhBuf, redq, qm_nxt, ok);
+        wide_write_q<D, G>(a, qr, smem + C::kSQh + nb * C::kQhBuf, redq, qm_nxt, ok);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(q_full0 + 8 * nb);
         it_nxt = ws_item(a, w + stride, n_nn);
         n_nn = ws_len(a, w + 2 * stride, items);
+        if (w + 2 * stride < items) wide_load_q<D, G>(a, w + 2 * stride, qr);
       }
-      if (!ok) break;
-      if (it.bad_len && tid == 0) raise_status(a.status, NVFP4_ERR_DEVICE_CHECK);
-      auto part_of = [&](int g) {
-        return (static_cast<int64_t>(it.b) * a.Hq + it.j * G + g) * a.splits + it.split;
-      };
       if (it.t1 > it.t0) {
-        float xmax[G];
-#pragma unroll
-        for (int g = 0; g < G; ++g) xmax[g] = -INFINITY;
-        for (int64_t tt = it.t0; tt < it.t1; tt += kTile, ++t) {
-          const uint32_t sb = t & 1u;
-          ok = __all_sync(0xFFFFFFFFu, ok && ws_wait(s_full0 + 8 * sb, (t >> 1) & 1u, ctl,
-                                                     a.status));
-          if (!ok) break;
-          tc_fence_after();
-          uint32_t sr[16];
-          tmem_ld16(tmem + lane_base + 192 + 16 * sb, sr);
-          tmem_ld_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(s_empty0 + 8 * sb);
-          const int64_t tok = tt + tid;
-          if (tok < it.t1) {
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-              const float x = __uint_as_float(sr[g]) * qm_cur[g];
-              xmax[g] = fmaxf(xmax[g], x);
-              a.ws_s[(static_cast<int64_t>(it.b) * a.Hq + it.j * G + g) * a.L_max + tok] = x;
-            }
-          }
-        }
+        for (; tt < it.t1; tt += kTile) score_tile(tt);
         float* rm = redm + (k & 1u) * 64;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
@@ -418,6 +447,7 @@ decode_scores_wide_kernel(const __grid_constant__ CUtensorMap tmk,
           a.ws_ml[2 * part_of(tid)] =
               fmaxf(fmaxf(rm[tid], rm[16 + tid]), fmaxf(rm[32 + tid], rm[48 + tid]));
       } else {                                           // no cached token in this split
+        if (!ok) break;
         for (int e = tid; e < G * D; e += 128) {
           const int g = e / D, d = e - g * D;
           a.ws_o[part_of(g) * D + d] = 0.0f;

@@ -405,9 +405,8 @@ decode_attention_ws_kernel(const __grid_constant__ CUtensorMap tmk,
     constexpr int QE = (G * D + 127) / 128;
     uint32_t qreg[QE];
     auto load_q = [&](int64_t w) {
-      const int64_t nsplit = a.splits;
-      const int j = static_cast<int>((w / nsplit) % a.Hkv);
-      const int b = static_cast<int>(w / (nsplit * a.Hkv));
+      const WsIdx x = ws_idx(a, w);
+      const int j = static_cast<int>(x.j), b = static_cast<int>(x.b);
       const uint16_t* qp = a.q + (static_cast<int64_t>(b) * a.Hq + j * G) * D;
 #pragma unroll
       for (int k = 0; k < QE; ++k) {
@@ -486,8 +485,11 @@ decode_attention_ws_kernel(const __grid_constant__ CUtensorMap tmk,
     for (int64_t w = w0; w < items && ok; w += stride, ++k) {
       const WsItem it = it_nxt;
       // q of the next item into the other buffer once the score MMAs of the
-      // item before have released it; then prefetch what the items after need
-      if (w + stride < items) {
+      // item before have released it, then the prefetches the items after
+      // need: after this item's first tile (whose P goes first; the softmax
+      // warps agree on ok there), or here when the item has no tile
+      bool q_pending = w + stride < items;
+      auto next_q = [&]() {
         const uint32_t nb = (k + 1) & 1u;
         if (k >= 1)
           ok = __all_sync(0xFFFFFFFFu, ok && ws_wait(q_empty0 + 8 * nb, ((k - 1) >> 1) & 1u, ctl,
@@ -496,7 +498,9 @@ decode_attention_ws_kernel(const __grid_constant__ CUtensorMap tmk,
         it_nxt = ws_item(a, w + stride, n_nn);
         n_nn = ws_len(a, w + 2 * stride, items);
         if (w + 2 * stride < items) load_q(w + 2 * stride);
-      }
+        q_pending = false;
+      };
+      if (q_pending && it.t1 <= it.t0) next_q();
       if (!ok) break;
       if (it.bad_len && s == 0) raise_status(a.status, NVFP4_ERR_DEVICE_CHECK);
       auto part_of = [&](int g) {
@@ -597,6 +601,7 @@ decode_attention_ws_kernel(const __grid_constant__ CUtensorMap tmk,
           if (rescaled) tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(p_full0 + 8 * ob);
+          if (q_pending) next_q();
         }
         // O of the item: the value MMAs of its last tile have completed
         float o[G];

@@ -113,19 +113,32 @@ __device__ __forceinline__ uint32_t ld_prefetch_u16(const uint16_t* p) {
   return v;
 }
 
+// Work item w as (split, KV head, sequence), in 32-bit arithmetic: the
+// items number fewer than 2^31 / 128 (fewer than 2^31 cache rows, at least
+// 128 tokens per split), and a 64-bit division costs every role hundreds of
+// cycles at each item boundary.
+struct WsIdx {
+  uint32_t split, j, b;
+};
+__device__ __forceinline__ WsIdx ws_idx(const AttnArgs& a, int64_t w) {
+  const uint32_t wu = static_cast<uint32_t>(w), ns = static_cast<uint32_t>(a.splits);
+  const uint32_t q = wu / ns;
+  return WsIdx{wu - q * ns, q % static_cast<uint32_t>(a.Hkv), q / static_cast<uint32_t>(a.Hkv)};
+}
+
 // The sequence length work item w reads (prefetched one item ahead by every
 // role, so that its latency stays off the item boundary).
 __device__ __forceinline__ int ws_len(const AttnArgs& a, int64_t w, int64_t items) {
   if (w >= items) return 0;
-  return ld_prefetch_s32(a.seq_lens + w / (static_cast<int64_t>(a.splits) * a.Hkv));
+  return ld_prefetch_s32(a.seq_lens + ws_idx(a, w).b);
 }
 
 __device__ __forceinline__ WsItem ws_item(const AttnArgs& a, int64_t w, int n) {
   WsItem it;
-  const int64_t nsplit = a.splits;
-  it.split = static_cast<int>(w % nsplit);
-  it.j = static_cast<int>((w / nsplit) % a.Hkv);
-  it.b = static_cast<int>(w / (nsplit * a.Hkv));
+  const WsIdx x = ws_idx(a, w);
+  it.split = static_cast<int>(x.split);
+  it.j = static_cast<int>(x.j);
+  it.b = static_cast<int>(x.b);
   it.bad_len = n < 0 || n > a.L_max;
   if (it.bad_len) n = 0;
   it.t0 = static_cast<int64_t>(it.split) * a.chunk;

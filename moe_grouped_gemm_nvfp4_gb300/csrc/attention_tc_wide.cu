@@ -97,9 +97,8 @@ struct WideQ {
 template <int D, int G>
 __device__ __forceinline__ void wide_load_q(const AttnArgs& a, int64_t w, WideQ<D, G>& q) {
   const int tid = threadIdx.x;
-  const int64_t nsplit = a.splits;
-  const int j = static_cast<int>((w / nsplit) % a.Hkv);
-  const int b = static_cast<int>(w / (nsplit * a.Hkv));
+  const WsIdx x = ws_idx(a, w);
+  const int j = static_cast<int>(x.j), b = static_cast<int>(x.b);
   const uint16_t* qp = a.q + (static_cast<int64_t>(b) * a.Hq + j * G) * D + tid;
 #pragma unroll
   for (int k = 0; k < WideQ<D, G>::kElems; k += 2)

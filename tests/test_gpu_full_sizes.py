@@ -134,3 +134,55 @@ def test_decode_down_full(name, sparse):
             ref[i] += np.float64(wts[t, slot[p]]) * y[0]
     got = bf16_to_np(out[torch.from_numpy(tokens).cuda()][:, torch.from_numpy(cols).cuda()])
     check_gemm(got, ref, name + (" sparse" if sparse else ""))
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,L,D", [
+    (16, 32, 8, 16384, 128),     # groups of 4 over 128-wide heads: the pipelined kernel
+    (16, 64, 8, 16384, 128),     # groups of 8
+    (16, 32, 8, 8192, 256),      # 256-wide heads: the scores and values passes
+    (8, 8, 2, 32768, 512),       # 512-wide heads
+])
+def test_decode_attention_full_size(B, Hq, Hkv, L, D):
+    """Decode attention over an NVFP4 KV cache at the benchmark's shapes, in the
+    launch configuration it times, checked on sampled (sequence, KV head)
+    groups: the oracle takes each cache's global from the whole tensor,
+    quantises the sampled groups' rows itself (codes and scales bit-exact
+    against the GPU's), and computes their heads' outputs.  Sequence lengths:
+    full, ragged (a split boundary's neighbourhood), and a single token."""
+    from moe_grouped_gemm_nvfp4_gb300 import attention
+    from test_gpu_attention import _check
+    G = Hq // Hkv
+    dev = "cuda"
+    kd = inputs.device_normal_bf16((B, Hkv, L, D), 1.0, 71, dev)
+    vd = inputs.device_normal_bf16((B, Hkv, L, D), 1.0, 72, dev)
+    q = inputs.device_normal_bf16((B, Hq, D), 1.0, 73, dev)
+    kq, vq = attention.quantize_kv(kd), attention.quantize_kv(vd)
+    g = inputs.rng(B * 7 + L + D)
+    lens = np.full(B, L, dtype=np.int64)
+    lens[1] = L // 2 + 1 + int(g.integers(0, 100))
+    lens[2] = 1
+    scale = 1.0 / np.sqrt(D)
+    plan = attention.DecodeAttention(B, Hq, Hkv, L, D, dev)
+    plan.out.view(torch.int16).fill_(0x7FC0)
+    out = plan.run(q, kq, vq, torch.from_numpy(lens.astype(np.int32)).to(dev), scale)
+    torch.cuda.synchronize()
+    assert F.nvfp4_device_status() == F.NVFP4_OK
+    gk = oracle.global_scale(kd.float().cpu().numpy())
+    gv = oracle.global_scale(vd.float().cpu().numpy())
+    assert kq[2].item() == gk and vq[2].item() == gv
+    qf = q.float().cpu().numpy()
+    outf = out.float().cpu().numpy().astype(np.float64)
+    for b, j in ((0, 0), (1, Hkv - 1), (2, Hkv // 2), (B - 1, 1 % Hkv)):
+        n = int(lens[b])
+        kf = kd[b, j, :n].float().cpu().numpy()
+        vf = vd[b, j, :n].float().cpu().numpy()
+        pk, sk = oracle.quantize_kv(kf, gk)
+        pv, sv = oracle.quantize_kv(vf, gv)
+        assert np.array_equal(kq[0][b, j, :n].cpu().numpy(), pk)
+        assert np.array_equal(kq[1][b, j, :n].cpu().numpy(), sk)
+        assert np.array_equal(vq[0][b, j, :n].cpu().numpy(), pv)
+        assert np.array_equal(vq[1][b, j, :n].cpu().numpy(), sv)
+        ref = oracle.decode_attention(qf[b:b + 1, j * G:(j + 1) * G],
+                                      oracle.dequantize_kv(pk, sk, gk)[None, None],
+                                      oracle.dequantize_kv(pv, sv, gv)[None, None], [n], scale)
+        _check(outf[b:b + 1, j * G:(j + 1) * G], ref, f"attention B{B} Hq{Hq} D{D} b{b} j{j}")

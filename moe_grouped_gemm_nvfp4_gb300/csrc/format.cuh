@@ -15,23 +15,15 @@ namespace nvfp4 {
 // Number formats (implemented from the format definitions)
 // ---------------------------------------------------------------------------
 
-// binary32 (s >= 0, finite) -> E4M3 code, round to nearest even, saturating
-// at 448 (0x7E).  Normal range: keep 3 mantissa bits with RNE (a carry into
-// the exponent is the correct next code).  Below 2^-6: subnormal quantum
-// 2^-9, so the code is s * 2^9 rounded to the nearest even integer.
+// binary32 (s >= 0) -> E4M3 code, round to nearest even, saturating at 448
+// (0x7E): the hardware conversion rounds once to nearest even over the whole
+// E4M3 range (subnormals included, quantum 2^-9 below 2^-6) and, with
+// .satfinite, clamps what lies beyond the largest finite value to 448.
 __device__ __forceinline__ uint32_t e4m3_from_f32(float s) {
   if (!(s < 448.0f)) return 0x7Eu;
-  const uint32_t b = __float_as_uint(s);
-  const uint32_t exp = (b >> 23) & 0xFFu;
-  if (exp >= 121u) {                       // s >= 2^-6
-    const uint32_t mant = b & 0x7FFFFFu;
-    const uint32_t keep = mant >> 20;
-    const uint32_t rest = mant & 0xFFFFFu;
-    uint32_t v = ((exp - 120u) << 3) | keep;
-    if (rest > 0x80000u || (rest == 0x80000u && (keep & 1u))) v += 1u;
-    return v;
-  }
-  return __float2uint_rn(s * 512.0f);      // 0..8; 8 is the smallest normal
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(s));
+  return r & 0xFFu;
 }
 
 // E4M3 code (never NaN here) -> binary32, exact.
@@ -210,27 +202,79 @@ __device__ __forceinline__ Block16 quantize16_with(float amax_b, const ScaleK& k
   return b;
 }
 
-// Sixteen BF16 values as eight words (value 2i in the low half of word i).
-// The block maximum compares BF16 magnitudes as unsigned 16-bit integers
-// (two per instruction); the element codes take their sign from the
-// conversion of the bracketing products, which carry the sign of v (E2M1
-// rounding is symmetric, and a product that rounds to zero keeps its sign).
-__device__ __forceinline__ Block16 quantize_bf16x16(const uint32_t (&w)[8], const ScaleK& k) {
-  uint32_t m = __vmaxu2(w[0] & 0x7FFF7FFFu, w[1] & 0x7FFF7FFFu);
-  m = __vmaxu2(m, __vmaxu2(w[2] & 0x7FFF7FFFu, w[3] & 0x7FFF7FFFu));
-  m = __vmaxu2(m, __vmaxu2(w[4] & 0x7FFF7FFFu, w[5] & 0x7FFF7FFFu));
-  m = __vmaxu2(m, __vmaxu2(w[6] & 0x7FFF7FFFu, w[7] & 0x7FFF7FFFu));
-  const uint32_t amax_bits = max(m & 0xFFFFu, m >> 16);
-  auto get = [&](int e) {
-    return __uint_as_float((e & 1) ? (w[e >> 1] & 0xFFFF0000u) : (w[e >> 1] << 16));
-  };
+// Element constants of one block-scale code c under a global scale g,
+// gathered per tensor into a table of 128 entries (E4M3 codes 0..0x7F) so
+// that a block looks up, instead of computing, its bracket: {lo, hi, d}
+// with d = e4m3(c) * g.  A zero d (g == 0 or c == 0) gets lo = hi = 0, whose
+// products are the signed zeros the exact path gives; a d whose reciprocal
+// leaves the normal range gets lo = -1, which sends its blocks to the exact
+// path.
+__device__ __forceinline__ float4 elem_consts(uint32_t c, float g) {
+  const float d = __fmul_rn(f32_from_e4m3(c), g);
+  const Bracket br = bracket_of(d);
+  if (br.ok) return make_float4(br.lo, br.hi, d, 0.0f);
+  return make_float4(d == 0.0f ? 0.0f : -1.0f, 0.0f, d, 0.0f);
+}
+
+constexpr int kElemTable = 128;
+
+// Fills a block's shared table of element constants (every thread of the
+// block calls it; the caller synchronises before the first lookup).
+__device__ __forceinline__ void fill_elem_table(float4* t, float g) {
+  for (int c = threadIdx.x; c < kElemTable; c += blockDim.x) t[c] = elem_consts(c, g);
+}
+
+// Codes of one code word (values kBase..kBase+7 of the block: words
+// kBase/2..kBase/2+3 of w) whose bracketing products disagreed (diff: the
+// XOR of the two code words) replaced by the exact code E2M1(RN(v / d));
+// only the disagreeing values are visited, typically one.
+template <int kBase>
+__device__ __forceinline__ uint32_t fix_codes_bf16(uint32_t c, uint32_t diff, float d,
+                                                   const uint32_t (&w)[8]) {
+  while (diff != 0u) {
+    const int n = (__ffs(diff) - 1) >> 2;           // first disagreeing value
+    const uint32_t mask = 0xFu << (4 * n);
+    diff &= ~mask;
+    const int i = n >> 1;
+    const uint32_t word = i == 0 ? w[kBase / 2] : i == 1 ? w[kBase / 2 + 1]
+                        : i == 2 ? w[kBase / 2 + 2] : w[kBase / 2 + 3];
+    const float v = __uint_as_float((n & 1) ? (word & 0xFFFF0000u) : (word << 16));
+    const float q = __fdiv_rn(v, d);
+    uint32_t code;
+    asm("{\n\t.reg .b8 t;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t, %2, %1;\n\t"
+        "cvt.u32.u8 %0, t;\n\t}"
+        : "=r"(code) : "f"(q), "f"(0.0f));
+    c = (c & ~mask) | ((code & 0xFu) << (4 * n));
+  }
+  return c;
+}
+
+// Per half: max(|a|, |b|) of two BF16 pairs, with the XOR of the signs in
+// the sign bit (which the caller drops).
+__device__ __forceinline__ uint32_t bf16x2_max_abs(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// Sixteen BF16 values as eight words (value 2i in the low half of word i),
+// with the tensor's table of element constants.  The block maximum takes
+// BF16 magnitudes two per instruction (finite inputs); the
+// element codes take their sign from the conversion of the bracketing
+// products, which carry the sign of v (E2M1 rounding is symmetric, and a
+// product that rounds to zero keeps its sign).
+__device__ __forceinline__ Block16 quantize_bf16x16(const uint32_t (&w)[8], const ScaleK& k,
+                                                    const float4* table) {
+  const uint32_t m = bf16x2_max_abs(bf16x2_max_abs(bf16x2_max_abs(w[0], w[1]), bf16x2_max_abs(w[2], w[3])),
+                                     bf16x2_max_abs(bf16x2_max_abs(w[4], w[5]), bf16x2_max_abs(w[6], w[7])));
+  const uint32_t amax_bits = bf16x2_max_abs(m, m >> 16) & 0x7FFFu;
   Block16 b;
   b.sf = block_scale_code(__uint_as_float(amax_bits << 16), k);
-  const float d = __fmul_rn(f32_from_e4m3(b.sf), k.g);
-  const Bracket br = bracket_of(d);
-  if (br.ok) {
+  const float4 t = table[b.sf];
+  if (t.x >= 0.0f) {
     float lo[16], hi[16];
-    const float2 l2 = make_float2(br.lo, br.lo), h2 = make_float2(br.hi, br.hi);
+    const float2 l2 = make_float2(t.x, t.x), h2 = make_float2(t.y, t.y);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const float2 v = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
@@ -243,13 +287,15 @@ __device__ __forceinline__ Block16 quantize_bf16x16(const uint32_t (&w)[8], cons
     uint32_t c0 = e2m1x8_rn_satfinite(lo), c1 = e2m1x8_rn_satfinite(lo + 8);
     const uint32_t x0 = c0 ^ e2m1x8_rn_satfinite(hi), x1 = c1 ^ e2m1x8_rn_satfinite(hi + 8);
     if ((x0 | x1) != 0u) {
-      c0 = fix_codes<0>(c0, x0, d, get);
-      c1 = fix_codes<8>(c1, x1, d, get);
+      c0 = fix_codes_bf16<0>(c0, x0, t.z, w);
+      c1 = fix_codes_bf16<8>(c1, x1, t.z, w);
     }
     b.packed = make_uint2(c0, c1);
     return b;
   }
-  b.packed = codes_exact(d, get);
+  b.packed = codes_exact(t.z, [&](int e) {
+    return __uint_as_float((e & 1) ? (w[e >> 1] & 0xFFFF0000u) : (w[e >> 1] << 16));
+  });
   return b;
 }
 

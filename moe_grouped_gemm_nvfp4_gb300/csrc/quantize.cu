@@ -72,13 +72,14 @@ __device__ __forceinline__ uint32_t gather4_bytes(uint32_t byte) {
   const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, byte, 1);
   const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, byte, 2);
   const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, byte, 3);
-  return (byte & 0xFFu) | ((b1 & 0xFFu) << 8) | ((b2 & 0xFFu) << 16) | ((b3 & 0xFFu) << 24);
+  return __byte_perm(__byte_perm(byte, b1, 0x0040u), __byte_perm(b2, b3, 0x0040u), 0x5410u);
 }
 
 // One 16-element block of BF16 (two 16-byte vectors) -> codes + scale.
-__device__ __forceinline__ Block16 quantize_block(const uint4 lo, const uint4 hi, const ScaleK& k) {
+__device__ __forceinline__ Block16 quantize_block(const uint4 lo, const uint4 hi, const ScaleK& k,
+                                                  const float4* table) {
   const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-  return quantize_bf16x16(w, k);
+  return quantize_bf16x16(w, k, table);
 }
 
 __device__ __forceinline__ int64_t atom_offset(int64_t r, int64_t c, int64_t n_cgroups) {
@@ -98,7 +99,11 @@ __global__ void __launch_bounds__(256, 5) quantize_kernel(const uint16_t* __rest
                                                        uint8_t* __restrict__ packed,
                                                        uint8_t* __restrict__ scales,
                                                        int sf_atoms, const float* g_ptr) {
-  const ScaleK k = scale_consts(*g_ptr);
+  __shared__ float4 s_elem[kElemTable];
+  const float g = *g_ptr;
+  const ScaleK k = scale_consts(g);
+  fill_elem_table(s_elem, g);
+  __syncthreads();
   const int lane = threadIdx.x & 31;
   const uint32_t bpr = static_cast<uint32_t>(cols >> 4);
   const uint32_t segs = (bpr + kQuantItemBlocks - 1) / kQuantItemBlocks;
@@ -126,7 +131,7 @@ __global__ void __launch_bounds__(256, 5) quantize_kernel(const uint16_t* __rest
       q.sf = 0u;
       if (valid) {
         const uint4* src = reinterpret_cast<const uint4*>(x + r * ld + b * 16);
-        q = quantize_block(__ldg(src), __ldg(src + 1), k);
+        q = quantize_block(__ldg(src), __ldg(src + 1), k, s_elem);
         *reinterpret_cast<uint2*>(packed + r * half_row + b * 8) = q.packed;
       }
       if (sf_atoms) {
@@ -244,6 +249,9 @@ __global__ void __launch_bounds__(256) quantize_dispatch_kernel(
     g = *g_ptr;
   }
   const ScaleK k = scale_consts(g);
+  __shared__ float4 s_elem[kElemTable];
+  fill_elem_table(s_elem, g);
+  __syncthreads();
   if (s_bad) return;
   // Work item: a warp quantises 32 consecutive 16-element blocks of one
   // source row (K % 64 == 0, so every group of four blocks is whole) and
@@ -266,7 +274,7 @@ __global__ void __launch_bounds__(256) quantize_dispatch_kernel(
     q.sf = 0u;
     if (valid) {
       const uint4* src = reinterpret_cast<const uint4*>(x + r * ld + static_cast<int64_t>(b) * 16);
-      q = quantize_block(__ldg(src), __ldg(src + 1), k);
+      q = quantize_block(__ldg(src), __ldg(src + 1), k, s_elem);
     }
     const uint32_t word = gather4_bytes(q.sf);
     const int64_t kb = b >> 4;

@@ -8,10 +8,12 @@
 // enlarges the tile).
 //
 // Roles (352 threads per CTA, one CTA per SM, clusters of two):
-//   warp 0      both CTAs: TMA producer.  A rows, B rows and their scale
-//               atoms into this CTA's stage; every copy completes on the
-//               leader CTA's full barrier (the leader expects both CTAs'
-//               bytes), so the leader alone knows when a stage has landed;
+//   warp 0      both CTAs: TMA producer.  A's and B's scale atoms, then A
+//               rows and B rows, into this CTA's stage; every copy completes
+//               on a barrier of the leader CTA (the leader expects both CTAs'
+//               bytes): the atoms on the stage's scale barrier, the codes on
+//               its full barrier, so the atoms' copies into tensor memory can
+//               start while the codes are still arriving;
 //   warp 6      leader: scale warp, tcgen05.cp of the stage's scale atoms
 //               into both CTAs' tensor memory (each from its own shared
 //               memory: A's scales of its own rows, all 256 rows of B's);
@@ -43,8 +45,8 @@ struct PairCfg {
   static constexpr int kStageBytes = kYsf + 2 * kPSfBytes;
   static_assert(kY % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle alignment");
   static constexpr int kBarOffset = kStages * kStageBytes;
-  // full[S], empty[S], scales_ready[S], acc_full, acc_empty, drain
-  static constexpr int kBarBytes = 8 * (3 * kStages + 3);
+  // full[S], empty[S], scales_ready[S], acc_full, acc_empty, drain, scales_full[S]
+  static constexpr int kBarBytes = 8 * (4 * kStages + 3);
   static constexpr int kCtlOffset = kBarOffset + kBarBytes;
   static constexpr int kSmemBytes = kCtlOffset + 64 + 1024;     // + alignment slack
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -98,6 +100,9 @@ nvfp4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmx,
   const uint32_t accf_bar = bar0 + 8u * (3 * C::kStages);
   const uint32_t acce_bar = accf_bar + 8u;
   const uint32_t drain_bar = accf_bar + 16u;
+  // scale atoms landed (both CTAs'), apart from the codes so that their
+  // copies into tensor memory run while the codes are still arriving
+  auto sff_bar = [&](int s) { return bar0 + 8u * (3 * C::kStages + 3 + s); };
   CtaCtl* ctl = reinterpret_cast<CtaCtl*>(smem + C::kCtlOffset);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kCtlOffset + 16);
   // stages issued by the other CTA's producer (written there into the leader)
@@ -120,6 +125,7 @@ nvfp4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmx,
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
       mbar_init(sfr_bar(s), 1);
+      mbar_init(sff_bar(s), 1);
     }
     mbar_init(accf_bar, 1);
     mbar_init(acce_bar, 2 * C::kEpiWarps);   // every epilogue warp of both CTAs
@@ -145,6 +151,7 @@ nvfp4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmx,
     // ------------------------------------------------------------ producer
     const uint64_t pol = l2_policy_evict_last();    // every operand row is read by many tiles
     const uint32_t full_leader = mapa_shared(full_bar(0), 0);
+    const uint32_t sff_leader = mapa_shared(sff_bar(0), 0);
     int stage = 0;
     uint32_t phase = 0;
     bool alive = true;
@@ -161,13 +168,17 @@ nvfp4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmx,
         }
         const uint32_t sx = sbase + stage * C::kStageBytes;
         const uint32_t fb = full_leader + 8u * stage;
-        if (leader) mbar_arrive_expect_tx_elect(full_bar(stage), 2 * C::kStageBytes);
-        tma_load_2d_pair_elect(sx, &tmx, fb, kb * kPRowBytes, xrow, pol);
-        tma_load_2d_pair_elect(sx + C::kXsf, &tsx, fb, 0, static_cast<int32_t>(xs + 4 * kb), pol);
-        tma_load_2d_pair_elect(sx + C::kY, &tmy, fb, kb * kPRowBytes, yrow, pol);
-        tma_load_2d_pair_elect(sx + C::kYsf, &tsy, fb, 0, static_cast<int32_t>(ys + 4 * kb), pol);
-        tma_load_2d_pair_elect(sx + C::kYsf + kPSfBytes, &tsy, fb, 0,
+        const uint32_t sfb = sff_leader + 8u * stage;
+        if (leader) {
+          mbar_arrive_expect_tx_elect(sff_bar(stage), 2 * 3 * kPSfBytes);
+          mbar_arrive_expect_tx_elect(full_bar(stage), 2 * 2 * kPCodeBytes);
+        }
+        tma_load_2d_pair_elect(sx + C::kXsf, &tsx, sfb, 0, static_cast<int32_t>(xs + 4 * kb), pol);
+        tma_load_2d_pair_elect(sx + C::kYsf, &tsy, sfb, 0, static_cast<int32_t>(ys + 4 * kb), pol);
+        tma_load_2d_pair_elect(sx + C::kYsf + kPSfBytes, &tsy, sfb, 0,
                                static_cast<int32_t>(ys + apr + 4 * kb), pol);
+        tma_load_2d_pair_elect(sx, &tmx, fb, kb * kPRowBytes, xrow, pol);
+        tma_load_2d_pair_elect(sx + C::kY, &tmy, fb, kb * kPRowBytes, yrow, pol);
         ++issued;
         if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
       }
@@ -183,7 +194,7 @@ nvfp4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmx,
       bool alive = true;
       for (int u = pair; u < units && alive; u += npairs) {
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!__all_sync(0xFFFFFFFFu, mbar_wait(full_bar(stage), phase, ctl, a.status))) {
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(sff_bar(stage), phase, ctl, a.status))) {
             alive = false;
             break;
           }
@@ -218,7 +229,8 @@ nvfp4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmx,
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(acce_bar, aphase ^ 1u, ctl, a.status))) break;
         tc_fence_after();
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!__all_sync(0xFFFFFFFFu, mbar_wait(sfr_bar(stage), phase, ctl, a.status))) {
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(sfr_bar(stage), phase, ctl, a.status) &&
+                                           mbar_wait(full_bar(stage), phase, ctl, a.status))) {
             alive = false;
             break;
           }
@@ -311,7 +323,7 @@ nvfp4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmx,
   }
 
   // Teardown.  Every copy either producer issued completes on the leader's
-  // full barriers: after the first cluster barrier the leader knows both
+  // scale and full barriers: after the first cluster barrier the leader knows both
   // producers' counts and waits for the last stages (already complete when
   // nothing aborted); then the pair frees its tensor memory together.
   tc_fence_before();
@@ -319,9 +331,12 @@ nvfp4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmx,
   if (leader && warp == 0 && lane == 0) {
     const uint32_t n = issued > *peer_issued ? issued : *peer_issued;
     const uint32_t first = n > static_cast<uint32_t>(C::kStages) ? n - C::kStages : 0u;
-    for (uint32_t i = first; i < n; ++i)
+    for (uint32_t i = first; i < n; ++i) {
+      pair_wait_drain(sff_bar(static_cast<int>(i % C::kStages)),
+                      (i / C::kStages) & 1u, ctl->timeout_ns);
       pair_wait_drain(full_bar(static_cast<int>(i % C::kStages)),
                       (i / C::kStages) & 1u, ctl->timeout_ns);
+    }
   }
   __syncwarp();
   cluster_sync_all();

@@ -154,7 +154,12 @@ struct Cfg {
   static_assert(kUnitRing > kStages + 1, "unit ring depth");
   static constexpr int kRingOffset = kCtlOffset + 32;
   static constexpr int kTablesOffset = kRingOffset + 4 * kUnitRing;
-  static constexpr int kSmemBytes = kTablesOffset + 4 * kTableInts + 1024;  // + align slack
+  // combine epilogue: 512 bytes per epilogue warp, where its 32 features x 4
+  // tokens of FP32 products are regrouped so that each reduction covers 16
+  // bytes of four features and a warp's reduction four whole 128-byte rows
+  static constexpr int kXchgOffset = (kTablesOffset + 4 * kTableInts + 15) & ~15;
+  static constexpr int kXchgBytes = 512 * 4 * kEpiGroups;
+  static constexpr int kSmemBytes = kXchgOffset + kXchgBytes + 1024;  // + align slack
   static_assert(kSmemBytes <= 232448 - 64, "shared memory budget");
 };
 
@@ -1102,53 +1107,72 @@ nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant
                 if (j < nc) dst[j] = f32_to_bf16_rn(__fmul_rn(__uint_as_float(r[j]), alpha));
             }
           }
+        } else if (emode == kGroupedCombine) {
+          // Combine.  Lane = feature f0 + lane, r[j] = token column c0 + j.
+          // Four token columns at a time go through this warp's 512 bytes of
+          // shared memory (feature fastest) and come back as lane = (token
+          // column lane / 8 of the four, features 4 (lane % 8) .. + 3), so
+          // each 16-byte reduction carries four consecutive features of one
+          // token and a warp's reduction instruction covers four whole
+          // 128-byte rows of the FP32 output (lanes on tokens would touch 32
+          // rows, 16 bytes each).
+          const int f0 = un.x_local0 + xt * 128 + q * 32;  // first feature of this warp
+          float* xb = reinterpret_cast<float*>(smem + C::kXchgOffset) + (grp * 4 + q) * 128;
+          int tok_l = c_tok[0];
+          float w_l = c_w[0];
+#pragma unroll
+          for (int ci = 1; ci < BN / 32; ++ci)
+            if (c0 == ci * 32) { tok_l = c_tok[ci]; w_l = c_w[ci]; }
+#pragma unroll
+          for (int sc = 0; sc < 8; ++sc) {
+            if (4 * sc >= nc) break;                 // uniform
+            __syncwarp();                            // the previous group's reads are done
+#pragma unroll
+            for (int jl = 0; jl < 4; ++jl)
+              xb[jl * 32 + lane] = __fmul_rn(__uint_as_float(r[4 * sc + jl]), alpha);
+            __syncwarp();
+            const int jc = 4 * sc + (lane >> 3);     // token column in the chunk
+            const float4 v =
+                *reinterpret_cast<const float4*>(xb + (lane >> 3) * 32 + 4 * (lane & 7));
+            const int tok = __shfl_sync(0xFFFFFFFFu, tok_l, jc);
+            const float w = __shfl_sync(0xFFFFFFFFu, w_l, jc);
+            if (jc < nc && tok >= 0) {               // (a rejected route has tok < 0)
+              float4 acc4;
+              acc4.x = __fmul_rn(w, v.x);
+              acc4.y = __fmul_rn(w, v.y);
+              acc4.z = __fmul_rn(w, v.z);
+              acc4.w = __fmul_rn(w, v.w);
+              red_add_v4(a.ws + static_cast<int64_t>(tok) * un.n_out + f0 + 4 * (lane & 7), acc4);
+            }
+          }
         } else {
           // Transposed orientations: lane l takes token column c0 + l and the
-          // 32 features of this warp, so stores and FP32 reductions are vectors.
+          // 32 features of this warp, so stores are vectors.
           warp_transpose32(r, lane);
           const int col = c0 + lane;
           const int f0 = un.x_local0 + xt * 128 + q * 32;  // first feature of this warp
           if (col < n_valid) {
             const int64_t y = un.y_row0 + col;
-            if (emode == kGroupedCombine) {
-              int tok = c_tok[0];
-              float w = c_w[0];
+            uint16_t* dst = reinterpret_cast<uint16_t*>(a.out) + y * a.ldc + f0;
+            const bool full = (mode == kGrouped) || (f0 + 32 <= a.rows_x);
+            if (full && a.vec_store) {
 #pragma unroll
-              for (int ci = 1; ci < BN / 32; ++ci)
-                if (c0 == ci * 32) { tok = c_tok[ci]; w = c_w[ci]; }
-              float* dst = a.ws + static_cast<int64_t>(tok) * un.n_out + f0;
+              for (int v = 0; v < 4; ++v) {
+                uint32_t w[4];
 #pragma unroll
-              for (int v = 0; v < 8; ++v) {
-                if (tok < 0) break;                  // rejected route (see above)
-                float4 acc4;
-                acc4.x = __fmul_rn(w, __fmul_rn(__uint_as_float(r[4 * v + 0]), alpha));
-                acc4.y = __fmul_rn(w, __fmul_rn(__uint_as_float(r[4 * v + 1]), alpha));
-                acc4.z = __fmul_rn(w, __fmul_rn(__uint_as_float(r[4 * v + 2]), alpha));
-                acc4.w = __fmul_rn(w, __fmul_rn(__uint_as_float(r[4 * v + 3]), alpha));
-                red_add_v4(dst + 4 * v, acc4);
+                for (int h = 0; h < 4; ++h) {
+                  const float v0 = __fmul_rn(__uint_as_float(r[8 * v + 2 * h]), alpha);
+                  const float v1 = __fmul_rn(__uint_as_float(r[8 * v + 2 * h + 1]), alpha);
+                  w[h] = static_cast<uint32_t>(f32_to_bf16_rn(v0)) |
+                         (static_cast<uint32_t>(f32_to_bf16_rn(v1)) << 16);
+                }
+                reinterpret_cast<uint4*>(dst)[v] = make_uint4(w[0], w[1], w[2], w[3]);
               }
             } else {
-              uint16_t* dst = reinterpret_cast<uint16_t*>(a.out) + y * a.ldc + f0;
-              const bool full = (mode == kGrouped) || (f0 + 32 <= a.rows_x);
-              if (full && a.vec_store) {
 #pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                  uint32_t w[4];
-#pragma unroll
-                  for (int h = 0; h < 4; ++h) {
-                    const float v0 = __fmul_rn(__uint_as_float(r[8 * v + 2 * h]), alpha);
-                    const float v1 = __fmul_rn(__uint_as_float(r[8 * v + 2 * h + 1]), alpha);
-                    w[h] = static_cast<uint32_t>(f32_to_bf16_rn(v0)) |
-                           (static_cast<uint32_t>(f32_to_bf16_rn(v1)) << 16);
-                  }
-                  reinterpret_cast<uint4*>(dst)[v] = make_uint4(w[0], w[1], w[2], w[3]);
-                }
-              } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                  if (mode == kGrouped || f0 + i < a.rows_x)
-                    dst[i] = f32_to_bf16_rn(__fmul_rn(__uint_as_float(r[i]), alpha));
-              }
+              for (int i = 0; i < 32; ++i)
+                if (mode == kGrouped || f0 + i < a.rows_x)
+                  dst[i] = f32_to_bf16_rn(__fmul_rn(__uint_as_float(r[i]), alpha));
             }
           }
         }

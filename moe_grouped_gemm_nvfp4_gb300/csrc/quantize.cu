@@ -87,14 +87,19 @@ __device__ __forceinline__ int64_t atom_offset(int64_t r, int64_t c, int64_t n_c
 }
 
 // Work item: a warp quantises 64 consecutive 16-element blocks of one row,
-// lane l taking blocks l and l + 32 of the item (each half 1 KB of coalesced
-// loads and 256 contiguous bytes of codes); atom-layout scales leave as one
-// word per four blocks.  The item index is split into (row, segment) once and
-// then stepped by the grid stride with a borrow, so no division sits in the
-// loop.
-constexpr uint32_t kQuantItemBlocks = 64;
+// lane l taking the two consecutive blocks 2l and 2l + 1 (64 bytes of BF16:
+// four 16-byte loads in flight per lane, whose lines the warp's loads fill
+// between them).  A lane stores its 16 bytes of codes with one 16-byte store;
+// in the atom layout the scale word of blocks 4j .. 4j + 3 is put together
+// by the even lane of a pair from its own two scale bytes and its neighbour's
+// (one shuffle), so the addressing and the stores are paid once per two
+// blocks.  (Four blocks per lane needed 78 registers and ran slower at three
+// blocks per SM.)  The item index is split into (row, segment) once and then
+// stepped by the grid stride with a borrow, so no division sits in the loop.
+constexpr uint32_t kQuantLaneBlocks = 2;
+constexpr uint32_t kQuantItemBlocks = 32 * kQuantLaneBlocks;
 
-__global__ void __launch_bounds__(256, 5) quantize_kernel(const uint16_t* __restrict__ x,
+__global__ void __launch_bounds__(256, 4) quantize_kernel(const uint16_t* __restrict__ x,
                                                        int64_t rows, int64_t cols, int64_t ld,
                                                        uint8_t* __restrict__ packed,
                                                        uint8_t* __restrict__ scales,
@@ -112,6 +117,11 @@ __global__ void __launch_bounds__(256, 5) quantize_kernel(const uint16_t* __rest
   const int64_t ncg = (cols + 63) >> 6;                 // 4-block scale groups per row
   const uint64_t j0 = static_cast<uint64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (j0 >= items) return;
+  // one 16-byte code store per lane when every row starts on 16 bytes; one
+  // 2-byte scale store (row-major scales) when every row's scales start on 2
+  const size_t half_row = static_cast<size_t>(cols >> 1);
+  const bool codes16 = (half_row % 16 == 0) && (reinterpret_cast<uintptr_t>(packed) % 16 == 0);
+  const bool sf16 = (bpr % 2 == 0) && (reinterpret_cast<uintptr_t>(scales) % 2 == 0);
   // Items run from the end of the tensor backwards: the tensor amax pass
   // that precedes this kernel swept it front to back, so its tail is what
   // L2 still holds.  Item it = items - 1 - j is (row r, segment sg).
@@ -120,29 +130,50 @@ __global__ void __launch_bounds__(256, 5) quantize_kernel(const uint16_t* __rest
   uint32_t sg = static_cast<uint32_t>(it0 - static_cast<uint64_t>(r) * segs);
   const int64_t dr = static_cast<int64_t>(wstride / segs);
   const uint32_t ds = static_cast<uint32_t>(wstride - static_cast<uint64_t>(dr) * segs);
-  const size_t half_row = static_cast<size_t>(cols >> 1);
   for (uint64_t j = j0; j < items; j += wstride) {
-#pragma unroll 1
-    for (int h = 0; h < 2; ++h) {
-      const uint32_t b = sg * kQuantItemBlocks + h * 32 + lane;
-      const bool valid = b < bpr;
-      Block16 q;
-      q.packed = make_uint2(0u, 0u);
-      q.sf = 0u;
-      if (valid) {
-        const uint4* src = reinterpret_cast<const uint4*>(x + r * ld + b * 16);
-        q = quantize_block(__ldg(src), __ldg(src + 1), k, s_elem);
-        *reinterpret_cast<uint2*>(packed + r * half_row + b * 8) = q.packed;
+    const uint32_t b0 = sg * kQuantItemBlocks + kQuantLaneBlocks * lane;   // lane's first block
+    uint32_t sfw = 0u;                             // the lane's scale bytes, block b0 lowest
+    if (b0 < bpr) {
+      const uint32_t nb = min(kQuantLaneBlocks, bpr - b0);                 // its valid blocks
+      const uint4* src = reinterpret_cast<const uint4*>(x + r * ld) + 2 * b0;
+      uint4 v[2 * kQuantLaneBlocks];
+#pragma unroll
+      for (int i = 0; i < 2 * static_cast<int>(kQuantLaneBlocks); ++i)
+        v[i] = (static_cast<uint32_t>(i >> 1) < nb) ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
+      uint32_t c[2 * kQuantLaneBlocks];
+#pragma unroll
+      for (int bb = 0; bb < static_cast<int>(kQuantLaneBlocks); ++bb) {
+        const Block16 q = quantize_block(v[2 * bb], v[2 * bb + 1], k, s_elem);
+        c[2 * bb] = q.packed.x;
+        c[2 * bb + 1] = q.packed.y;
+        sfw |= q.sf << (8 * bb);
       }
-      if (sf_atoms) {
-        // blocks 4j..4j+3 share one word of an atom (padding columns past the
-        // row end get zero scales)
-        const uint32_t word = gather4_bytes(q.sf);
-        if ((lane & 3) == 0 && b < static_cast<uint32_t>(ncg * 4))
-          *reinterpret_cast<uint32_t*>(scales + atom_offset(r, b, ncg)) = word;
-      } else if (valid) {
-        scales[r * bpr + b] = static_cast<uint8_t>(q.sf);
+      uint8_t* dst = packed + r * half_row + static_cast<size_t>(b0) * 8;
+      if (codes16 && nb == kQuantLaneBlocks) {
+        *reinterpret_cast<uint4*>(dst) = make_uint4(c[0], c[1], c[2], c[3]);
+      } else {
+#pragma unroll
+        for (int bb = 0; bb < static_cast<int>(kQuantLaneBlocks); ++bb)
+          if (static_cast<uint32_t>(bb) < nb)
+            reinterpret_cast<uint2*>(dst)[bb] = make_uint2(c[2 * bb], c[2 * bb + 1]);
       }
+      if (!sf_atoms) {
+        uint8_t* sdst = scales + r * bpr + b0;
+        if (sf16 && nb == kQuantLaneBlocks) {
+          *reinterpret_cast<uint16_t*>(sdst) = static_cast<uint16_t>(sfw);
+        } else {
+#pragma unroll
+          for (int bb = 0; bb < static_cast<int>(kQuantLaneBlocks); ++bb)
+            if (static_cast<uint32_t>(bb) < nb) sdst[bb] = static_cast<uint8_t>(sfw >> (8 * bb));
+        }
+      }
+    }
+    if (sf_atoms) {
+      // cols % 64 == 0: an even lane's pair of lanes covers one whole
+      // 4-block scale word (both lanes valid or neither)
+      const uint32_t other = __shfl_down_sync(0xFFFFFFFFu, sfw, 1);
+      if ((lane & 1) == 0 && b0 < bpr)
+        *reinterpret_cast<uint32_t*>(scales + atom_offset(r, b0, ncg)) = sfw | (other << 16);
     }
     // the next item: it - wstride = (r - dr) * segs + (sg - ds), with a borrow
     if (sg >= ds) {

@@ -559,7 +559,8 @@ static nvfp4_status grouped_gemm_impl(const uint8_t* A_tiles, const float* gA,
     const uint64_t nkb = static_cast<uint64_t>((K + 255) / 256);
     const uint64_t x_rows = static_cast<uint64_t>(E) * static_cast<uint64_t>(N / 128) * nkb * 144;
     const uint64_t y_rows = static_cast<uint64_t>(grouped_token_tiles(R, E)) * nkb * 144;
-    if (make_tile_rows_map(&pm.x_tiles, W_tiles, x_rows, 144) != NVFP4_OK ||
+    if (make_tile_rows_map(&pm.x_codes, W_tiles, x_rows, 128) != NVFP4_OK ||
+        make_tile_rows_map(&pm.x_scales, W_tiles, x_rows, 16) != NVFP4_OK ||
         make_tile_rows_map(&pm.y_codes, A_tiles, y_rows, static_cast<uint32_t>(pair_width / 2)) !=
             NVFP4_OK ||
         make_tile_rows_map(&pm.y_scales, A_tiles, y_rows, 16) != NVFP4_OK)

@@ -19,9 +19,12 @@
 // columns that are never stored.
 //
 // Roles (352 threads per CTA, clusters of two):
-//   warp 0      both CTAs: producer (this CTA's weight tile, its half of the
-//               token tile, the token tile's scale atoms); every copy
-//               completes on the leader's full barrier;
+//   warp 0      both CTAs: producer (the scale atoms of this CTA's weight
+//               tile and of the token tile, then the weight tile's codes and
+//               this CTA's half of the token tile's codes); the atoms
+//               complete on the leader's scale barrier, the codes on its full
+//               barrier, so the atoms' copies into tensor memory can start
+//               while the codes are still arriving;
 //   warp 6      leader: scale warp, tcgen05.cp of the stage's atoms into
 //               both CTAs' tensor memory;
 //   warp 1      both: tensor-memory allocation; leader: MMAs and commits;
@@ -55,8 +58,8 @@ struct GPairCfg {
   static constexpr int kSfColsPerStage = 16 + 16 * kYAtoms;
   static_assert(kSfColBase + kStages * kSfColsPerStage <= 512, "tensor memory budget");
   static constexpr int kBarOffset = kStages * kStageBytes;
-  // full[S], empty[S], scales_ready[S], acc_full, acc_empty, drain
-  static constexpr int kBarBytes = 8 * (3 * kStages + 3);
+  // full[S], empty[S], scales_ready[S], acc_full, acc_empty, drain, scales_full[S]
+  static constexpr int kBarBytes = 8 * (4 * kStages + 3);
   static constexpr int kCtlOffset = kBarOffset + kBarBytes;
   static constexpr int kTablesOffset = kCtlOffset + 64;
   static constexpr int kTableInts = 3 * (kGroupedMaxExperts + 1);
@@ -140,7 +143,8 @@ __device__ __forceinline__ GPairUnit gp_unit(int u, const GemmArgs& a, const int
 }
 
 __global__ void __launch_bounds__(GPairCfg::kThreads, 1)
-nvfp4_grouped_pair_kernel(const __grid_constant__ CUtensorMap tmx,   // weight tiles, 144-row boxes
+nvfp4_grouped_pair_kernel(const __grid_constant__ CUtensorMap tmx,   // weight tiles, 128-row boxes
+                          const __grid_constant__ CUtensorMap tmxs,  // weight tiles, 16-row boxes
                           const __grid_constant__ CUtensorMap tmy,   // token tiles, 128-row boxes
                           const __grid_constant__ CUtensorMap tms,   // token tiles, 16-row boxes
                           const GemmArgs a) {
@@ -157,6 +161,9 @@ nvfp4_grouped_pair_kernel(const __grid_constant__ CUtensorMap tmx,   // weight t
   const uint32_t accf_bar = bar0 + 8u * (3 * C::kStages);
   const uint32_t acce_bar = accf_bar + 8u;
   const uint32_t drain_bar = accf_bar + 16u;
+  // scale atoms landed (both CTAs'), apart from the codes so that their
+  // copies into tensor memory run while the codes are still arriving
+  auto sff_bar = [&](int s) { return bar0 + 8u * (3 * C::kStages + 3 + s); };
   CtaCtl* ctl = reinterpret_cast<CtaCtl*>(smem + C::kCtlOffset);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kCtlOffset + 16);
   volatile uint32_t* peer_issued = reinterpret_cast<volatile uint32_t*>(smem + C::kCtlOffset + 20);
@@ -179,6 +186,7 @@ nvfp4_grouped_pair_kernel(const __grid_constant__ CUtensorMap tmx,   // weight t
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
       mbar_init(sfr_bar(s), 1);
+      mbar_init(sff_bar(s), 1);
     }
     mbar_init(accf_bar, 1);
     mbar_init(acce_bar, 2 * C::kEpiWarps);   // every epilogue warp of both CTAs
@@ -252,6 +260,7 @@ nvfp4_grouped_pair_kernel(const __grid_constant__ CUtensorMap tmx,   // weight t
     const uint64_t pol_again = l2_policy_evict_normal();
     const uint64_t pol_y = l2_policy_evict_last();
     const uint32_t full_leader = mapa_shared(full_bar(0), 0);
+    const uint32_t sff_leader = mapa_shared(sff_bar(0), 0);
     int stage = 0;
     uint32_t phase = 0;
     bool alive = true;
@@ -271,16 +280,23 @@ nvfp4_grouped_pair_kernel(const __grid_constant__ CUtensorMap tmx,   // weight t
         }
         const uint32_t sx = sbase + stage * C::kStageBytes;
         const uint32_t fb = full_leader + 8u * stage;
-        if (leader) mbar_arrive_expect_tx_elect(full_bar(stage), 2 * C::kStageBytes);
-        tma_load_2d_pair_elect(sx, &tmx, fb, 0, (un.x_tile * nkb + kb) * kGpTileRows, pol_x);
+        const uint32_t sfb = sff_leader + 8u * stage;
+        if (leader) {
+          mbar_arrive_expect_tx_elect(sff_bar(stage), 2 * 2048 * (1 + C::kYAtoms));
+          mbar_arrive_expect_tx_elect(full_bar(stage), 2 * (16384 + C::kYRows * 128));
+        }
+        // the scale rows (rows 128-143 of each operand tile) first, then the codes
+        const int32_t xt_row = (un.x_tile * nkb + kb) * kGpTileRows;
+        tma_load_2d_pair_elect(sx + C::kXsf, &tmxs, sfb, 0, xt_row + 128, pol_x);
+#pragma unroll
+        for (int j = 0; j < C::kYAtoms; ++j)
+          tma_load_2d_pair_elect(sx + C::kYsf + 2048 * j, &tms, sfb, 0,
+                                 ((un.y_tile + j) * nkb + kb) * kGpTileRows + 128, pol_y);
+        tma_load_2d_pair_elect(sx, &tmx, fb, 0, xt_row, pol_x);
         // this CTA's half of the token tile: operand tile y_tile + rank
         tma_load_2d_pair_elect(sx + C::kY, &tmy, fb, 0,
                                ((un.y_tile + static_cast<int>(rank)) * nkb + kb) * kGpTileRows,
                                pol_y);
-#pragma unroll
-        for (int j = 0; j < C::kYAtoms; ++j)
-          tma_load_2d_pair_elect(sx + C::kYsf + 2048 * j, &tms, fb, 0,
-                                 ((un.y_tile + j) * nkb + kb) * kGpTileRows + 128, pol_y);
         ++issued;
         if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
       }
@@ -296,7 +312,7 @@ nvfp4_grouped_pair_kernel(const __grid_constant__ CUtensorMap tmx,   // weight t
       bool alive = true;
       for (int u = pair; u < units && alive; u += npairs) {
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!__all_sync(0xFFFFFFFFu, mbar_wait(full_bar(stage), phase, ctl, a.status))) {
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(sff_bar(stage), phase, ctl, a.status))) {
             alive = false;
             break;
           }
@@ -331,7 +347,8 @@ nvfp4_grouped_pair_kernel(const __grid_constant__ CUtensorMap tmx,   // weight t
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(acce_bar, aphase ^ 1u, ctl, a.status))) break;
         tc_fence_after();
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!__all_sync(0xFFFFFFFFu, mbar_wait(sfr_bar(stage), phase, ctl, a.status))) {
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(sfr_bar(stage), phase, ctl, a.status) &&
+                                           mbar_wait(full_bar(stage), phase, ctl, a.status))) {
             alive = false;
             break;
           }
@@ -423,9 +440,12 @@ nvfp4_grouped_pair_kernel(const __grid_constant__ CUtensorMap tmx,   // weight t
   if (leader && warp == 0 && lane == 0) {
     const uint32_t n = issued > *peer_issued ? issued : *peer_issued;
     const uint32_t first = n > static_cast<uint32_t>(C::kStages) ? n - C::kStages : 0u;
-    for (uint32_t i = first; i < n; ++i)
+    for (uint32_t i = first; i < n; ++i) {
+      gp_wait_drain(sff_bar(static_cast<int>(i % C::kStages)), (i / C::kStages) & 1u,
+                    ctl->timeout_ns);
       gp_wait_drain(full_bar(static_cast<int>(i % C::kStages)), (i / C::kStages) & 1u,
                     ctl->timeout_ns);
+    }
   }
   __syncwarp();
   cluster_sync_all();
@@ -486,7 +506,8 @@ cudaError_t launch_grouped_pair(const GroupedPairMaps& m, const GemmArgs& a, int
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, nvfp4_grouped_pair_kernel, m.x_tiles, m.y_codes, m.y_scales,
+  return cudaLaunchKernelEx(&cfg, nvfp4_grouped_pair_kernel, m.x_codes, m.x_scales, m.y_codes,
+                            m.y_scales,
                             a);
 }
 

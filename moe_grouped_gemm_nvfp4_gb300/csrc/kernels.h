@@ -153,7 +153,7 @@ cudaError_t launch_gemm_pair(const CUtensorMap& tmx, const CUtensorMap& tmy,
 // with boxes of 144 rows, the token tiles with boxes of 128 rows (codes) and
 // of 16 rows (scales).
 struct GroupedPairMaps {
-  CUtensorMap x_tiles, y_codes, y_scales;
+  CUtensorMap x_codes, x_scales, y_codes, y_scales;
 };
 cudaError_t init_grouped_pair_attributes();
 // 256 when the pair kernel takes this launch, else 0

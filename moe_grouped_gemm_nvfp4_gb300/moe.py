@@ -200,22 +200,31 @@ class DecodeLayer:
         self.gate_up = GroupedPlan(w_gate_up, T, topk, "gather", device)
         self.down = GroupedPlan(w_down, T, topk, "combine", device, routing_from=self.gate_up)
         self._side = torch.cuda.Stream(device=torch.device(device))
+        self._side_h = torch.cuda.Stream(device=torch.device(device))
 
     def step(self, x, topk_ids, h, topk_weights, stream=None, timing=None):
         """x [T, K1] BF16, topk_ids [T, k] int32, h [R, K2] BF16 (route order),
         topk_weights [T, k] FP32 -> (gate_up out [R, N1], down out [T, N2]).
 
-        `timing`, if given, is a pair of (start, end) CUDA-event lists that
-        bracket the two grouped-GEMM calls."""
+        h is an input of its own, so its quantisation (amax, then dispatch
+        into the down projection's tiles) needs only the routing: it runs on
+        a side stream beside x's quantisation and the gate_up GEMM, and the
+        down GEMM waits for it (fork and join by events, which CUDA graph
+        capture records).  `timing`, if given, is a pair of (start, end)
+        CUDA-event lists that bracket the two grouped-GEMM calls."""
         gu, dn = self.gate_up, self.down
+        main = torch.cuda.current_stream() if stream is None else stream
         _route_and_amax(gu, x, topk_ids, self._side, stream)
+        self._side_h.wait_stream(main)              # after the routing
+        with torch.cuda.stream(self._side_h):
+            dn.quantize(h, self._side_h)
         gu.quantize(x, stream, amax_done=True)
         if timing is not None:
             timing[0][0].record()
         gu.gemm(None, stream)
         if timing is not None:
             timing[0][1].record()
-        dn.quantize(h, stream)
+        main.wait_stream(self._side_h)
         if timing is not None:
             timing[1][0].record()
         dn.gemm(topk_weights, stream)
